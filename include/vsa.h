@@ -1,0 +1,204 @@
+/*
+ * vsa.h - C ABI of libvsa.so: VSA coarse-to-fine video sparse attention on
+ * one GB300 (sm_103a), forward and backward.
+ *
+ * The operation ("VSA: Faster Video Diffusion with Trainable Sparse
+ * Attention", §2 Methods and App. B "Pseudocode of VSA"):
+ *   1. tile   : a (T,H,W) video latent is cut into (4,4,4) cubes; each cube's
+ *               64 tokens form one tile (§2 "VSA design").
+ *   2. pool   : Q_c, K_c, V_c = per-cube means of Q, K, V (§2 "Coarse stage").
+ *   3. coarse : A_c = softmax(Q_c K_c^T * scale), O_c = A_c V_c; each query
+ *               cube keeps its top-K key cubes (default K = 32), turned into an
+ *               index list in the same kernel (paper notes, 损失函数/训练策略:
+ *               softmax, top-K and mask-to-index fused).  The dynamic-compute
+ *               variant keeps a variable count per query cube ("Improving Video
+ *               Sparse Attention with Fine-grained Router and Sparse Rebasing",
+ *               abstract): the smallest top-ranked set with coarse mass >= mass,
+ *               clamped to [kmin, kmax].
+ *   4. fine   : token-level softmax(Q K^T * scale) V over the 64x64 tiles of the
+ *               selected key cubes only (§2 "Fine stage"; App. B masked fine
+ *               attention).
+ *   5. combine: O = repeat(O_c over its cube) (.) G_c + O_f (.) G_f, then untile
+ *               (paper notes 关键设计 3 gating; App. B).
+ * Backward returns dQ, dK, dV, dG_c, dG_f; the selection is held fixed.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are contiguous [batch, heads, N, head_dim] with N = T*H*W, either
+ *    in raster order (token (t,h,w) at row (t*H + h)*W + w) or in cube order
+ *    (row c*64 + o, c = ((t/4)*(H/4) + h/4)*(W/4) + w/4,
+ *    o = (t%4)*16 + (h%4)*4 + w%4), as cfg->layout says.  Q, K, V, G_c, G_f,
+ *    dO and O are bf16; the pooled/coarse tensors, O_f, log-sum-exps and all
+ *    gradients are fp32.
+ *  - All pointers named without a "host" prefix are device pointers owned by
+ *    the caller, 16-byte aligned.  The library never allocates, frees or
+ *    synchronises (except vsa_check_device_status).  Scratch comes from the
+ *    caller's `ws` buffer of vsa_workspace_bytes() bytes; data the backward
+ *    pass needs comes from the caller's `saved` buffer of vsa_saved_bytes().
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.
+ *  - Arguments are checked on the host before anything is launched; an error
+ *    return leaves every output untouched.  VSA_ERR_CUDA reports a launch
+ *    failure.  Faults found on the device (a bounded wait that expired, an
+ *    index out of range) are recorded in a status word inside `ws` and read
+ *    back by vsa_check_device_status().
+ *  - Gradients are written (not accumulated).
+ */
+#ifndef VSA_H_
+#define VSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VSA_OK = 0,
+  VSA_ERR_INVALID_ARG = 1,  /* null pointer, bad count, K out of range */
+  VSA_ERR_SHAPE = 2,        /* T, H or W not a multiple of 4, or too large */
+  VSA_ERR_UNSUPPORTED = 3,  /* head_dim not 64 or 128 */
+  VSA_ERR_ALIGNMENT = 4,    /* a pointer is not 16-byte aligned */
+  VSA_ERR_CUDA = 5,         /* a CUDA call or launch failed */
+  VSA_ERR_TIMEOUT = 6,      /* a device-side bounded wait expired */
+  VSA_ERR_DEVICE_CHECK = 7  /* a device-side range check failed */
+} vsa_status_t;
+
+enum { VSA_SELECT_TOPK = 0, VSA_SELECT_MASS = 1 };
+enum { VSA_LAYOUT_RASTER = 0, VSA_LAYOUT_CUBE = 1 };
+
+/* Largest supported sizes. */
+#define VSA_MAX_CUBES 8192   /* cubes per (batch, head) */
+#define VSA_MAX_LIST 256     /* index-list capacity per query cube */
+
+typedef struct {
+  int32_t batch, heads;     /* B, number of heads */
+  int32_t T, H, W;          /* latent size, each a positive multiple of 4 */
+  int32_t head_dim;         /* D: 64 or 128 */
+  int32_t select_mode;      /* VSA_SELECT_TOPK or VSA_SELECT_MASS */
+  int32_t topk;             /* TOPK: cubes kept per query cube, 1..min(Nc, VSA_MAX_LIST) */
+  float mass;               /* MASS: coarse-probability threshold in (0, 1] */
+  int32_t kmin, kmax;       /* MASS: count clamp, 1 <= kmin <= kmax <= VSA_MAX_LIST */
+  float scale;              /* softmax scale for both stages; <= 0 means 1/sqrt(D) */
+  int32_t layout;           /* VSA_LAYOUT_RASTER or VSA_LAYOUT_CUBE (caller tensors) */
+} vsa_config_t;
+
+/* Byte offsets of the pieces of the `saved` buffer written by vsa_forward.
+ * Each piece starts on a 256-byte boundary; absent pieces have size 0. */
+typedef struct {
+  size_t q_cube, k_cube, v_cube; /* bf16 [B,heads,N,D] cube order (raster layout only) */
+  size_t qc, kc, vc, oc;         /* fp32 [B,heads,Nc,D]: pooled Q/K/V, coarse output */
+  size_t lse_c;                  /* fp32 [B,heads,Nc]: coarse log-sum-exp (natural log) */
+  size_t idx;                    /* int32 [B,heads,Nc,list_cap]: ascending key-cube ids, -1 padded */
+  size_t cnt;                    /* int32 [B,heads,Nc]: entries used per list */
+  size_t o_f;                    /* fp32 [B,heads,N,D] cube order: fine output */
+  size_t lse_f;                  /* fp32 [B,heads,N] cube order: fine log-sum-exp */
+  size_t total;                  /* = vsa_saved_bytes() */
+  int32_t list_cap;              /* topk (TOPK) or kmax (MASS) */
+} vsa_saved_layout_t;
+
+/* Checks a configuration.  VSA_OK or the reason it is rejected. */
+vsa_status_t vsa_validate(const vsa_config_t* cfg);
+
+/* Short English text for a status code (static storage). */
+const char* vsa_status_string(vsa_status_t s);
+
+/* Bytes of the caller-owned `saved` buffer; fills *layout if not NULL.
+ * Returns 0 for an invalid configuration. */
+size_t vsa_saved_bytes(const vsa_config_t* cfg, vsa_saved_layout_t* layout);
+
+/* Bytes of the caller-owned scratch buffer `ws` for the forward pass
+ * (with_backward = 0) or for forward and backward (with_backward = 1).
+ * Returns 0 for an invalid configuration. */
+size_t vsa_workspace_bytes(const vsa_config_t* cfg, int with_backward);
+
+/* Zeroes the device status word at the start of `ws` (asynchronously).  Call
+ * once after allocating `ws`. */
+vsa_status_t vsa_reset_device_status(void* ws, void* stream);
+
+/* Synchronises `stream` and returns VSA_ERR_TIMEOUT / VSA_ERR_DEVICE_CHECK if
+ * a kernel recorded a device-side failure in `ws` since the last reset. */
+vsa_status_t vsa_check_device_status(void* ws, void* stream);
+
+/* Tile / untile (App. B: tiling and untiling rearrange tokens between
+ * sequence and cube order).  inverse = 0: raster -> cube order; 1: cube ->
+ * raster.  in, out: bf16 [B,heads,N,D], distinct buffers.  cfg->layout is
+ * ignored. */
+vsa_status_t vsa_permute(const vsa_config_t* cfg, const void* in, void* out, int inverse,
+                         void* stream);
+
+/* Coarse stage (§2 "Coarse stage"): per-cube means, dense attention on the
+ * pooled sequence, selection and index lists, in one pass.
+ * q, k, v : bf16 [B,heads,N,D] in CUBE order (whatever cfg->layout says).
+ * qc, kc, vc, oc : fp32 [B,heads,Nc,D] outputs (pooled inputs, O_c).
+ * lse_c   : fp32 [B,heads,Nc] output, natural-log log-sum-exp of the logits.
+ * idx     : int32 [B,heads,Nc,list_cap] output, ascending key-cube ids, -1 padded.
+ * cnt     : int32 [B,heads,Nc] output. */
+vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const void* k,
+                               const void* v, float* qc, float* kc, float* vc, float* oc,
+                               float* lse_c, int32_t* idx, int32_t* cnt, void* ws,
+                               void* stream);
+
+/* Fine stage and combine (§2 "Fine stage"; App. B): block-sparse attention
+ * over the listed key cubes, fused with O = repeat(O_c) G_c + O_f G_f.
+ * q, k, v : bf16 CUBE order.  idx, cnt: lists as written by vsa_coarse_select
+ * (any ascending lists with entries in [0, Nc) work, e.g. injected ones).
+ * gc, gf  : bf16 gates in cfg->layout order.  oc: fp32 [B,heads,Nc,D].
+ * o       : bf16 output in cfg->layout order.
+ * o_f     : fp32 CUBE order fine output, or NULL (not needed for inference).
+ * lse_f   : fp32 [B,heads,N] CUBE order, or NULL. */
+vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const int32_t* cnt, const void* gc,
+                          const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
+                          void* ws, void* stream);
+
+/* Backward of the combine (gradient of O = repeat(O_c) G_c + O_f G_f).
+ * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp32 CUBE order; oc: fp32.
+ * dgc, dgf   : fp32 outputs in cfg->layout order.
+ * dof        : bf16 CUBE order output, dO (.) G_f.
+ * doc        : fp32 [B,heads,Nc,D] output, per-cube sum of dO (.) G_c.
+ * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof (.) o_f). */
+vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
+                             const void* gf, const float* o_f, const float* oc, float* dgc,
+                             float* dgf, void* dof, float* doc, float* delta, void* stream);
+
+/* Backward of the coarse attention on the pooled sequence, selection held
+ * fixed.  Outputs dqc, dkc, dvc: fp32 [B,heads,Nc,D] (gradients w.r.t. the
+ * pooled means). */
+vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const float* kc,
+                            const float* vc, const float* oc, const float* lse_c,
+                            const float* doc, float* dqc, float* dkc, float* dvc, void* ws,
+                            void* stream);
+
+/* Backward of the fine stage plus the pooling: writes
+ *   dq = dQ_fine + repeat(dqc)/64, dk = dK_fine + repeat(dkc)/64,
+ *   dv = dV_fine + repeat(dvc)/64
+ * as fp32 in cfg->layout order.  q, k, v, dof: bf16 CUBE order; lse_f, delta:
+ * fp32 CUBE order; dqc/dkc/dvc may be NULL (no pooled contribution). */
+vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const int32_t* cnt, const float* lse_f,
+                          const void* dof, const float* delta, const float* dqc,
+                          const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
+                          void* ws, void* stream);
+
+/* Whole forward: tile, coarse stage, fine stage + combine, untile.
+ * q, k, v, gc, gf: bf16 in cfg->layout order; o: bf16 output, same order.
+ * saved: vsa_saved_bytes() bytes, filled for vsa_backward (O_f is written only
+ * when with_backward != 0). */
+vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
+                         const void* gc, const void* gf, void* o, void* saved,
+                         int with_backward, void* ws, void* stream);
+
+/* Whole backward from the upstream gradient d_o (bf16, cfg->layout order).
+ * q, k, v, gc, gf: the forward's inputs; saved: as filled by vsa_forward
+ * with with_backward = 1.  Outputs fp32 in cfg->layout order. */
+vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* q, const void* k,
+                          const void* v, const void* gc, const void* gf, const void* saved,
+                          const void* d_o, float* dq, float* dk, float* dv, float* dgc,
+                          float* dgf, void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSA_H_ */

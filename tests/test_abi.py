@@ -1,0 +1,101 @@
+"""The C ABI library: it loads, exports what include/vsa.h declares, and its
+host-side argument checks answer correctly.  No GPU is needed: none of these
+calls launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from trainable_block_sparse_gb300 import build, vsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return vsa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "vsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/vsa.h but not exported"
+
+
+def _cfg(**kw):
+    base = dict(batch=1, heads=2, T=8, H=8, W=8, head_dim=64, topk=2)
+    base.update(kw)
+    return vsa.make_config(base.pop("batch"), base.pop("heads"), base.pop("T"), base.pop("H"),
+                           base.pop("W"), base.pop("head_dim"), **base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, vsa.OK),
+    ({"T": 6}, vsa.ERR_SHAPE),
+    ({"W": 0}, vsa.ERR_SHAPE),
+    ({"head_dim": 96}, vsa.ERR_UNSUPPORTED),
+    ({"topk": 0}, vsa.ERR_INVALID_ARG),
+    ({"topk": 9}, vsa.ERR_INVALID_ARG),          # more than the 8 cubes
+    ({"batch": 0}, vsa.ERR_INVALID_ARG),
+    ({"select": "mass", "kmin": 9, "kmax": 8}, vsa.ERR_INVALID_ARG),
+    ({"select": "mass", "mass": 0.0}, vsa.ERR_INVALID_ARG),
+    ({"select": "mass", "kmax": 300}, vsa.ERR_INVALID_ARG),
+    ({"select": "mass"}, vsa.OK),
+    ({"T": 4096, "H": 64, "W": 64}, vsa.ERR_SHAPE),  # too many cubes
+])
+def test_validate(lib, kw, status):
+    cfg = _cfg(**kw)
+    assert lib.vsa_validate(ctypes.byref(cfg)) == status
+
+
+def test_null_config_and_pointers(lib):
+    assert lib.vsa_validate(None) == vsa.ERR_INVALID_ARG
+    cfg = _cfg()
+    # null tensors are rejected on the host, before any launch
+    assert lib.vsa_permute(ctypes.byref(cfg), None, None, 0, None) == vsa.ERR_INVALID_ARG
+    assert lib.vsa_forward(ctypes.byref(cfg), *([None] * 7), 1, None, None) == vsa.ERR_INVALID_ARG
+
+
+def test_misaligned_pointer_is_rejected(lib):
+    cfg = _cfg()
+    a = ctypes.c_void_p(0x1000)
+    b = ctypes.c_void_p(0x2008)  # not 16-byte aligned
+    assert lib.vsa_permute(ctypes.byref(cfg), a, b, 0, None) == vsa.ERR_ALIGNMENT
+    assert lib.vsa_permute(ctypes.byref(cfg), a, a, 0, None) == vsa.ERR_INVALID_ARG
+
+
+def test_buffer_sizes(lib):
+    cfg = _cfg()
+    L = vsa.saved_layout(cfg)
+    # pieces are 256-byte aligned, in order, and fit the total
+    offs = [L.q_cube, L.k_cube, L.v_cube, L.qc, L.kc, L.vc, L.oc, L.lse_c, L.idx, L.cnt, L.o_f,
+            L.lse_f]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs) and L.total > offs[-1]
+    assert L.list_cap == 2
+    n_tok = 2 * 512
+    assert L.o_f - L.cnt >= 2 * 8 * 4 and L.total - L.lse_f >= n_tok * 4
+    fwd = vsa.workspace_bytes(cfg, False)
+    bwd = vsa.workspace_bytes(cfg, True)
+    assert 0 < fwd < bwd
+    bad = _cfg(T=5)
+    assert lib.vsa_saved_bytes(ctypes.byref(bad), None) == 0
+    assert lib.vsa_workspace_bytes(ctypes.byref(bad), 1) == 0
+    # cube-order callers need no cube copies
+    Lc = vsa.saved_layout(_cfg(layout="cube"))
+    assert Lc.total < L.total
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert len(lib.vsa_status_string(s)) > 0
+    assert lib.vsa_status_string(99) == b"unknown status"

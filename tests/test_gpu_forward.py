@@ -1,0 +1,265 @@
+"""Forward parity of the CUDA path against the fp64 oracle.
+
+Index lists must match bit for bit (inputs are drawn so that no selection
+boundary is closer than 1e-3 in logit); floating-point outputs must be within
+max-abs 2e-2 and relative-L2 1e-2 of the oracle.  Small layers are compared
+element by element; full-size layers on sampled (batch, head) slices and
+cubes, in the same launch configuration the benchmark times.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import vsa_oracle as O
+from tests.helpers import assert_close, cuda_inputs, enforce_gaps, to_np
+from trainable_block_sparse_gb300 import build, synth, vsa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@functools.lru_cache(maxsize=2)
+def gapped(name, **over):
+    wl = synth.WORKLOADS[name].replace(**over) if over else synth.WORKLOADS[name]
+    inp = synth.Inputs(wl, with_grad=True)
+    enforce_gaps(inp)
+    return inp
+
+
+def run_forward(inp, layout="raster"):
+    wl = inp.wl
+    cfg = vsa.config_for(wl, layout)
+    t = cuda_inputs(inp)
+    if layout == "cube":
+        for n in ("q", "k", "v", "gc", "gf"):
+            t[n] = vsa.permute(cfg, t[n])
+    bufs = vsa.Buffers(cfg, "cuda", with_backward=True)
+    o = vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, with_backward=True)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == vsa.OK
+    B, H, N, D, nc, cap = wl.batch, wl.heads, wl.tokens, wl.head_dim, wl.cubes, wl.list_capacity
+    views = {
+        "idx": bufs.view("idx", torch.int32, (B, H, nc, cap)),
+        "cnt": bufs.view("cnt", torch.int32, (B, H, nc)),
+        "qc": bufs.view("qc", torch.float32, (B, H, nc, D)),
+        "oc": bufs.view("oc", torch.float32, (B, H, nc, D)),
+        "lse_c": bufs.view("lse_c", torch.float32, (B, H, nc)),
+        "o_f": bufs.view("o_f", torch.float32, (B, H, N, D)),
+        "lse_f": bufs.view("lse_f", torch.float32, (B, H, N)),
+    }
+    if layout == "cube":
+        o = vsa.permute(cfg, o, inverse=True)
+    return cfg, t, bufs, o, views
+
+
+def slices_of(wl, full):
+    if full:
+        return [(b, h) for b in range(wl.batch) for h in range(wl.heads)]
+    return sorted({(0, 0), (wl.batch - 1, wl.heads - 1), (0, wl.heads // 2)})
+
+
+def cubes_of(wl, full, seed=0):
+    if full:
+        return list(range(wl.cubes))
+    r = np.random.default_rng(seed)
+    extra = r.choice(wl.cubes, size=3, replace=False).tolist()
+    return sorted({0, 1, wl.cubes - 1, wl.cubes // 2, *extra})
+
+
+def check_forward(inp, layout="raster", full=False):
+    wl = inp.wl
+    cfg, t, bufs, o, v = run_forward(inp, layout)
+    o_np = to_np(o)
+    for b, h in slices_of(wl, full):
+        hd = O.head_of(inp, b, h)
+        # selection: bit-exact lists and counts for every query cube of the slice
+        cnt = v["cnt"][b, h].cpu().numpy()
+        idx = v["idx"][b, h].cpu().numpy()
+        assert np.array_equal(cnt, hd.cnt), f"counts differ in slice {(b, h)}"
+        assert np.array_equal(idx, hd.idx), f"index lists differ in slice {(b, h)}"
+        assert_close("O_c", to_np(v["oc"][b, h]), hd.coarse["out"])
+        assert_close("lse_c", to_np(v["lse_c"][b, h]), hd.coarse["lse"])
+        assert_close("Q_c", to_np(v["qc"][b, h]), hd.qc, atol=1e-5, rtol_l2=1e-6)
+        cubes = cubes_of(wl, full, seed=b * 1000 + h)
+        of_g = to_np(v["o_f"][b, h]).reshape(wl.cubes, 64, wl.head_dim)
+        lse_g = to_np(v["lse_f"][b, h]).reshape(wl.cubes, 64)
+        ref_o, got_o, ref_of, got_of, ref_l, got_l = [], [], [], [], [], []
+        for c in cubes:
+            _, of, lse = hd.rows(c)
+            ref_of.append(of)
+            got_of.append(of_g[c])
+            ref_l.append(lse)
+            got_l.append(lse_g[c])
+            ref_o.append(hd.output_tiled(c))
+            got_o.append(o_np[b, h, synth.raster_rows_of_cube(wl, c)])
+        assert_close("O_f", np.stack(got_of), np.stack(ref_of))
+        assert_close("lse_f", np.stack(got_l), np.stack(ref_l))
+        assert_close("O", np.stack(got_o), np.stack(ref_o))
+
+
+def test_forward_tiny_full():
+    check_forward(gapped("tiny"), full=True)
+
+
+def test_forward_tiny_cube_layout():
+    check_forward(gapped("tiny"), layout="cube", full=True)
+
+
+@pytest.mark.parametrize("name", ["pretrain", "wan13b", "dynamic"])
+def test_forward_sampled(name):
+    check_forward(gapped(name))
+
+
+@pytest.mark.slow
+def test_forward_sampled_720p():
+    check_forward(gapped("p720"))
+
+
+def test_permute_is_oracle_tiling():
+    inp = gapped("tiny")
+    wl = inp.wl
+    cfg = vsa.config_for(wl)
+    q = inp.q.cuda()
+    qt = vsa.permute(cfg, q)
+    ref = np.stack([O.tile(O.f64(inp.q[0, h]), wl.T, wl.H, wl.W) for h in range(wl.heads)])
+    assert np.array_equal(to_np(qt)[0], ref)  # bit-exact: a pure rearrangement
+    assert torch.equal(vsa.permute(cfg, qt, inverse=True), q)
+
+
+def test_pooled_means_within_fp32_summation_bound():
+    inp = gapped("pretrain")
+    wl = inp.wl
+    cfg = vsa.config_for(wl)
+    qt = vsa.permute(cfg, inp.q.cuda())
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    qc = vsa.coarse_select(cfg, qt, qt, qt, ws)[0]
+    for b, h in slices_of(wl, False):
+        x = O.tile(O.f64(inp.q[b, h]), wl.T, wl.H, wl.W).reshape(wl.cubes, 64, wl.head_dim)
+        exact = x.mean(axis=1)
+        bound = 63 * 2.0 ** -24 * np.abs(x).mean(axis=1) + 1e-30
+        assert np.all(np.abs(to_np(qc[b, h]) - exact) <= bound)
+
+
+@pytest.mark.parametrize("name", ["tiny", "pretrain"])
+def test_fine_stage_with_injected_oracle_lists(name):
+    """The fine stage alone, fed the oracle's lists, pooled O_c and tiled inputs."""
+    inp = gapped(name)
+    wl = inp.wl
+    cfg = vsa.config_for(wl, layout="cube")
+    heads = {(b, h): O.head_of(inp, b, h) for b, h in slices_of(wl, True)}
+    idx = np.stack([[heads[(b, h)].idx for h in range(wl.heads)] for b in range(wl.batch)])
+    cnt = np.stack([[heads[(b, h)].cnt for h in range(wl.heads)] for b in range(wl.batch)])
+    oc = np.stack([[heads[(b, h)].coarse["out"] for h in range(wl.heads)] for b in range(wl.batch)])
+
+    def tiled(x):
+        return torch.from_numpy(O.tile(O.f64(x), wl.T, wl.H, wl.W)).to(torch.bfloat16).cuda()
+
+    q, k, v, gc, gf = (tiled(getattr(inp, n)) for n in ("q", "k", "v", "gc", "gf"))
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
+    o, of, lse = vsa.fine_fwd(cfg, q, k, v, torch.from_numpy(idx).int().cuda(),
+                              torch.from_numpy(cnt).int().cuda(), gc, gf,
+                              torch.from_numpy(oc).float().cuda(), ws)
+    torch.cuda.synchronize()
+    assert vsa.lib().vsa_check_device_status(vsa._ptr(ws), vsa._stream()) == vsa.OK
+    for (b, h), hd in heads.items():
+        for c in cubes_of(wl, name == "tiny", seed=h):
+            _, of_r, lse_r = hd.rows(c)
+            sl = slice(c * 64, (c + 1) * 64)
+            assert_close("O_f", to_np(of[b, h, sl]), of_r)
+            assert_close("lse_f", to_np(lse[b, h, sl]), lse_r)
+            assert_close("O", to_np(o[b, h, sl]), hd.output_tiled(c))
+
+
+# ------------------------------------------------------------------ edge cases
+
+def _custom(T, H, W, D, topk, seed, select="topk", heads=2, batch=1):
+    wl = synth.Workload(f"edge_{T}x{H}x{W}_d{D}_k{topk}", batch, heads, D, T, H, W, select,
+                        topk=topk, seed=seed)
+    inp = synth.Inputs(wl, with_grad=True)
+    enforce_gaps(inp)
+    return inp
+
+
+@pytest.mark.parametrize("thw,D,topk", [
+    ((4, 4, 12), 64, 2),    # odd number of cubes: the last pair has one cube
+    ((4, 4, 4), 128, 1),    # a single cube
+    ((8, 4, 12), 128, 5),   # odd K, tail step with one key cube
+    ((4, 8, 8), 64, 4),     # K = all cubes
+])
+def test_forward_edge_shapes(thw, D, topk):
+    check_forward(_custom(*thw, D, topk, seed=7 + topk), full=True)
+
+
+def test_full_selection_with_fine_only_gates_is_dense_attention():
+    """K = all cubes, G_c = 0, G_f = 1: the output is dense softmax attention."""
+    inp = _custom(4, 8, 8, 64, 4, seed=11)
+    inp.gc = torch.zeros_like(inp.gc)
+    inp.gf = torch.ones_like(inp.gf)
+    wl = inp.wl
+    _, t, _, o, _ = run_forward(inp)
+    for h in range(wl.heads):
+        q, k, v = (O.f64(getattr(inp, n)[0, h]) for n in ("q", "k", "v"))
+        s = q @ k.T / np.sqrt(wl.head_dim)
+        p = np.exp(s - s.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        assert_close("dense", to_np(o[0, h]), p @ v)
+
+
+def test_fine_gates_zero_gives_repeated_coarse_output():
+    inp = _custom(8, 8, 8, 64, 2, seed=12)
+    inp.gf = torch.zeros_like(inp.gf)
+    inp.gc = torch.ones_like(inp.gc)
+    wl = inp.wl
+    _, _, _, o, v = run_forward(inp)
+    oc = to_np(v["oc"])
+    for h in range(wl.heads):
+        for c in range(wl.cubes):
+            rows = synth.raster_rows_of_cube(wl, c)
+            ref = np.broadcast_to(oc[0, h, c], (64, wl.head_dim))
+            # O is bf16: equal to the bf16 rounding of O_c
+            want = torch.from_numpy(np.ascontiguousarray(ref)).float().to(torch.bfloat16).double().numpy()
+            assert np.array_equal(to_np(o[0, h])[rows], want)
+
+
+def test_bad_index_lists_are_reported_not_faulted():
+    """Out-of-range ids, unsorted lists and bad counts: flagged, dropped, no fault."""
+    inp = _custom(8, 8, 8, 64, 2, seed=13)
+    wl = inp.wl
+    cfg = vsa.config_for(wl, layout="cube")
+    t = cuda_inputs(inp)
+    q, k, v = (vsa.permute(cfg, t[n]) for n in ("q", "k", "v"))
+    idx = torch.tensor([[[[0, 1]] * wl.cubes] * wl.heads], dtype=torch.int32)
+    idx[0, 0, 1] = torch.tensor([5, 99])       # id out of range
+    idx[0, 0, 2] = torch.tensor([-3, 1])       # negative id
+    idx[0, 1, 3] = torch.tensor([4, 2])        # not ascending
+    cnt = torch.full((1, wl.heads, wl.cubes), 2, dtype=torch.int32)
+    cnt[0, 1, 5] = 7                           # count above capacity
+    oc = torch.zeros(1, wl.heads, wl.cubes, wl.head_dim, device="cuda")
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
+    vsa.fine_fwd(cfg, q, k, v, idx.cuda(), cnt.cuda(), t["gc"], t["gf"], oc, ws)
+    torch.cuda.synchronize()
+    st = vsa.lib().vsa_check_device_status(vsa._ptr(ws), vsa._stream())
+    assert st == vsa.ERR_DEVICE_CHECK
+    # the context is still usable
+    assert torch.cuda.is_available() and (torch.ones(4, device="cuda") * 2).sum().item() == 8
+
+
+def test_worked_example_ties_keep_lower_ids():
+    """Q = 0: all logits tie; top-1 keeps cube 0 and O_f is cube 0's mean of V."""
+    inp = _custom(4, 4, 8, 64, 1, seed=14)
+    inp.q = torch.zeros_like(inp.q)
+    wl = inp.wl
+    _, _, _, o, v = run_forward(inp)
+    assert v["idx"].cpu().flatten().tolist() == [0] * (wl.heads * wl.cubes)
+    vt = O.tile(O.f64(inp.v[0, 0]), wl.T, wl.H, wl.W)
+    assert_close("O_f", to_np(v["o_f"][0, 0]), np.broadcast_to(vt[:64].mean(0), (128, 64)))

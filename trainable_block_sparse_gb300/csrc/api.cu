@@ -1,0 +1,427 @@
+// Host side of the C ABI declared in include/vsa.h: argument checks, carving
+// of the caller's `saved` and `ws` buffers, and the launch sequences of the
+// forward and backward passes.  Nothing here allocates device memory.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/vsa.h"
+#include "sm103_ptx.cuh"
+#include "vsa_common.cuh"
+
+namespace vsa {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
+  if (!cfg) return VSA_ERR_INVALID_ARG;
+  if (cfg->batch < 1 || cfg->heads < 1) return VSA_ERR_INVALID_ARG;
+  if (cfg->T < 4 || cfg->H < 4 || cfg->W < 4 || cfg->T % 4 || cfg->H % 4 || cfg->W % 4)
+    return VSA_ERR_SHAPE;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return VSA_ERR_UNSUPPORTED;
+  if (cfg->layout != VSA_LAYOUT_RASTER && cfg->layout != VSA_LAYOUT_CUBE)
+    return VSA_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(cfg->batch) * cfg->heads;
+  const long long n = static_cast<long long>(cfg->T) * cfg->H * cfg->W;
+  const long long nc = n / kTile;
+  if (bh > 65535) return VSA_ERR_SHAPE;
+  if (nc > VSA_MAX_CUBES || bh * n > 0x7fffffffLL) return VSA_ERR_SHAPE;
+  int cap;
+  if (cfg->select_mode == VSA_SELECT_TOPK) {
+    if (cfg->topk < 1 || cfg->topk > nc || cfg->topk > VSA_MAX_LIST) return VSA_ERR_INVALID_ARG;
+    cap = cfg->topk;
+  } else if (cfg->select_mode == VSA_SELECT_MASS) {
+    if (!(cfg->mass > 0.f && cfg->mass <= 1.f)) return VSA_ERR_INVALID_ARG;
+    if (cfg->kmin < 1 || cfg->kmin > cfg->kmax || cfg->kmax > VSA_MAX_LIST)
+      return VSA_ERR_INVALID_ARG;
+    cap = cfg->kmax;
+  } else {
+    return VSA_ERR_INVALID_ARG;
+  }
+  if (bh * nc * cap > 0x7fffffffLL) return VSA_ERR_SHAPE;
+  float scale = cfg->scale;
+  if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(cfg->head_dim));
+  if (!std::isfinite(scale)) return VSA_ERR_INVALID_ARG;
+  g->B = cfg->batch;
+  g->heads = cfg->heads;
+  g->T = cfg->T;
+  g->H = cfg->H;
+  g->W = cfg->W;
+  g->D = cfg->head_dim;
+  g->BH = static_cast<int>(bh);
+  g->N = static_cast<int>(n);
+  g->Nc = static_cast<int>(nc);
+  g->ct = cfg->T / 4;
+  g->ch = cfg->H / 4;
+  g->cw = cfg->W / 4;
+  g->cap = cap;
+  g->raster = cfg->layout == VSA_LAYOUT_RASTER;
+  g->scale = scale;
+  return VSA_OK;
+}
+
+size_t bf16_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 2; }
+size_t f32_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 4; }
+size_t pooled_bytes(const Geom& g) { return static_cast<size_t>(g.BH) * g.Nc * g.D * 4; }
+
+void saved_layout(const Geom& g, vsa_saved_layout_t* L) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  const size_t cube_copy = g.raster ? bf16_tensor(g) : 0;
+  L->q_cube = take(cube_copy);
+  L->k_cube = take(cube_copy);
+  L->v_cube = take(cube_copy);
+  L->qc = take(pooled_bytes(g));
+  L->kc = take(pooled_bytes(g));
+  L->vc = take(pooled_bytes(g));
+  L->oc = take(pooled_bytes(g));
+  L->lse_c = take(static_cast<size_t>(g.BH) * g.Nc * 4);
+  L->idx = take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4);
+  L->cnt = take(static_cast<size_t>(g.BH) * g.Nc * 4);
+  L->o_f = take(f32_tensor(g));
+  L->lse_f = take(static_cast<size_t>(g.BH) * g.N * 4);
+  L->total = off;
+  L->list_cap = g.cap;
+}
+
+// Carves `ws`; returns the bytes needed.  With base == nullptr only sizes.
+size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
+  size_t off = 0;
+  char* b = static_cast<char*>(base);
+  auto take = [&](size_t bytes) -> void* {
+    void* p = b ? b + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  };
+  Workspace ws{};
+  const int npairs = g.BH * ((g.Nc + 1) / 2);
+  ws.status = static_cast<uint32_t*>(take(4));
+  ws.counter = static_cast<int*>(take(64));
+  ws.n_qpairs = npairs;
+  ws.qpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
+  ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
+  if (with_backward) {
+    const size_t words = (g.Nc + 31) / 32;
+    ws.dof = take(bf16_tensor(g));
+    ws.delta = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.N * 4));
+    ws.doc = static_cast<float*>(take(pooled_bytes(g)));
+    ws.dqc = static_cast<float*>(take(pooled_bytes(g)));
+    ws.dkc = static_cast<float*>(take(pooled_bytes(g)));
+    ws.dvc = static_cast<float*>(take(pooled_bytes(g)));
+    ws.cprob = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
+    ws.cgrad = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
+    ws.tmask = static_cast<uint32_t*>(take(static_cast<size_t>(g.BH) * g.Nc * words * 4));
+    ws.toff = static_cast<int*>(take(static_cast<size_t>(g.BH) * (g.Nc + 1) * 4));
+    ws.tlist = static_cast<int*>(take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4));
+    ws.n_kpairs = npairs;
+    ws.kpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
+    ws.klist = static_cast<uint32_t*>(take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4));
+  }
+  if (w) *w = ws;
+  return off;
+}
+
+vsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? VSA_OK : VSA_ERR_CUDA; }
+
+template <typename... Ptrs>
+bool all_aligned(Ptrs... ps) {
+  return (aligned16(ps) && ...);
+}
+
+template <typename... Ptrs>
+bool all_set(Ptrs... ps) {
+  return ((ps != nullptr) && ...);
+}
+
+using bf16 = __nv_bfloat16;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_cols) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace vsa
+
+using namespace vsa;
+
+extern "C" {
+
+vsa_status_t vsa_validate(const vsa_config_t* cfg) {
+  Geom g;
+  return make_geom(cfg, &g);
+}
+
+const char* vsa_status_string(vsa_status_t s) {
+  switch (s) {
+    case VSA_OK: return "ok";
+    case VSA_ERR_INVALID_ARG: return "invalid argument";
+    case VSA_ERR_SHAPE: return "unsupported shape (T, H, W must be positive multiples of 4; size limits)";
+    case VSA_ERR_UNSUPPORTED: return "unsupported head_dim (64 or 128)";
+    case VSA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case VSA_ERR_CUDA: return "CUDA error";
+    case VSA_ERR_TIMEOUT: return "device-side wait timed out";
+    case VSA_ERR_DEVICE_CHECK: return "device-side range check failed (bad index list)";
+  }
+  return "unknown status";
+}
+
+size_t vsa_saved_bytes(const vsa_config_t* cfg, vsa_saved_layout_t* layout) {
+  Geom g;
+  if (make_geom(cfg, &g) != VSA_OK) return 0;
+  vsa_saved_layout_t L;
+  saved_layout(g, &L);
+  if (layout) *layout = L;
+  return L.total;
+}
+
+size_t vsa_workspace_bytes(const vsa_config_t* cfg, int with_backward) {
+  Geom g;
+  if (make_geom(cfg, &g) != VSA_OK) return 0;
+  return carve_ws(g, with_backward, nullptr, nullptr);
+}
+
+vsa_status_t vsa_reset_device_status(void* ws, void* stream) {
+  if (!ws) return VSA_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, 4, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status_t vsa_check_device_status(void* ws, void* stream) {
+  if (!ws) return VSA_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (word & kDevTimeout) return VSA_ERR_TIMEOUT;
+  if (word & kDevBadIndex) return VSA_ERR_DEVICE_CHECK;
+  return VSA_OK;
+}
+
+vsa_status_t vsa_permute(const vsa_config_t* cfg, const void* in, void* out, int inverse,
+                         void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(in, out) || in == out || (inverse != 0 && inverse != 1))
+    return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(in, out)) return VSA_ERR_ALIGNMENT;
+  return cuda_status(launch_permute(g, static_cast<const bf16*>(in), static_cast<bf16*>(out),
+                                    inverse, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const void* k,
+                               const void* v, float* qc, float* kc, float* vc, float* oc,
+                               float* lse_c, int32_t* idx, int32_t* cnt, void* ws,
+                               void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt)) return VSA_ERR_ALIGNMENT;
+  (void)ws;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_pool(g, static_cast<const bf16*>(q), qc, s) != cudaSuccess ||
+      launch_pool(g, static_cast<const bf16*>(k), kc, s) != cudaSuccess ||
+      launch_pool(g, static_cast<const bf16*>(v), vc, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  return cuda_status(launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin,
+                                          cfg->kmax, qc, kc, vc, oc, lse_c, idx, cnt, s));
+}
+
+vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const int32_t* cnt, const void* gc,
+                          const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
+                          void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(q, k, v, idx, cnt, gc, gf, oc, o, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, idx, cnt, gc, gf, oc, o, ws) || !aligned16(o_f) || !aligned16(lse_f))
+    return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_fwd(g, static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                     static_cast<const bf16*>(v), static_cast<const bf16*>(gc),
+                                     static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
+                                     o_f, lse_f, w, s));
+}
+
+vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
+                             const void* gf, const float* o_f, const float* oc, float* dgc,
+                             float* dgf, void* dof, float* doc, float* delta, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(d_o, gc, gf, o_f, oc, dgc, dgf, dof, doc, delta)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(d_o, gc, gf, o_f, oc, dgc, dgf, dof, doc, delta)) return VSA_ERR_ALIGNMENT;
+  return cuda_status(launch_combine_bwd(
+      g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
+      static_cast<const bf16*>(gf), o_f, oc, dgc, dgf, static_cast<bf16*>(dof), doc, delta,
+      static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const float* kc,
+                            const float* vc, const float* oc, const float* lse_c,
+                            const float* doc, float* dqc, float* dkc, float* dvc, void* ws,
+                            void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(qc, kc, vc, oc, lse_c, doc, dqc, dkc, dvc, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(qc, kc, vc, oc, lse_c, doc, dqc, dkc, dvc, ws)) return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 1, ws, &w);
+  return cuda_status(launch_coarse_bwd(g, qc, kc, vc, oc, lse_c, doc, dqc, dkc, dvc, w,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const int32_t* cnt, const float* lse_f,
+                          const void* dof, const float* delta, const float* dqc,
+                          const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
+                          void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(q, k, v, idx, cnt, lse_f, dof, delta, dq, dk, dv, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, idx, cnt, lse_f, dof, delta, dq, dk, dv, ws) || !aligned16(dqc) ||
+      !aligned16(dkc) || !aligned16(dvc))
+    return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 1, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_bwd(g, static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                     static_cast<const bf16*>(v), lse_f,
+                                     static_cast<const bf16*>(dof), delta, dqc, dkc, dvc, dq, dk,
+                                     dv, w, s));
+}
+
+vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
+                         const void* gc, const void* gf, void* o, void* saved,
+                         int with_backward, void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_ALIGNMENT;
+  vsa_saved_layout_t L;
+  saved_layout(g, &L);
+  char* sv = static_cast<char*>(saved);
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bf16 *qt, *kt, *vt;
+  float* qc = reinterpret_cast<float*>(sv + L.qc);
+  float* kc = reinterpret_cast<float*>(sv + L.kc);
+  float* vc = reinterpret_cast<float*>(sv + L.vc);
+  if (g.raster) {
+    bf16* qo = reinterpret_cast<bf16*>(sv + L.q_cube);
+    bf16* ko = reinterpret_cast<bf16*>(sv + L.k_cube);
+    bf16* vo = reinterpret_cast<bf16*>(sv + L.v_cube);
+    if (launch_permute_pool(g, static_cast<const bf16*>(q), qo, qc, s) != cudaSuccess ||
+        launch_permute_pool(g, static_cast<const bf16*>(k), ko, kc, s) != cudaSuccess ||
+        launch_permute_pool(g, static_cast<const bf16*>(v), vo, vc, s) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    qt = qo;
+    kt = ko;
+    vt = vo;
+  } else {
+    qt = static_cast<const bf16*>(q);
+    kt = static_cast<const bf16*>(k);
+    vt = static_cast<const bf16*>(v);
+    if (launch_pool(g, qt, qc, s) != cudaSuccess || launch_pool(g, kt, kc, s) != cudaSuccess ||
+        launch_pool(g, vt, vc, s) != cudaSuccess)
+      return VSA_ERR_CUDA;
+  }
+  float* oc = reinterpret_cast<float*>(sv + L.oc);
+  int* idx = reinterpret_cast<int*>(sv + L.idx);
+  int* cnt = reinterpret_cast<int*>(sv + L.cnt);
+  if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
+                           kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt,
+                           s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_fwd(g, qt, kt, vt, static_cast<const bf16*>(gc),
+                                     static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
+                                     with_backward ? reinterpret_cast<float*>(sv + L.o_f) : nullptr,
+                                     reinterpret_cast<float*>(sv + L.lse_f), w, s));
+}
+
+vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* q, const void* k,
+                          const void* v, const void* gc, const void* gf, const void* saved,
+                          const void* d_o, float* dq, float* dk, float* dv, float* dgc,
+                          float* dgf, void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(q, k, v, gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws))
+    return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws))
+    return VSA_ERR_ALIGNMENT;
+  vsa_saved_layout_t L;
+  saved_layout(g, &L);
+  const char* sv = static_cast<const char*>(saved);
+  Workspace w;
+  carve_ws(g, 1, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bf16* qt = g.raster ? reinterpret_cast<const bf16*>(sv + L.q_cube) : static_cast<const bf16*>(q);
+  const bf16* kt = g.raster ? reinterpret_cast<const bf16*>(sv + L.k_cube) : static_cast<const bf16*>(k);
+  const bf16* vt = g.raster ? reinterpret_cast<const bf16*>(sv + L.v_cube) : static_cast<const bf16*>(v);
+  const float* of = reinterpret_cast<const float*>(sv + L.o_f);
+  const float* oc = reinterpret_cast<const float*>(sv + L.oc);
+  const int* idx = reinterpret_cast<const int*>(sv + L.idx);
+  const int* cnt = reinterpret_cast<const int*>(sv + L.cnt);
+  if (launch_combine_bwd(g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
+                         static_cast<const bf16*>(gf), of, oc, dgc, dgf,
+                         static_cast<bf16*>(w.dof), w.doc, w.delta, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_coarse_bwd(g, reinterpret_cast<const float*>(sv + L.qc),
+                        reinterpret_cast<const float*>(sv + L.kc),
+                        reinterpret_cast<const float*>(sv + L.vc), oc,
+                        reinterpret_cast<const float*>(sv + L.lse_c), w.doc, w.dqc, w.dkc, w.dvc,
+                        w, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_bwd(g, qt, kt, vt, reinterpret_cast<const float*>(sv + L.lse_f),
+                                     static_cast<const bf16*>(w.dof), w.delta, w.dqc, w.dkc,
+                                     w.dvc, dq, dk, dv, w, s));
+}
+
+}  // extern "C"

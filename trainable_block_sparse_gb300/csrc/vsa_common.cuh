@@ -1,0 +1,119 @@
+// Shared definitions for the VSA kernels: problem geometry, the cube <-> raster
+// index maps, the internal launch interface between the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace vsa {
+
+constexpr int kTile = 64;  // tokens per (4,4,4) cube
+
+// Geometry of one call, derived from vsa_config_t on the host.
+struct Geom {
+  int B, heads, T, H, W, D;
+  int BH;        // batch * heads
+  int N;         // tokens per (batch, head)
+  int Nc;        // cubes per (batch, head)
+  int ct, ch, cw;  // cubes along T, H, W
+  int cap;       // index-list capacity per query cube
+  int raster;    // 1: caller tensors in raster order, 0: cube order
+  float scale;   // softmax scale (both stages)
+};
+
+// Raster row of token o (0..63) of cube c: cube (4,4,4) with in-cube order
+// o = (t%4)*16 + (h%4)*4 + w%4, cubes ordered (t/4, h/4, w/4) row-major.
+__host__ __device__ __forceinline__ int raster_row(const Geom& g, int c, int o) {
+  const int cw_ = c % g.cw;
+  const int tmp = c / g.cw;
+  const int ch_ = tmp % g.ch;
+  const int ct_ = tmp / g.ch;
+  const int t = ct_ * 4 + (o >> 4);
+  const int h = ch_ * 4 + ((o >> 2) & 3);
+  const int w = cw_ * 4 + (o & 3);
+  return (t * g.H + h) * g.W + w;
+}
+
+// Row (within one (batch, head) slice) where a caller-layout tensor holds
+// token o of cube c.
+__host__ __device__ __forceinline__ int caller_row(const Geom& g, int c, int o) {
+  return g.raster ? raster_row(g, c, o) : c * kTile + o;
+}
+
+// Union-list entry of a query-cube pair: key cube id in the low 16 bits, bit
+// 16 set when the first query cube selected it, bit 17 for the second.
+constexpr uint32_t kSelA = 1u << 16;
+constexpr uint32_t kSelB = 1u << 17;
+
+// A unit of block-sparse work: two query cubes (or two key cubes) of one
+// (batch, head) and the union of their lists.
+struct PairItem {
+  int bh;
+  int a;       // first cube
+  int b;       // second cube, or -1
+  int count;   // entries in the union list
+  int off;     // offset of the union list in its list array
+};
+
+// Pieces of the workspace, carved by the host (api.cu).
+struct Workspace {
+  uint32_t* status;       // device status word
+  int* counter;           // scratch counters
+  PairItem* qpairs;       // query-cube pairs
+  uint32_t* qlist;        // [n_qpairs][2*cap] union lists
+  int n_qpairs;
+  // backward
+  void* dof;              // bf16 cube order
+  float* delta;           // fp32 [BH, N]
+  float* doc;             // fp32 [BH, Nc, D]
+  float* dqc; float* dkc; float* dvc;
+  float* cprob;           // fp32 [BH, Nc, Nc]  coarse probabilities
+  float* cgrad;           // fp32 [BH, Nc, Nc]  coarse logit gradients
+  uint32_t* tmask;        // [BH, Nc, ceil(Nc/32)] selection bit matrix
+  int* toff;              // [BH, Nc + 1] offsets of transposed lists
+  int* tlist;             // [BH, Nc * cap] transposed lists (query cubes per key cube)
+  PairItem* kpairs;       // key-cube pairs
+  uint32_t* klist;        // [BH, Nc * cap] union lists of key-cube pairs
+  int n_kpairs;
+};
+
+// ------------------------------------------------------------------ launches
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_permute(const Geom& g, const __nv_bfloat16* in, __nv_bfloat16* out,
+                           int inverse, cudaStream_t s);
+cudaError_t launch_permute_pool(const Geom& g, const __nv_bfloat16* in, __nv_bfloat16* out_cube,
+                                float* pooled, cudaStream_t s);
+cudaError_t launch_pool(const Geom& g, const __nv_bfloat16* in_cube, float* pooled,
+                        cudaStream_t s);
+cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
+                                 int kmax, const float* qc, const float* kc, const float* vc,
+                                 float* oc, float* lse_c, int* idx, int* cnt, cudaStream_t s);
+cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
+                                const Workspace& ws, cudaStream_t s);
+cudaError_t launch_fine_fwd(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, const __nv_bfloat16* gc,
+                            const __nv_bfloat16* gf, const float* oc, __nv_bfloat16* o,
+                            float* o_f, float* lse_f, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
+                               const __nv_bfloat16* gc, const __nv_bfloat16* gf,
+                               const float* o_f, const float* oc, float* dgc, float* dgf,
+                               __nv_bfloat16* dof, float* doc, float* delta, cudaStream_t s);
+cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
+                              const float* oc, const float* lse_c, const float* doc,
+                              float* dqc, float* dkc, float* dvc, const Workspace& ws,
+                              cudaStream_t s);
+cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
+                                const Workspace& ws, cudaStream_t s);
+cudaError_t launch_fine_bwd(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, const float* lse_f,
+                            const __nv_bfloat16* dof, const float* delta, const float* dqc,
+                            const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
+                            const Workspace& ws, cudaStream_t s);
+
+// Driver entry point for tensor-map encoding, resolved once (api.cu).
+bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_cols);
+
+}  // namespace vsa

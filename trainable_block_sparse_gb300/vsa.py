@@ -1,0 +1,283 @@
+"""Thin Python binding of libvsa.so (include/vsa.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+passes device pointers, sizes and the current torch stream through ctypes,
+and raises when the library is missing or a call fails.  There is no CPU path.
+
+User entry point: `video_sparse_attention(q, k, v, gc, gf, video_shape, ...)`,
+differentiable through `torch.autograd`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libvsa.so")
+
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, \
+    ERR_DEVICE_CHECK = range(8)
+SELECT_TOPK, SELECT_MASS = 0, 1
+LAYOUT_RASTER, LAYOUT_CUBE = 0, 1
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("W", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("select_mode", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("mass", ctypes.c_float),
+                ("kmin", ctypes.c_int32), ("kmax", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("layout", ctypes.c_int32)]
+
+
+class SavedLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("q_cube", "k_cube", "v_cube", "qc", "kc", "vc", "oc", "lse_c", "idx", "cnt",
+                 "o_f", "lse_f", "total")] + [("list_cap", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "vsa_validate": [ctypes.POINTER(Config)],
+    "vsa_status_string": [ctypes.c_int],
+    "vsa_saved_bytes": [ctypes.POINTER(Config), ctypes.POINTER(SavedLayout)],
+    "vsa_workspace_bytes": [ctypes.POINTER(Config), ctypes.c_int],
+    "vsa_reset_device_status": [_P, _P],
+    "vsa_check_device_status": [_P, _P],
+    "vsa_permute": [ctypes.POINTER(Config), _P, _P, ctypes.c_int, _P],
+    "vsa_coarse_select": [ctypes.POINTER(Config)] + [_P] * 12,
+    "vsa_fine_fwd": [ctypes.POINTER(Config)] + [_P] * 13,
+    "vsa_combine_bwd": [ctypes.POINTER(Config)] + [_P] * 11,
+    "vsa_coarse_bwd": [ctypes.POINTER(Config)] + [_P] * 11,
+    "vsa_fine_bwd": [ctypes.POINTER(Config)] + [_P] * 16,
+    "vsa_forward": [ctypes.POINTER(Config)] + [_P] * 7 + [ctypes.c_int, _P, _P],
+    "vsa_backward": [ctypes.POINTER(Config)] + [_P] * 14,
+}
+_RESTYPES = {"vsa_status_string": ctypes.c_char_p, "vsa_saved_bytes": ctypes.c_size_t,
+             "vsa_workspace_bytes": ctypes.c_size_t}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libvsa.so not found at {LIB_PATH}; build it with "
+                "`python -m trainable_block_sparse_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = _RESTYPES.get(name, ctypes.c_int)
+        _lib = L
+    return _lib
+
+
+class VSAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().vsa_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def check(status: int, where: str) -> None:
+    if status != OK:
+        raise VSAError(status, where)
+
+
+def make_config(batch, heads, T, H, W, head_dim, *, topk=32, select="topk", mass=0.9,
+                kmin=8, kmax=64, scale=0.0, layout="raster") -> Config:
+    return Config(batch, heads, T, H, W, head_dim,
+                  SELECT_TOPK if select == "topk" else SELECT_MASS, topk, mass, kmin, kmax,
+                  scale, LAYOUT_RASTER if layout == "raster" else LAYOUT_CUBE)
+
+
+def config_for(wl, layout="raster") -> Config:
+    """Config of a synth.Workload."""
+    return make_config(wl.batch, wl.heads, wl.T, wl.H, wl.W, wl.head_dim, topk=wl.topk,
+                       select=wl.select, mass=wl.mass, kmin=wl.kmin, kmax=wl.kmax,
+                       layout=layout)
+
+
+def saved_layout(cfg: Config) -> SavedLayout:
+    L = SavedLayout()
+    n = lib().vsa_saved_bytes(ctypes.byref(cfg), ctypes.byref(L))
+    if n == 0:
+        check(lib().vsa_validate(ctypes.byref(cfg)), "vsa_saved_bytes")
+    return L
+
+
+def workspace_bytes(cfg: Config, with_backward: bool) -> int:
+    n = lib().vsa_workspace_bytes(ctypes.byref(cfg), int(with_backward))
+    if n == 0:
+        check(lib().vsa_validate(ctypes.byref(cfg)), "vsa_workspace_bytes")
+    return n
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libvsa takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libvsa takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+class Buffers:
+    """Caller-owned device buffers of one layer: the `saved` context and `ws` scratch."""
+
+    def __init__(self, cfg: Config, device, with_backward: bool):
+        self.cfg = cfg
+        self.layout = saved_layout(cfg)
+        self.saved = torch.empty(self.layout.total, dtype=torch.uint8, device=device)
+        self.ws = torch.empty(workspace_bytes(cfg, with_backward), dtype=torch.uint8,
+                              device=device)
+        check(lib().vsa_reset_device_status(_ptr(self.ws), _stream()), "vsa_reset_device_status")
+
+    def view(self, name: str, dtype, shape):
+        off = getattr(self.layout, name)
+        n = 1
+        for s in shape:
+            n *= s
+        itemsize = torch.empty((), dtype=dtype).element_size()
+        return self.saved[off: off + n * itemsize].view(dtype).view(*shape)
+
+    def device_status(self) -> int:
+        return lib().vsa_check_device_status(_ptr(self.ws), _stream())
+
+
+# ------------------------------------------------------------------ entry points
+
+def permute(cfg: Config, x: torch.Tensor, inverse: bool = False) -> torch.Tensor:
+    out = torch.empty_like(x)
+    check(lib().vsa_permute(ctypes.byref(cfg), _ptr(x), _ptr(out), int(inverse), _stream()),
+          "vsa_permute")
+    return out
+
+
+def coarse_select(cfg: Config, q, k, v, ws):
+    """Cube-order q, k, v -> (qc, kc, vc, oc, lse_c, idx, cnt)."""
+    B, Hd, N, D = q.shape
+    nc = N // 64
+    cap = cfg.topk if cfg.select_mode == SELECT_TOPK else cfg.kmax
+    f = dict(dtype=torch.float32, device=q.device)
+    qc, kc, vc, oc = (torch.empty(B, Hd, nc, D, **f) for _ in range(4))
+    lse = torch.empty(B, Hd, nc, **f)
+    idx = torch.empty(B, Hd, nc, cap, dtype=torch.int32, device=q.device)
+    cnt = torch.empty(B, Hd, nc, dtype=torch.int32, device=q.device)
+    check(lib().vsa_coarse_select(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(qc),
+                                  _ptr(kc), _ptr(vc), _ptr(oc), _ptr(lse), _ptr(idx), _ptr(cnt),
+                                  _ptr(ws), _stream()), "vsa_coarse_select")
+    return qc, kc, vc, oc, lse, idx, cnt
+
+
+def fine_fwd(cfg: Config, q, k, v, idx, cnt, gc, gf, oc, ws, want_saved=True):
+    """Cube-order q, k, v; caller-layout gates -> (o, o_f, lse_f)."""
+    B, Hd, N, D = q.shape
+    o = torch.empty_like(gc)
+    of = torch.empty(B, Hd, N, D, dtype=torch.float32, device=q.device) if want_saved else None
+    lse = torch.empty(B, Hd, N, dtype=torch.float32, device=q.device) if want_saved else None
+    check(lib().vsa_fine_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(cnt),
+                             _ptr(gc), _ptr(gf), _ptr(oc), _ptr(o), _ptr(of), _ptr(lse),
+                             _ptr(ws), _stream()), "vsa_fine_fwd")
+    return o, of, lse
+
+
+def combine_bwd(cfg: Config, d_o, gc, gf, o_f, oc):
+    B, Hd, N, D = d_o.shape
+    f = dict(dtype=torch.float32, device=d_o.device)
+    dgc, dgf = torch.empty(B, Hd, N, D, **f), torch.empty(B, Hd, N, D, **f)
+    dof = torch.empty_like(d_o)
+    doc = torch.empty(B, Hd, N // 64, D, **f)
+    delta = torch.empty(B, Hd, N, **f)
+    check(lib().vsa_combine_bwd(ctypes.byref(cfg), _ptr(d_o), _ptr(gc), _ptr(gf), _ptr(o_f),
+                                _ptr(oc), _ptr(dgc), _ptr(dgf), _ptr(dof), _ptr(doc),
+                                _ptr(delta), _stream()), "vsa_combine_bwd")
+    return dgc, dgf, dof, doc, delta
+
+
+def coarse_bwd(cfg: Config, qc, kc, vc, oc, lse_c, doc, ws):
+    dqc, dkc, dvc = (torch.empty_like(qc) for _ in range(3))
+    check(lib().vsa_coarse_bwd(ctypes.byref(cfg), _ptr(qc), _ptr(kc), _ptr(vc), _ptr(oc),
+                               _ptr(lse_c), _ptr(doc), _ptr(dqc), _ptr(dkc), _ptr(dvc),
+                               _ptr(ws), _stream()), "vsa_coarse_bwd")
+    return dqc, dkc, dvc
+
+
+def fine_bwd(cfg: Config, q, k, v, idx, cnt, lse_f, dof, delta, dqc, dkc, dvc, ws):
+    B, Hd, N, D = q.shape
+    f = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dv = (torch.empty(B, Hd, N, D, **f) for _ in range(3))
+    check(lib().vsa_fine_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(cnt),
+                             _ptr(lse_f), _ptr(dof), _ptr(delta), _ptr(dqc), _ptr(dkc),
+                             _ptr(dvc), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _stream()),
+          "vsa_fine_bwd")
+    return dq, dk, dv
+
+
+def forward(cfg: Config, q, k, v, gc, gf, bufs: Buffers, with_backward=True, out=None):
+    o = torch.empty_like(q) if out is None else out
+    check(lib().vsa_forward(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gc), _ptr(gf),
+                            _ptr(o), _ptr(bufs.saved), int(with_backward), _ptr(bufs.ws),
+                            _stream()), "vsa_forward")
+    return o
+
+
+def backward(cfg: Config, q, k, v, gc, gf, d_o, bufs: Buffers, grads=None):
+    B, Hd, N, D = q.shape
+    if grads is None:
+        grads = tuple(torch.empty(B, Hd, N, D, dtype=torch.float32, device=q.device)
+                      for _ in range(5))
+    dq, dk, dv, dgc, dgf = grads
+    check(lib().vsa_backward(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gc), _ptr(gf),
+                             _ptr(bufs.saved), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(dgc), _ptr(dgf), _ptr(bufs.ws), _stream()), "vsa_backward")
+    return grads
+
+
+# ------------------------------------------------------------------ autograd
+
+class _VSAFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, gc, gf, cfg_tuple):
+        cfg = Config(*cfg_tuple)
+        need = any(t.requires_grad for t in (q, k, v, gc, gf))
+        bufs = Buffers(cfg, q.device, with_backward=need)
+        o = forward(cfg, q, k, v, gc, gf, bufs, with_backward=need)
+        ctx.cfg, ctx.bufs = cfg, bufs
+        ctx.save_for_backward(q, k, v, gc, gf)
+        return o
+
+    @staticmethod
+    def backward(ctx, d_o):
+        q, k, v, gc, gf = ctx.saved_tensors
+        d_o = d_o.to(torch.bfloat16).contiguous()
+        dq, dk, dv, dgc, dgf = backward(ctx.cfg, q, k, v, gc, gf, d_o, ctx.bufs)
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dgc.to(gc.dtype),
+                dgf.to(gf.dtype), None)
+
+
+def video_sparse_attention(q, k, v, gc, gf, video_shape, *, topk=32, select="topk", mass=0.9,
+                           kmin=8, kmax=64, scale=0.0, layout="raster"):
+    """VSA attention of [B, heads, T*H*W, D] bf16 CUDA tensors (raster or cube order).
+
+    gc, gf: per-token, per-channel gates (same shape and dtype).  Returns O, bf16.
+    Gradients flow to q, k, v, gc, gf (the cube selection is held fixed).
+    """
+    T, H, W = video_shape
+    B, Hd, N, D = q.shape
+    cfg = make_config(B, Hd, T, H, W, D, topk=topk, select=select, mass=mass, kmin=kmin,
+                      kmax=kmax, scale=scale, layout=layout)
+    check(lib().vsa_validate(ctypes.byref(cfg)), "video_sparse_attention")
+    cfg_tuple = tuple(getattr(cfg, n) for n, _ in Config._fields_)
+    return _VSAFunction.apply(q, k, v, gc, gf, cfg_tuple)
