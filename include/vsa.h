@@ -29,6 +29,11 @@
  *    o = (t%4)*16 + (h%4)*4 + w%4), as cfg->layout says.  Q, K, V, G_c, G_f,
  *    dO and O are bf16; the pooled/coarse tensors, O_f, log-sum-exps and all
  *    gradients are fp32.
+ *  - The tensor-core operands (Q, K, V and dO (.) G_f) are staged as fp16 copies
+ *    in cube order ("staged" below): bf16 -> fp16 is exact for magnitudes in
+ *    [6.1e-5, 65504], and the fp16 significand keeps the rounding of the
+ *    softmax probabilities 8x smaller than bf16 would.  Inputs whose magnitude
+ *    exceeds 65504 (or are not finite) are reported as VSA_ERR_DEVICE_CHECK.
  *  - All pointers named without a "host" prefix are device pointers owned by
  *    the caller, 16-byte aligned.  The library never allocates, frees or
  *    synchronises (except vsa_check_device_status).  Scratch comes from the
@@ -61,7 +66,7 @@ typedef enum {
   VSA_ERR_ALIGNMENT = 4,    /* a pointer is not 16-byte aligned */
   VSA_ERR_CUDA = 5,         /* a CUDA call or launch failed */
   VSA_ERR_TIMEOUT = 6,      /* a device-side bounded wait expired */
-  VSA_ERR_DEVICE_CHECK = 7  /* a device-side range check failed */
+  VSA_ERR_DEVICE_CHECK = 7  /* a device-side range check failed (index list, fp16 range) */
 } vsa_status_t;
 
 enum { VSA_SELECT_TOPK = 0, VSA_SELECT_MASS = 1 };
@@ -86,7 +91,7 @@ typedef struct {
 /* Byte offsets of the pieces of the `saved` buffer written by vsa_forward.
  * Each piece starts on a 256-byte boundary; absent pieces have size 0. */
 typedef struct {
-  size_t q_cube, k_cube, v_cube; /* bf16 [B,heads,N,D] cube order (raster layout only) */
+  size_t q16, k16, v16;          /* fp16 [B,heads,N,D] cube order: staged Q, K, V */
   size_t qc, kc, vc, oc;         /* fp32 [B,heads,Nc,D]: pooled Q/K/V, coarse output */
   size_t lse_c;                  /* fp32 [B,heads,Nc]: coarse log-sum-exp (natural log) */
   size_t idx;                    /* int32 [B,heads,Nc,list_cap]: ascending key-cube ids, -1 padded */
@@ -127,9 +132,15 @@ vsa_status_t vsa_check_device_status(void* ws, void* stream);
 vsa_status_t vsa_permute(const vsa_config_t* cfg, const void* in, void* out, int inverse,
                          void* stream);
 
+/* Staging of one tensor-core operand: x (bf16, cfg->layout order) ->
+ * x16 (fp16, cube order; may be NULL) and its cube means pooled (fp32
+ * [B,heads,Nc,D]; may be NULL, not both).  ws receives the range flag. */
+vsa_status_t vsa_stage(const vsa_config_t* cfg, const void* x, void* x16, float* pooled,
+                       void* ws, void* stream);
+
 /* Coarse stage (§2 "Coarse stage"): per-cube means, dense attention on the
  * pooled sequence, selection and index lists, in one pass.
- * q, k, v : bf16 [B,heads,N,D] in CUBE order (whatever cfg->layout says).
+ * q, k, v : bf16 [B,heads,N,D] in cfg->layout order.
  * qc, kc, vc, oc : fp32 [B,heads,Nc,D] outputs (pooled inputs, O_c).
  * lse_c   : fp32 [B,heads,Nc] output, natural-log log-sum-exp of the logits.
  * idx     : int32 [B,heads,Nc,list_cap] output, ascending key-cube ids, -1 padded.
@@ -141,26 +152,28 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
 
 /* Fine stage and combine (§2 "Fine stage"; App. B): block-sparse attention
  * over the listed key cubes, fused with O = repeat(O_c) G_c + O_f G_f.
- * q, k, v : bf16 CUBE order.  idx, cnt: lists as written by vsa_coarse_select
+ * q16, k16, v16 : staged fp16 CUBE order (vsa_stage).  idx, cnt: lists as written by vsa_coarse_select
  * (any ascending lists with entries in [0, Nc) work, e.g. injected ones).
  * gc, gf  : bf16 gates in cfg->layout order.  oc: fp32 [B,heads,Nc,D].
  * o       : bf16 output in cfg->layout order.
  * o_f     : fp32 CUBE order fine output, or NULL (not needed for inference).
  * lse_f   : fp32 [B,heads,N] CUBE order, or NULL. */
-vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
-                          const int32_t* idx, const int32_t* cnt, const void* gc,
+vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* k16,
+                          const void* v16, const int32_t* idx, const int32_t* cnt, const void* gc,
                           const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
                           void* ws, void* stream);
 
 /* Backward of the combine (gradient of O = repeat(O_c) G_c + O_f G_f).
  * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp32 CUBE order; oc: fp32.
  * dgc, dgf   : fp32 outputs in cfg->layout order.
- * dof        : bf16 CUBE order output, dO (.) G_f.
+ * dof16      : fp16 CUBE order output (staged), dO (.) G_f.
  * doc        : fp32 [B,heads,Nc,D] output, per-cube sum of dO (.) G_c.
- * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof (.) o_f). */
+ * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof16 (.) o_f).
+ * ws receives the range flag. */
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
                              const void* gf, const float* o_f, const float* oc, float* dgc,
-                             float* dgf, void* dof, float* doc, float* delta, void* stream);
+                             float* dgf, void* dof16, float* doc, float* delta, void* ws,
+                             void* stream);
 
 /* Backward of the coarse attention on the pooled sequence, selection held
  * fixed.  Outputs dqc, dkc, dvc: fp32 [B,heads,Nc,D] (gradients w.r.t. the
@@ -173,13 +186,14 @@ vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const floa
 /* Backward of the fine stage plus the pooling: writes
  *   dq = dQ_fine + repeat(dqc)/64, dk = dK_fine + repeat(dkc)/64,
  *   dv = dV_fine + repeat(dvc)/64
- * as fp32 in cfg->layout order.  q, k, v, dof: bf16 CUBE order; lse_f, delta:
- * fp32 CUBE order; dqc/dkc/dvc may be NULL (no pooled contribution). */
-vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
-                          const int32_t* idx, const int32_t* cnt, const float* lse_f,
-                          const void* dof, const float* delta, const float* dqc,
-                          const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
-                          void* ws, void* stream);
+ * as fp32 in cfg->layout order.  q16, k16, v16, dof16: staged fp16 CUBE
+ * order; lse_f, delta: fp32 CUBE order; dqc/dkc/dvc may be NULL (no pooled
+ * contribution). */
+vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* k16,
+                          const void* v16, const int32_t* idx, const int32_t* cnt,
+                          const float* lse_f, const void* dof16, const float* delta,
+                          const float* dqc, const float* dkc, const float* dvc, float* dq,
+                          float* dk, float* dv, void* ws, void* stream);
 
 /* Whole forward: tile, coarse stage, fine stage + combine, untile.
  * q, k, v, gc, gf: bf16 in cfg->layout order; o: bf16 output, same order.
@@ -190,12 +204,12 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
                          int with_backward, void* ws, void* stream);
 
 /* Whole backward from the upstream gradient d_o (bf16, cfg->layout order).
- * q, k, v, gc, gf: the forward's inputs; saved: as filled by vsa_forward
- * with with_backward = 1.  Outputs fp32 in cfg->layout order. */
-vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* q, const void* k,
-                          const void* v, const void* gc, const void* gf, const void* saved,
-                          const void* d_o, float* dq, float* dk, float* dv, float* dgc,
-                          float* dgf, void* ws, void* stream);
+ * gc, gf: the forward's gates; saved: as filled by vsa_forward with
+ * with_backward = 1 (it holds the staged Q, K, V).  Outputs fp32 in
+ * cfg->layout order. */
+vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* gf,
+                          const void* saved, const void* d_o, float* dq, float* dk, float* dv,
+                          float* dgc, float* dgf, void* ws, void* stream);
 
 #ifdef __cplusplus
 }

@@ -77,7 +77,7 @@ def test_buffer_sizes(lib):
     cfg = _cfg()
     L = vsa.saved_layout(cfg)
     # pieces are 256-byte aligned, in order, and fit the total
-    offs = [L.q_cube, L.k_cube, L.v_cube, L.qc, L.kc, L.vc, L.oc, L.lse_c, L.idx, L.cnt, L.o_f,
+    offs = [L.q16, L.k16, L.v16, L.qc, L.kc, L.vc, L.oc, L.lse_c, L.idx, L.cnt, L.o_f,
             L.lse_f]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and L.total > offs[-1]
@@ -90,9 +90,8 @@ def test_buffer_sizes(lib):
     bad = _cfg(T=5)
     assert lib.vsa_saved_bytes(ctypes.byref(bad), None) == 0
     assert lib.vsa_workspace_bytes(ctypes.byref(bad), 1) == 0
-    # cube-order callers need no cube copies
-    Lc = vsa.saved_layout(_cfg(layout="cube"))
-    assert Lc.total < L.total
+    # staged fp16 copies of Q, K, V come first, one [B, heads, N, D] each
+    assert L.k16 - L.q16 >= n_tok * 64 * 2 and L.qc - L.v16 >= n_tok * 64 * 2
 
 
 def test_status_strings(lib):

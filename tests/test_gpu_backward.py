@@ -30,7 +30,7 @@ def run_fwd_bwd(inp, layout="raster"):
             t[n] = vsa.permute(cfg, t[n])
     bufs = vsa.Buffers(cfg, "cuda", with_backward=True)
     vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, with_backward=True)
-    grads = vsa.backward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], t["do"], bufs)
+    grads = vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs)
     torch.cuda.synchronize()
     assert bufs.device_status() == vsa.OK
     if layout == "cube":

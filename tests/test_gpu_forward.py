@@ -138,9 +138,17 @@ def test_pooled_means_within_fp32_summation_bound():
     inp = gapped("pretrain")
     wl = inp.wl
     cfg = vsa.config_for(wl)
-    qt = vsa.permute(cfg, inp.q.cuda())
+    q = inp.q.cuda()
     ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
-    qc = vsa.coarse_select(cfg, qt, qt, qt, ws)[0]
+    qc = vsa.coarse_select(cfg, q, q, q, ws)[0]
+    q16, qc2 = vsa.stage(cfg, q, ws, want_pooled=True)
+    assert torch.equal(qc, qc2)
+    # the staged copy is the fp16 value of every bf16 input, in cube order: exact
+    # in the normal fp16 range, within half a subnormal step (2^-25) below it
+    ref = vsa.permute(cfg, q).float()
+    normal = ref.abs() >= 2.0 ** -14
+    assert torch.equal(q16.float()[normal], ref[normal])
+    assert (q16.float() - ref).abs().max().item() <= 2.0 ** -25
     for b, h in slices_of(wl, False):
         x = O.tile(O.f64(inp.q[b, h]), wl.T, wl.H, wl.W).reshape(wl.cubes, 64, wl.head_dim)
         exact = x.mean(axis=1)
@@ -165,6 +173,7 @@ def test_fine_stage_with_injected_oracle_lists(name):
     q, k, v, gc, gf = (tiled(getattr(inp, n)) for n in ("q", "k", "v", "gc", "gf"))
     ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
     vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
+    q, k, v = (vsa.stage(cfg, x, ws) for x in (q, k, v))
     o, of, lse = vsa.fine_fwd(cfg, q, k, v, torch.from_numpy(idx).int().cuda(),
                               torch.from_numpy(cnt).int().cuda(), gc, gf,
                               torch.from_numpy(oc).float().cuda(), ws)
@@ -236,7 +245,9 @@ def test_bad_index_lists_are_reported_not_faulted():
     wl = inp.wl
     cfg = vsa.config_for(wl, layout="cube")
     t = cuda_inputs(inp)
-    q, k, v = (vsa.permute(cfg, t[n]) for n in ("q", "k", "v"))
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
+    q, k, v = (vsa.stage(cfg, vsa.permute(cfg, t[n]), ws) for n in ("q", "k", "v"))
     idx = torch.tensor([[[[0, 1]] * wl.cubes] * wl.heads], dtype=torch.int32)
     idx[0, 0, 1] = torch.tensor([5, 99])       # id out of range
     idx[0, 0, 2] = torch.tensor([-3, 1])       # negative id
@@ -244,14 +255,26 @@ def test_bad_index_lists_are_reported_not_faulted():
     cnt = torch.full((1, wl.heads, wl.cubes), 2, dtype=torch.int32)
     cnt[0, 1, 5] = 7                           # count above capacity
     oc = torch.zeros(1, wl.heads, wl.cubes, wl.head_dim, device="cuda")
-    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
-    vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
     vsa.fine_fwd(cfg, q, k, v, idx.cuda(), cnt.cuda(), t["gc"], t["gf"], oc, ws)
     torch.cuda.synchronize()
     st = vsa.lib().vsa_check_device_status(vsa._ptr(ws), vsa._stream())
     assert st == vsa.ERR_DEVICE_CHECK
     # the context is still usable
     assert torch.cuda.is_available() and (torch.ones(4, device="cuda") * 2).sum().item() == 8
+
+
+def test_values_outside_fp16_range_are_reported():
+    inp = _custom(4, 4, 8, 64, 1, seed=15)
+    wl = inp.wl
+    cfg = vsa.config_for(wl)
+    q = inp.q.clone()
+    q[0, 1, 77, 5] = 1.0e5
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
+    vsa.stage(cfg, inp.k.cuda(), ws)
+    assert vsa.lib().vsa_check_device_status(vsa._ptr(ws), vsa._stream()) == vsa.OK
+    vsa.stage(cfg, q.cuda(), ws)
+    assert vsa.lib().vsa_check_device_status(vsa._ptr(ws), vsa._stream()) == vsa.ERR_DEVICE_CHECK
 
 
 def test_worked_example_ties_keep_lower_ids():

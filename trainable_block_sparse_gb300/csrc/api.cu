@@ -67,7 +67,7 @@ vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
   return VSA_OK;
 }
 
-size_t bf16_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 2; }
+size_t half_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 2; }
 size_t f32_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 4; }
 size_t pooled_bytes(const Geom& g) { return static_cast<size_t>(g.BH) * g.Nc * g.D * 4; }
 
@@ -78,10 +78,9 @@ void saved_layout(const Geom& g, vsa_saved_layout_t* L) {
     off += align_up(bytes);
     return o;
   };
-  const size_t cube_copy = g.raster ? bf16_tensor(g) : 0;
-  L->q_cube = take(cube_copy);
-  L->k_cube = take(cube_copy);
-  L->v_cube = take(cube_copy);
+  L->q16 = take(half_tensor(g));
+  L->k16 = take(half_tensor(g));
+  L->v16 = take(half_tensor(g));
   L->qc = take(pooled_bytes(g));
   L->kc = take(pooled_bytes(g));
   L->vc = take(pooled_bytes(g));
@@ -113,7 +112,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
   if (with_backward) {
     const size_t words = (g.Nc + 31) / 32;
-    ws.dof = take(bf16_tensor(g));
+    ws.dof = take(half_tensor(g));
     ws.delta = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.N * 4));
     ws.doc = static_cast<float*>(take(pooled_bytes(g)));
     ws.dqc = static_cast<float*>(take(pooled_bytes(g)));
@@ -145,12 +144,14 @@ bool all_set(Ptrs... ps) {
 }
 
 using bf16 = __nv_bfloat16;
+using f16 = __half;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 }  // namespace
 
+// 2-D fp16 tensor map with 128-byte swizzle (the staged operands).
 bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols) {
   std::call_once(g_encode_once, [] {
@@ -166,7 +167,7 @@ bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
   const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t es[2] = {1, 1};
-  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -192,7 +193,8 @@ const char* vsa_status_string(vsa_status_t s) {
     case VSA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case VSA_ERR_CUDA: return "CUDA error";
     case VSA_ERR_TIMEOUT: return "device-side wait timed out";
-    case VSA_ERR_DEVICE_CHECK: return "device-side range check failed (bad index list)";
+    case VSA_ERR_DEVICE_CHECK:
+      return "device-side range check failed (bad index list, or a value outside the fp16 range)";
   }
   return "unknown status";
 }
@@ -225,7 +227,7 @@ vsa_status_t vsa_check_device_status(void* ws, void* stream) {
     return VSA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return VSA_ERR_CUDA;
   if (word & kDevTimeout) return VSA_ERR_TIMEOUT;
-  if (word & kDevBadIndex) return VSA_ERR_DEVICE_CHECK;
+  if (word & (kDevBadIndex | kDevRange)) return VSA_ERR_DEVICE_CHECK;
   return VSA_OK;
 }
 
@@ -241,6 +243,19 @@ vsa_status_t vsa_permute(const vsa_config_t* cfg, const void* in, void* out, int
                                     inverse, static_cast<cudaStream_t>(stream)));
 }
 
+vsa_status_t vsa_stage(const vsa_config_t* cfg, const void* x, void* x16, float* pooled,
+                       void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(x, ws) || (!x16 && !pooled)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(x, ws) || !aligned16(x16) || !aligned16(pooled)) return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  return cuda_status(launch_stage(g, static_cast<const bf16*>(x), g.raster, static_cast<f16*>(x16),
+                                  pooled, w.status, static_cast<cudaStream_t>(stream)));
+}
+
 vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const void* k,
                                const void* v, float* qc, float* kc, float* vc, float* oc,
                                float* lse_c, int32_t* idx, int32_t* cnt, void* ws,
@@ -248,50 +263,56 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt)) return VSA_ERR_INVALID_ARG;
-  if (!all_aligned(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt)) return VSA_ERR_ALIGNMENT;
-  (void)ws;
+  if (!all_set(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt, ws)) return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_pool(g, static_cast<const bf16*>(q), qc, s) != cudaSuccess ||
-      launch_pool(g, static_cast<const bf16*>(k), kc, s) != cudaSuccess ||
-      launch_pool(g, static_cast<const bf16*>(v), vc, s) != cudaSuccess)
+  if (launch_stage(g, static_cast<const bf16*>(q), g.raster, nullptr, qc, w.status, s) ||
+      launch_stage(g, static_cast<const bf16*>(k), g.raster, nullptr, kc, w.status, s) ||
+      launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s))
     return VSA_ERR_CUDA;
   return cuda_status(launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin,
                                           cfg->kmax, qc, kc, vc, oc, lse_c, idx, cnt, s));
 }
 
-vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
-                          const int32_t* idx, const int32_t* cnt, const void* gc,
+vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* k16,
+                          const void* v16, const int32_t* idx, const int32_t* cnt, const void* gc,
                           const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
                           void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(q, k, v, idx, cnt, gc, gf, oc, o, ws)) return VSA_ERR_INVALID_ARG;
-  if (!all_aligned(q, k, v, idx, cnt, gc, gf, oc, o, ws) || !aligned16(o_f) || !aligned16(lse_f))
+  if (!all_set(q16, k16, v16, idx, cnt, gc, gf, oc, o, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q16, k16, v16, idx, cnt, gc, gf, oc, o, ws) || !aligned16(o_f) ||
+      !aligned16(lse_f))
     return VSA_ERR_ALIGNMENT;
   Workspace w;
   carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
-  return cuda_status(launch_fine_fwd(g, static_cast<const bf16*>(q), static_cast<const bf16*>(k),
-                                     static_cast<const bf16*>(v), static_cast<const bf16*>(gc),
+  return cuda_status(launch_fine_fwd(g, static_cast<const f16*>(q16), static_cast<const f16*>(k16),
+                                     static_cast<const f16*>(v16), static_cast<const bf16*>(gc),
                                      static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
                                      o_f, lse_f, w, s));
 }
 
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
                              const void* gf, const float* o_f, const float* oc, float* dgc,
-                             float* dgf, void* dof, float* doc, float* delta, void* stream) {
+                             float* dgf, void* dof16, float* doc, float* delta, void* ws,
+                             void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(d_o, gc, gf, o_f, oc, dgc, dgf, dof, doc, delta)) return VSA_ERR_INVALID_ARG;
-  if (!all_aligned(d_o, gc, gf, o_f, oc, dgc, dgf, dof, doc, delta)) return VSA_ERR_ALIGNMENT;
+  if (!all_set(d_o, gc, gf, o_f, oc, dgc, dgf, dof16, doc, delta, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(d_o, gc, gf, o_f, oc, dgc, dgf, dof16, doc, delta, ws))
+    return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
   return cuda_status(launch_combine_bwd(
       g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
-      static_cast<const bf16*>(gf), o_f, oc, dgc, dgf, static_cast<bf16*>(dof), doc, delta,
-      static_cast<cudaStream_t>(stream)));
+      static_cast<const bf16*>(gf), o_f, oc, dgc, dgf, static_cast<f16*>(dof16), doc, delta,
+      w.status, static_cast<cudaStream_t>(stream)));
 }
 
 vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const float* kc,
@@ -309,26 +330,27 @@ vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const floa
                                        static_cast<cudaStream_t>(stream)));
 }
 
-vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
-                          const int32_t* idx, const int32_t* cnt, const float* lse_f,
-                          const void* dof, const float* delta, const float* dqc,
-                          const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
-                          void* ws, void* stream) {
+vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* k16,
+                          const void* v16, const int32_t* idx, const int32_t* cnt,
+                          const float* lse_f, const void* dof16, const float* delta,
+                          const float* dqc, const float* dkc, const float* dvc, float* dq,
+                          float* dk, float* dv, void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(q, k, v, idx, cnt, lse_f, dof, delta, dq, dk, dv, ws)) return VSA_ERR_INVALID_ARG;
-  if (!all_aligned(q, k, v, idx, cnt, lse_f, dof, delta, dq, dk, dv, ws) || !aligned16(dqc) ||
-      !aligned16(dkc) || !aligned16(dvc))
+  if (!all_set(q16, k16, v16, idx, cnt, lse_f, dof16, delta, dq, dk, dv, ws))
+    return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q16, k16, v16, idx, cnt, lse_f, dof16, delta, dq, dk, dv, ws) ||
+      !aligned16(dqc) || !aligned16(dkc) || !aligned16(dvc))
     return VSA_ERR_ALIGNMENT;
   Workspace w;
   carve_ws(g, 1, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
-  return cuda_status(launch_fine_bwd(g, static_cast<const bf16*>(q), static_cast<const bf16*>(k),
-                                     static_cast<const bf16*>(v), lse_f,
-                                     static_cast<const bf16*>(dof), delta, dqc, dkc, dvc, dq, dk,
+  return cuda_status(launch_fine_bwd(g, static_cast<const f16*>(q16), static_cast<const f16*>(k16),
+                                     static_cast<const f16*>(v16), lse_f,
+                                     static_cast<const f16*>(dof16), delta, dqc, dkc, dvc, dq, dk,
                                      dv, w, s));
 }
 
@@ -346,29 +368,16 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   Workspace w;
   carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bf16 *qt, *kt, *vt;
+  f16* q16 = reinterpret_cast<f16*>(sv + L.q16);
+  f16* k16 = reinterpret_cast<f16*>(sv + L.k16);
+  f16* v16 = reinterpret_cast<f16*>(sv + L.v16);
   float* qc = reinterpret_cast<float*>(sv + L.qc);
   float* kc = reinterpret_cast<float*>(sv + L.kc);
   float* vc = reinterpret_cast<float*>(sv + L.vc);
-  if (g.raster) {
-    bf16* qo = reinterpret_cast<bf16*>(sv + L.q_cube);
-    bf16* ko = reinterpret_cast<bf16*>(sv + L.k_cube);
-    bf16* vo = reinterpret_cast<bf16*>(sv + L.v_cube);
-    if (launch_permute_pool(g, static_cast<const bf16*>(q), qo, qc, s) != cudaSuccess ||
-        launch_permute_pool(g, static_cast<const bf16*>(k), ko, kc, s) != cudaSuccess ||
-        launch_permute_pool(g, static_cast<const bf16*>(v), vo, vc, s) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    qt = qo;
-    kt = ko;
-    vt = vo;
-  } else {
-    qt = static_cast<const bf16*>(q);
-    kt = static_cast<const bf16*>(k);
-    vt = static_cast<const bf16*>(v);
-    if (launch_pool(g, qt, qc, s) != cudaSuccess || launch_pool(g, kt, kc, s) != cudaSuccess ||
-        launch_pool(g, vt, vc, s) != cudaSuccess)
-      return VSA_ERR_CUDA;
-  }
+  if (launch_stage(g, static_cast<const bf16*>(q), g.raster, q16, qc, w.status, s) ||
+      launch_stage(g, static_cast<const bf16*>(k), g.raster, k16, kc, w.status, s) ||
+      launch_stage(g, static_cast<const bf16*>(v), g.raster, v16, vc, w.status, s))
+    return VSA_ERR_CUDA;
   float* oc = reinterpret_cast<float*>(sv + L.oc);
   int* idx = reinterpret_cast<int*>(sv + L.idx);
   int* cnt = reinterpret_cast<int*>(sv + L.cnt);
@@ -377,39 +386,36 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
                            s) != cudaSuccess)
     return VSA_ERR_CUDA;
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
-  return cuda_status(launch_fine_fwd(g, qt, kt, vt, static_cast<const bf16*>(gc),
+  return cuda_status(launch_fine_fwd(g, q16, k16, v16, static_cast<const bf16*>(gc),
                                      static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
                                      with_backward ? reinterpret_cast<float*>(sv + L.o_f) : nullptr,
                                      reinterpret_cast<float*>(sv + L.lse_f), w, s));
 }
 
-vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* q, const void* k,
-                          const void* v, const void* gc, const void* gf, const void* saved,
-                          const void* d_o, float* dq, float* dk, float* dv, float* dgc,
-                          float* dgf, void* ws, void* stream) {
+vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* gf,
+                          const void* saved, const void* d_o, float* dq, float* dk, float* dv,
+                          float* dgc, float* dgf, void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(q, k, v, gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws))
-    return VSA_ERR_INVALID_ARG;
-  if (!all_aligned(q, k, v, gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws))
-    return VSA_ERR_ALIGNMENT;
+  if (!all_set(gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws)) return VSA_ERR_ALIGNMENT;
   vsa_saved_layout_t L;
   saved_layout(g, &L);
   const char* sv = static_cast<const char*>(saved);
   Workspace w;
   carve_ws(g, 1, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bf16* qt = g.raster ? reinterpret_cast<const bf16*>(sv + L.q_cube) : static_cast<const bf16*>(q);
-  const bf16* kt = g.raster ? reinterpret_cast<const bf16*>(sv + L.k_cube) : static_cast<const bf16*>(k);
-  const bf16* vt = g.raster ? reinterpret_cast<const bf16*>(sv + L.v_cube) : static_cast<const bf16*>(v);
+  const f16* q16 = reinterpret_cast<const f16*>(sv + L.q16);
+  const f16* k16 = reinterpret_cast<const f16*>(sv + L.k16);
+  const f16* v16 = reinterpret_cast<const f16*>(sv + L.v16);
   const float* of = reinterpret_cast<const float*>(sv + L.o_f);
   const float* oc = reinterpret_cast<const float*>(sv + L.oc);
   const int* idx = reinterpret_cast<const int*>(sv + L.idx);
   const int* cnt = reinterpret_cast<const int*>(sv + L.cnt);
   if (launch_combine_bwd(g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
                          static_cast<const bf16*>(gf), of, oc, dgc, dgf,
-                         static_cast<bf16*>(w.dof), w.doc, w.delta, s) != cudaSuccess)
+                         static_cast<f16*>(w.dof), w.doc, w.delta, w.status, s) != cudaSuccess)
     return VSA_ERR_CUDA;
   if (launch_coarse_bwd(g, reinterpret_cast<const float*>(sv + L.qc),
                         reinterpret_cast<const float*>(sv + L.kc),
@@ -419,8 +425,8 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* q, const void* k,
     return VSA_ERR_CUDA;
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
-  return cuda_status(launch_fine_bwd(g, qt, kt, vt, reinterpret_cast<const float*>(sv + L.lse_f),
-                                     static_cast<const bf16*>(w.dof), w.delta, w.dqc, w.dkc,
+  return cuda_status(launch_fine_bwd(g, q16, k16, v16, reinterpret_cast<const float*>(sv + L.lse_f),
+                                     static_cast<const f16*>(w.dof), w.delta, w.dqc, w.dkc,
                                      w.dvc, dq, dk, dv, w, s));
 }
 

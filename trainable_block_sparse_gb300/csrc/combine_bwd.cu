@@ -2,10 +2,12 @@
 // notes 关键设计 3; "VSA: Faster Video Diffusion with Trainable Sparse
 // Attention", App. B: the coarse output is repeated across its block):
 //   dG_c = dO (.) repeat(O_c)          dG_f = dO (.) O_f
-//   dO_f = dO (.) G_f                  dO_c[cube] = sum over the cube of dO (.) G_c
+//   dO_f = dO (.) G_f (fp16, the tensor-core operand of the fine backward)
+//   dO_c[cube] = sum over the cube of dO (.) G_c
 //   delta[row] = sum_d dO_f (.) O_f    (the softmax-backward row term of the fine stage)
 // HBM-bound: one CTA per (batch, head, cube) reads dO, G_c, G_f (bf16, caller
 // layout) and O_f (fp32, cube order) once and writes each output once.
+#include "sm103_ptx.cuh"
 #include "vsa_common.cuh"
 
 namespace vsa {
@@ -18,7 +20,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     Geom g, const uint4* __restrict__ d_o, const uint4* __restrict__ gc,
     const uint4* __restrict__ gf, const float* __restrict__ o_f, const float* __restrict__ oc,
     float* __restrict__ dgc, float* __restrict__ dgf, uint4* __restrict__ dof,
-    float* __restrict__ doc, float* __restrict__ delta) {
+    float* __restrict__ doc, float* __restrict__ delta, uint32_t* status) {
   constexpr int VPR = D / 8;              // 8-element vectors per row
   constexpr int GROUPS = kThreads / VPR;  // rows processed side by side
   __shared__ float red[GROUPS][D];
@@ -30,6 +32,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
 #pragma unroll
   for (int i = 0; i < 8; ++i) ocv[i] = ocr[i];
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  bool bad = false;
   for (int o = grp; o < kTile; o += GROUPS) {
     const size_t crow = slice + caller_row(g, c, o);
     const size_t frow = slice + static_cast<size_t>(c) * kTile + o;
@@ -42,7 +45,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const float ofv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
     float vdgc[8], vdgf[8];
     uint4 udof;
-    __nv_bfloat162* pof = reinterpret_cast<__nv_bfloat162*>(&udof);
+    __half2* pof = reinterpret_cast<__half2*>(&udof);
     float dsum = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -55,8 +58,10 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
       vdgf[2 * e + 1] = dd.y * ofv[2 * e + 1];
       acc[2 * e] += dd.x * cc.x;
       acc[2 * e + 1] += dd.y * cc.y;
-      pof[e] = __floats2bfloat162_rn(dd.x * ff.x, dd.y * ff.y);
-      const float2 r = __bfloat1622float2(pof[e]);  // delta uses the rounded dO_f the MMAs see
+      const float2 raw = make_float2(dd.x * ff.x, dd.y * ff.y);
+      bad |= !(fabsf(raw.x) <= 65504.f) || !(fabsf(raw.y) <= 65504.f);
+      pof[e] = __floats2half2_rn(raw.x, raw.y);
+      const float2 r = __half22float2(pof[e]);  // delta uses the rounded dO_f the MMAs see
       dsum = fmaf(r.x, ofv[2 * e], fmaf(r.y, ofv[2 * e + 1], dsum));
     }
     float4* dc = reinterpret_cast<float4*>(dgc + crow * D + col * 8);
@@ -71,6 +76,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     for (int off = VPR / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
     if (col == 0) delta[frow] = dsum;
   }
+  if (bad) flag_error(status, kDevRange);
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[grp][col * 8 + i] = acc[i];
   __syncthreads();
@@ -87,16 +93,17 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
                                const float* o_f, const float* oc, float* dgc, float* dgf,
-                               __nv_bfloat16* dof, float* doc, float* delta, cudaStream_t s) {
+                               __half* dof, float* doc, float* delta, uint32_t* status,
+                               cudaStream_t s) {
   dim3 grid(g.Nc, g.BH);
   auto u4 = [](const void* p) { return reinterpret_cast<const uint4*>(p); };
   if (g.D == 64)
     combine_bwd_kernel<64><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), o_f, oc, dgc, dgf,
-                                                     reinterpret_cast<uint4*>(dof), doc, delta);
+                                                     reinterpret_cast<uint4*>(dof), doc, delta, status);
   else
     combine_bwd_kernel<128><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), o_f, oc, dgc,
                                                       dgf, reinterpret_cast<uint4*>(dof), doc,
-                                                      delta);
+                                                      delta, status);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,7 @@
 //  * kKeyMajor = false (dQ pass): work item = two query cubes (M = 128 query
 //    rows), walking the union of their index lists.  Per step of two key
 //    cubes: S = Q K^T and dP = dO V^T into TMEM, the softmax warps turn them
-//    into dS (bf16, back into TMEM), then dQ += dS K.
+//    into dS (fp16, back into TMEM), then dQ += dS K.
 //  * kKeyMajor = true (dK/dV pass): work item = two key cubes (M = 128 key
 //    rows), walking the union of their transposed lists (query cubes that
 //    selected them).  Per step of two query cubes: S^T = K Q^T and
@@ -19,6 +19,7 @@
 //    per-column lse and delta come through shared memory), then
 //    dV += P^T dO and dK += dS^T Q.
 // TMEM: S at column 0, dP at 128, accumulators at 256 and 384 (512 columns).
+// Operands are the fp16 staged copies of Q, K, V and dO_f; P and dS are fp16.
 // Roles, bounded waits and the abort path are as in the forward kernel.
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
@@ -211,9 +212,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
   } else if (warp == 1) {
     // ===================================================== UMMA issuer
-    const uint32_t id_s128 = idesc_bf16(128, 128, 0, 0);
-    const uint32_t id_s64 = idesc_bf16(128, 64, 0, 0);
-    const uint32_t id_acc = idesc_bf16(128, D, 0, 1);
+    const uint32_t id_s128 = idesc_f16(128, 128, 0, 0);
+    const uint32_t id_s64 = idesc_f16(128, 64, 0, 0);
+    const uint32_t id_acc = idesc_f16(128, D, 0, 1);
     const uint64_t x1d0 = sdesc_sw128(smem_u32(sX1), 16, 1024);
     const uint64_t x2d0 = sdesc_sw128(smem_u32(sX2), 16, 1024);
     const uint64_t yk0 = sdesc_sw128(smem_u32(sY), 16, 1024);                 // K-major view
@@ -350,8 +351,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 p[u] = ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
                 d[u] = p[u] * (__uint_as_float(dv[j]) - dl);
               }
-              pk[i] = pack_bf16x2(p[0], p[1]);
-              dk[i] = pack_bf16x2(d[0], d[1]);
+              pk[i] = pack_f16x2(p[0], p[1]);
+              dk[i] = pack_f16x2(d[0], d[1]);
             }
           }
           // chunk ch of 32 values packs into 16 columns at ch*16 (already-read columns)
@@ -409,8 +410,8 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
 }
 
 template <int D>
-cudaError_t bwd_impl(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
-                     const __nv_bfloat16* v, const float* lse_f, const __nv_bfloat16* dof,
+cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __half* v,
+                     const float* lse_f, const __half* dof,
                      const float* delta, const float* dqc, const float* dkc, const float* dvc,
                      float* dq, float* dk, float* dv, const Workspace& ws, cudaStream_t s) {
   BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, lse_f, delta, dqc, nullptr, dq, nullptr,
@@ -423,11 +424,10 @@ cudaError_t bwd_impl(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16*
 
 }  // namespace
 
-cudaError_t launch_fine_bwd(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
-                            const __nv_bfloat16* v, const float* lse_f,
-                            const __nv_bfloat16* dof, const float* delta, const float* dqc,
-                            const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
-                            const Workspace& ws, cudaStream_t s) {
+cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
+                            const float* lse_f, const __half* dof, const float* delta,
+                            const float* dqc, const float* dkc, const float* dvc, float* dq,
+                            float* dk, float* dv, const Workspace& ws, cudaStream_t s) {
   if (g.D == 64) return bwd_impl<64>(g, q, k, v, lse_f, dof, delta, dqc, dkc, dvc, dq, dk, dv, ws, s);
   return bwd_impl<128>(g, q, k, v, lse_f, dof, delta, dqc, dkc, dvc, dq, dk, dv, ws, s);
 }

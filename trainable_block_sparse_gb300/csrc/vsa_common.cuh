@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace vsa {
 
@@ -83,34 +84,35 @@ struct Workspace {
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_permute(const Geom& g, const __nv_bfloat16* in, __nv_bfloat16* out,
                            int inverse, cudaStream_t s);
-cudaError_t launch_permute_pool(const Geom& g, const __nv_bfloat16* in, __nv_bfloat16* out_cube,
-                                float* pooled, cudaStream_t s);
-cudaError_t launch_pool(const Geom& g, const __nv_bfloat16* in_cube, float* pooled,
-                        cudaStream_t s);
+// bf16 caller tensor (raster when in_raster, else cube order) -> fp16 cube-order
+// staged copy (nullable) and fp32 cube means (nullable); values outside the
+// fp16 range set kDevRange in *status.
+cudaError_t launch_stage(const Geom& g, const __nv_bfloat16* in, int in_raster, __half* out16,
+                         float* pooled, uint32_t* status, cudaStream_t s);
 cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
                                  int kmax, const float* qc, const float* kc, const float* vc,
                                  float* oc, float* lse_c, int* idx, int* cnt, cudaStream_t s);
 cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
-cudaError_t launch_fine_fwd(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
-                            const __nv_bfloat16* v, const __nv_bfloat16* gc,
-                            const __nv_bfloat16* gf, const float* oc, __nv_bfloat16* o,
-                            float* o_f, float* lse_f, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, const __half* v,
+                            const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
+                            __nv_bfloat16* o, float* o_f, float* lse_f, const Workspace& ws,
+                            cudaStream_t s);
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
                                const float* o_f, const float* oc, float* dgc, float* dgf,
-                               __nv_bfloat16* dof, float* doc, float* delta, cudaStream_t s);
+                               __half* dof, float* doc, float* delta, uint32_t* status,
+                               cudaStream_t s);
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
                               const float* oc, const float* lse_c, const float* doc,
                               float* dqc, float* dkc, float* dvc, const Workspace& ws,
                               cudaStream_t s);
 cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
-cudaError_t launch_fine_bwd(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
-                            const __nv_bfloat16* v, const float* lse_f,
-                            const __nv_bfloat16* dof, const float* delta, const float* dqc,
-                            const float* dkc, const float* dvc, float* dq, float* dk, float* dv,
-                            const Workspace& ws, cudaStream_t s);
+cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
+                            const float* lse_f, const __half* dof, const float* delta,
+                            const float* dqc, const float* dkc, const float* dvc, float* dq,
+                            float* dk, float* dv, const Workspace& ws, cudaStream_t s);
 
 // Driver entry point for tensor-map encoding, resolved once (api.cu).
 bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,

@@ -34,7 +34,7 @@ class Config(ctypes.Structure):
 
 class SavedLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("q_cube", "k_cube", "v_cube", "qc", "kc", "vc", "oc", "lse_c", "idx", "cnt",
+                ("q16", "k16", "v16", "qc", "kc", "vc", "oc", "lse_c", "idx", "cnt",
                  "o_f", "lse_f", "total")] + [("list_cap", ctypes.c_int32)]
 
 
@@ -47,13 +47,14 @@ _SIGS = {
     "vsa_reset_device_status": [_P, _P],
     "vsa_check_device_status": [_P, _P],
     "vsa_permute": [ctypes.POINTER(Config), _P, _P, ctypes.c_int, _P],
+    "vsa_stage": [ctypes.POINTER(Config)] + [_P] * 5,
     "vsa_coarse_select": [ctypes.POINTER(Config)] + [_P] * 12,
     "vsa_fine_fwd": [ctypes.POINTER(Config)] + [_P] * 13,
-    "vsa_combine_bwd": [ctypes.POINTER(Config)] + [_P] * 11,
+    "vsa_combine_bwd": [ctypes.POINTER(Config)] + [_P] * 12,
     "vsa_coarse_bwd": [ctypes.POINTER(Config)] + [_P] * 11,
     "vsa_fine_bwd": [ctypes.POINTER(Config)] + [_P] * 16,
     "vsa_forward": [ctypes.POINTER(Config)] + [_P] * 7 + [ctypes.c_int, _P, _P],
-    "vsa_backward": [ctypes.POINTER(Config)] + [_P] * 14,
+    "vsa_backward": [ctypes.POINTER(Config)] + [_P] * 11,
 }
 _RESTYPES = {"vsa_status_string": ctypes.c_char_p, "vsa_saved_bytes": ctypes.c_size_t,
              "vsa_workspace_bytes": ctypes.c_size_t}
@@ -165,8 +166,19 @@ def permute(cfg: Config, x: torch.Tensor, inverse: bool = False) -> torch.Tensor
     return out
 
 
+def stage(cfg: Config, x, ws, want_pooled=False):
+    """bf16 x (cfg.layout order) -> fp16 cube-order staged copy (and cube means)."""
+    B, Hd, N, D = x.shape
+    x16 = torch.empty(B, Hd, N, D, dtype=torch.float16, device=x.device)
+    pooled = (torch.empty(B, Hd, N // 64, D, dtype=torch.float32, device=x.device)
+              if want_pooled else None)
+    check(lib().vsa_stage(ctypes.byref(cfg), _ptr(x), _ptr(x16), _ptr(pooled), _ptr(ws),
+                          _stream()), "vsa_stage")
+    return (x16, pooled) if want_pooled else x16
+
+
 def coarse_select(cfg: Config, q, k, v, ws):
-    """Cube-order q, k, v -> (qc, kc, vc, oc, lse_c, idx, cnt)."""
+    """bf16 q, k, v (cfg.layout order) -> (qc, kc, vc, oc, lse_c, idx, cnt)."""
     B, Hd, N, D = q.shape
     nc = N // 64
     cap = cfg.topk if cfg.select_mode == SELECT_TOPK else cfg.kmax
@@ -181,8 +193,9 @@ def coarse_select(cfg: Config, q, k, v, ws):
     return qc, kc, vc, oc, lse, idx, cnt
 
 
-def fine_fwd(cfg: Config, q, k, v, idx, cnt, gc, gf, oc, ws, want_saved=True):
-    """Cube-order q, k, v; caller-layout gates -> (o, o_f, lse_f)."""
+def fine_fwd(cfg: Config, q16, k16, v16, idx, cnt, gc, gf, oc, ws, want_saved=True):
+    """Staged fp16 cube-order q, k, v; caller-layout bf16 gates -> (o, o_f, lse_f)."""
+    q, k, v = q16, k16, v16
     B, Hd, N, D = q.shape
     o = torch.empty_like(gc)
     of = torch.empty(B, Hd, N, D, dtype=torch.float32, device=q.device) if want_saved else None
@@ -193,16 +206,16 @@ def fine_fwd(cfg: Config, q, k, v, idx, cnt, gc, gf, oc, ws, want_saved=True):
     return o, of, lse
 
 
-def combine_bwd(cfg: Config, d_o, gc, gf, o_f, oc):
+def combine_bwd(cfg: Config, d_o, gc, gf, o_f, oc, ws):
     B, Hd, N, D = d_o.shape
     f = dict(dtype=torch.float32, device=d_o.device)
     dgc, dgf = torch.empty(B, Hd, N, D, **f), torch.empty(B, Hd, N, D, **f)
-    dof = torch.empty_like(d_o)
+    dof = torch.empty(B, Hd, N, D, dtype=torch.float16, device=d_o.device)
     doc = torch.empty(B, Hd, N // 64, D, **f)
     delta = torch.empty(B, Hd, N, **f)
     check(lib().vsa_combine_bwd(ctypes.byref(cfg), _ptr(d_o), _ptr(gc), _ptr(gf), _ptr(o_f),
                                 _ptr(oc), _ptr(dgc), _ptr(dgf), _ptr(dof), _ptr(doc),
-                                _ptr(delta), _stream()), "vsa_combine_bwd")
+                                _ptr(delta), _ptr(ws), _stream()), "vsa_combine_bwd")
     return dgc, dgf, dof, doc, delta
 
 
@@ -214,7 +227,9 @@ def coarse_bwd(cfg: Config, qc, kc, vc, oc, lse_c, doc, ws):
     return dqc, dkc, dvc
 
 
-def fine_bwd(cfg: Config, q, k, v, idx, cnt, lse_f, dof, delta, dqc, dkc, dvc, ws):
+def fine_bwd(cfg: Config, q16, k16, v16, idx, cnt, lse_f, dof16, delta, dqc, dkc, dvc, ws):
+    """Staged fp16 operands -> fp32 dq, dk, dv in cfg.layout order."""
+    q, k, v, dof = q16, k16, v16, dof16
     B, Hd, N, D = q.shape
     f = dict(dtype=torch.float32, device=q.device)
     dq, dk, dv = (torch.empty(B, Hd, N, D, **f) for _ in range(3))
@@ -233,15 +248,15 @@ def forward(cfg: Config, q, k, v, gc, gf, bufs: Buffers, with_backward=True, out
     return o
 
 
-def backward(cfg: Config, q, k, v, gc, gf, d_o, bufs: Buffers, grads=None):
-    B, Hd, N, D = q.shape
+def backward(cfg: Config, gc, gf, d_o, bufs: Buffers, grads=None):
+    B, Hd, N, D = gc.shape
     if grads is None:
-        grads = tuple(torch.empty(B, Hd, N, D, dtype=torch.float32, device=q.device)
+        grads = tuple(torch.empty(B, Hd, N, D, dtype=torch.float32, device=gc.device)
                       for _ in range(5))
     dq, dk, dv, dgc, dgf = grads
-    check(lib().vsa_backward(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gc), _ptr(gf),
-                             _ptr(bufs.saved), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
-                             _ptr(dgc), _ptr(dgf), _ptr(bufs.ws), _stream()), "vsa_backward")
+    check(lib().vsa_backward(ctypes.byref(cfg), _ptr(gc), _ptr(gf), _ptr(bufs.saved), _ptr(d_o),
+                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgc), _ptr(dgf), _ptr(bufs.ws),
+                             _stream()), "vsa_backward")
     return grads
 
 
@@ -255,16 +270,17 @@ class _VSAFunction(torch.autograd.Function):
         bufs = Buffers(cfg, q.device, with_backward=need)
         o = forward(cfg, q, k, v, gc, gf, bufs, with_backward=need)
         ctx.cfg, ctx.bufs = cfg, bufs
-        ctx.save_for_backward(q, k, v, gc, gf)
+        ctx.dtypes = (q.dtype, k.dtype, v.dtype)
+        ctx.save_for_backward(gc, gf)
         return o
 
     @staticmethod
     def backward(ctx, d_o):
-        q, k, v, gc, gf = ctx.saved_tensors
+        gc, gf = ctx.saved_tensors
         d_o = d_o.to(torch.bfloat16).contiguous()
-        dq, dk, dv, dgc, dgf = backward(ctx.cfg, q, k, v, gc, gf, d_o, ctx.bufs)
-        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dgc.to(gc.dtype),
-                dgf.to(gf.dtype), None)
+        dq, dk, dv, dgc, dgf = backward(ctx.cfg, gc, gf, d_o, ctx.bufs)
+        tq, tk, tv = ctx.dtypes
+        return (dq.to(tq), dk.to(tk), dv.to(tv), dgc.to(gc.dtype), dgf.to(gf.dtype), None)
 
 
 def video_sparse_attention(q, k, v, gc, gf, video_shape, *, topk=32, select="topk", mass=0.9,
