@@ -18,12 +18,15 @@ Recipe (one (batch, head) slice at a time, raster token order r=(t*H+h)*W+w):
 * Gates G_c, G_f = bf16(sigmoid(N(0,1))), one per token x channel.
 * Upstream gradient dO = bf16(N(0,1)).
 
-Every workload has its own PCG64 seed.  A query cube whose noise must be drawn
-again (test-side gap enforcement) takes a fresh stream keyed on
-(seed, batch, head, cube, attempt), so the redraw touches that cube only.
+Every workload has its own seed; each (tensor, batch, head) slice draws from
+its own PCG64 stream keyed on (seed, tensor, batch, head).  A query cube whose
+noise must be drawn again (test-side gap enforcement) takes a fresh stream
+keyed on (seed, tensor, batch, head, cube, attempt), so the redraw touches
+that cube only.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
 
@@ -90,7 +93,7 @@ WORKLOADS = {
                      "topk", topk=32, seed=20260003),
     # dynamic compute: smallest top-ranked set with coarse mass >= 0.9, in [8,64]
     "dynamic": Workload("dynamic_16x32x32_b2h12d64_mass0.9", 2, 12, 64, 16, 32, 32,
-                        "mass", mass=0.9, kmin=8, kmax=64, amplitude=1.0,
+                        "mass", mass=0.9, kmin=8, kmax=64, amplitude=1.3,
                         seed=20260004),
 }
 
@@ -132,44 +135,63 @@ def raster_rows_of_cube(wl: Workload, cube: int) -> np.ndarray:
     return ((t * wl.H + h) * wl.W + w).reshape(-1)
 
 
-class Inputs:
-    """The seeded tensors of one workload (CPU, bf16, [B, heads, N, D] raster)."""
+_Q, _K, _V, _GC, _GF, _DO, _FIELD_QK, _FIELD_V = range(8)
 
-    def __init__(self, wl: Workload, with_grad: bool | None = None):
+
+def _stream(seed: int, *key: int) -> np.random.Generator:
+    """An independent PCG64 stream per (workload seed, tensor, batch, head)."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, *key])))
+
+
+class Inputs:
+    """The seeded tensors of one workload (CPU, bf16, [B, heads, N, D] raster).
+
+    Every (tensor, batch, head) slice is drawn from its own keyed stream, so
+    the values do not depend on how many threads generate them.
+    """
+
+    def __init__(self, wl: Workload, with_grad: bool | None = None, threads: int = 16):
         self.wl = wl
         if with_grad is None:
             with_grad = wl.backward
         B, Hd, N, D = wl.batch, wl.heads, wl.tokens, wl.head_dim
-        rng = np.random.Generator(np.random.PCG64(wl.seed))
-        self._qk_field = {}
-        q = np.empty((B, Hd, N, D), np.float32)
-        k = np.empty_like(q)
-        v = np.empty_like(q)
-        for b in range(B):
-            for h in range(Hd):
-                s = smooth_field(rng, wl.T, wl.H, wl.W, D, wl.amplitude)
-                s2 = smooth_field(rng, wl.T, wl.H, wl.W, D, wl.amplitude)
-                self._qk_field[(b, h)] = s
-                q[b, h] = rng.standard_normal((N, D), dtype=np.float32) + s
-                k[b, h] = rng.standard_normal((N, D), dtype=np.float32) + s
-                v[b, h] = rng.standard_normal((N, D), dtype=np.float32) + s2
-        self.q = to_bf16(q)
-        del q
-        self.k = to_bf16(k)
-        del k
-        self.v = to_bf16(v)
-        del v
-        self.gc = to_bf16(_sigmoid(rng.standard_normal((B, Hd, N, D), dtype=np.float32)))
-        self.gf = to_bf16(_sigmoid(rng.standard_normal((B, Hd, N, D), dtype=np.float32)))
-        self.do = (to_bf16(rng.standard_normal((B, Hd, N, D), dtype=np.float32))
-                   if with_grad else None)
+        slices = [(b, h) for b in range(B) for h in range(Hd)]
+
+        def field(b, h, which):
+            return smooth_field(_stream(wl.seed, which, b, h), wl.T, wl.H, wl.W, D, wl.amplitude)
+
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            fields = list(ex.map(lambda bh: field(*bh, _FIELD_QK), slices))
+            self._qk_field = dict(zip(slices, fields))
+            vfields = dict(zip(slices, ex.map(lambda bh: field(*bh, _FIELD_V), slices)))
+
+            def make(tensor, add=None, transform=None):
+                out = torch.empty((B, Hd, N, D), dtype=torch.bfloat16)
+
+                def one(bh):
+                    b, h = bh
+                    x = _stream(wl.seed, tensor, b, h).standard_normal((N, D), dtype=np.float32)
+                    if add is not None:
+                        x += add[bh]
+                    if transform is not None:
+                        x = transform(x)
+                    out[b, h] = to_bf16(x)
+
+                list(ex.map(one, slices))
+                return out
+
+            self.q = make(_Q, self._qk_field)
+            self.k = make(_K, self._qk_field)
+            self.v = make(_V, vfields)
+            self.gc = make(_GC, transform=_sigmoid)
+            self.gf = make(_GF, transform=_sigmoid)
+            self.do = make(_DO) if with_grad else None
         self.redraws = 0
 
     def redraw_query_cube(self, b: int, h: int, cube: int, attempt: int) -> None:
         """Draw new noise for the 64 query tokens of one cube, keeping the field."""
         wl = self.wl
-        ss = np.random.SeedSequence([wl.seed, b, h, cube, attempt, 0x51])
-        rng = np.random.Generator(np.random.PCG64(ss))
+        rng = _stream(wl.seed, _Q, b, h, cube, attempt)
         rows = raster_rows_of_cube(wl, cube)
         noise = rng.standard_normal((TILE, wl.head_dim), dtype=np.float32)
         vals = noise + self._qk_field[(b, h)][rows]
