@@ -75,6 +75,7 @@ enum { VSA_LAYOUT_RASTER = 0, VSA_LAYOUT_CUBE = 1 };
 /* Largest supported sizes. */
 #define VSA_MAX_CUBES 8192   /* cubes per (batch, head) */
 #define VSA_MAX_LIST 256     /* index-list capacity per query cube */
+#define VSA_NOALLOC_SCRATCH_BYTES (8u << 20)  /* fixed scratch of vsa_fine_fwd_noalloc */
 
 typedef struct {
   int32_t batch, heads;     /* B, number of heads */
@@ -162,6 +163,31 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
                           const void* v16, const int32_t* idx, const int32_t* cnt, const void* gc,
                           const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
                           void* ws, void* stream);
+
+/* vsa_fine_fwd for callers that cannot provide a scratch buffer.  The pages
+ * have no counterpart: this is a calling convention, not a step of the method.
+ * A caller with no device allocator of its own (for example a plugin run by a
+ * host engine that owns all device memory and hands the plugin only its
+ * inputs and outputs) cannot supply the `ws` buffer of vsa_fine_fwd; this
+ * entry point takes no `ws` and allocates nothing.  Its scratch (status word,
+ * query-pair work items and union lists) lives in a fixed array of
+ * VSA_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that loads
+ * the library until the process exits.
+ *  - Arguments and results are those of vsa_fine_fwd, without `ws`.
+ *  - status: optional device pointer to a uint32 (4-byte aligned, NULL to
+ *    skip) that receives this call's device status bits (1: a bounded wait
+ *    expired, 2: a bad index list entry, 4: a value outside the fp16 range).
+ *  - Returns VSA_ERR_SHAPE, before any other check and any launch, when the
+ *    configuration needs more scratch than VSA_NOALLOC_SCRATCH_BYTES
+ *    (B*heads*ceil(Nc/2) query pairs, each with 20 bytes + 8*list_cap bytes).
+ *  - The first call on each device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - Every call shares the one array: calls that overlap on the GPU (other
+ *    streams, other threads) race and must be serialised by the caller. */
+vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void* q16, const void* k16,
+                                  const void* v16, const int32_t* idx, const int32_t* cnt,
+                                  const void* gc, const void* gf, const float* oc, void* o,
+                                  float* o_f, float* lse_f, uint32_t* status, void* stream);
 
 /* Backward of the combine (gradient of O = repeat(O_c) G_c + O_f G_f).
  * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp32 CUBE order; oc: fp32.

@@ -1,0 +1,126 @@
+// vsa_fine_fwd_noalloc: the fine stage + combine of vsa_fine_fwd for callers
+// that cannot hand the library a scratch buffer.
+//
+// Some callers hold no device allocator of their own: a plugin run by a host
+// engine that owns all device memory and gives the plugin only its input and
+// output buffers, or a fixed-footprint runtime that reserves every byte before
+// it starts.  Such a caller cannot call cudaMalloc and cannot provide the `ws`
+// buffer the other entry points take.  This variant keeps its scratch (the
+// status word, the query-pair work items and their union lists) in a
+// fixed-size array in device memory that belongs to the library itself.
+//
+// The array is a file-scope __device__ variable: every GPU that loads the
+// library holds its kNoallocScratchBytes until the process exits.  Host code
+// cannot pass the array's name to a kernel (on the host the name is only a
+// stand-in, not a device address), so the first call on each device, with that
+// device current, looks the device address up with cudaGetSymbolAddress and
+// caches it; make that first call before any stream capture.  Every call shares
+// the one array, so calls that overlap on the GPU race with each other; the
+// status word is cleared at the start of each call, the rest is fully
+// rewritten before it is read.
+#include <cmath>
+#include <mutex>
+
+#include "../../include/vsa.h"
+#include "sm103_ptx.cuh"
+#include "vsa_common.cuh"
+
+namespace vsa {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = VSA_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of this device's scratch array (looked up once per device).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The geometry of a configuration that vsa_validate accepted.
+Geom geometry(const vsa_config_t* c) {
+  Geom g{};
+  g.B = c->batch;
+  g.heads = c->heads;
+  g.T = c->T;
+  g.H = c->H;
+  g.W = c->W;
+  g.D = c->head_dim;
+  g.BH = c->batch * c->heads;
+  g.N = c->T * c->H * c->W;
+  g.Nc = g.N / kTile;
+  g.ct = c->T / 4;
+  g.ch = c->H / 4;
+  g.cw = c->W / 4;
+  g.cap = c->select_mode == VSA_SELECT_TOPK ? c->topk : c->kmax;
+  g.raster = c->layout == VSA_LAYOUT_RASTER;
+  g.scale = c->scale > 0.f ? c->scale : 1.0f / sqrtf(static_cast<float>(c->head_dim));
+  return g;
+}
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace vsa
+
+using namespace vsa;
+
+extern "C" vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void* q16,
+                                             const void* k16, const void* v16,
+                                             const int32_t* idx, const int32_t* cnt,
+                                             const void* gc, const void* gf, const float* oc,
+                                             void* o, float* o_f, float* lse_f,
+                                             uint32_t* status, void* stream) {
+  const vsa_status_t st = vsa_validate(cfg);
+  if (st != VSA_OK) return st;
+  const Geom g = geometry(cfg);
+  // scratch: status word | pair items | union lists (2 * capacity entries per pair)
+  const size_t npairs = static_cast<size_t>(g.BH) * ((g.Nc + 1) / 2);
+  const size_t items_off = 256;
+  const size_t lists_off = items_off + round256(sizeof(PairItem) * npairs);
+  const size_t need = lists_off + round256(sizeof(uint32_t) * npairs * 2 * g.cap);
+  if (need > kNoallocScratchBytes) return VSA_ERR_SHAPE;  // beyond the fixed scratch array
+  if (!q16 || !k16 || !v16 || !idx || !cnt || !gc || !gf || !oc || !o) return VSA_ERR_INVALID_ARG;
+  if (!aligned(q16) || !aligned(k16) || !aligned(v16) || !aligned(idx) || !aligned(cnt) ||
+      !aligned(gc) || !aligned(gf) || !aligned(oc) || !aligned(o) || !aligned(o_f) ||
+      !aligned(lse_f) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return VSA_ERR_ALIGNMENT;
+  void* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return VSA_ERR_CUDA;
+  char* b = static_cast<char*>(base);
+  Workspace w{};
+  w.status = reinterpret_cast<uint32_t*>(b);
+  w.qpairs = reinterpret_cast<PairItem*>(b + items_off);
+  w.qlist = reinterpret_cast<uint32_t*>(b + lists_off);
+  w.n_qpairs = static_cast<int>(npairs);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(w.status, 0, sizeof(uint32_t), s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (launch_fine_fwd(g, static_cast<const __half*>(q16), static_cast<const __half*>(k16),
+                      static_cast<const __half*>(v16), static_cast<const __nv_bfloat16*>(gc),
+                      static_cast<const __nv_bfloat16*>(gf), oc, static_cast<__nv_bfloat16*>(o),
+                      o_f, lse_f, w, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (status &&
+      cudaMemcpyAsync(status, w.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  return VSA_OK;
+}
