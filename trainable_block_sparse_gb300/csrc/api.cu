@@ -110,6 +110,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.n_qpairs = npairs;
   ws.qpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
+  ws.clogit = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
   if (with_backward) {
     const size_t words = (g.Nc + 31) / 32;
     ws.dof = take(half_tensor(g));
@@ -120,6 +121,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
     ws.dvc = static_cast<float*>(take(pooled_bytes(g)));
     ws.cprob = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
     ws.cgrad = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
+    ws.cdelta = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * 4));
     ws.tmask = static_cast<uint32_t*>(take(static_cast<size_t>(g.BH) * g.Nc * words * 4));
     ws.toff = static_cast<int*>(take(static_cast<size_t>(g.BH) * (g.Nc + 1) * 4));
     ws.tlist = static_cast<int*>(take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4));
@@ -273,7 +275,8 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
       launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s))
     return VSA_ERR_CUDA;
   return cuda_status(launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin,
-                                          cfg->kmax, qc, kc, vc, oc, lse_c, idx, cnt, s));
+                                          cfg->kmax, qc, kc, vc, w.clogit, oc, lse_c, idx, cnt,
+                                          s));
 }
 
 vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* k16,
@@ -382,7 +385,7 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   int* idx = reinterpret_cast<int*>(sv + L.idx);
   int* cnt = reinterpret_cast<int*>(sv + L.cnt);
   if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
-                           kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt,
+                           kc, vc, w.clogit, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt,
                            s) != cudaSuccess)
     return VSA_ERR_CUDA;
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       mbar_init(&sb.y_empty[i], 1);
     }
     mbar_init(&sb.sp_full, 1);
-    mbar_init(&sb.ps_full, 128);
+    mbar_init(&sb.ps_full, 4);  // one arrival per softmax warp
     mbar_init(&sb.acc_full, 1);
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
@@ -361,7 +361,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&sb.ps_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sb.ps_full);
       }
       if (!ok) break;
       // ---------------------------------------------- epilogue

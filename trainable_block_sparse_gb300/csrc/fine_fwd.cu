@@ -11,21 +11,28 @@
 //  * Steps take two key cubes at a time, so S = Q K^T is an M=128, N=128 UMMA
 //    chain and O += P V an M=128, N=D, K=128 chain (N=64 UMMAs run at ~60% of
 //    the tensor pipe, N=128 at ~97%).
-//  * Warp 0 issues TMA tile loads (Q once per item; K and V tiles gathered by
-//    list entry into a ring of stages), warp 1 issues UMMAs, warps 2-5 run the
-//    online softmax one token row per thread straight out of TMEM and write P
-//    back into TMEM as the A operand of the PV product.
 //  * Q, K, V arrive as fp16 cube-order staged copies and P is written in fp16:
 //    with the running maximum kept stale (below), the largest P entries are
 //    rounded too, and fp16's 11-bit significand keeps that error 8x below
 //    bf16's.  Every UMMA is fp16 x fp16 with fp32 accumulation.
-//  * S is double-buffered in TMEM so QK^T of step t+1 overlaps the softmax of
-//    step t.  The running maximum is only moved (and O rescaled in TMEM) when
-//    it grows by more than 2^8, which keeps exp arguments bounded and makes the
-//    rescale rare.
-//  * The epilogue normalises O_f, applies the gates with the cube's coarse
-//    output, and writes O (bf16, caller layout: un-permuted on the way out),
-//    O_f (fp32, kept for the backward) and the log-sum-exp.
+//  * Sixteen warps:
+//      warps 0-7   softmax: warp w reads TMEM lane quarter w%4 (32 token rows)
+//                  and key tile w/4 of the step (64 columns), so each thread
+//                  owns half a row; the two halves of a row agree on the
+//                  running maximum through shared memory once per step, and
+//                  P goes back into TMEM as the A operand of the PV product;
+//      warps 8-11  epilogue: normalise O_f, apply the gates with the cube's
+//                  coarse output, write O (bf16, caller layout, un-permuted on
+//                  the way out), O_f (fp32, kept for the backward) and the
+//                  log-sum-exp;
+//      warp 12     TMA: Q once per item, then K tiles gathered by list entry;
+//      warp 13     UMMA issue (whole warp converged, one elected lane);
+//      warp 14     TMA: V tiles gathered by list entry.
+//  * TMEM (512 columns): two S buffers (QK^T of step t+1 overlaps the softmax
+//    of step t) and two O accumulators (the epilogue of item i drains one
+//    while item i+1 accumulates into the other).
+//  * The running maximum is only moved (and O rescaled in TMEM) when it grows
+//    by more than 2^8, which keeps exp arguments bounded and the rescale rare.
 // Every mbarrier wait is bounded; a time-out is recorded in the status word and
 // the CTA unwinds, waits for its own in-flight copies and MMAs, frees TMEM and
 // exits.
@@ -37,10 +44,12 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreadsFwd = 192;           // 6 warps
+constexpr int kThreadsFwd = 512;           // 16 warps
+constexpr int kSoftmaxWarps = 8, kEpiWarps = 4;
+constexpr int kWarpEpi = 8, kWarpK = 12, kWarpMma = 13, kWarpV = 14;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;              // S buffers at columns 0 and 128
-constexpr uint32_t kColO = 256;            // O accumulator
+constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -49,18 +58,24 @@ struct FwdSmem {
   static constexpr int kChunkBytes = 128 * 128;       // one chunk of 128 rows
   static constexpr int kQBytes = kChunks * kChunkBytes;
   static constexpr int kKVBytes = kChunks * kChunkBytes;  // 2 key tiles
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStagesK = (D == 128) ? 3 : 6;
+  static constexpr int kStagesV = (D == 128) ? 2 : 6;
   static constexpr int kTileBytes = 64 * D * 2;       // one 64-row tile
-  static constexpr int kBytes = kQBytes + 2 * kStages * kKVBytes + 1024;
+  static constexpr int kBytes = kQBytes + (kStagesK + kStagesV) * kKVBytes + 1024;
 };
 
 struct FwdBars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_ready, o_full, final_mma;
+  uint64_t o_ready, o_full[2], o_free[2];
+  uint64_t st_full[2], st_free[2];
+  uint64_t final_mma;
   uint32_t tmem_base;
   int abort;
+  float red[2][2][128];    // [step parity][row half]: the half-row maxima of a step
+  float l_part[2][2][128]; // [O buffer][row half]: partial running sums
+  float m_fin[2][128];     // [O buffer]: final running maximum (log2 units)
 };
 
 struct FwdParams {
@@ -77,19 +92,40 @@ struct FwdParams {
   uint32_t* status;
 };
 
+// Arrival of a whole warp counted once: lanes finish their own work first.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Named barrier over the two softmax warps that share a TMEM lane quarter,
+// returning the OR of `fail` over both warps, so the pair always takes the
+// same branch after it (a warp that left alone would strand its partner at the
+// next barrier, which has no time limit).
+__device__ __forceinline__ bool pair_sync_or(int quarter, bool fail) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(fail)), "r"(1 + quarter)
+      : "memory");
+  return r != 0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, FwdParams P) {
   using L = FwdSmem<D>;
-  constexpr int kS = L::kStages;
+  constexpr int kSK = L::kStagesK, kSV = L::kStagesV;
   constexpr int kKSteps = D / 16;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + L::kQBytes;
-  uint8_t* sV = sK + kS * L::kKVBytes;
+  uint8_t* sV = sK + kSK * L::kKVBytes;
   __shared__ FwdBars sb;
   int* abort_flag = &sb.abort;
 
@@ -99,23 +135,28 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sb.q_full, 1);
     mbar_init(&sb.q_empty, 1);
-    for (int i = 0; i < kS; ++i) {
+    for (int i = 0; i < kSK; ++i) {
       mbar_init(&sb.k_full[i], 1);
       mbar_init(&sb.k_empty[i], 1);
+    }
+    for (int i = 0; i < kSV; ++i) {
       mbar_init(&sb.v_full[i], 1);
       mbar_init(&sb.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.p_full[i], 128);
+      mbar_init(&sb.p_full[i], kSoftmaxWarps);  // one arrival per softmax warp
+      mbar_init(&sb.o_full[i], 1);
+      mbar_init(&sb.o_free[i], kEpiWarps);      // one arrival per epilogue warp
+      mbar_init(&sb.st_full[i], kSoftmaxWarps);
+      mbar_init(&sb.st_free[i], kEpiWarps);
     }
     mbar_init(&sb.o_ready, 1);
-    mbar_init(&sb.o_full, 1);
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sb.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -124,12 +165,20 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
   tc_fence_after();
   const uint32_t tb = sb.tmem_base;
 
-  if (warp == 0) {
-    // ===================================================== TMA producer
+  if (warp == kWarpK || warp == kWarpV) {
+    // ===================================================== TMA producers
+    // One warp loads Q (once per item) and the K tiles, another the V tiles,
+    // each through its own ring, so K for step t is fetched as soon as QK^T of
+    // step t - kSK has consumed its slot, independently of the PV products.
+    const bool is_k = warp == kWarpK;
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
+      const CUtensorMap* tmap = is_k ? &tk : &tv;
+      uint64_t* full = is_k ? sb.k_full : sb.v_full;
+      uint64_t* empty = is_k ? sb.k_empty : sb.v_empty;
+      uint8_t* ring = is_k ? sK : sV;
+      const uint32_t kS = is_k ? kSK : kSV;
+      tma_prefetch_desc(tmap);
+      if (is_k) tma_prefetch_desc(&tq);
       uint32_t step = 0;
       int it = 0;  // items with work seen by this CTA
       for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag);
@@ -137,14 +186,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const PairItem pi = P.items[item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
-        if (it > 0 && !wait1(&sb.q_empty, (it - 1) & 1, abort_flag, P.status)) break;
-        mbar_arrive_expect_tx(&sb.q_full, L::kQBytes);
-        const int row_a = pi.bh * g.N + pi.a * kTile;
-        const int row_b = pi.bh * g.N + (pi.b >= 0 ? pi.b : pi.a) * kTile;
+        if (is_k) {
+          if (it > 0 && !wait1(&sb.q_empty, (it - 1) & 1, abort_flag, P.status)) break;
+          mbar_arrive_expect_tx(&sb.q_full, L::kQBytes);
+          const int row_a = pi.bh * g.N + pi.a * kTile;
+          const int row_b = pi.bh * g.N + (pi.b >= 0 ? pi.b : pi.a) * kTile;
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_2d(sQ + c * L::kChunkBytes, &tq, c * 64, row_a, &sb.q_full);
-          tma_load_2d(sQ + c * L::kChunkBytes + 8192, &tq, c * 64, row_b, &sb.q_full);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_2d(sQ + c * L::kChunkBytes, &tq, c * 64, row_a, &sb.q_full);
+            tma_load_2d(sQ + c * L::kChunkBytes + 8192, &tq, c * 64, row_b, &sb.q_full);
+          }
         }
         ++it;
         const int nsteps = (pi.count + 1) / 2;
@@ -154,41 +205,29 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           const bool two = 2 * s + 1 < pi.count;
           const int t0 = static_cast<int>(list[2 * s] & 0xFFFFu);
           const int t1 = two ? static_cast<int>(list[2 * s + 1] & 0xFFFFu) : t0;
-          const uint32_t bytes = (two ? 2 : 1) * L::kTileBytes;
-          if (step >= static_cast<uint32_t>(kS) &&
-              (!wait1(&sb.k_empty[slot], ph ^ 1, abort_flag, P.status) ||
-               !wait1(&sb.v_empty[slot], ph ^ 1, abort_flag, P.status))) {
+          if (step >= kS &&
+              !wait1(&empty[slot], ph ^ 1, abort_flag, P.status)) {
             ok = false;
             break;
           }
-          uint8_t* dk = sK + slot * L::kKVBytes;
-          uint8_t* dv = sV + slot * L::kKVBytes;
+          uint8_t* dst = ring + slot * L::kKVBytes;
           const int r0 = pi.bh * g.N + t0 * kTile, r1 = pi.bh * g.N + t1 * kTile;
-          mbar_arrive_expect_tx(&sb.k_full[slot], bytes);
+          mbar_arrive_expect_tx(&full[slot], (two ? 2 : 1) * L::kTileBytes);
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_2d(dk + c * L::kChunkBytes, &tk, c * 64, r0, &sb.k_full[slot]);
-            if (two) tma_load_2d(dk + c * L::kChunkBytes + 8192, &tk, c * 64, r1, &sb.k_full[slot]);
-          }
-          mbar_arrive_expect_tx(&sb.v_full[slot], bytes);
-#pragma unroll
-          for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_2d(dv + c * L::kChunkBytes, &tv, c * 64, r0, &sb.v_full[slot]);
-            if (two) tma_load_2d(dv + c * L::kChunkBytes + 8192, &tv, c * 64, r1, &sb.v_full[slot]);
+            tma_load_2d(dst + c * L::kChunkBytes, tmap, c * 64, r0, &full[slot]);
+            if (two) tma_load_2d(dst + c * L::kChunkBytes + 8192, tmap, c * 64, r1, &full[slot]);
           }
           ++step;
         }
         if (!ok) break;
       }
       // Drain: every copy issued must land before the CTA can exit.
-      const uint32_t first = step > static_cast<uint32_t>(kS) ? step - kS : 0;
-      for (uint32_t t = first; t < step; ++t) {
-        mbar_wait(&sb.k_full[t % kS], (t / kS) & 1, kWaitNs);
-        mbar_wait(&sb.v_full[t % kS], (t / kS) & 1, kWaitNs);
-      }
-      if (it > 0) mbar_wait(&sb.q_full, (it - 1) & 1, kWaitNs);
+      const uint32_t first = step > kS ? step - kS : 0;
+      for (uint32_t t = first; t < step; ++t) mbar_wait(&full[t % kS], (t / kS) & 1, kWaitNs);
+      if (is_k && it > 0) mbar_wait(&sb.q_full, (it - 1) & 1, kWaitNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ===================================================== UMMA issuer
     const uint32_t idesc_s128 = idesc_f16(128, 128, 0, 0);
     const uint32_t idesc_s64 = idesc_f16(128, 64, 0, 0);
@@ -200,14 +239,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
     for (int k = 0; k < kKSteps; ++k) qd[k] = qd0 + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
 
-    // O += P V for global step gstep (P from the S buffer of that step).
-    auto issue_pv = [&](uint32_t gstep, bool two, bool first) -> bool {
-      const uint32_t slot = gstep % kS, sbuf = gstep & 1;
+    // O[obuf] += P V for global step gstep (P from the S buffer of that step).
+    auto issue_pv = [&](uint32_t gstep, bool two, bool first, int obuf) -> bool {
+      const uint32_t slot = gstep % kSV, sbuf = gstep & 1;
       if (!waitw(&sb.p_full[sbuf], (gstep >> 1) & 1, abort_flag, P.status)) return false;
-      if (!waitw(&sb.v_full[slot], (gstep / kS) & 1, abort_flag, P.status)) return false;
+      if (!waitw(&sb.v_full[slot], (gstep / kSV) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
-      issue_ts_rows(tb + kColO, tb + kColS + sbuf * 128, vd0 + ((slot * L::kKVBytes) >> 4), two,
-                    idesc_pv, !first);
+      issue_ts_rows(tb + kColO + obuf * 128, tb + kColS + sbuf * 128,
+                    vd0 + ((slot * L::kKVBytes) >> 4), two, idesc_pv, !first);
       commit_elect(&sb.v_empty[slot]);
       commit_elect(&sb.o_ready);
       return true;
@@ -221,14 +260,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const PairItem pi = P.items[item];
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
+      const int obuf = it & 1;
       if (!waitw(&sb.q_full, it & 1, abort_flag, P.status)) break;
-      ++it;
       tc_fence_after();
       bool prev_two = false;
       for (int s = 0; s < nsteps; ++s, ++step) {
-        const uint32_t slot = step % kS, sbuf = step & 1;
+        const uint32_t slot = step % kSK, sbuf = step & 1;
         const bool two = 2 * s + 1 < pi.count;
-        if (!waitw(&sb.k_full[slot], (step / kS) & 1, abort_flag, P.status)) { ok = false; break; }
+        if (!waitw(&sb.k_full[slot], (step / kSK) & 1, abort_flag, P.status)) { ok = false; break; }
         tc_fence_after();
         uint64_t kd[kKSteps];
         const uint64_t kb = kd0 + ((slot * L::kKVBytes) >> 4);
@@ -238,173 +277,228 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         commit_elect(&sb.s_full[sbuf]);
         commit_elect(&sb.k_empty[slot]);
         if (s == nsteps - 1) commit_elect(&sb.q_empty);
-        if (s > 0 && !issue_pv(step - 1, prev_two, s == 1)) { ok = false; break; }
+        if (s == 1 && it >= 2 &&
+            !waitw(&sb.o_free[obuf], ((it >> 1) - 1) & 1, abort_flag, P.status)) {
+          ok = false;  // the epilogue of item it-2 has not released O[obuf]
+          break;
+        }
+        if (s > 0 && !issue_pv(step - 1, prev_two, s == 1, obuf)) { ok = false; break; }
         prev_two = two;
       }
       if (!ok) break;
-      if (!issue_pv(step - 1, prev_two, nsteps == 1)) break;
-      commit_elect(&sb.o_full);
+      if (nsteps == 1 && it >= 2 &&
+          !waitw(&sb.o_free[obuf], ((it >> 1) - 1) & 1, abort_flag, P.status))
+        break;
+      if (!issue_pv(step - 1, prev_two, nsteps == 1, obuf)) break;
+      commit_elect(&sb.o_full[obuf]);
+      ++it;
     }
     // all issued MMAs complete before TMEM is released
     commit_elect(&sb.final_mma);
     mbar_wait(&sb.final_mma, 0, kWaitNs);
-  } else {
-    // ===================================================== softmax + epilogue
+  } else if (warp < kSoftmaxWarps) {
+    // ===================================================== softmax
     const int quarter = warp & 3;                // TMEM lane quarter of this warp
+    const int hc = warp >> 2;                    // key tile of the step = column half
     const int row = quarter * 32 + lane;         // tile row 0..127
-    const int half = row >> 6;                   // 0: first cube, 1: second cube
-    const uint32_t mybit = half ? kSelB : kSelA;
+    const uint32_t mybit = (row >> 6) ? kSelB : kSelA;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = g.scale * 1.4426950408889634f;  // scale * log2(e)
     uint32_t step = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-         item += gridDim.x) {
+    // No abort test in the loop condition: both warps of a pair must walk the
+    // same items and leave together (see pair_sync_or).
+    for (int item = blockIdx.x; item < P.n_items && ok; item += gridDim.x) {
       const PairItem pi = P.items[item];
       if (pi.count == 0) continue;
       const uint32_t* list = P.lists + pi.off;
       const int nsteps = (pi.count + 1) / 2;
+      const int obuf = it & 1;
       float m_run = -INFINITY, l_run = 0.f;
       for (int s = 0; s < nsteps; ++s, ++step) {
         const uint32_t sbuf = step & 1;
         const bool two = 2 * s + 1 < pi.count;
-        const bool v0 = (list[2 * s] & mybit) != 0;
-        const bool v1 = two && (list[2 * s + 1] & mybit) != 0;
-        if (!waitw(&sb.s_full[sbuf], (step >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
-        tc_fence_after();
+        const bool have = hc == 0 || two;  // this step has a key tile for this half
+        const bool valid = have && (list[2 * s + hc] & mybit) != 0;
+        const bool got = waitw(&sb.s_full[sbuf], (step >> 1) & 1, abort_flag, P.status);
         const uint32_t ts = tb + lane_addr + kColS + sbuf * 128;
-        uint32_t x[128];  // S row; its first 64 words are reused for the packed P
-        if (!v0 && !v1) {
+        uint32_t x[64];  // this half-row of S; its first 32 words are reused for packed P
+        float mx = -INFINITY;
+        if (got) {
+          tc_fence_after();
+          if (valid) {
+            tmem_ld32(ts + 64 * hc, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tmem_ld32(ts + 64 * hc + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            tmem_wait_ld();
+            float m8[8];
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = 0u;
-        } else {
-          tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-          tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-          if (two) {
-            tmem_ld32(ts + 64, *reinterpret_cast<uint32_t(*)[32]>(&x[64]));
-            tmem_ld32(ts + 96, *reinterpret_cast<uint32_t(*)[32]>(&x[96]));
-          }
-          tmem_wait_ld();
-          float mx = -INFINITY;
-          if (v0) {
+            for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(x[i]));
+            for (int i = 0; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(x[i]));
+            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
           }
-          if (v1) {
+        }
+        sb.red[step & 1][hc][row] = mx;
+        // Both halves' S loads are complete before either half writes P (the
+        // half-1 P columns overlap the half-0 S columns).
+        tc_fence_before();
+        if (pair_sync_or(quarter, !got)) { ok = false; break; }
+        tc_fence_after();
+        const float m_new = fmaxf(m_run, fmaxf(mx, sb.red[step & 1][hc ^ 1][row]) * c);
+        bool resc = false;
+        float alpha = 1.f;
+        if (m_new > m_run + kRescaleThreshold) {
+          if (m_run != -INFINITY) {
+            alpha = ex2_approx(m_run - m_new);
+            l_run *= alpha;
+            resc = true;
+          }
+          m_run = m_new;
+        }
+        if (valid) {
+          float ls[8];
 #pragma unroll
-            for (int i = 64; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(x[i]));
-          }
-          const float m_new = fmaxf(m_run, mx * c);
-          bool resc = false;
-          float alpha = 1.f;
-          if (m_new > m_run + kRescaleThreshold) {
-            if (m_run != -INFINITY) {
-              alpha = ex2_approx(m_run - m_new);
-              l_run *= alpha;
-              resc = true;
-            }
-            m_run = m_new;
-          }
-          if (__any_sync(0xffffffffu, resc)) {
-            // O holds the previous steps' sum: wait for the last PV, scale in TMEM
-            if (!waitw(&sb.o_ready, (step - 1) & 1, abort_flag, P.status)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t to = tb + lane_addr + kColO;
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-              uint32_t ov[32];
-              tmem_ld32(to + cc, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-              tmem_st32(to + cc, ov);
-            }
-            tmem_wait_st();
-          }
-          float lsum = 0.f;
+          for (int u = 0; u < 8; ++u) ls[u] = 0.f;
           const float mb = m_run;
-          // x[i] <- bf16x2(p[2i], p[2i+1]); x[2i], x[2i+1] are read before x[i] is written
+          // x[i] <- f16x2(p[2i], p[2i+1]); x[2i], x[2i+1] are read before x[i] is written
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const bool valid = (i < 32) ? v0 : v1;
-            float p0 = 0.f, p1 = 0.f;
-            if (valid) {
-              p0 = ex2_approx(fmaf(__uint_as_float(x[2 * i]), c, -mb));
-              p1 = ex2_approx(fmaf(__uint_as_float(x[2 * i + 1]), c, -mb));
-            }
-            lsum += p0 + p1;
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * i]), c, -mb));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * i + 1]), c, -mb));
+            ls[i & 7] += p0 + p1;
             x[i] = pack_f16x2(p0, p1);
           }
-          l_run += lsum;
+          l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = 0u;
         }
-        // P overwrites the first 64 columns of this S buffer (already in registers)
-        tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-        if (two) tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+        // P of key tile hc goes to columns [32 hc, 32 hc + 32) of this S buffer
+        if (have) {
+          tmem_st32(ts + 32 * hc, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds the previous steps' sum: wait for the last PV product,
+          // then scale this half's columns of O in TMEM.  Both warps of the
+          // pair see the same rows, so both take this branch.  (Done after P
+          // is stored, so no part of x[] is live here.)
+          const bool ready = waitw(&sb.o_ready, (step - 1) & 1, abort_flag, P.status);
+          if (pair_sync_or(quarter, !ready)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t to = tb + lane_addr + kColO + obuf * 128 + hc * (D / 2);
+#pragma unroll 1
+          for (int cc = 0; cc < D / 2; cc += 32) {
+            uint32_t ov[32];
+            tmem_ld32(to + cc, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(to + cc, ov);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&sb.p_full[sbuf]);
+        warp_arrive(&sb.p_full[sbuf]);
       }
       if (!ok) break;
-      // ---------------------------------------------- epilogue
-      if (!waitw(&sb.o_full, it & 1, abort_flag, P.status)) break;
+      // Hand this row's statistics to the epilogue through the stats buffer of
+      // O[obuf]; the epilogue of item it-2 must have read it first.
+      const bool got = it < 2 || waitw(&sb.st_free[obuf], ((it >> 1) - 1) & 1, abort_flag, P.status);
+      if (pair_sync_or(quarter, !got)) break;
+      sb.l_part[obuf][hc][row] = l_run;
+      if (hc == 0) sb.m_fin[obuf][row] = m_run;
+      warp_arrive(&sb.st_full[obuf]);
       ++it;
-      tc_fence_after();
-      if (half == 0 || pi.b >= 0) {
-        const int cube = half ? pi.b : pi.a;
-        const int o_in = row & 63;
-        const float inv_l = 1.f / l_run;
-        const size_t crow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, o_in);
-        const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + o_in;
-        const float* ocr = P.oc + (static_cast<size_t>(pi.bh) * g.Nc + cube) * D;
-        const uint32_t to = tb + lane_addr + kColO;
+    }
+  } else if (warp >= kWarpEpi && warp < kWarpEpi + kEpiWarps) {
+    // ===================================================== epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int half = row >> 6;                   // 0: first cube, 1: second cube
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    int it = 0;
+    for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
+      const PairItem pi = P.items[item];
+      if (pi.count == 0) continue;
+      const int obuf = it & 1;
+      const bool live = half == 0 || pi.b >= 0;
+      const int cube = (half && pi.b >= 0) ? pi.b : pi.a;
+      const int o_in = row & 63;
+      const size_t crow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, o_in);
+      const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + o_in;
+      const float* ocr = P.oc + (static_cast<size_t>(pi.bh) * g.Nc + cube) * D;
+      // Gates and O_c of this row go to L2 while the item is still running, so
+      // the chunk loads below hit L2.
+      if (live) {
+        const char* gcl = reinterpret_cast<const char*>(P.gc + crow * D);
+        const char* gfl = reinterpret_cast<const char*>(P.gf + crow * D);
 #pragma unroll
+        for (int l = 0; l < D / 64; ++l) {
+          prefetch_l2(gcl + 128 * l);
+          prefetch_l2(gfl + 128 * l);
+        }
+      }
+      if (lane < D / 32) prefetch_l2(ocr + 32 * lane);  // 4*D bytes of O_c: D/32 lines
+      if (!waitw(&sb.st_full[obuf], (it >> 1) & 1, abort_flag, P.status)) break;
+      const float l_sum = sb.l_part[obuf][0][row] + sb.l_part[obuf][1][row];
+      const float m_fin = sb.m_fin[obuf][row];
+      warp_arrive(&sb.st_free[obuf]);
+      if (!waitw(&sb.o_full[obuf], (it >> 1) & 1, abort_flag, P.status)) break;
+      tc_fence_after();
+      if (live) {
+        const float inv_l = 1.f / l_sum;
+        const uint32_t to = tb + lane_addr + kColO + obuf * 128;
+#pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           uint32_t ov[32];
           tmem_ld32(to + cc, ov);
           tmem_wait_ld();
-          float of[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(ov[i]) * inv_l;
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv_l);
           if (P.o_f) {
             float4* dst = reinterpret_cast<float4*>(P.o_f + frow * D + cc);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(of[4 * i], of[4 * i + 1], of[4 * i + 2], of[4 * i + 3]);
+              dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                                   __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
           }
+          uint4* op = reinterpret_cast<uint4*>(P.o + crow * D + cc);
           const uint4* gcp = reinterpret_cast<const uint4*>(P.gc + crow * D + cc);
           const uint4* gfp = reinterpret_cast<const uint4*>(P.gf + crow * D + cc);
-          const float4* ocp = reinterpret_cast<const float4*>(ocr + cc);
-          uint4* op = reinterpret_cast<uint4*>(P.o + crow * D + cc);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 ga = gcp[v], gb = gfp[v];
-            const float4 oa = ocp[2 * v], ob = ocp[2 * v + 1];
-            const float ocv[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
-            const __nv_bfloat162* g2c = reinterpret_cast<const __nv_bfloat162*>(&ga);
-            const __nv_bfloat162* g2f = reinterpret_cast<const __nv_bfloat162*>(&gb);
+            const uint4 gcr = gcp[v], gfr = gfp[v];
+            const __nv_bfloat162* g2c = reinterpret_cast<const __nv_bfloat162*>(&gcr);
+            const __nv_bfloat162* g2f = reinterpret_cast<const __nv_bfloat162*>(&gfr);
             uint4 res;
             uint32_t* rp = reinterpret_cast<uint32_t*>(&res);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
+              const int d = cc + 8 * v + 2 * e;
               const float2 fc = __bfloat1622float2(g2c[e]);
               const float2 ff = __bfloat1622float2(g2f[e]);
-              const float y0 = fmaf(ocv[2 * e], fc.x, of[8 * v + 2 * e] * ff.x);
-              const float y1 = fmaf(ocv[2 * e + 1], fc.y, of[8 * v + 2 * e + 1] * ff.y);
+              const float2 oc2 = *reinterpret_cast<const float2*>(ocr + d);
+              const float y0 = fmaf(oc2.x, fc.x, __uint_as_float(ov[8 * v + 2 * e]) * ff.x);
+              const float y1 = fmaf(oc2.y, fc.y, __uint_as_float(ov[8 * v + 2 * e + 1]) * ff.y);
               rp[e] = pack_bf16x2(y0, y1);
             }
             op[v] = res;
           }
         }
-        if (P.lse_f) P.lse_f[frow] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        if (P.lse_f) P.lse_f[frow] = (m_fin + __log2f(l_sum)) * 0.6931471805599453f;
       }
+      tc_fence_before();
+      warp_arrive(&sb.o_free[obuf]);
+      ++it;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tb, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tb, kTmemCols);
 }
 
 template <int D>

@@ -65,6 +65,7 @@ struct Workspace {
   PairItem* qpairs;       // query-cube pairs
   uint32_t* qlist;        // [n_qpairs][2*cap] union lists
   int n_qpairs;
+  float* clogit;          // fp32 [BH, Nc, Nc] coarse logits, then A_c (forward)
   // backward
   void* dof;              // bf16 cube order
   float* delta;           // fp32 [BH, N]
@@ -72,6 +73,7 @@ struct Workspace {
   float* dqc; float* dkc; float* dvc;
   float* cprob;           // fp32 [BH, Nc, Nc]  coarse probabilities
   float* cgrad;           // fp32 [BH, Nc, Nc]  coarse logit gradients
+  float* cdelta;          // fp32 [BH, Nc]      rowsum(dO_c (.) O_c)
   uint32_t* tmask;        // [BH, Nc, ceil(Nc/32)] selection bit matrix
   int* toff;              // [BH, Nc + 1] offsets of transposed lists
   int* tlist;             // [BH, Nc * cap] transposed lists (query cubes per key cube)
@@ -91,7 +93,8 @@ cudaError_t launch_stage(const Geom& g, const __nv_bfloat16* in, int in_raster, 
                          float* pooled, uint32_t* status, cudaStream_t s);
 cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
                                  int kmax, const float* qc, const float* kc, const float* vc,
-                                 float* oc, float* lse_c, int* idx, int* cnt, cudaStream_t s);
+                                 float* logits, float* oc, float* lse_c, int* idx, int* cnt,
+                                 cudaStream_t s);
 cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
 cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, const __half* v,
