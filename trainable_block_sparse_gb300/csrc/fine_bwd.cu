@@ -20,14 +20,30 @@
 //    dV += P^T dO and dK += dS^T Q.
 // TMEM: S at column 0, dP at 128, accumulators at 256 and 384 (512 columns).
 // Operands are the fp16 staged copies of Q, K, V and dO_f; P and dS are fp16.
-// Roles, bounded waits and the abort path are as in the forward kernel.
+//
+// Overlap with one S and one dP buffer: the softmax warps work in two phases
+// per step, each with its own signal to the UMMA warp.
+//   phase 1: S -> P in registers (and P^T into TMEM in the key-major pass);
+//            from here the S columns are free again;
+//   phase 2: dP -> dS into TMEM.
+// The UMMA warp issues, per step t:  [dV(t)]  S(t+1)  dQ(t)|dK(t)  dP(t+1),
+// each waiting only for the phase it reads, so the next step's S product runs
+// while the softmax warps compute dS, and dP(t+1) while they compute P(t+1).
+// (In-order execution of one CTA's UMMAs keeps S(t+1) from overwriting the P^T
+// that dV(t) reads, and dP(t+1) from overwriting the dS that dQ/dK(t) read.)
+// Warps 0-7: softmax and epilogue; warp w reads TMEM lane quarter w%4 (32
+// rows) and the 64 columns of step tile w/4, so each thread owns half a row.
+// Warp 8: TMA producer.  Warp 9: UMMA issue.
+// Bounded waits and the abort path are as in the forward kernel.
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
 
 namespace vsa {
 namespace {
 
-constexpr int kThreadsBwd = 192;
+constexpr int kThreadsBwd = 320;  // 10 warps
+constexpr int kSoftmaxWarpsBwd = 8;
+constexpr int kWarpLoad = 8, kWarpIssue = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
 
@@ -45,7 +61,8 @@ struct BwdSmem {
 struct BwdBars {
   uint64_t x_full, x_empty;
   uint64_t y_full[4], y_empty[4];
-  uint64_t sp_full, ps_full, acc_full, final_mma;
+  uint64_t s_full, dp_full, p_done, ds_done;
+  uint64_t acc_full, acc_free, final_mma;
   uint32_t tmem_base;
   int abort;
 };
@@ -64,14 +81,19 @@ struct BwdParams {
   uint32_t* status;
 };
 
-// Writes one fp32 row of D values from a TMEM accumulator (times `mul`) plus
-// pooled[cube]/64 into a caller-layout tensor.
+__device__ __forceinline__ void warp_arrive_bwd(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Writes columns [c0, c0 + D/2) of one fp32 row from a TMEM accumulator
+// (times `mul`) plus pooled[cube]/64 into a caller-layout tensor.
 template <int D>
-__device__ __forceinline__ void store_row(uint32_t tacc, float mul, const float* pooled,
-                                          size_t pooled_row, float* out, size_t out_row,
-                                          bool have_acc) {
-#pragma unroll
-  for (int cc = 0; cc < D; cc += 32) {
+__device__ __forceinline__ void store_half_row(uint32_t tacc, int c0, float mul,
+                                               const float* pooled, size_t pooled_row, float* out,
+                                               size_t out_row, bool have_acc) {
+#pragma unroll 1
+  for (int cc = c0; cc < c0 + D / 2; cc += 32) {
     uint32_t v[32];
     if (have_acc) {
       tmem_ld32(tacc + cc, v);
@@ -128,14 +150,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       mbar_init(&sb.y_full[i], 1);
       mbar_init(&sb.y_empty[i], 1);
     }
-    mbar_init(&sb.sp_full, 1);
-    mbar_init(&sb.ps_full, 4);  // one arrival per softmax warp
+    mbar_init(&sb.s_full, 1);
+    mbar_init(&sb.dp_full, 1);
+    mbar_init(&sb.p_done, kSoftmaxWarpsBwd);   // one arrival per softmax warp
+    mbar_init(&sb.ds_done, kSoftmaxWarpsBwd);
     mbar_init(&sb.acc_full, 1);
+    mbar_init(&sb.acc_free, kSoftmaxWarpsBwd);
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpIssue) {
     tmem_alloc(&sb.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -144,7 +169,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   tc_fence_after();
   const uint32_t tb = sb.tmem_base;
 
-  if (warp == 0) {
+  if (warp == kWarpLoad) {
     // ===================================================== TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tx1);
@@ -210,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       for (uint32_t t = first; t < step; ++t) mbar_wait(&sb.y_full[t % kS], (t / kS) & 1, kWaitNs);
       if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpIssue) {
     // ===================================================== UMMA issuer
     const uint32_t id_s128 = idesc_f16(128, 128, 0, 0);
     const uint32_t id_s64 = idesc_f16(128, 64, 0, 0);
@@ -226,63 +251,112 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       x1d[k] = x1d0 + o;
       x2d[k] = x2d0 + o;
     }
-    uint32_t step = 0;
+    // K-major descriptors of operand `which` (0: Y1, 1: Y2) of stage `slot`
+    auto ydesc = [&](uint32_t slot, int which, uint64_t (&yd)[kKSteps]) {
+      const uint32_t off = (slot * 2 * L::kXBytes + which * L::kXBytes) >> 4;
+#pragma unroll
+      for (int k = 0; k < kKSteps; ++k)
+        yd[k] = yk0 + off + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
+    };
+    auto ymn = [&](uint32_t slot, int which) -> uint64_t {
+      return ym0 + ((slot * 2 * L::kXBytes + which * L::kXBytes) >> 4);
+    };
+    uint32_t step = 0;  // global index of the current item's first step
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
          item += gridDim.x) {
       const PairItem pi = P.items[item];
       if (pi.count == 0) continue;
-      if (!waitw(&sb.x_full, it & 1, abort_flag, P.status)) break;
-      ++it;
-      tc_fence_after();
       const int nsteps = (pi.count + 1) / 2;
-      for (int s = 0; s < nsteps; ++s, ++step) {
+      if (!waitw(&sb.x_full, it & 1, abort_flag, P.status)) break;
+      // S(0) and dP(0) of this item
+      {
         const uint32_t slot = step % kS;
+        const uint32_t ids = pi.count > 1 ? id_s128 : id_s64;
+        if (!waitw(&sb.y_full[slot], (step / kS) & 1, abort_flag, P.status)) break;
+        tc_fence_after();
+        uint64_t yd[kKSteps];
+        ydesc(slot, 0, yd);
+        issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, ids);   // S   (or S^T)
+        commit_elect(&sb.s_full);
+        ydesc(slot, 1, yd);
+        issue_ss_chain<kKSteps>(tb + kColDP, x2d, yd, ids);  // dP  (or dP^T)
+        commit_elect(&sb.dp_full);
+        if (nsteps == 1) commit_elect(&sb.x_empty);
+      }
+      for (int s = 0; s < nsteps; ++s) {
+        const uint32_t t = step + s;
+        const uint32_t slot = t % kS;
         const bool two = 2 * s + 1 < pi.count;
-        if (!waitw(&sb.y_full[slot], (step / kS) & 1, abort_flag, P.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t y1off = (slot * 2 * L::kXBytes) >> 4;
-        const uint32_t y2off = (slot * 2 * L::kXBytes + L::kXBytes) >> 4;
-        uint64_t y1d[kKSteps], y2d[kKSteps];
-#pragma unroll
-        for (int k = 0; k < kKSteps; ++k) {
-          const uint32_t o = ((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4;
-          y1d[k] = yk0 + y1off + o;
-          y2d[k] = yk0 + y2off + o;
+        const bool more = s + 1 < nsteps;
+        const uint32_t nslot = (t + 1) % kS;
+        const uint32_t nids = (2 * s + 3 < pi.count) ? id_s128 : id_s64;
+        if (kKeyMajor) {
+          // dV += P^T dO   (P^T in the S columns, dO = Y2 of this stage)
+          if (!waitw(&sb.p_done, t & 1, abort_flag, P.status)) { ok = false; break; }
+          if (s == 0 && it > 0 && !waitw(&sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_ts_rows(tb + kColA1, tb + kColS, ymn(slot, 1), two, id_acc, s > 0, 64);
         }
-        const uint32_t ids = two ? id_s128 : id_s64;
-        issue_ss_chain<kKSteps>(tb + kColS, x1d, y1d, ids);   // S   (or S^T)
-        issue_ss_chain<kKSteps>(tb + kColDP, x2d, y2d, ids);  // dP  (or dP^T)
-        commit_elect(&sb.sp_full);
-        if (s == nsteps - 1) commit_elect(&sb.x_empty);
-        if (!waitw(&sb.ps_full, step & 1, abort_flag, P.status)) { ok = false; break; }
+        if (more) {
+          // S(t+1): the softmax warps are done reading S(t)
+          if (!kKeyMajor && !waitw(&sb.p_done, t & 1, abort_flag, P.status)) { ok = false; break; }
+          if (!waitw(&sb.y_full[nslot], ((t + 1) / kS) & 1, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint64_t yd[kKSteps];
+          ydesc(nslot, 0, yd);
+          issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, nids);
+          commit_elect(&sb.s_full);
+        }
+        if (!waitw(&sb.ds_done, t & 1, abort_flag, P.status)) { ok = false; break; }
+        if (!kKeyMajor && s == 0 && it > 0 &&
+            !waitw(&sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const bool acc = s > 0;
         if (!kKeyMajor) {
           // dQ += dS K   (dS in the dP columns, K = Y1 as an MN-major operand)
-          issue_ts_rows(tb + kColA1, tb + kColDP, ym0 + y1off, two, id_acc, acc);
+          issue_ts_rows(tb + kColA1, tb + kColDP, ymn(slot, 0), two, id_acc, s > 0, 64);
         } else {
-          // dV += P^T dO   (P^T in the S columns, dO = Y2);  dK += dS^T Q  (Q = Y1)
-          issue_ts_rows(tb + kColA1, tb + kColS, ym0 + y2off, two, id_acc, acc);
-          issue_ts_rows(tb + kColA2, tb + kColDP, ym0 + y1off, two, id_acc, acc);
+          // dK += dS^T Q   (Q = Y1)
+          issue_ts_rows(tb + kColA2, tb + kColDP, ymn(slot, 0), two, id_acc, s > 0, 64);
         }
         commit_elect(&sb.y_empty[slot]);
+        if (more) {
+          uint64_t yd[kKSteps];
+          ydesc(nslot, 1, yd);
+          issue_ss_chain<kKSteps>(tb + kColDP, x2d, yd, nids);
+          commit_elect(&sb.dp_full);
+          if (s + 2 == nsteps) commit_elect(&sb.x_empty);  // last read of X1/X2 issued
+        }
       }
       if (!ok) break;
       commit_elect(&sb.acc_full);
+      step += nsteps;
+      ++it;
     }
     commit_elect(&sb.final_mma);
     mbar_wait(&sb.final_mma, 0, kWaitNs);
-  } else {
+  } else if (warp < kSoftmaxWarpsBwd) {
     // ===================================================== softmax-backward + epilogue
     const int quarter = warp & 3;
+    const int hc = warp >> 2;                 // step tile = column half of S and dP
     const int row = quarter * 32 + lane;
     const int half = row >> 6;
     const uint32_t mybit = half ? kSelB : kSelA;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr float kLog2e = 1.4426950408889634f;
     const float c = g.scale * kLog2e;
+    const uint32_t ts = tb + lane_addr + kColS + 64 * hc;
+    const uint32_t tdp = tb + lane_addr + kColDP + 64 * hc;
     uint32_t step = 0;
     int it = 0;
     bool ok = true;
@@ -296,8 +370,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         if (row_live) {
           const size_t orow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, row & 63);
           const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
-          store_row<D>(0, 0.f, P.pooled1, prow, P.out1, orow, false);
-          if (kKeyMajor) store_row<D>(0, 0.f, P.pooled2, prow, P.out2, orow, false);
+          store_half_row<D>(0, hc * (D / 2), 0.f, P.pooled1, prow, P.out1, orow, false);
+          if (kKeyMajor)
+            store_half_row<D>(0, hc * (D / 2), 0.f, P.pooled2, prow, P.out2, orow, false);
         }
         continue;
       }
@@ -311,12 +386,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       const int nsteps = (pi.count + 1) / 2;
       for (int s = 0; s < nsteps; ++s, ++step) {
         const bool two = 2 * s + 1 < pi.count;
-        const uint32_t e0 = list[2 * s];
-        const uint32_t e1 = two ? list[2 * s + 1] : 0u;
-        const bool v0 = (e0 & mybit) != 0;
-        const bool v1 = two && (e1 & mybit) != 0;
+        const bool have = hc == 0 || two;   // this step has a tile for this column half
+        const bool valid = have && (list[2 * s + hc] & mybit) != 0;
         const uint32_t slot = step % kS;
-        if (!waitw(&sb.sp_full, step & 1, abort_flag, P.status)) { ok = false; break; }
+        if (!waitw(&sb.s_full, step & 1, abort_flag, P.status)) { ok = false; break; }
         // the column data arrived with the stage's tiles (already complete: the
         // MMAs that produced S waited for it); waiting makes it visible here
         if (kKeyMajor && !waitw(&sb.y_full[slot], (step / kS) & 1, abort_flag, P.status)) {
@@ -324,69 +397,93 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           break;
         }
         tc_fence_after();
-        const float* col_lse = sCol + slot * 256;
+        const float* col_lse = sCol + slot * 256 + 64 * hc;
         const float* col_delta = col_lse + 128;
-        const uint32_t ts = tb + lane_addr + kColS;
-        const uint32_t tdp = tb + lane_addr + kColDP;
-        const int nchunks = two ? 4 : 2;  // 32-column chunks
-        for (int ch = 0; ch < nchunks; ++ch) {
-          const bool valid = (ch < 2) ? v0 : v1;
-          uint32_t pk[16], dk[16];
-          if (!valid) {
+        // ---- phase 1: P from S
+        float p[64];
+        if (valid) {
+          uint32_t sv[64];
+          tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+          tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = dk[i] = 0u;
-          } else {
-            uint32_t sv[32], dv[32];
-            tmem_ld32(ts + ch * 32, sv);
-            tmem_ld32(tdp + ch * 32, dv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float p[2], d[2];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int j = 2 * i + u;
-                const float lse2 = kKeyMajor ? col_lse[ch * 32 + j] * kLog2e : row_lse;
-                const float dl = kKeyMajor ? col_delta[ch * 32 + j] : row_delta;
-                p[u] = ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
-                d[u] = p[u] * (__uint_as_float(dv[j]) - dl);
-              }
-              pk[i] = pack_f16x2(p[0], p[1]);
-              dk[i] = pack_f16x2(d[0], d[1]);
-            }
+          for (int j = 0; j < 64; ++j) {
+            const float lse2 = kKeyMajor ? col_lse[j] * kLog2e : row_lse;
+            p[j] = ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
           }
-          // chunk ch of 32 values packs into 16 columns at ch*16 (already-read columns)
-          if (kKeyMajor) tmem_st16(ts + ch * 16, pk);
-          tmem_st16(tdp + ch * 16, dk);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) p[j] = 0.f;
         }
-        tmem_wait_st();
+        if (kKeyMajor && have) {
+          // P^T of this tile: 64 values pack into 32 columns at the tile's start
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_f16x2(p[2 * i], p[2 * i + 1]);
+          tmem_st32(ts, pk);
+          tmem_wait_st();
+        }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sb.ps_full);
+        warp_arrive_bwd(&sb.p_done);
+        // ---- phase 2: dS = P (.) (dP - delta)
+        if (!waitw(&sb.dp_full, step & 1, abort_flag, P.status)) { ok = false; break; }
+        tc_fence_after();
+        if (have) {
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t dk[16];
+            if (valid) {
+              uint32_t dv[32];
+              tmem_ld32(tdp + 32 * ch, dv);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float d[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int j = 32 * ch + 2 * i + u;
+                  const float dl = kKeyMajor ? col_delta[j] : row_delta;
+                  d[u] = p[j] * (__uint_as_float(dv[2 * i + u]) - dl);
+                }
+                dk[i] = pack_f16x2(d[0], d[1]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) dk[i] = 0u;
+            }
+            // chunk ch (32 values) packs into 16 columns at 16*ch: already-read columns
+            tmem_st16(tdp + 16 * ch, dk);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        warp_arrive_bwd(&sb.ds_done);
       }
       if (!ok) break;
       // ---------------------------------------------- epilogue
       if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
-      ++it;
       tc_fence_after();
       if (row_live) {
         const size_t orow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, row & 63);
         const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
+        const uint32_t ta = tb + lane_addr;
         if (!kKeyMajor) {
-          store_row<D>(tb + lane_addr + kColA1, g.scale, P.pooled1, prow, P.out1, orow, true);
+          store_half_row<D>(ta + kColA1, hc * (D / 2), g.scale, P.pooled1, prow, P.out1, orow, true);
         } else {
-          store_row<D>(tb + lane_addr + kColA1, 1.f, P.pooled1, prow, P.out1, orow, true);
-          store_row<D>(tb + lane_addr + kColA2, g.scale, P.pooled2, prow, P.out2, orow, true);
+          store_half_row<D>(ta + kColA1, hc * (D / 2), 1.f, P.pooled1, prow, P.out1, orow, true);
+          store_half_row<D>(ta + kColA2, hc * (D / 2), g.scale, P.pooled2, prow, P.out2, orow, true);
         }
       }
       tc_fence_before();
+      warp_arrive_bwd(&sb.acc_free);
+      ++it;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tb, kTmemCols);
+  if (warp == kWarpIssue) tmem_dealloc(tb, kTmemCols);
 }
 
 template <int D, bool kKeyMajor>

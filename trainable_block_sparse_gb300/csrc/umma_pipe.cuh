@@ -91,12 +91,15 @@ __device__ __forceinline__ void issue_ts4(uint32_t d_tmem, uint32_t a_tmem, uint
 
 // D (+)= A[tmem, 128 x 64*ntiles] * B[smem, MN-major rows of 128 bytes]: the
 // B stage holds 128 K-rows per 64-wide N chunk, K-steps of 16 rows = 2048 bytes.
+// The packed A columns of the second 64 values of K start `a_second` columns
+// after those of the first.
 __device__ __forceinline__ void issue_ts_rows(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              bool two, uint32_t idesc, bool accumulate) {
+                                              bool two, uint32_t idesc, bool accumulate,
+                                              uint32_t a_second = 32) {
   issue_ts4(d_tmem, a_tmem, b_desc, b_desc + (2048 >> 4), b_desc + (4096 >> 4),
             b_desc + (6144 >> 4), idesc, accumulate ? 1u : 0u);
   if (two)
-    issue_ts4(d_tmem, a_tmem + 32, b_desc + (8192 >> 4), b_desc + (10240 >> 4),
+    issue_ts4(d_tmem, a_tmem + a_second, b_desc + (8192 >> 4), b_desc + (10240 >> 4),
               b_desc + (12288 >> 4), b_desc + (14336 >> 4), idesc, 1u);
 }
 
