@@ -154,8 +154,8 @@ std::once_flag g_encode_once;
 }  // namespace
 
 // 2-D fp16 tensor map with 128-byte swizzle (the staged operands).
-bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, uint32_t box_cols) {
+// The driver's tensor-map encoder, looked up once per process.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q{};
     void* fn = nullptr;
@@ -164,7 +164,12 @@ bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
-  if (!g_encode) return false;
+  return g_encode;
+}
+
+bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_cols) {
+  if (!encoder()) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {box_cols, box_rows};
@@ -173,6 +178,28 @@ bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_out_f32(void* map, float* base, const Geom& g) {
+  if (!encoder()) return false;
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const uint64_t D = static_cast<uint64_t>(g.D);
+  if (g.raster) {
+    const cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(g.W), static_cast<cuuint64_t>(g.H),
+                                static_cast<cuuint64_t>(g.BH) * g.T};
+    const cuuint64_t strides[3] = {D * 4, D * 4 * g.W, D * 4 * g.W * g.H};
+    const cuuint32_t box[4] = {32, 4, 4, 4};
+    return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims,
+                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(g.BH) * g.N};
+  const cuuint64_t strides[1] = {D * 4};
+  const cuuint32_t box[2] = {32, 64};
+  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace vsa

@@ -9,31 +9,33 @@
 //
 // One tcgen05 kernel template runs two deterministic, atomic-free passes:
 //  * kKeyMajor = false (dQ pass): work item = two query cubes (M = 128 query
-//    rows), walking the union of their index lists.  Per step of two key
-//    cubes: S = Q K^T and dP = dO V^T into TMEM, the softmax warps turn them
-//    into dS (fp16, back into TMEM), then dQ += dS K.
+//    rows), walking the union of their index lists.  X1 = Q, X2 = dO_f of the
+//    item; per step of two key cubes Y1 = K, Y2 = V:
+//    S = Q K^T, dP = dO V^T, the softmax warps turn them into dS, dQ += dS K.
 //  * kKeyMajor = true (dK/dV pass): work item = two key cubes (M = 128 key
 //    rows), walking the union of their transposed lists (query cubes that
-//    selected them).  Per step of two query cubes: S^T = K Q^T and
-//    dP^T = V dO^T, the softmax warps write P^T and dS^T into TMEM (the
-//    per-column lse and delta come through shared memory), then
-//    dV += P^T dO and dK += dS^T Q.
-// TMEM: S at column 0, dP at 128, accumulators at 256 and 384 (512 columns).
+//    selected them).  X1 = K, X2 = V; per step of two query cubes Y1 = Q,
+//    Y2 = dO: S^T = K Q^T, dP^T = V dO^T, the softmax warps write P^T and dS^T
+//    (fp16) into the dP columns, then dV += P^T dO and dK += dS^T Q.
 // Operands are the fp16 staged copies of Q, K, V and dO_f; P and dS are fp16.
 //
-// Overlap with one S and one dP buffer: the softmax warps work in two phases
-// per step, each with its own signal to the UMMA warp.
-//   phase 1: S -> P in registers (and P^T into TMEM in the key-major pass);
-//            from here the S columns are free again;
-//   phase 2: dP -> dS into TMEM.
-// The UMMA warp issues, per step t:  [dV(t)]  S(t+1)  dQ(t)|dK(t)  dP(t+1),
-// each waiting only for the phase it reads, so the next step's S product runs
-// while the softmax warps compute dS, and dP(t+1) while they compute P(t+1).
-// (In-order execution of one CTA's UMMAs keeps S(t+1) from overwriting the P^T
-// that dV(t) reads, and dP(t+1) from overwriting the dS that dQ/dK(t) read.)
+// Per step the softmax warps signal twice: once S has been read (so the next
+// step's S product can be issued at once) and once dS is in TMEM.  TMEM
+// (512 columns): S at 0, dP at 128, the dQ or dV accumulator at 256, and at
+// 384 either the dK accumulator or, in the dQ pass, a second dP buffer (dP of
+// step t+1 is computed while dS of step t is still being written).
+// Y1 and Y2 come through separate TMA rings (Y1 is read by the last product
+// of a step, Y2 earlier, so Y1 gets the deeper ring).
+// Epilogue: the accumulators (times the scale, plus the pooled gradient) are
+// written to shared memory in the X operand buffers, which are free once the
+// item's products are done, and leave through TMA stores (a 4-D box of one
+// 4x4x4 cube x 32 columns for the raster layout), so the global writes are
+// whole lines; the next item's X is loaded after those stores have read
+// shared memory.
 // Warps 0-7: softmax and epilogue; warp w reads TMEM lane quarter w%4 (32
 // rows) and the 64 columns of step tile w/4, so each thread owns half a row.
-// Warp 8: TMA producer.  Warp 9: UMMA issue.
+// Warp 8: TMA loads of Y1/Y2.  Warp 9: UMMA issue.  Warp 10: TMA stores of the
+// epilogue and TMA loads of X.
 // Bounded waits and the abort path are as in the forward kernel.
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
@@ -41,28 +43,33 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreadsBwd = 320;  // 10 warps
+constexpr int kThreadsBwd = 352;  // 11 warps
 constexpr int kSoftmaxWarpsBwd = 8;
-constexpr int kWarpLoad = 8, kWarpIssue = 9;
+constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpStore = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdSmem {
   static constexpr int kChunks = D / 64;
-  static constexpr int kChunkBytes = 128 * 128;       // 128 rows x 128 bytes
+  static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 bytes
   static constexpr int kXBytes = kChunks * kChunkBytes;  // one 128-row operand
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStages1 = (D == 128) ? 3 : 4;    // Y1 ring
+  static constexpr int kStages2 = (D == 128) ? 2 : 4;    // Y2 ring
   static constexpr int kTileBytes = 64 * D * 2;
-  static constexpr int kColBytes = 4 * 64 * 4;        // lse, delta of two query cubes
-  static constexpr int kBytes = 2 * kXBytes + kStages * (2 * kXBytes + kColBytes) + 1024;
+  // epilogue staging (128 rows x D fp32, 32-column chunks of 16 KB) = X1 + X2
+  static constexpr int kStageChunk = 128 * 128;
+  static_assert((D / 32) * kStageChunk == 2 * kXBytes, "staging must fill X1 + X2");
+  static constexpr int kBytes = (2 + kStages1 + kStages2) * kXBytes + 1024;
 };
 
 struct BwdBars {
-  uint64_t x_full, x_empty;
-  uint64_t y_full[4], y_empty[4];
-  uint64_t s_full, dp_full, p_done, ds_done;
+  uint64_t x_full;
+  uint64_t y1_full[4], y1_empty[4], y2_full[4], y2_empty[4];
+  uint64_t s_full, s_read, dp_full[2], ds_full[2];  // dP/dS barriers by step parity
   uint64_t acc_full, acc_free, final_mma;
+  uint64_t stage_full[2], stage_free[2];  // by column half = staging region X1 / X2
   uint32_t tmem_base;
   int abort;
 };
@@ -86,38 +93,45 @@ __device__ __forceinline__ void warp_arrive_bwd(uint64_t* bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// Writes columns [c0, c0 + D/2) of one fp32 row from a TMEM accumulator
-// (times `mul`) plus pooled[cube]/64 into a caller-layout tensor.
+// Columns [c0, c0 + D/2) of one output row of an item with no selected
+// blocks: only pooled[cube]/64 reaches it (plain stores; a rare path).
 template <int D>
-__device__ __forceinline__ void store_half_row(uint32_t tacc, int c0, float mul,
-                                               const float* pooled, size_t pooled_row, float* out,
-                                               size_t out_row, bool have_acc) {
+__device__ __forceinline__ void store_pooled_half(int c0, const float* pooled, size_t pooled_row,
+                                                  float* out, size_t out_row) {
 #pragma unroll 1
-  for (int cc = c0; cc < c0 + D / 2; cc += 32) {
-    uint32_t v[32];
-    if (have_acc) {
-      tmem_ld32(tacc + cc, v);
-      tmem_wait_ld();
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0u;
+  for (int cc = c0; cc < c0 + D / 2; cc += 4) {
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (pooled) {
+      const float4 a = *reinterpret_cast<const float4*>(pooled + pooled_row * D + cc);
+      r = make_float4(a.x * (1.f / kTile), a.y * (1.f / kTile), a.z * (1.f / kTile),
+                      a.w * (1.f / kTile));
     }
-    float4* dst = reinterpret_cast<float4*>(out + out_row * D + cc);
-    const float4* pp =
-        pooled ? reinterpret_cast<const float4*>(pooled + pooled_row * D + cc) : nullptr;
+    *reinterpret_cast<float4*>(out + out_row * D + cc) = r;
+  }
+}
+
+// Accumulator row (times `mul`, plus pooled/64) -> staging, columns of this
+// thread's half, in the SW128 image the TMA store expects: 16-byte unit u of
+// row r of a 32-column chunk sits at unit position u ^ (r % 8).  pr[cc] holds,
+// in lane l, column 32*cc + l of this half of the warp's pooled row.
+template <int D>
+__device__ __forceinline__ void stage_half_row(uint32_t tacc, int hc, int row, float mul,
+                                               const float (&pr)[D / 64], uint8_t* staging) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float4 r = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
-                             __uint_as_float(v[4 * i + 2]) * mul,
-                             __uint_as_float(v[4 * i + 3]) * mul);
-      if (pp) {
-        const float4 a = pp[i];
-        r.x += a.x * (1.f / kTile);
-        r.y += a.y * (1.f / kTile);
-        r.z += a.z * (1.f / kTile);
-        r.w += a.w * (1.f / kTile);
-      }
-      dst[i] = r;
+  for (int cc = 0; cc < D / 64; ++cc) {
+    const int c = hc * (D / 64) + cc;  // 32-column chunk index
+    uint32_t v[32];
+    tmem_ld32(tacc + 32 * c, v);
+    tmem_wait_ld();
+    uint8_t* rowp = staging + c * (128 * 128) + row * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float r[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        r[e] = fmaf(__shfl_sync(0xffffffffu, pr[cc], 4 * u + e), 1.f / kTile,
+                    __uint_as_float(v[4 * u + e]) * mul);
+      *reinterpret_cast<float4*>(rowp + ((u ^ (row & 7)) << 4)) = make_float4(r[0], r[1], r[2], r[3]);
     }
   }
 }
@@ -126,18 +140,20 @@ template <int D, bool kKeyMajor>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
     fine_bwd_kernel(const __grid_constant__ CUtensorMap tx1, const __grid_constant__ CUtensorMap tx2,
                     const __grid_constant__ CUtensorMap ty1, const __grid_constant__ CUtensorMap ty2,
+                    const __grid_constant__ CUtensorMap to1, const __grid_constant__ CUtensorMap to2,
                     BwdParams P) {
   using L = BwdSmem<D>;
-  constexpr int kS = L::kStages;
+  constexpr int kS1 = L::kStages1, kS2 = L::kStages2;
   constexpr int kKSteps = D / 16;
+  constexpr int kRounds = kKeyMajor ? 2 : 1;  // epilogue outputs through the staging buffer
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sX1 = smem;
   uint8_t* sX2 = sX1 + L::kXBytes;
-  uint8_t* sY = sX2 + L::kXBytes;  // stage s: Y1 at s*2*kXBytes, Y2 right after
-  // key-major pass, per stage: lse[128] then delta[128] of the step's query cubes
-  float* sCol = reinterpret_cast<float*>(sY + kS * 2 * L::kXBytes);
+  uint8_t* sY1 = sX2 + L::kXBytes;  // ring of kS1 operands
+  uint8_t* sY2 = sY1 + kS1 * L::kXBytes;
+  uint8_t* staging = sX1;           // X1 + X2, once the item's products are done
   __shared__ BwdBars sb;
   int* abort_flag = &sb.abort;
   const Geom& g = P.g;
@@ -145,17 +161,26 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sb.x_full, 1);
-    mbar_init(&sb.x_empty, 1);
-    for (int i = 0; i < kS; ++i) {
-      mbar_init(&sb.y_full[i], 1);
-      mbar_init(&sb.y_empty[i], 1);
+    for (int i = 0; i < kS1; ++i) {
+      mbar_init(&sb.y1_full[i], 1);
+      mbar_init(&sb.y1_empty[i], 1);
+    }
+    for (int i = 0; i < kS2; ++i) {
+      mbar_init(&sb.y2_full[i], 1);
+      mbar_init(&sb.y2_empty[i], 1);
     }
     mbar_init(&sb.s_full, 1);
-    mbar_init(&sb.dp_full, 1);
-    mbar_init(&sb.p_done, kSoftmaxWarpsBwd);   // one arrival per softmax warp
-    mbar_init(&sb.ds_done, kSoftmaxWarpsBwd);
+    mbar_init(&sb.s_read, kSoftmaxWarpsBwd);   // one arrival per softmax warp
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.dp_full[i], 1);
+      mbar_init(&sb.ds_full[i], kSoftmaxWarpsBwd);
+    }
     mbar_init(&sb.acc_full, 1);
     mbar_init(&sb.acc_free, kSoftmaxWarpsBwd);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.stage_full[i], kSoftmaxWarpsBwd / 2);  // the four warps of a column half
+      mbar_init(&sb.stage_free[i], 1);
+    }
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
     fence_barrier_init();
@@ -168,72 +193,66 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = sb.tmem_base;
+  // dP buffer of global step t
+  auto dpcol = [](uint32_t t) -> uint32_t {
+    return (!kKeyMajor && (t & 1)) ? kColA2 : kColDP;
+  };
 
-  if (warp == kWarpLoad) {
-    // ===================================================== TMA producer
+  if (warp == kWarpLoadY) {
+    // ===================================================== TMA loads of Y1, Y2
     if (lane == 0) {
-      tma_prefetch_desc(&tx1);
-      tma_prefetch_desc(&tx2);
       tma_prefetch_desc(&ty1);
       tma_prefetch_desc(&ty2);
-      uint32_t step = 0;
-      int it = 0;
+      uint32_t n1 = 0, n2 = 0;  // steps whose Y1 / Y2 copies were issued
       bool ok = true;
       for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
            item += gridDim.x) {
         const PairItem pi = P.items[item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
-        if (it > 0 && !wait1(&sb.x_empty, (it - 1) & 1, abort_flag, P.status)) break;
-        mbar_arrive_expect_tx(&sb.x_full, 2 * L::kXBytes);
-        const int ra = pi.bh * g.N + pi.a * kTile;
-        const int rb = pi.bh * g.N + (pi.b >= 0 ? pi.b : pi.a) * kTile;
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_2d(sX1 + c * L::kChunkBytes, &tx1, c * 64, ra, &sb.x_full);
-          tma_load_2d(sX1 + c * L::kChunkBytes + 8192, &tx1, c * 64, rb, &sb.x_full);
-          tma_load_2d(sX2 + c * L::kChunkBytes, &tx2, c * 64, ra, &sb.x_full);
-          tma_load_2d(sX2 + c * L::kChunkBytes + 8192, &tx2, c * 64, rb, &sb.x_full);
-        }
-        ++it;
         const int nsteps = (pi.count + 1) / 2;
         for (int s = 0; s < nsteps; ++s) {
-          const uint32_t slot = step % kS, ph = (step / kS) & 1;
+          const uint32_t step = n1;
           const bool two = 2 * s + 1 < pi.count;
           const int t0 = static_cast<int>(list[2 * s] & 0xFFFFu);
           const int t1 = two ? static_cast<int>(list[2 * s + 1] & 0xFFFFu) : t0;
-          if (step >= static_cast<uint32_t>(kS) &&
-              !wait1(&sb.y_empty[slot], ph ^ 1, abort_flag, P.status)) {
+          const int r0 = pi.bh * g.N + t0 * kTile, r1 = pi.bh * g.N + t1 * kTile;
+          const uint32_t bytes = (two ? 2 : 1) * L::kTileBytes;
+          const uint32_t sl1 = step % kS1, sl2 = step % kS2;
+          if (step >= static_cast<uint32_t>(kS1) &&
+              !wait1(&sb.y1_empty[sl1], ((step / kS1) & 1) ^ 1, abort_flag, P.status)) {
             ok = false;
             break;
           }
-          uint8_t* y1 = sY + slot * 2 * L::kXBytes;
-          uint8_t* y2 = y1 + L::kXBytes;
-          const int r0 = pi.bh * g.N + t0 * kTile, r1 = pi.bh * g.N + t1 * kTile;
-          mbar_arrive_expect_tx(&sb.y_full[slot], 2 * (two ? 2 : 1) * L::kTileBytes +
-                                                      (kKeyMajor ? L::kColBytes : 0));
-          if (kKeyMajor) {
-            float* col = sCol + slot * 256;
-            bulk_load(col, P.lse + r0, 256, &sb.y_full[slot]);
-            bulk_load(col + 64, P.lse + r1, 256, &sb.y_full[slot]);
-            bulk_load(col + 128, P.delta + r0, 256, &sb.y_full[slot]);
-            bulk_load(col + 192, P.delta + r1, 256, &sb.y_full[slot]);
-          }
+          uint8_t* y1 = sY1 + sl1 * L::kXBytes;
+          mbar_arrive_expect_tx(&sb.y1_full[sl1], bytes);
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_2d(y1 + c * L::kChunkBytes, &ty1, c * 64, r0, &sb.y_full[slot]);
-            tma_load_2d(y2 + c * L::kChunkBytes, &ty2, c * 64, r0, &sb.y_full[slot]);
-            if (two) {
-              tma_load_2d(y1 + c * L::kChunkBytes + 8192, &ty1, c * 64, r1, &sb.y_full[slot]);
-              tma_load_2d(y2 + c * L::kChunkBytes + 8192, &ty2, c * 64, r1, &sb.y_full[slot]);
-            }
+            tma_load_2d(y1 + c * L::kChunkBytes, &ty1, c * 64, r0, &sb.y1_full[sl1]);
+            if (two) tma_load_2d(y1 + c * L::kChunkBytes + 8192, &ty1, c * 64, r1, &sb.y1_full[sl1]);
           }
-          ++step;
+          ++n1;
+          if (step >= static_cast<uint32_t>(kS2) &&
+              !wait1(&sb.y2_empty[sl2], ((step / kS2) & 1) ^ 1, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* y2 = sY2 + sl2 * L::kXBytes;
+          mbar_arrive_expect_tx(&sb.y2_full[sl2], bytes);
+#pragma unroll
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_2d(y2 + c * L::kChunkBytes, &ty2, c * 64, r0, &sb.y2_full[sl2]);
+            if (two) tma_load_2d(y2 + c * L::kChunkBytes + 8192, &ty2, c * 64, r1, &sb.y2_full[sl2]);
+          }
+          ++n2;
         }
       }
-      const uint32_t first = step > static_cast<uint32_t>(kS) ? step - kS : 0;
-      for (uint32_t t = first; t < step; ++t) mbar_wait(&sb.y_full[t % kS], (t / kS) & 1, kWaitNs);
-      if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);
+      // Drain: every copy issued must land before the CTA can exit (slots
+      // older than one ring length were already waited for before reuse).
+      for (uint32_t t = n1 > static_cast<uint32_t>(kS1) ? n1 - kS1 : 0; t < n1; ++t)
+        mbar_wait(&sb.y1_full[t % kS1], (t / kS1) & 1, kWaitNs);
+      for (uint32_t t = n2 > static_cast<uint32_t>(kS2) ? n2 - kS2 : 0; t < n2; ++t)
+        mbar_wait(&sb.y2_full[t % kS2], (t / kS2) & 1, kWaitNs);
     }
   } else if (warp == kWarpIssue) {
     // ===================================================== UMMA issuer
@@ -242,8 +261,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     const uint32_t id_acc = idesc_f16(128, D, 0, 1);
     const uint64_t x1d0 = sdesc_sw128(smem_u32(sX1), 16, 1024);
     const uint64_t x2d0 = sdesc_sw128(smem_u32(sX2), 16, 1024);
-    const uint64_t yk0 = sdesc_sw128(smem_u32(sY), 16, 1024);                 // K-major view
-    const uint64_t ym0 = sdesc_sw128(smem_u32(sY), L::kChunkBytes, 1024);     // MN-major view
+    const uint64_t y1k0 = sdesc_sw128(smem_u32(sY1), 16, 1024);              // K-major views
+    const uint64_t y2k0 = sdesc_sw128(smem_u32(sY2), 16, 1024);
+    const uint64_t y1m0 = sdesc_sw128(smem_u32(sY1), L::kChunkBytes, 1024);  // MN-major views
+    const uint64_t y2m0 = sdesc_sw128(smem_u32(sY2), L::kChunkBytes, 1024);
     uint64_t x1d[kKSteps], x2d[kKSteps];
 #pragma unroll
     for (int k = 0; k < kKSteps; ++k) {
@@ -251,15 +272,34 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       x1d[k] = x1d0 + o;
       x2d[k] = x2d0 + o;
     }
-    // K-major descriptors of operand `which` (0: Y1, 1: Y2) of stage `slot`
-    auto ydesc = [&](uint32_t slot, int which, uint64_t (&yd)[kKSteps]) {
-      const uint32_t off = (slot * 2 * L::kXBytes + which * L::kXBytes) >> 4;
+    auto kdesc = [&](uint64_t base, uint32_t slot, uint64_t (&yd)[kKSteps]) {
+      const uint32_t off = (slot * L::kXBytes) >> 4;
 #pragma unroll
       for (int k = 0; k < kKSteps; ++k)
-        yd[k] = yk0 + off + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
+        yd[k] = base + off + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
     };
-    auto ymn = [&](uint32_t slot, int which) -> uint64_t {
-      return ym0 + ((slot * 2 * L::kXBytes + which * L::kXBytes) >> 4);
+    // S (or S^T) of global step t: X1 x Y1^T
+    auto issue_s = [&](uint32_t t, uint32_t ids) -> bool {
+      const uint32_t sl = t % kS1;
+      if (!waitw(&sb.y1_full[sl], (t / kS1) & 1, abort_flag, P.status)) return false;
+      tc_fence_after();
+      uint64_t yd[kKSteps];
+      kdesc(y1k0, sl, yd);
+      issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, ids);
+      commit_elect(&sb.s_full);
+      return true;
+    };
+    // dP (or dP^T) of global step t: X2 x Y2^T
+    auto issue_dp = [&](uint32_t t, uint32_t ids) -> bool {
+      const uint32_t sl = t % kS2;
+      if (!waitw(&sb.y2_full[sl], (t / kS2) & 1, abort_flag, P.status)) return false;
+      tc_fence_after();
+      uint64_t yd[kKSteps];
+      kdesc(y2k0, sl, yd);
+      issue_ss_chain<kKSteps>(tb + dpcol(t), x2d, yd, ids);
+      commit_elect(&sb.dp_full[t & 1]);
+      if (!kKeyMajor) commit_elect(&sb.y2_empty[sl]);  // V feeds only dP in the dQ pass
+      return true;
     };
     uint32_t step = 0;  // global index of the current item's first step
     int it = 0;
@@ -270,52 +310,38 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
       if (!waitw(&sb.x_full, it & 1, abort_flag, P.status)) break;
-      // S(0) and dP(0) of this item
-      {
-        const uint32_t slot = step % kS;
-        const uint32_t ids = pi.count > 1 ? id_s128 : id_s64;
-        if (!waitw(&sb.y_full[slot], (step / kS) & 1, abort_flag, P.status)) break;
-        tc_fence_after();
-        uint64_t yd[kKSteps];
-        ydesc(slot, 0, yd);
-        issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, ids);   // S   (or S^T)
-        commit_elect(&sb.s_full);
-        ydesc(slot, 1, yd);
-        issue_ss_chain<kKSteps>(tb + kColDP, x2d, yd, ids);  // dP  (or dP^T)
-        commit_elect(&sb.dp_full);
-        if (nsteps == 1) commit_elect(&sb.x_empty);
-      }
+      const uint32_t ids0 = pi.count > 1 ? id_s128 : id_s64;
+      if (!issue_s(step, ids0) || !issue_dp(step, ids0)) break;
       for (int s = 0; s < nsteps; ++s) {
         const uint32_t t = step + s;
-        const uint32_t slot = t % kS;
         const bool two = 2 * s + 1 < pi.count;
         const bool more = s + 1 < nsteps;
-        const uint32_t nslot = (t + 1) % kS;
         const uint32_t nids = (2 * s + 3 < pi.count) ? id_s128 : id_s64;
+        const uint32_t sl1 = t % kS1, sl2 = t % kS2;
+        // softmax phase 1 of step t is done: S(t) has been read (and, in the
+        // key-major pass, replaced by P^T)
+        if ((kKeyMajor || more) && !waitw(&sb.s_read, t & 1, abort_flag, P.status)) {
+          ok = false;
+          break;
+        }
         if (kKeyMajor) {
-          // dV += P^T dO   (P^T in the S columns, dO = Y2 of this stage)
-          if (!waitw(&sb.p_done, t & 1, abort_flag, P.status)) { ok = false; break; }
           if (s == 0 && it > 0 && !waitw(&sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_ts_rows(tb + kColA1, tb + kColS, ymn(slot, 1), two, id_acc, s > 0, 64);
+          // dV += P^T dO   (P^T packed in the S columns, dO = Y2)
+          issue_ts_rows(tb + kColA1, tb + kColS, y2m0 + ((sl2 * L::kXBytes) >> 4), two, id_acc,
+                        s > 0, 64);
+          commit_elect(&sb.y2_empty[sl2]);
         }
         if (more) {
-          // S(t+1): the softmax warps are done reading S(t)
-          if (!kKeyMajor && !waitw(&sb.p_done, t & 1, abort_flag, P.status)) { ok = false; break; }
-          if (!waitw(&sb.y_full[nslot], ((t + 1) / kS) & 1, abort_flag, P.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint64_t yd[kKSteps];
-          ydesc(nslot, 0, yd);
-          issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, nids);
-          commit_elect(&sb.s_full);
+          // S(t+1) overwrites S(t) (or P^T(t), after dV(t) has read it)
+          if (!issue_s(t + 1, nids)) { ok = false; break; }
+          // dQ pass: dP(t+1) goes to the other dP buffer right away
+          if (!kKeyMajor && !issue_dp(t + 1, nids)) { ok = false; break; }
         }
-        if (!waitw(&sb.ds_done, t & 1, abort_flag, P.status)) { ok = false; break; }
+        if (!waitw(&sb.ds_full[t & 1], (t >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
         if (!kKeyMajor && s == 0 && it > 0 &&
             !waitw(&sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
           ok = false;
@@ -323,19 +349,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
         tc_fence_after();
         if (!kKeyMajor) {
-          // dQ += dS K   (dS in the dP columns, K = Y1 as an MN-major operand)
-          issue_ts_rows(tb + kColA1, tb + kColDP, ymn(slot, 0), two, id_acc, s > 0, 64);
+          // dQ += dS K   (dS packed in dP buffer t, K = Y1 as an MN-major operand)
+          issue_ts_rows(tb + kColA1, tb + dpcol(t), y1m0 + ((sl1 * L::kXBytes) >> 4), two, id_acc,
+                        s > 0, 64);
+          commit_elect(&sb.y1_empty[sl1]);
         } else {
-          // dK += dS^T Q   (Q = Y1)
-          issue_ts_rows(tb + kColA2, tb + kColDP, ymn(slot, 0), two, id_acc, s > 0, 64);
-        }
-        commit_elect(&sb.y_empty[slot]);
-        if (more) {
-          uint64_t yd[kKSteps];
-          ydesc(nslot, 1, yd);
-          issue_ss_chain<kKSteps>(tb + kColDP, x2d, yd, nids);
-          commit_elect(&sb.dp_full);
-          if (s + 2 == nsteps) commit_elect(&sb.x_empty);  // last read of X1/X2 issued
+          // dK += dS^T Q   (dS^T packed in the dP columns, Q = Y1)
+          issue_ts_rows(tb + kColA2, tb + kColDP, y1m0 + ((sl1 * L::kXBytes) >> 4), two, id_acc,
+                        s > 0, 64);
+          commit_elect(&sb.y1_empty[sl1]);
+          // dP(t+1) overwrites the dP columns after dK(t) has read them
+          if (more && !issue_dp(t + 1, nids)) { ok = false; break; }
         }
       }
       if (!ok) break;
@@ -345,18 +369,94 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
     commit_elect(&sb.final_mma);
     mbar_wait(&sb.final_mma, 0, kWaitNs);
+  } else if (warp == kWarpStore) {
+    // ===================================================== epilogue stores + X loads
+    if (lane == 0) {
+      tma_prefetch_desc(&tx1);
+      tma_prefetch_desc(&tx2);
+      tma_prefetch_desc(&to1);
+      if (kKeyMajor) tma_prefetch_desc(&to2);
+      // one bulk group: column half h of one output of item pi, from staging region h
+      auto store_half = [&](const PairItem& pi, const CUtensorMap* map, int h) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const int cube = hh ? pi.b : pi.a;
+          if (cube < 0) continue;
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) {
+            const int c = h * (D / 64) + cc;
+            const uint8_t* src = staging + c * L::kStageChunk + hh * (64 * 128);
+            if (g.raster) {
+              const int cw = cube % g.cw, ch = (cube / g.cw) % g.ch, ct = cube / (g.cw * g.ch);
+              tma_store_4d(map, src, 32 * c, 4 * cw, 4 * ch, pi.bh * g.T + 4 * ct);
+            } else {
+              tma_store_2d(map, src, 32 * c, pi.bh * g.N + cube * kTile);
+            }
+          }
+        }
+        bulk_commit_group();
+      };
+      // every output of item ie; on return the last round's two groups may still be reading
+      auto store_item = [&](const PairItem& pi, int ie) -> bool {
+        for (int r = 0; r < kRounds; ++r) {
+          const CUtensorMap* map = r == 0 ? &to1 : &to2;
+          for (int h = 0; h < 2; ++h) {
+            if (!wait1(&sb.stage_full[h], (ie * kRounds + r) & 1, abort_flag, P.status)) return false;
+            store_half(pi, map, h);
+          }
+          if (r + 1 < kRounds) {
+            bulk_wait_group_read1();
+            mbar_arrive(&sb.stage_free[0]);
+            bulk_wait_group_read0();
+            mbar_arrive(&sb.stage_free[1]);
+          }
+        }
+        return true;
+      };
+      // X1 (h = 0) or X2 (h = 1) of item pi
+      auto load_x = [&](const PairItem& pi, int h) {
+        const CUtensorMap* m = h ? &tx2 : &tx1;
+        uint8_t* dst = h ? sX2 : sX1;
+        const int ra = pi.bh * g.N + pi.a * kTile;
+        const int rb = pi.bh * g.N + (pi.b >= 0 ? pi.b : pi.a) * kTile;
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_2d(dst + c * L::kChunkBytes, m, c * 64, ra, &sb.x_full);
+          tma_load_2d(dst + c * L::kChunkBytes + 8192, m, c * 64, rb, &sb.x_full);
+        }
+      };
+      int it = 0;
+      bool ok = true;
+      PairItem prev{};
+      for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
+           item += gridDim.x) {
+        const PairItem pi = P.items[item];
+        if (pi.count == 0) continue;
+        // X shares its buffer with the previous item's staging: each half is
+        // loaded as soon as the stores from that region have read it
+        if (it > 0 && !store_item(prev, it - 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&sb.x_full, 2 * L::kXBytes);
+        if (it > 0) bulk_wait_group_read1();
+        load_x(pi, 0);
+        if (it > 0) bulk_wait_group_read0();
+        load_x(pi, 1);
+        prev = pi;
+        ++it;
+      }
+      if (ok && it > 0 && !is_aborted(abort_flag)) store_item(prev, it - 1);
+      bulk_wait_group0();
+      if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);
+    }
   } else if (warp < kSoftmaxWarpsBwd) {
     // ===================================================== softmax-backward + epilogue
     const int quarter = warp & 3;
     const int hc = warp >> 2;                 // step tile = column half of S and dP
     const int row = quarter * 32 + lane;
-    const int half = row >> 6;
+    const int half = row >> 6;                // warp-uniform: the item cube of these rows
     const uint32_t mybit = half ? kSelB : kSelA;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr float kLog2e = 1.4426950408889634f;
     const float c = g.scale * kLog2e;
     const uint32_t ts = tb + lane_addr + kColS + 64 * hc;
-    const uint32_t tdp = tb + lane_addr + kColDP + 64 * hc;
+    constexpr uint32_t kFull = 0xffffffffu;
     uint32_t step = 0;
     int it = 0;
     bool ok = true;
@@ -365,18 +465,29 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       const PairItem pi = P.items[item];
       const int cube = half ? pi.b : pi.a;
       const bool row_live = half == 0 || pi.b >= 0;
+      const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
       if (pi.count == 0) {
         // no fine contribution: only the pooled gradient reaches these rows
         if (row_live) {
           const size_t orow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, row & 63);
-          const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
-          store_half_row<D>(0, hc * (D / 2), 0.f, P.pooled1, prow, P.out1, orow, false);
-          if (kKeyMajor)
-            store_half_row<D>(0, hc * (D / 2), 0.f, P.pooled2, prow, P.out2, orow, false);
+          store_pooled_half<D>(hc * (D / 2), P.pooled1, prow, P.out1, orow);
+          if (kKeyMajor) store_pooled_half<D>(hc * (D / 2), P.pooled2, prow, P.out2, orow);
         }
         continue;
       }
       const uint32_t* list = P.lists + pi.off;
+      // this warp's half of the pooled rows, lane l holding column 32cc + l
+      float pr1[D / 64], pr2[D / 64];
+      {
+        const float* s1 = (row_live && P.pooled1) ? P.pooled1 + prow * D + hc * (D / 2) : nullptr;
+        const float* s2 = (kKeyMajor && row_live && P.pooled2) ? P.pooled2 + prow * D + hc * (D / 2)
+                                                               : nullptr;
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          pr1[cc] = s1 ? __ldg(s1 + 32 * cc + lane) : 0.f;
+          pr2[cc] = s2 ? __ldg(s2 + 32 * cc + lane) : 0.f;
+        }
+      }
       float row_lse = 0.f, row_delta = 0.f;
       if (!kKeyMajor && row_live) {
         const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + (row & 63);
@@ -384,39 +495,46 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         row_delta = P.delta[frow];
       }
       const int nsteps = (pi.count + 1) / 2;
+      // key-major: lse (log2 units) and delta of the step tile's 64 query rows,
+      // lane l holding rows l and 32 + l; fetched one step ahead
+      auto tile_rows = [&](int s2, float& l0, float& l1, float& d0, float& d1) {
+        const bool h2 = hc == 0 || 2 * s2 + 1 < pi.count;
+        const uint32_t e2 = h2 ? list[2 * s2 + hc] : 0u;
+        const size_t q0 = static_cast<size_t>(pi.bh) * g.N + (e2 & 0xFFFFu) * kTile;
+        l0 = __ldg(P.lse + q0 + lane) * kLog2e;
+        l1 = __ldg(P.lse + q0 + 32 + lane) * kLog2e;
+        d0 = __ldg(P.delta + q0 + lane);
+        d1 = __ldg(P.delta + q0 + 32 + lane);
+      };
+      float cl0 = 0.f, cl1 = 0.f, cd0 = 0.f, cd1 = 0.f;
+      if (kKeyMajor) tile_rows(0, cl0, cl1, cd0, cd1);
       for (int s = 0; s < nsteps; ++s, ++step) {
         const bool two = 2 * s + 1 < pi.count;
         const bool have = hc == 0 || two;   // this step has a tile for this column half
-        const bool valid = have && (list[2 * s + hc] & mybit) != 0;
-        const uint32_t slot = step % kS;
+        const bool valid = have && (list[2 * s + hc] & mybit) != 0;  // warp-uniform
+        float nl0 = 0.f, nl1 = 0.f, nd0 = 0.f, nd1 = 0.f;
+        if (kKeyMajor && s + 1 < nsteps) tile_rows(s + 1, nl0, nl1, nd0, nd1);
         if (!waitw(&sb.s_full, step & 1, abort_flag, P.status)) { ok = false; break; }
-        // the column data arrived with the stage's tiles (already complete: the
-        // MMAs that produced S waited for it); waiting makes it visible here
-        if (kKeyMajor && !waitw(&sb.y_full[slot], (step / kS) & 1, abort_flag, P.status)) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
-        const float* col_lse = sCol + slot * 256 + 64 * hc;
-        const float* col_delta = col_lse + 128;
-        // ---- phase 1: P from S
+        // ---- phase 1: P from S (key-major: P^T packed over the S columns)
         float p[64];
         if (valid) {
-          uint32_t sv[64];
-          tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-          tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float lse2 = kKeyMajor ? col_lse[j] * kLog2e : row_lse;
-            p[j] = ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t sv[32];
+            tmem_ld32(ts + 32 * ch, sv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float l2 = kKeyMajor ? __shfl_sync(kFull, ch ? cl1 : cl0, j) : row_lse;
+              p[32 * ch + j] = ex2_approx(fmaf(__uint_as_float(sv[j]), c, -l2));
+            }
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 64; ++j) p[j] = 0.f;
         }
         if (kKeyMajor && have) {
-          // P^T of this tile: 64 values pack into 32 columns at the tile's start
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = pack_f16x2(p[2 * i], p[2 * i + 1]);
@@ -424,10 +542,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        warp_arrive_bwd(&sb.p_done);
+        warp_arrive_bwd(&sb.s_read);
         // ---- phase 2: dS = P (.) (dP - delta)
-        if (!waitw(&sb.dp_full, step & 1, abort_flag, P.status)) { ok = false; break; }
+        const uint32_t b = step & 1;
+        if (!waitw(&sb.dp_full[b], (step >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t tdp = tb + lane_addr + dpcol(step) + 64 * hc;
         if (have) {
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
@@ -441,9 +561,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 float d[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                  const int j = 32 * ch + 2 * i + u;
-                  const float dl = kKeyMajor ? col_delta[j] : row_delta;
-                  d[u] = p[j] * (__uint_as_float(dv[2 * i + u]) - dl);
+                  const int j = 2 * i + u;
+                  const float dl = kKeyMajor ? __shfl_sync(kFull, ch ? cd1 : cd0, j) : row_delta;
+                  d[u] = p[32 * ch + j] * (__uint_as_float(dv[j]) - dl);
                 }
                 dk[i] = pack_f16x2(d[0], d[1]);
               }
@@ -451,31 +571,40 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 #pragma unroll
               for (int i = 0; i < 16; ++i) dk[i] = 0u;
             }
-            // chunk ch (32 values) packs into 16 columns at 16*ch: already-read columns
+            // chunk ch packs into 16 columns at 16*ch (columns already read)
             tmem_st16(tdp + 16 * ch, dk);
           }
           tmem_wait_st();
         }
         tc_fence_before();
-        warp_arrive_bwd(&sb.ds_done);
+        warp_arrive_bwd(&sb.ds_full[b]);
+        cl0 = nl0;
+        cl1 = nl1;
+        cd0 = nd0;
+        cd1 = nd1;
       }
       if (!ok) break;
       // ---------------------------------------------- epilogue
       if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
       tc_fence_after();
-      if (row_live) {
-        const size_t orow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, row & 63);
-        const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
-        const uint32_t ta = tb + lane_addr;
-        if (!kKeyMajor) {
-          store_half_row<D>(ta + kColA1, hc * (D / 2), g.scale, P.pooled1, prow, P.out1, orow, true);
-        } else {
-          store_half_row<D>(ta + kColA1, hc * (D / 2), 1.f, P.pooled1, prow, P.out1, orow, true);
-          store_half_row<D>(ta + kColA2, hc * (D / 2), g.scale, P.pooled2, prow, P.out2, orow, true);
-        }
+      if (row_live)
+        stage_half_row<D>(tb + lane_addr + kColA1, hc, row, kKeyMajor ? 1.f : g.scale, pr1, staging);
+      if (!kKeyMajor) {
+        tc_fence_before();
+        warp_arrive_bwd(&sb.acc_free);
       }
-      tc_fence_before();
-      warp_arrive_bwd(&sb.acc_free);
+      fence_proxy_async_smem();  // staging writes -> visible to the TMA store
+      warp_arrive_bwd(&sb.stage_full[hc]);
+      if (kKeyMajor) {
+        // dK once the stores of dV have read this half of the staging buffer
+        if (!waitw(&sb.stage_free[hc], it & 1, abort_flag, P.status)) break;
+        if (row_live)
+          stage_half_row<D>(tb + lane_addr + kColA2, hc, row, g.scale, pr2, staging);
+        tc_fence_before();
+        warp_arrive_bwd(&sb.acc_free);
+        fence_proxy_async_smem();
+        warp_arrive_bwd(&sb.stage_full[hc]);
+      }
       ++it;
     }
   }
@@ -489,10 +618,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 template <int D, bool kKeyMajor>
 cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y1, const void* y2,
                     BwdParams p, cudaStream_t s) {
-  alignas(64) CUtensorMap m1, m2, m3, m4;
+  alignas(64) CUtensorMap m1, m2, m3, m4, mo1, mo2;
   const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
   if (!encode_tiled_2d(&m1, x1, rows, D, 64, 64) || !encode_tiled_2d(&m2, x2, rows, D, 64, 64) ||
-      !encode_tiled_2d(&m3, y1, rows, D, 64, 64) || !encode_tiled_2d(&m4, y2, rows, D, 64, 64))
+      !encode_tiled_2d(&m3, y1, rows, D, 64, 64) || !encode_tiled_2d(&m4, y2, rows, D, 64, 64) ||
+      !encode_out_f32(&mo1, p.out1, g) || !encode_out_f32(&mo2, kKeyMajor ? p.out2 : p.out1, g))
     return cudaErrorInvalidValue;
   const int smem = BwdSmem<D>::kBytes;
   auto kern = fine_bwd_kernel<D, kKeyMajor>;
@@ -503,7 +633,7 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = p.n_items < sms ? p.n_items : sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreadsBwd, smem, s>>>(m1, m2, m3, m4, p);
+  kern<<<grid, kThreadsBwd, smem, s>>>(m1, m2, m3, m4, mo1, mo2, p);
   return cudaGetLastError();
 }
 
