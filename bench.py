@@ -41,8 +41,11 @@ from trainable_block_sparse_gb300 import build, flops, synth  # noqa: E402
 
 METRIC = "VSA fwd/fwd+bwd ms/layer & executed TFLOPS (% of BF16 peak), 16K–70K tokens"
 WORKLOAD = "p720"
-LAUNCHES_FWD = 6   # stage x3, coarse select, pair lists, fine forward
-LAUNCHES_BWD = 9   # combine bwd, coarse bwd x2, pair lists, transposed lists x3, fine bwd x2
+# kernels per call of vsa_forward / vsa_backward
+LAUNCHES_FWD = 8   # stage x3, coarse logits GEMM + select + O_c GEMM, pair lists, fine forward
+LAUNCHES_BWD = 15  # combine bwd, coarse bwd (row dot + 5 GEMMs), pair lists,
+                   # transposed lists (mask, count, scan, fill, pairs), fine bwd x2
+SIDE_WORKLOADS = ("wan13b", "dynamic")  # timed per stage beside the headline layer
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -164,6 +167,7 @@ def gpu_arm(args, rank, world):
     fwd()
     torch.cuda.synchronize()
     pairs = int(bufs.view("cnt", torch.int32, (B, H, wl.cubes)).sum().item())
+    balance = balance_report(vsa, bufs, wl, dev)
     work = executed_flops(wl, pairs)
     step_flops = sum(work.values())
 
@@ -184,8 +188,64 @@ def gpu_arm(args, rank, world):
 
     stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev)
     e2e = end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args)
+    side = {}
+    if rank == 0 and not args.no_side:
+        del bufs, grads, o, t
+        torch.cuda.empty_cache()
+        side = {name: side_workload(vsa, name, dev) for name in SIDE_WORKLOADS}
     return {"wl": wl, "work": work, "pairs": pairs, "ms_step": ms_max, "ms_fwd": ms_fwd,
-            "clocks": clk.summary(), "stages": stages, "e2e": e2e, "inp": inp}
+            "clocks": clk.summary(), "stages": stages, "e2e": e2e, "inp": inp,
+            "balance": balance, "side": side}
+
+
+def balance_report(vsa, bufs, wl, dev):
+    """Per-CTA work of the persistent fine kernels under their static item
+    assignment (max/mean of the step counts) and the list-length histogram."""
+    from trainable_block_sparse_gb300 import schedule
+    B, H, nc, cap = wl.batch, wl.heads, wl.cubes, wl.list_capacity
+    idx = bufs.view("idx", torch.int32, (B * H, nc, cap)).cpu().numpy()
+    cnt = bufs.view("cnt", torch.int32, (B * H, nc)).cpu().numpy()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return schedule.load_balance(idx, cnt, sms)
+
+
+def side_workload(vsa, name, dev):
+    """Per-stage times of another configuration of the same layer (inputs
+    resident, 3 repetitions per stage), its fwd and fwd+bwd time per layer,
+    and the fine kernels' work distribution."""
+    wl = synth.WORKLOADS[name]
+    inp = synth.Inputs(wl, with_grad=True)
+    cfg = vsa.config_for(wl)
+    t = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "gc", "gf", "do")}
+    bufs = vsa.Buffers(cfg, dev, with_backward=True)
+    B, H, N, D = wl.batch, wl.heads, wl.tokens, wl.head_dim
+    o = torch.empty_like(t["q"])
+    grads = tuple(torch.empty(B, H, N, D, dtype=torch.float32, device=dev) for _ in range(5))
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, True, out=o)
+
+    def step():
+        fwd()
+        vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs, grads)
+
+    ms_fwd = timed(fwd, 5, 3, stream)
+    ms_step = timed(step, 5, 3, stream)
+    if bufs.device_status() != vsa.OK:
+        raise RuntimeError(f"{name}: device status {bufs.device_status()}")
+    pairs = int(bufs.view("cnt", torch.int32, (B, H, wl.cubes)).sum().item())
+    work = executed_flops(wl, pairs)
+    balance = balance_report(vsa, bufs, wl, dev)
+    stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev)
+    peaks, _ = load_peaks()
+    return {"workload": wl.name, "selected_pairs": pairs, "fwd_ms_per_layer": ms_fwd,
+            "fwdbwd_ms_per_layer": ms_step, "stages_ms": stages,
+            "fine_fwd_tflops": work["fine_fwd"] / (stages["fine_fwd"] * 1e-3) / 1e12,
+            "fine_fwd_frac_of_peak": work["fine_fwd"] / (stages["fine_fwd"] * 1e-3) / 1e12
+            / peaks["bf16_tflops"],
+            "fine_bwd_tflops": work["fine_bwd"] / (stages["fine_bwd"] * 1e-3) / 1e12,
+            "load_balance": balance}
 
 
 def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=3):
@@ -392,6 +452,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the per-stage timing of the other configurations")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the layer with this many heads instead of 40 (smaller "
                          "profiling case of the same kernels)")
@@ -438,7 +500,10 @@ def main():
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"],
                 "ms_per_step": r["e2e"]["ms"]},
         "gpu_launches": (LAUNCHES_FWD + LAUNCHES_BWD) * args.steps,
+        "load_balance": r["balance"],
     }
+    if r["side"]:
+        line["other_configs"] = r["side"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(r["inp"], step_flops)
     print(json.dumps(line), flush=True)

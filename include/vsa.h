@@ -126,6 +126,16 @@ vsa_status_t vsa_reset_device_status(void* ws, void* stream);
  * a kernel recorded a device-side failure in `ws` since the last reset. */
 vsa_status_t vsa_check_device_status(void* ws, void* stream);
 
+/* Diagnostic (no counterpart in the method): runs one CTA that waits, with
+ * the same bounded mbarrier wait every pipelined kernel of this library uses,
+ * on a barrier nothing ever arrives at.  After `limit_us` microseconds
+ * (1..10,000,000) the wait gives up, records a time-out in the status word of
+ * `ws` and the kernel returns, leaving the context usable; the next
+ * vsa_check_device_status() then returns VSA_ERR_TIMEOUT.  ws: as for every
+ * other entry point (only its status word is touched).  Returns
+ * VSA_ERR_INVALID_ARG for a NULL ws or a limit outside the range. */
+vsa_status_t vsa_probe_wait_timeout(void* ws, uint32_t limit_us, void* stream);
+
 /* Tile / untile (App. B: tiling and untiling rearrange tokens between
  * sequence and cube order).  inverse = 0: raster -> cube order; 1: cube ->
  * raster.  in, out: bf16 [B,heads,N,D], distinct buffers.  cfg->layout is

@@ -98,3 +98,11 @@ def test_status_strings(lib):
     for s in range(8):
         assert len(lib.vsa_status_string(s)) > 0
     assert lib.vsa_status_string(99) == b"unknown status"
+
+
+def test_wait_probe_arguments_are_checked_on_the_host(lib):
+    ws = ctypes.c_void_p(0x1000)
+    assert lib.vsa_probe_wait_timeout(None, 1000, None) == vsa.ERR_INVALID_ARG
+    assert lib.vsa_probe_wait_timeout(ws, 0, None) == vsa.ERR_INVALID_ARG
+    assert lib.vsa_probe_wait_timeout(ws, 20_000_000, None) == vsa.ERR_INVALID_ARG
+    assert lib.vsa_probe_wait_timeout(ctypes.c_void_p(0x1008), 1000, None) == vsa.ERR_ALIGNMENT

@@ -1,0 +1,67 @@
+"""Host-side work-distribution report of the persistent fine kernels, checked
+against a plain set-based recomputation on small random selections."""
+import math
+import random
+
+import numpy as np
+
+from trainable_block_sparse_gb300 import schedule
+
+
+def _random_lists(rng, bh, nc, cap):
+    idx = np.full((bh, nc, cap), -1, dtype=np.int32)
+    cnt = np.zeros((bh, nc), dtype=np.int32)
+    for b in range(bh):
+        for i in range(nc):
+            c = rng.randint(1, cap)
+            sel = sorted(rng.sample(range(nc), c))
+            idx[b, i, :c] = sel
+            cnt[b, i] = c
+    return idx, cnt
+
+
+def _brute(idx, cnt, sms):
+    bh, nc, _ = idx.shape
+    lists = [[set(idx[b, i, : cnt[b, i]].tolist()) for i in range(nc)] for b in range(bh)]
+    tlists = [[{i for i in range(nc) if j in lists[b][i]} for j in range(nc)] for b in range(bh)]
+    res = {}
+    for name, L in (("fine_fwd", lists), ("fine_bwd_dkdv", tlists)):
+        steps = []
+        for b in range(bh):
+            for p in range((nc + 1) // 2):
+                u = set(L[b][2 * p])
+                if 2 * p + 1 < nc:
+                    u |= L[b][2 * p + 1]
+                steps.append(math.ceil(len(u) / 2))
+        grid = min(len(steps), sms)
+        work = [sum(steps[k] for k in range(c, len(steps), grid)) for c in range(grid)]
+        res[name] = (steps, work)
+    return res
+
+
+def test_item_steps_and_cta_work_match_set_recomputation():
+    rng = random.Random(7)
+    for bh, nc, cap, sms in ((1, 8, 3, 3), (3, 9, 5, 4), (2, 17, 6, 152)):
+        idx, cnt = _random_lists(rng, bh, nc, cap)
+        sel = schedule.selection_matrix(idx, cnt)
+        steps = schedule.item_steps(sel)
+        ref = _brute(idx, cnt, sms)
+        for name in ("fine_fwd", "fine_bwd_dkdv"):
+            assert steps[name].tolist() == ref[name][0]
+            assert schedule.cta_work(steps[name], sms).tolist() == ref[name][1]
+        assert steps["fine_bwd_dq"].tolist() == ref["fine_fwd"][0]
+
+
+def test_load_balance_report():
+    # 1 head, 4 cubes; cube i selects {i} except cube 0 selects everything
+    idx = np.array([[[0, 1, 2, 3], [1, -1, -1, -1], [2, -1, -1, -1], [3, -1, -1, -1]]],
+                   dtype=np.int32)
+    cnt = np.array([[4, 1, 1, 1]], dtype=np.int32)
+    r = schedule.load_balance(idx, cnt, sms=2)
+    # query pairs (0,1): union 4 -> 2 steps; (2,3): union 2 -> 1 step
+    assert r["fine_fwd"]["cta_steps_max"] == 2
+    assert r["fine_fwd"]["max_over_mean"] == 2 / 1.5
+    # transposed: key cubes 0..3 are selected by {0},{0,1},{0,2},{0,3}
+    # pairs (0,1): union {0,1} -> 1 step; (2,3): {0,2,3} -> 2 steps
+    assert r["fine_bwd_dkdv"]["steps_total"] == 3
+    assert r["count_histogram"] == {1: 3, 4: 1}

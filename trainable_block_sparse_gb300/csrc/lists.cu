@@ -89,34 +89,93 @@ __global__ void build_mask_kernel(Geom g, const int* __restrict__ idx,
   }
 }
 
-// Transposed lists of one (batch, head): for key cube j, the ascending query
-// cubes whose bit j is set.  One CTA per (batch, head).
-__global__ void __launch_bounds__(1024) build_transpose_kernel(Geom g, Workspace ws) {
-  extern __shared__ int offs[];  // [Nc + 1]
-  const int bh = blockIdx.x;
+// Transposed lists: for key cube j of a (batch, head), the ascending query
+// cubes whose selection bit j is set.  Three small kernels, each over
+// (batch*head) x (32-cube columns of the bit matrix) or per (batch*head):
+//   count: per key cube, how many query cubes selected it;
+//   scan:  exclusive prefix of the counts = CSR offsets;
+//   fill:  each warp of the CTA takes a contiguous range of query cubes, so
+//          the entries of each key cube come out in ascending order.
+constexpr int kTransposeWarps = 8;
+
+// Per-warp counts of bit (lane) of column word w over the warp's row range.
+__device__ __forceinline__ int column_count(const uint32_t* m, int words, int w, int i0, int i1) {
+  const int lane = threadIdx.x & 31;
+  int c = 0;
+  for (int i = i0; i < i1; ++i) c += (m[static_cast<size_t>(i) * words + w] >> lane) & 1u;
+  return c;
+}
+
+__global__ void __launch_bounds__(kTransposeWarps * 32) transpose_count_kernel(Geom g, Workspace ws) {
+  __shared__ int part[kTransposeWarps][32];
+  const int bh = blockIdx.x, w = blockIdx.y;
   const int words = (g.Nc + 31) / 32;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int chunk = (g.Nc + kTransposeWarps - 1) / kTransposeWarps;
+  const int i0 = min(warp * chunk, g.Nc), i1 = min(i0 + chunk, g.Nc);
   const uint32_t* m = ws.tmask + static_cast<size_t>(bh) * g.Nc * words;
-  for (int j = threadIdx.x; j < g.Nc; j += blockDim.x) {
+  part[warp][lane] = column_count(m, words, w, i0, i1);
+  __syncthreads();
+  if (warp == 0) {
     int c = 0;
-    const uint32_t bit = 1u << (j & 31);
-    for (int i = 0; i < g.Nc; ++i) c += (m[static_cast<size_t>(i) * words + (j >> 5)] & bit) != 0;
-    offs[j + 1] = c;
+    for (int k = 0; k < kTransposeWarps; ++k) c += part[k][lane];
+    const int j = 32 * w + lane;
+    if (j < g.Nc) ws.toff[static_cast<size_t>(bh) * (g.Nc + 1) + j + 1] = c;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    offs[0] = 0;
-    for (int j = 0; j < g.Nc; ++j) offs[j + 1] += offs[j];
+}
+
+// In-place inclusive scan of toff[1..Nc] (holding counts) with toff[0] = 0.
+__global__ void __launch_bounds__(1024) transpose_scan_kernel(Geom g, Workspace ws) {
+  __shared__ int wsum[32];
+  int* toff = ws.toff + static_cast<size_t>(blockIdx.x) * (g.Nc + 1);
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int carry = 0;
+  for (int base = 0; base < g.Nc; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int v = j < g.Nc ? toff[j + 1] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v += u;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int x = lane < static_cast<int>(blockDim.x / 32) ? wsum[lane] : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += u;
+      }
+      wsum[lane] = x;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int total = wsum[blockDim.x / 32 - 1];
+    if (warp > 0) v += wsum[warp - 1];
+    if (j < g.Nc) toff[j + 1] = carry + v;
+    carry += total;
+    __syncthreads();
   }
+  if (threadIdx.x == 0) toff[0] = 0;
+}
+
+__global__ void __launch_bounds__(kTransposeWarps * 32) transpose_fill_kernel(Geom g, Workspace ws) {
+  __shared__ int part[kTransposeWarps][32];
+  const int bh = blockIdx.x, w = blockIdx.y;
+  const int words = (g.Nc + 31) / 32;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int chunk = (g.Nc + kTransposeWarps - 1) / kTransposeWarps;
+  const int i0 = min(warp * chunk, g.Nc), i1 = min(i0 + chunk, g.Nc);
+  const uint32_t* m = ws.tmask + static_cast<size_t>(bh) * g.Nc * words;
+  part[warp][lane] = column_count(m, words, w, i0, i1);
   __syncthreads();
-  int* toff = ws.toff + static_cast<size_t>(bh) * (g.Nc + 1);
+  const int j = 32 * w + lane;
+  if (j >= g.Nc) return;
+  int n = ws.toff[static_cast<size_t>(bh) * (g.Nc + 1) + j];
+  for (int k = 0; k < warp; ++k) n += part[k][lane];
   int* tl = ws.tlist + static_cast<size_t>(bh) * g.Nc * g.cap;
-  for (int j = threadIdx.x; j <= g.Nc; j += blockDim.x) toff[j] = offs[j];
-  for (int j = threadIdx.x; j < g.Nc; j += blockDim.x) {
-    int n = offs[j];
-    const uint32_t bit = 1u << (j & 31);
-    for (int i = 0; i < g.Nc; ++i)
-      if (m[static_cast<size_t>(i) * words + (j >> 5)] & bit) tl[n++] = i;
-  }
+  for (int i = i0; i < i1; ++i)
+    if ((m[static_cast<size_t>(i) * words + w] >> lane) & 1u) tl[n++] = i;
 }
 
 __global__ void build_kpairs_kernel(Geom g, Workspace ws) {
@@ -150,8 +209,12 @@ cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
   build_mask_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, s>>>(g, idx, cnt, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(int) * (g.Nc + 1);
-  build_transpose_kernel<<<g.BH, 1024, smem, s>>>(g, ws);
+  const dim3 grid(g.BH, (g.Nc + 31) / 32);
+  transpose_count_kernel<<<grid, kTransposeWarps * 32, 0, s>>>(g, ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  transpose_scan_kernel<<<g.BH, 1024, 0, s>>>(g, ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  transpose_fill_kernel<<<grid, kTransposeWarps * 32, 0, s>>>(g, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int items = g.BH * ((g.Nc + 1) / 2);
   build_kpairs_kernel<<<(items + 127) / 128, 128, 0, s>>>(g, ws);

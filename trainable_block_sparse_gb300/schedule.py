@@ -1,0 +1,83 @@
+"""Work distribution of the persistent fine-stage kernels: a host-side report.
+
+The fine forward kernel and both fine backward passes launch one CTA per SM
+(grid = min(items, SMs)), and CTA b processes work items b, b + grid,
+b + 2*grid, ... in that order.  An item is a pair of neighbouring cubes
+(2p, 2p + 1) of one (batch, head), item index = bh * ceil(Nc / 2) + p:
+
+  * forward and dQ pass: two query cubes walking the union of their index
+    lists;
+  * key-major pass: two key cubes walking the union of their transposed
+    lists (the query cubes that selected them).
+
+Each step of an item covers two key (or query) tiles, so an item costs
+ceil(|union| / 2) steps.  This module recomputes those costs from the index
+lists that the coarse stage emitted and reports how evenly the static
+assignment spreads them over the CTAs ("VSA: Faster Video Diffusion with
+Trainable Sparse Attention", §2: the fine stage attends only within the
+selected blocks, so per-cube work varies with the selection, most of all
+with the coarse-mass rule of the dynamic variant).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def selection_matrix(idx: np.ndarray, cnt: np.ndarray) -> np.ndarray:
+    """Boolean [BH, Nc, Nc]: row i has column j set when key cube j is in the
+    first cnt[i] entries of query cube i's list."""
+    idx = np.asarray(idx).reshape(-1, idx.shape[-2], idx.shape[-1])
+    cnt = np.asarray(cnt).reshape(idx.shape[0], idx.shape[1])
+    bh, nc, cap = idx.shape
+    live = np.arange(cap)[None, None, :] < cnt[:, :, None]
+    sel = np.zeros((bh, nc, nc), dtype=bool)
+    b, i, e = np.nonzero(live)
+    sel[b, i, idx[b, i, e]] = True
+    return sel
+
+
+def pair_union_sizes(sel: np.ndarray) -> np.ndarray:
+    """|list(2p) U list(2p+1)| per pair, [BH, ceil(Nc/2)]; a lone last cube
+    pairs with nothing."""
+    bh, nc, _ = sel.shape
+    even = sel[:, 0::2]
+    odd = np.zeros_like(even)
+    odd[:, : nc // 2] = sel[:, 1::2]
+    return (even | odd).sum(-1)
+
+
+def item_steps(sel: np.ndarray) -> dict[str, np.ndarray]:
+    """Steps per work item, flattened in item order, for each fine kernel."""
+    fwd = (pair_union_sizes(sel) + 1) // 2
+    key = (pair_union_sizes(np.swapaxes(sel, 1, 2)) + 1) // 2
+    return {"fine_fwd": fwd.ravel(), "fine_bwd_dq": fwd.ravel(), "fine_bwd_dkdv": key.ravel()}
+
+
+def cta_work(steps: np.ndarray, sms: int) -> np.ndarray:
+    """Total steps of each CTA under the static round-robin assignment."""
+    n = steps.size
+    grid = min(n, sms)
+    if grid == 0:
+        return np.zeros(0, dtype=np.int64)
+    padded = np.zeros(-(-n // grid) * grid, dtype=np.int64)
+    padded[:n] = steps
+    return padded.reshape(-1, grid).sum(0)
+
+
+def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int) -> dict:
+    """max/mean per-CTA steps of each fine kernel, the step count of the
+    biggest item, and the histogram of per-cube list lengths."""
+    sel = selection_matrix(idx, cnt)
+    out = {}
+    for name, steps in item_steps(sel).items():
+        w = cta_work(steps, sms)
+        mean = float(w.mean()) if w.size else 0.0
+        out[name] = {"items": int(steps.size), "ctas": int(w.size),
+                     "steps_total": int(steps.sum()),
+                     "cta_steps_max": int(w.max()) if w.size else 0,
+                     "cta_steps_mean": mean,
+                     "max_over_mean": float(w.max() / mean) if mean > 0 else 1.0,
+                     "item_steps_max": int(steps.max()) if steps.size else 0}
+    counts = np.bincount(np.asarray(cnt).ravel(), minlength=1)
+    out["count_histogram"] = {int(c): int(n) for c, n in enumerate(counts) if n}
+    return out
