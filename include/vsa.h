@@ -136,6 +136,13 @@ vsa_status_t vsa_check_device_status(void* ws, void* stream);
  * VSA_ERR_INVALID_ARG for a NULL ws or a limit outside the range. */
 vsa_status_t vsa_probe_wait_timeout(void* ws, uint32_t limit_us, void* stream);
 
+/* Diagnostic (no counterpart in the method): y[i] = 2^x[i] for i < n, by
+ * the exponential the fine-stage softmax kernels use: which = 0 the ex2
+ * unit (approximate, ~2^-22 relative), which = 1 the FMA-pipe polynomial
+ * (relative error below 7.5e-5 for x in [-126, 128); inputs below -126 give
+ * results below 2^-125).  x, y: device float arrays of n elements. */
+vsa_status_t vsa_probe_exp2(const float* x, float* y, int32_t n, int32_t which, void* stream);
+
 /* Tile / untile (App. B: tiling and untiling rearrange tokens between
  * sequence and cube order).  inverse = 0: raster -> cube order; 1: cube ->
  * raster.  in, out: bf16 [B,heads,N,D], distinct buffers.  cfg->layout is

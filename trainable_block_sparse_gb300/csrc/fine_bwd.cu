@@ -49,6 +49,15 @@ constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpStore = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
 constexpr float kLog2e = 1.4426950408889634f;
+// Of every 8 exponentials of P, this many run as the FMA-pipe polynomial and
+// the rest on the ex2 unit (none: the polynomial measured slower here too).
+constexpr int kPolyOf8Bwd = 0;
+
+template <int J>
+__device__ __forceinline__ float ex2_split_bwd(float x) {
+  if constexpr ((J & 7) < kPolyOf8Bwd) return ex2_poly(x);
+  else return ex2_approx(x);
+}
 
 template <int D>
 struct BwdSmem {
@@ -496,7 +505,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       }
       const int nsteps = (pi.count + 1) / 2;
       // key-major: lse (log2 units) and delta of the step tile's 64 query rows,
-      // lane l holding rows l and 32 + l; fetched one step ahead
+      // lane l holding rows l and 32 + l, broadcast with shuffles; fetched one
+      // step ahead.  (Warp-uniform 16-byte loads from L1 instead of the
+      // shuffles measured 13% slower on the 720p layer.)
       auto tile_rows = [&](int s2, float& l0, float& l1, float& d0, float& d1) {
         const bool h2 = hc == 0 || 2 * s2 + 1 < pi.count;
         const uint32_t e2 = h2 ? list[2 * s2 + hc] : 0u;
@@ -519,17 +530,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         // ---- phase 1: P from S (key-major: P^T packed over the S columns)
         float p[64];
         if (valid) {
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
+          unroll_for<2>([&](auto CH) {
+            constexpr int ch = decltype(CH)::value;
             uint32_t sv[32];
             tmem_ld32(ts + 32 * ch, sv);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            unroll_for<32>([&](auto J) {
+              constexpr int j = decltype(J)::value;
               const float l2 = kKeyMajor ? __shfl_sync(kFull, ch ? cl1 : cl0, j) : row_lse;
-              p[32 * ch + j] = ex2_approx(fmaf(__uint_as_float(sv[j]), c, -l2));
-            }
-          }
+              p[32 * ch + j] = ex2_split_bwd<32 * ch + j>(fmaf(__uint_as_float(sv[j]), c, -l2));
+            });
+          });
         } else {
 #pragma unroll
           for (int j = 0; j < 64; ++j) p[j] = 0.f;

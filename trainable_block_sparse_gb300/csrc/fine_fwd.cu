@@ -51,6 +51,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;              // S buffers at columns 0 and 128
 constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Of every 8 exponentials of the softmax, this many run as the FMA-pipe
+// polynomial and the rest on the ex2 unit.  Measured on the 720p layer,
+// moving 2, 3 or 4 of 8 to the polynomial made the kernel 4-10% slower, so
+// the ex2 unit takes them all.
+constexpr int kPolyOf8 = 0;
+
+// 2^x for element j of a row: ex2 unit or FMA-pipe polynomial by position.
+template <int J>
+__device__ __forceinline__ float ex2_split(float x) {
+  if constexpr ((J & 7) < kPolyOf8) return ex2_poly(x);
+  else return ex2_approx(x);
+}
 
 template <int D>
 struct FwdSmem {
@@ -363,13 +375,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           for (int u = 0; u < 8; ++u) ls[u] = 0.f;
           const float mb = m_run;
           // x[i] <- f16x2(p[2i], p[2i+1]); x[2i], x[2i+1] are read before x[i] is written
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * i]), c, -mb));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * i + 1]), c, -mb));
+          unroll_for<32>([&](auto I) {
+            constexpr int i = decltype(I)::value;
+            const float p0 = ex2_split<2 * i>(fmaf(__uint_as_float(x[2 * i]), c, -mb));
+            const float p1 = ex2_split<2 * i + 1>(fmaf(__uint_as_float(x[2 * i + 1]), c, -mb));
             ls[i & 7] += p0 + p1;
             x[i] = pack_f16x2(p0, p1);
-          }
+          });
           l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         } else {
 #pragma unroll

@@ -157,6 +157,10 @@ __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
@@ -330,6 +334,26 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA pipe, for splitting a softmax's exponentials between this
+// and the ex2 unit.  Range reduction x = n + f, n = round(x) taken from the
+// low mantissa bits of x + 1.5*2^23, f in [-1/2, 1/2]; 2^f from a degree-3
+// polynomial fitted for minimum maximum relative error on that interval
+// (coefficients from exp2_fit.py, relative error below 7.5e-5); 2^n added to
+// the exponent field.  Inputs are clamped to >= -126 (results there are below
+// 2^-125, i.e. zero once rounded to fp16); x must be < 128.
+__device__ __forceinline__ float ex2_poly(float x) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  x = fmaxf(x, -126.0f);
+  const float t = __fadd_rn(x, kShift);
+  const float f = __fsub_rn(x, __fsub_rn(t, kShift));
+  float p = 0x1.c3f76p-5f;               // c3
+  p = __fmaf_rn(p, f, 0x1.f0de1ap-3f);    // c2
+  p = __fmaf_rn(p, f, 0x1.62f31ap-1f);    // c1
+  p = __fmaf_rn(p, f, 0x1.fff692p-1f);    // c0
+  const int n = __float_as_int(t) - 0x4B400000;
+  return __int_as_float(__float_as_int(p) + (n << 23));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {

@@ -4,11 +4,23 @@
 // about twice the tensor-pipe time of an M=128, N=128, K=16 MMA).
 #pragma once
 
+#include <type_traits>
+
 #include "sm103_ptx.cuh"
 
 namespace vsa {
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+
+// Compile-time loop: f(std::integral_constant<int, i>) for i = 0 .. N-1, so
+// the index can select code paths with `if constexpr`.
+template <int N, int I = 0, class F>
+__device__ __forceinline__ void unroll_for(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    unroll_for<N, I + 1>(f);
+  }
+}
 
 __device__ __forceinline__ bool is_aborted(const int* flag) {
   return *reinterpret_cast<const volatile int*>(flag) != 0;

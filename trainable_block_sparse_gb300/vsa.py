@@ -56,6 +56,7 @@ _SIGS = {
     "vsa_forward": [ctypes.POINTER(Config)] + [_P] * 7 + [ctypes.c_int, _P, _P],
     "vsa_backward": [ctypes.POINTER(Config)] + [_P] * 11,
     "vsa_probe_wait_timeout": [_P, ctypes.c_uint32, _P],
+    "vsa_probe_exp2": [_P, _P, ctypes.c_int32, ctypes.c_int32, _P],
 }
 _RESTYPES = {"vsa_status_string": ctypes.c_char_p, "vsa_saved_bytes": ctypes.c_size_t,
              "vsa_workspace_bytes": ctypes.c_size_t}
