@@ -111,6 +111,19 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.qpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
   ws.clogit = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
+  // tf32 pairs of the coarse GEMM operands
+  const size_t ldc = static_cast<size_t>((g.Nc + 3) & ~3);
+  const size_t pc_bytes = static_cast<size_t>(g.BH) * g.Nc * ldc * 4;  // [BH, Nc, ldc]
+  const size_t dc_bytes = static_cast<size_t>(g.BH) * g.D * ldc * 4;   // [BH, D, ldc]
+  auto f32 = [&](size_t bytes) { return static_cast<float*>(take(bytes)); };
+  ws.qh = f32(pooled_bytes(g));
+  ws.ql = f32(pooled_bytes(g));
+  ws.kh = f32(pooled_bytes(g));
+  ws.kl = f32(pooled_bytes(g));
+  ws.vth = f32(dc_bytes);
+  ws.vtl = f32(dc_bytes);
+  ws.ach = f32(pc_bytes);
+  ws.acl = f32(pc_bytes);
   if (with_backward) {
     const size_t words = (g.Nc + 31) / 32;
     ws.dof = take(half_tensor(g));
@@ -119,8 +132,20 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
     ws.dqc = static_cast<float*>(take(pooled_bytes(g)));
     ws.dkc = static_cast<float*>(take(pooled_bytes(g)));
     ws.dvc = static_cast<float*>(take(pooled_bytes(g)));
-    ws.cprob = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
-    ws.cgrad = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
+    ws.vh = f32(pooled_bytes(g));
+    ws.vl = f32(pooled_bytes(g));
+    ws.doh = f32(pooled_bytes(g));
+    ws.dol = f32(pooled_bytes(g));
+    ws.kth = f32(dc_bytes);
+    ws.ktl = f32(dc_bytes);
+    ws.qth = f32(dc_bytes);
+    ws.qtl = f32(dc_bytes);
+    ws.doth = f32(dc_bytes);
+    ws.dotl = f32(dc_bytes);
+    ws.pth = f32(pc_bytes);
+    ws.ptl = f32(pc_bytes);
+    ws.dlth = f32(pc_bytes);
+    ws.dltl = f32(pc_bytes);
     ws.cdelta = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * 4));
     ws.tmask = static_cast<uint32_t*>(take(static_cast<size_t>(g.BH) * g.Nc * words * 4));
     ws.toff = static_cast<int*>(take(static_cast<size_t>(g.BH) * (g.Nc + 1) * 4));
@@ -178,6 +203,21 @@ bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t rows,
+                         uint64_t cols, uint64_t ld, uint64_t batch_stride, uint32_t box_cols,
+                         uint32_t box_rows) {
+  if (!encoder()) return false;
+  const cuuint64_t dims[3] = {cols, rows, batch};
+  const cuuint64_t strides[2] = {ld * 4, batch_stride * 4};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encoder()(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<float*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_out_f32(void* map, float* base, const Geom& g) {
@@ -302,8 +342,7 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
       launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s))
     return VSA_ERR_CUDA;
   return cuda_status(launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin,
-                                          cfg->kmax, qc, kc, vc, w.clogit, oc, lse_c, idx, cnt,
-                                          s));
+                                          cfg->kmax, qc, kc, vc, oc, lse_c, idx, cnt, w, s));
 }
 
 vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* k16,
@@ -412,7 +451,7 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   int* idx = reinterpret_cast<int*>(sv + L.idx);
   int* cnt = reinterpret_cast<int*>(sv + L.cnt);
   if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
-                           kc, vc, w.clogit, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt,
+                           kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt, w,
                            s) != cudaSuccess)
     return VSA_ERR_CUDA;
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;

@@ -3,23 +3,23 @@
 // dense attention on the pooled (64x shorter) sequence, the row-wise selection
 // of key cubes and the mask-to-index conversion; and its backward.
 //
-// All contractions are fp32 on the CUDA cores, not on the tensor cores: the
-// selection is an integer decision taken on these logits, and rounding the
-// pooled vectors to bf16 or tf32 moves a logit by ~1e-3, the size of the
-// smallest gap the selection has to resolve.  In fp32 the error is ~1e-6.
+// The selection is an integer decision taken on these logits, so every
+// contraction keeps fp32 accuracy: they run on the tensor cores as
+// error-compensated tf32 products (each operand split into a tf32 pair
+// hi + lo, three products per step; tgemm.cu), about 1e-6 relative, where a
+// single bf16 or tf32 product would move a logit by ~1e-3, the size of the
+// smallest gap the selection has to resolve.
 //
-// Structure (per (batch, head) slice, Nc cubes):
-//   forward : L = scale Q_c K_c^T            (batched fp32 GEMM)
+// Structure (per (batch, head) slice, Nc cubes; "pair" = tf32 hi/lo pair):
+//   forward : L = scale Q_c K_c^T                   (GEMM -> L, fp32)
 //             softmax statistics, A_c, top-K / mass selection, index lists
-//                                            (one fused kernel, warp per row)
-//             O_c = A_c V_c                  (batched fp32 GEMM)
-//   backward: A_c = exp(scale Q_c K_c^T - lse)            (GEMM, fused exp)
-//             dL  = A_c (.) (dO_c V_c^T - rowsum(dO_c O_c)) (GEMM, fused)
-//             dQ_c = scale dL K_c, dK_c = scale dL^T Q_c, dV_c = A_c^T dO_c
-// The GEMM is register-tiled: a CTA computes a 128 x 64 tile with 256
-// threads, 8 x 4 outputs per thread, operands staged k-major in shared memory
-// (double-buffered through registers), so each 16-wide k step costs 3
-// vector shared loads per 32 FMAs.
+//                                                   (one kernel, warp per row;
+//                                                    A_c written as a pair)
+//             O_c = A_c V_c                         (GEMM)
+//   backward: P  = exp(scale Q_c K_c^T - lse)       (GEMM -> P fp32, P^T pair)
+//             dL = P (.) (dO_c V_c^T - rowsum(dO_c O_c))
+//                                                   (GEMM -> dL pair, dL^T pair)
+//             dQ_c = scale dL K_c, dK_c = scale dL^T Q_c, dV_c = P^T dO_c
 #include <cfloat>
 
 #include "sm103_ptx.cuh"
@@ -27,149 +27,6 @@
 
 namespace vsa {
 namespace {
-
-constexpr int kBM = 128, kBN = 64, kBK = 16;
-constexpr int kGemmThreads = 256;
-
-enum Epi { kEpiStore = 0, kEpiExpLse = 1, kEpiDLogit = 2 };
-
-struct GemmArgs {
-  int M, N, K;
-  const float* A; long long lda, strideA;  // element strides; batch stride
-  const float* B; long long ldb, strideB;
-  float* C; long long ldc, strideC;
-  float alpha;
-  // epilogue operands (per batch, row-major M x N like C; row vectors of M)
-  const float* rowvec; long long strideRow;  // lse (kEpiExpLse) or delta (kEpiDLogit)
-  const float* P; long long ldp, strideP;    // probabilities (kEpiDLogit)
-};
-
-// C[b] = alpha * op(A[b]) op(B[b]) with op(A) M x K, op(B) K x N.
-// TA: A is stored K x M (so op(A) = A^T); otherwise M x K.  TB: B is stored
-// N x K; otherwise K x N.  All row-major.
-template <bool TA, bool TB, int EPI>
-__global__ void __launch_bounds__(kGemmThreads) sgemm_kernel(GemmArgs g) {
-  __shared__ __align__(16) float As[2][kBK][kBM + 4];
-  __shared__ __align__(16) float Bs[2][kBK][kBN + 4];
-  const int b = blockIdx.z;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
-  const float* A = g.A + b * g.strideA;
-  const float* B = g.B + b * g.strideB;
-  const int tid = threadIdx.x;
-  const int tx = tid % 16, ty = tid / 16;  // 16 x 16 threads; outputs rows ty*8.., cols tx*4..
-
-  // per-thread load slots: A tile 128 x 16 = 2048 values = 8 per thread,
-  // B tile 16 x 64 = 1024 values = 4 per thread
-  float ra[8], rb[4];
-  auto load_a = [&](int k0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = tid + i * kGemmThreads;  // 0..2047
-      int m, k;
-      if (TA) { k = e / kBM; m = e % kBM; }  // contiguous along m
-      else    { m = e / kBK; k = e % kBK; }  // contiguous along k
-      const int gm = m0 + m, gk = k0 + k;
-      float v = 0.f;
-      if (gm < g.M && gk < g.K) v = TA ? A[gk * g.lda + gm] : A[gm * g.lda + gk];
-      ra[i] = v;
-    }
-  };
-  auto store_a = [&](int buf) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = tid + i * kGemmThreads;
-      int m, k;
-      if (TA) { k = e / kBM; m = e % kBM; }
-      else    { m = e / kBK; k = e % kBK; }
-      As[buf][k][m] = ra[i];
-    }
-  };
-  auto load_b = [&](int k0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = tid + i * kGemmThreads;  // 0..1023
-      int n, k;
-      if (TB) { n = e / kBK; k = e % kBK; }  // contiguous along k
-      else    { k = e / kBN; n = e % kBN; }  // contiguous along n
-      const int gn = n0 + n, gk = k0 + k;
-      float v = 0.f;
-      if (gn < g.N && gk < g.K) v = TB ? B[gn * g.ldb + gk] : B[gk * g.ldb + gn];
-      rb[i] = v;
-    }
-  };
-  auto store_b = [&](int buf) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = tid + i * kGemmThreads;
-      int n, k;
-      if (TB) { n = e / kBK; k = e % kBK; }
-      else    { k = e / kBN; n = e % kBN; }
-      Bs[buf][k][n] = rb[i];
-    }
-  };
-
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-  const int nk = (g.K + kBK - 1) / kBK;
-  load_a(0);
-  load_b(0);
-  store_a(0);
-  store_b(0);
-  __syncthreads();
-  for (int t = 0; t < nk; ++t) {
-    const int cur = t & 1;
-    if (t + 1 < nk) {
-      load_a((t + 1) * kBK);
-      load_b((t + 1) * kBK);
-    }
-#pragma unroll
-    for (int k = 0; k < kBK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 8 + 4]);
-      const float4 bv = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bw[j], acc[i][j]);
-    }
-    if (t + 1 < nk) {
-      store_a(cur ^ 1);
-      store_b(cur ^ 1);
-    }
-    __syncthreads();
-  }
-
-  float* C = g.C + b * g.strideC;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + ty * 8 + i;
-    if (gm >= g.M) continue;
-    float rv = 0.f;
-    if (EPI != kEpiStore) rv = g.rowvec[b * g.strideRow + gm];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int gn = n0 + tx * 4 + j;
-      if (gn >= g.N) continue;
-      float v = g.alpha * acc[i][j];
-      if (EPI == kEpiExpLse) v = expf(v - rv);
-      if (EPI == kEpiDLogit) v = g.P[b * g.strideP + gm * g.ldp + gn] * (v - rv);
-      C[gm * g.ldc + gn] = v;
-    }
-  }
-}
-
-template <bool TA, bool TB, int EPI>
-cudaError_t sgemm(const GemmArgs& a, int batch, cudaStream_t s) {
-  dim3 grid((a.N + kBN - 1) / kBN, (a.M + kBM - 1) / kBM, batch);
-  sgemm_kernel<TA, TB, EPI><<<grid, kGemmThreads, 0, s>>>(a);
-  return cudaGetLastError();
-}
 
 constexpr int kSelThreads = 256;
 
@@ -190,11 +47,13 @@ struct SelectArgs {
   float mass;
 };
 
-// One warp per query cube: softmax statistics of its logits row, the row of
-// A_c written in place of the logits, the selection by repeated warp argmax
-// (ties go to the lower cube id), and the ascending index list.
+// One warp per query cube: softmax statistics of its logits row, its row of
+// A_c as a tf32 pair (ach, acl; row stride ldc), the selection by repeated
+// warp argmax (ties go to the lower cube id), and the ascending index list.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs sa, int rows_per_cta,
-                                                             float* __restrict__ logits,
+                                                             const float* __restrict__ logits,
+                                                             float* __restrict__ ach,
+                                                             float* __restrict__ acl, int ldc,
                                                              float* __restrict__ lse_c,
                                                              int* __restrict__ idx,
                                                              int* __restrict__ cnt) {
@@ -205,7 +64,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs 
   if (warp >= rows_per_cta || row >= Nc) return;
   float* Lsm = sel_smem + static_cast<size_t>(warp) * (Nc + g.cap);
   int* S = reinterpret_cast<int*>(Lsm + Nc);
-  float* Lg = logits + (static_cast<size_t>(bh) * Nc + row) * Nc;
+  const float* Lg = logits + (static_cast<size_t>(bh) * Nc + row) * Nc;
+  const size_t arow = (static_cast<size_t>(bh) * Nc + row) * ldc;
   float m = -FLT_MAX;
   for (int j = lane; j < Nc; j += 32) {
     const float v = Lg[j];
@@ -219,7 +79,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs 
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
   const float inv = 1.f / z;
-  for (int j = lane; j < Nc; j += 32) Lg[j] = expf(Lsm[j] - m) * inv;  // A_c row
+  for (int j = lane; j < Nc; j += 32) {  // A_c row
+    const float p = expf(Lsm[j] - m) * inv;
+    const float h = round_tf32(p);
+    ach[arow + j] = h;
+    acl[arow + j] = round_tf32(p - h);
+  }
   if (lane == 0) lse_c[static_cast<size_t>(bh) * Nc + row] = m + logf(z);
   __syncwarp();
 
@@ -275,16 +140,20 @@ __global__ void rowdot_kernel(int rows, int D, const float* __restrict__ a,
   if (lane == 0) out[row] = s;
 }
 
-GemmArgs gemm_args(const Geom& g, int M, int N, int K, const float* A, long long lda, long long sA,
-                   const float* B, long long ldb, long long sB, float* C, long long ldc,
-                   long long sC, float alpha) {
-  GemmArgs a{};
-  a.M = M; a.N = N; a.K = K;
-  a.A = A; a.lda = lda; a.strideA = sA;
-  a.B = B; a.ldb = ldb; a.strideB = sB;
-  a.C = C; a.ldc = ldc; a.strideC = sC;
+int ldc_of(const Geom& g) { return (g.Nc + 3) & ~3; }
+
+TgemmOperand pair(const float* hi, const float* lo, int ld, long long stride) {
+  return TgemmOperand{hi, lo, ld, stride};
+}
+
+TgemmArgs gemm(const Geom& g, int M, int N, int K, float alpha) {
+  TgemmArgs a{};
+  a.batch = g.BH;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.mode = kTgScale;
   a.alpha = alpha;
-  (void)g;
   return a;
 }
 
@@ -292,15 +161,26 @@ GemmArgs gemm_args(const Geom& g, int M, int N, int K, const float* A, long long
 
 cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
                                  int kmax, const float* qc, const float* kc, const float* vc,
-                                 float* logits, float* oc, float* lse_c, int* idx, int* cnt,
+                                 float* oc, float* lse_c, int* idx, int* cnt, const Workspace& ws,
                                  cudaStream_t s) {
-  const long long Nc = g.Nc, D = g.D, NN = Nc * Nc, ND = Nc * D;
+  const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
+  const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
+  const long long DC = static_cast<long long>(D) * ldc, NN = static_cast<long long>(Nc) * Nc;
   cudaError_t e;
-  // L = scale * Q_c K_c^T
-  GemmArgs a = gemm_args(g, g.Nc, g.Nc, g.D, qc, D, ND, kc, D, ND, logits, Nc, NN, g.scale);
-  if ((e = sgemm<false, true, kEpiStore>(a, g.BH, s)) != cudaSuccess) return e;
-  // softmax, selection and index lists; A_c replaces the logits
-  const size_t per_row = sizeof(float) * (static_cast<size_t>(g.Nc) + g.cap);
+  // operand pairs: Q_c, K_c ([Nc, D]) and V_c^T ([D, Nc])
+  if ((e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qh, ws.ql, D, ND, false, s)) ||
+      (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kh, ws.kl, D, ND, false, s)) ||
+      (e = launch_split_tf32(vc, D, ND, Nc, D, g.BH, ws.vth, ws.vtl, ldc, DC, true, s)))
+    return e;
+  // L = scale Q_c K_c^T
+  TgemmArgs a = gemm(g, Nc, Nc, D, g.scale);
+  a.out = ws.clogit;
+  a.out_ld = Nc;
+  a.out_stride = NN;
+  if ((e = launch_tgemm(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND), ws.status, s)))
+    return e;
+  // softmax, selection and index lists; A_c as a pair
+  const size_t per_row = sizeof(float) * (static_cast<size_t>(Nc) + g.cap);
   int rows = static_cast<int>((160 * 1024) / per_row);
   rows = rows < 1 ? 1 : (rows > 8 ? 8 : rows);
   const size_t smem = per_row * rows;
@@ -308,45 +188,90 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
                                 static_cast<int>(smem))) != cudaSuccess)
     return e;
   SelectArgs sa{mode, topk, kmin, kmax, mass};
-  select_kernel<<<dim3((g.Nc + rows - 1) / rows, g.BH), kSelThreads, smem, s>>>(
-      g, sa, rows, logits, lse_c, idx, cnt);
+  select_kernel<<<dim3((Nc + rows - 1) / rows, g.BH), kSelThreads, smem, s>>>(
+      g, sa, rows, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // O_c = A_c V_c
-  a = gemm_args(g, g.Nc, g.D, g.Nc, logits, Nc, NN, vc, D, ND, oc, D, ND, 1.f);
-  return sgemm<false, false, kEpiStore>(a, g.BH, s);
+  a = gemm(g, Nc, D, Nc, 1.f);
+  a.out = oc;
+  a.out_ld = D;
+  a.out_stride = ND;
+  return launch_tgemm(a, pair(ws.ach, ws.acl, ldc, NC), pair(ws.vth, ws.vtl, ldc, DC), ws.status,
+                      s);
 }
 
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
                               const float* oc, const float* lse_c, const float* doc,
                               float* dqc, float* dkc, float* dvc, const Workspace& ws,
                               cudaStream_t s) {
-  const long long Nc = g.Nc, D = g.D, NN = Nc * Nc, ND = Nc * D;
+  const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
+  const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
+  const long long DC = static_cast<long long>(D) * ldc, NN = static_cast<long long>(Nc) * Nc;
   cudaError_t e;
-  const int rows = g.BH * g.Nc;
-  rowdot_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, g.D, doc, oc, ws.cdelta);
+  const int rows = g.BH * Nc;
+  rowdot_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, D, doc, oc, ws.cdelta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // A_c = exp(scale Q_c K_c^T - lse_c)
-  GemmArgs a = gemm_args(g, g.Nc, g.Nc, g.D, qc, D, ND, kc, D, ND, ws.cprob, Nc, NN, g.scale);
-  a.rowvec = lse_c;
-  a.strideRow = Nc;
-  if ((e = sgemm<false, true, kEpiExpLse>(a, g.BH, s)) != cudaSuccess) return e;
-  // dL = A_c (.) (dO_c V_c^T - delta_c)
-  a = gemm_args(g, g.Nc, g.Nc, g.D, doc, D, ND, vc, D, ND, ws.cgrad, Nc, NN, 1.f);
-  a.rowvec = ws.cdelta;
-  a.strideRow = Nc;
-  a.P = ws.cprob;
-  a.ldp = Nc;
-  a.strideP = NN;
-  if ((e = sgemm<false, true, kEpiDLogit>(a, g.BH, s)) != cudaSuccess) return e;
+  // operand pairs, both orientations where a product contracts over cubes
+  if ((e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qh, ws.ql, D, ND, false, s)) ||
+      (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kh, ws.kl, D, ND, false, s)) ||
+      (e = launch_split_tf32(vc, D, ND, Nc, D, g.BH, ws.vh, ws.vl, D, ND, false, s)) ||
+      (e = launch_split_tf32(doc, D, ND, Nc, D, g.BH, ws.doh, ws.dol, D, ND, false, s)) ||
+      (e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qth, ws.qtl, ldc, DC, true, s)) ||
+      (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kth, ws.ktl, ldc, DC, true, s)) ||
+      (e = launch_split_tf32(doc, D, ND, Nc, D, g.BH, ws.doth, ws.dotl, ldc, DC, true, s)))
+    return e;
+  // P = exp(scale Q_c K_c^T - lse_c): fp32 P for dL, and P^T as a pair for dV_c
+  constexpr float kLog2e = 1.4426950408889634f;
+  TgemmArgs a = gemm(g, Nc, Nc, D, g.scale * kLog2e);
+  a.mode = kTgExpRow;
+  a.beta = kLog2e;
+  a.rowv = lse_c;
+  a.rowv_stride = Nc;
+  a.out = ws.clogit;
+  a.out_ld = Nc;
+  a.out_stride = NN;
+  a.outt_hi = ws.pth;
+  a.outt_lo = ws.ptl;
+  a.splitt_ld = ldc;
+  a.splitt_stride = NC;
+  if ((e = launch_tgemm(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND), ws.status, s)))
+    return e;
+  // dL = P (.) (dO_c V_c^T - delta_c), as pairs in both orientations
+  a = gemm(g, Nc, Nc, D, 1.f);
+  a.mode = kTgDLogitRow;
+  a.rowv = ws.cdelta;
+  a.rowv_stride = Nc;
+  a.pin = ws.clogit;
+  a.pin_ld = Nc;
+  a.pin_stride = NN;
+  a.out_hi = ws.ach;
+  a.out_lo = ws.acl;
+  a.split_ld = ldc;
+  a.split_stride = NC;
+  a.outt_hi = ws.dlth;
+  a.outt_lo = ws.dltl;
+  a.splitt_ld = ldc;
+  a.splitt_stride = NC;
+  if ((e = launch_tgemm(a, pair(ws.doh, ws.dol, D, ND), pair(ws.vh, ws.vl, D, ND), ws.status, s)))
+    return e;
   // dQ_c = scale dL K_c
-  a = gemm_args(g, g.Nc, g.D, g.Nc, ws.cgrad, Nc, NN, kc, D, ND, dqc, D, ND, g.scale);
-  if ((e = sgemm<false, false, kEpiStore>(a, g.BH, s)) != cudaSuccess) return e;
+  a = gemm(g, Nc, D, Nc, g.scale);
+  a.out = dqc;
+  a.out_ld = D;
+  a.out_stride = ND;
+  if ((e = launch_tgemm(a, pair(ws.ach, ws.acl, ldc, NC), pair(ws.kth, ws.ktl, ldc, DC),
+                        ws.status, s)))
+    return e;
   // dK_c = scale dL^T Q_c
-  a = gemm_args(g, g.Nc, g.D, g.Nc, ws.cgrad, Nc, NN, qc, D, ND, dkc, D, ND, g.scale);
-  if ((e = sgemm<true, false, kEpiStore>(a, g.BH, s)) != cudaSuccess) return e;
-  // dV_c = A_c^T dO_c
-  a = gemm_args(g, g.Nc, g.D, g.Nc, ws.cprob, Nc, NN, doc, D, ND, dvc, D, ND, 1.f);
-  return sgemm<true, false, kEpiStore>(a, g.BH, s);
+  a.out = dkc;
+  if ((e = launch_tgemm(a, pair(ws.dlth, ws.dltl, ldc, NC), pair(ws.qth, ws.qtl, ldc, DC),
+                        ws.status, s)))
+    return e;
+  // dV_c = P^T dO_c
+  a.alpha = 1.f;
+  a.out = dvc;
+  return launch_tgemm(a, pair(ws.pth, ws.ptl, ldc, NC), pair(ws.doth, ws.dotl, ldc, DC),
+                      ws.status, s);
 }
 
 }  // namespace vsa

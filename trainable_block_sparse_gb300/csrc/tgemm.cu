@@ -1,0 +1,362 @@
+// fp32-accurate batched GEMM on the tensor cores, for the coarse stage of VSA
+// ("VSA: Faster Video Diffusion with Trainable Sparse Attention", §2 "Coarse
+// stage": attention among the mean-pooled cubes, its softmax and, for
+// training, its gradients).  The coarse logits decide which blocks the fine
+// stage attends to, so they need fp32 accuracy: a single tf32 or bf16 product
+// would move them by ~1e-3.  Each fp32 operand x is split into two tf32 values
+// x = hi + lo (hi = round(x), lo = round(x - hi), |x - hi - lo| <= 2^-22 |x|)
+// and a.b is accumulated as lo_a.hi_b + hi_a.lo_b + hi_a.hi_b; the dropped
+// lo_a.lo_b term is below 2^-22 |a b|, comparable to fp32 rounding.
+//
+// D[b] = A[b] B[b]^T (A [M x K], B [N x K], both K-major), 128 x 128 output
+// tiles, k-blocks of 32 (one 128-byte swizzled row per operand row).
+// Persistent, one CTA per SM, six warps:
+//   warp 0    TMA: the four operand tiles of each k-block (A hi, A lo, B hi,
+//             B lo; zero-filled outside the matrices) into a 3-stage ring;
+//   warp 1    UMMA: 12 kind::tf32 products per k-block into one of two TMEM
+//             accumulators (the epilogue of tile i overlaps tile i+1);
+//   warps 2-5 epilogue: one accumulator row per thread; row-major outputs go
+//             through a padded shared-memory transpose so each warp writes
+//             whole 128-byte row segments; transposed outputs are already
+//             coalesced from that layout.
+// Every mbarrier wait is bounded; a time-out sets the status word and the CTA
+// unwinds as the fine kernels do.
+#include "umma_pipe.cuh"
+#include "vsa_common.cuh"
+
+namespace vsa {
+namespace {
+
+constexpr int kTgThreads = 192;
+constexpr int kTgStages = 3;
+constexpr int kTM = 128, kTN = 128, kTK = 32;
+constexpr int kOpBytes = kTM * kTK * 4;            // one 128 x 32 fp32 operand tile
+constexpr int kStageBytes = 4 * kOpBytes;          // A hi, A lo, B hi, B lo
+constexpr int kPad = 33;                           // padded 32 x 32 transpose tile
+constexpr int kEpiBytes = 4 * 32 * kPad * 4;
+constexpr int kTgSmem = kTgStages * kStageBytes + kEpiBytes + 1024;
+constexpr uint32_t kTgTmemCols = 256;              // two 128-column accumulators
+
+struct TgBars {
+  uint64_t full[kTgStages], empty[kTgStages];
+  uint64_t acc_full[2], acc_free[2];
+  uint64_t final_mma;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// 12 products of one k-block: 4 k-steps of K = 8 (32 bytes of each swizzled
+// row), each lo_a.hi_b + hi_a.lo_b + hi_a.hi_b; one elected lane issues all.
+__device__ __forceinline__ void issue_kblock_tf32(uint32_t d, uint64_t ah, uint64_t al,
+                                                  uint64_t bh, uint64_t bl, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b64 ah, al, bh, bl;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %6, 0;\n\tsetp.eq.b32 t, %6, %6;\n\t"
+      "mov.b64 ah, %1;\n\tmov.b64 al, %2;\n\tmov.b64 bh, %3;\n\tmov.b64 bl, %4;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], al, bh, %5, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bl, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %5, t;\n\t"
+      "add.s64 ah, ah, 2;\n\tadd.s64 al, al, 2;\n\tadd.s64 bh, bh, 2;\n\tadd.s64 bl, bl, 2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], al, bh, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bl, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %5, t;\n\t"
+      "add.s64 ah, ah, 2;\n\tadd.s64 al, al, 2;\n\tadd.s64 bh, bh, 2;\n\tadd.s64 bl, bl, 2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], al, bh, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bl, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %5, t;\n\t"
+      "add.s64 ah, ah, 2;\n\tadd.s64 al, al, 2;\n\tadd.s64 bh, bh, 2;\n\tadd.s64 bl, bl, 2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], al, bh, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bl, %5, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %5, t;\n\t}" ::"r"(d),
+      "l"(ah), "l"(al), "l"(bh), "l"(bl), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+struct TileCoord {
+  int b, tm, tn;
+};
+
+__device__ __forceinline__ TileCoord tile_of(int t, int tiles_m, int tiles_n) {
+  TileCoord c;
+  c.tn = t % tiles_n;
+  c.tm = (t / tiles_n) % tiles_m;
+  c.b = t / (tiles_n * tiles_m);
+  return c;
+}
+
+__global__ void __launch_bounds__(kTgThreads, 1)
+    tgemm_kernel(const __grid_constant__ CUtensorMap tah, const __grid_constant__ CUtensorMap tal,
+                 const __grid_constant__ CUtensorMap tbh, const __grid_constant__ CUtensorMap tbl,
+                 TgemmArgs P, uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  float* epi_smem = reinterpret_cast<float*>(smem + kTgStages * kStageBytes);
+  __shared__ TgBars sb;
+  int* abort_flag = &sb.abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tiles_m = (P.M + kTM - 1) / kTM, tiles_n = (P.N + kTN - 1) / kTN;
+  const int ntiles = P.batch * tiles_m * tiles_n;
+  const int kblocks = (P.K + kTK - 1) / kTK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTgStages; ++i) {
+      mbar_init(&sb.full[i], 1);
+      mbar_init(&sb.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.acc_full[i], 1);
+      mbar_init(&sb.acc_free[i], 4);  // the four epilogue warps
+    }
+    mbar_init(&sb.final_mma, 1);
+    sb.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sb.tmem_base, kTgTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = sb.tmem_base;
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tah);
+      tma_prefetch_desc(&tal);
+      tma_prefetch_desc(&tbh);
+      tma_prefetch_desc(&tbl);
+      uint32_t n = 0;  // k-blocks issued
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok && !is_aborted(abort_flag); t += gridDim.x) {
+        const TileCoord c = tile_of(t, tiles_m, tiles_n);
+        for (int kb = 0; kb < kblocks; ++kb, ++n) {
+          const uint32_t slot = n % kTgStages;
+          if (n >= static_cast<uint32_t>(kTgStages) &&
+              !wait1(&sb.empty[slot], ((n / kTgStages) & 1) ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + slot * kStageBytes;
+          mbar_arrive_expect_tx(&sb.full[slot], kStageBytes);
+          tma_load_3d(st, &tah, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
+          tma_load_3d(st + kOpBytes, &tal, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
+          tma_load_3d(st + 2 * kOpBytes, &tbh, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
+          tma_load_3d(st + 3 * kOpBytes, &tbl, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
+        }
+      }
+      const uint32_t first = n > static_cast<uint32_t>(kTgStages) ? n - kTgStages : 0;
+      for (uint32_t i = first; i < n; ++i)
+        mbar_wait(&sb.full[i % kTgStages], (i / kTgStages) & 1, kWaitNs);
+    }
+  } else if (warp == 1) {
+    // ===================================================== UMMA issuer
+    const uint32_t idesc = idesc_tf32(kTM, kTN);
+    const uint64_t d0 = sdesc_sw128(smem_u32(smem), 16, 1024);
+    uint32_t n = 0;
+    int lt = 0;  // tiles of this CTA
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok && !is_aborted(abort_flag); t += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      if (lt >= 2 && !waitw(&sb.acc_free[buf], ((lt >> 1) - 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+      const uint32_t dt = tb + buf * kTN;
+      for (int kb = 0; kb < kblocks; ++kb, ++n) {
+        const uint32_t slot = n % kTgStages;
+        if (!waitw(&sb.full[slot], (n / kTgStages) & 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t base = d0 + ((slot * kStageBytes) >> 4);
+        issue_kblock_tf32(dt, base, base + (kOpBytes >> 4), base + ((2 * kOpBytes) >> 4),
+                          base + ((3 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
+        commit_elect(&sb.empty[slot]);
+      }
+      if (!ok) break;
+      commit_elect(&sb.acc_full[buf]);
+    }
+    commit_elect(&sb.final_mma);
+    mbar_wait(&sb.final_mma, 0, kWaitNs);
+  } else {
+    // ===================================================== epilogue
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    float* tr = epi_smem + quarter * 32 * kPad;  // this warp's 32 x 33 transpose tile
+    int lt = 0;
+    for (int t = blockIdx.x; t < ntiles && !is_aborted(abort_flag); t += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      const TileCoord c = tile_of(t, tiles_m, tiles_n);
+      const int mbase = c.tm * kTM + quarter * 32;
+      const int m = mbase + lane;
+      const bool mlive = m < P.M;
+      float rv = 0.f;
+      if (P.mode != kTgScale && mlive) rv = P.rowv[c.b * P.rowv_stride + m];
+      if (!waitw(&sb.acc_full[buf], (lt >> 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int ch = 0; ch < kTN / 32; ++ch) {
+        const int n0 = c.tn * kTN + 32 * ch;
+        if (n0 >= P.N) break;
+        uint32_t v[32];
+        tmem_ld32(tb + lane_addr + buf * kTN + 32 * ch, v);
+        tmem_wait_ld();
+        float pv[32];
+        if (P.mode == kTgDLogitRow) {
+          // this warp's 32 x 32 block of pin, row by row (each load a 128-byte
+          // segment), 16 loads in flight at a time
+          const float* src = P.pin + c.b * P.pin_stride;
+#pragma unroll
+          for (int r0 = 0; r0 < 32; r0 += 16) {
+            float pr[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              const int mr = mbase + r0 + r;
+              pr[r] = (mr < P.M && n0 + lane < P.N)
+                          ? __ldg(src + static_cast<size_t>(mr) * P.pin_ld + n0 + lane)
+                          : 0.f;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) tr[(r0 + r) * kPad + lane] = pr[r];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pv[j] = tr[lane * kPad + j];
+          __syncwarp();
+        }
+        float val[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float a = __uint_as_float(v[j]);
+          if (P.mode == kTgScale) {
+            val[j] = P.alpha * a;
+          } else if (P.mode == kTgExpRow) {
+            val[j] = ex2_approx(fmaf(P.alpha, a, -P.beta * rv));
+          } else {
+            val[j] = pv[j] * fmaf(P.alpha, a, -rv);
+          }
+        }
+        const int ncols = min(32, P.N - n0);
+        // row-major outputs through the transpose tile: each warp store is a
+        // 128-byte segment of one row
+        auto store_rows = [&](float* dst, int ld, long long stride, auto f) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tr[lane * kPad + j] = f(val[j]);
+          __syncwarp();
+          float* base = dst + c.b * stride;
+          for (int r = 0; r < 32; ++r) {
+            const int mr = mbase + r;
+            if (mr < P.M && lane < ncols)
+              base[static_cast<size_t>(mr) * ld + n0 + lane] = tr[r * kPad + lane];
+          }
+          __syncwarp();
+        };
+        if (P.out) store_rows(P.out, P.out_ld, P.out_stride, [](float x) { return x; });
+        if (P.out_hi) {
+          store_rows(P.out_hi, P.split_ld, P.split_stride, [](float x) { return round_tf32(x); });
+          store_rows(P.out_lo, P.split_ld, P.split_stride,
+                     [](float x) { return round_tf32(x - round_tf32(x)); });
+        }
+        if (P.outt_hi && mlive) {
+          // transposed: for each column, the warp's 32 rows are 32 consecutive floats
+          float* th = P.outt_hi + c.b * P.splitt_stride;
+          float* tl = P.outt_lo + c.b * P.splitt_stride;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < ncols) {
+              const float h = round_tf32(val[j]);
+              const size_t o = static_cast<size_t>(n0 + j) * P.splitt_ld + m;
+              th[o] = h;
+              tl[o] = round_tf32(val[j] - h);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.acc_free[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tb, kTgTmemCols);
+}
+
+__global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ src, int ld_src,
+                                                    long long stride_src, int rows, int cols,
+                                                    float* __restrict__ hi, float* __restrict__ lo,
+                                                    int ld_dst, long long stride_dst,
+                                                    int transpose) {
+  __shared__ float t[32][33];
+  const int b = blockIdx.z, r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const float* s = src + b * stride_src;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int rr = r0 + r, cc = c0 + threadIdx.x;
+    t[r][threadIdx.x] = (rr < rows && cc < cols) ? s[static_cast<size_t>(rr) * ld_src + cc] : 0.f;
+  }
+  __syncthreads();
+  float* h = hi + b * stride_dst;
+  float* l = lo + b * stride_dst;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    if (!transpose) {
+      const int rr = r0 + r, cc = c0 + threadIdx.x;
+      if (rr < rows && cc < cols) {
+        const float x = t[r][threadIdx.x];
+        const float xh = round_tf32(x);
+        h[static_cast<size_t>(rr) * ld_dst + cc] = xh;
+        l[static_cast<size_t>(rr) * ld_dst + cc] = round_tf32(x - xh);
+      }
+    } else {
+      const int cc = c0 + r, rr = r0 + threadIdx.x;  // output row = input column
+      if (rr < rows && cc < cols) {
+        const float x = t[threadIdx.x][r];
+        const float xh = round_tf32(x);
+        h[static_cast<size_t>(cc) * ld_dst + rr] = xh;
+        l[static_cast<size_t>(cc) * ld_dst + rr] = round_tf32(x - xh);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
+                         uint32_t* status, cudaStream_t s) {
+  if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
+  if ((A.ld & 3) || (B.ld & 3) || (A.stride & 3) || (B.stride & 3)) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap mah, mal, mbh, mbl;
+  if (!encode_tiled_3d_f32(&mah, A.hi, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) ||
+      !encode_tiled_3d_f32(&mal, A.lo, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) ||
+      !encode_tiled_3d_f32(&mbh, B.hi, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN) ||
+      !encode_tiled_3d_f32(&mbl, B.lo, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN))
+    return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTgSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long ntiles = static_cast<long long>(a.batch) * ((a.M + kTM - 1) / kTM) *
+                           ((a.N + kTN - 1) / kTN);
+  const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
+  tgemm_kernel<<<grid, kTgThreads, kTgSmem, s>>>(mah, mal, mbh, mbl, a, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_tf32(const float* src, int ld_src, long long stride_src, int rows,
+                              int cols, int batch, float* hi, float* lo, int ld_dst,
+                              long long stride_dst, bool transpose, cudaStream_t s) {
+  if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
+  const dim3 grid((cols + 31) / 32, (rows + 31) / 32, batch);
+  split_kernel<<<grid, dim3(32, 8), 0, s>>>(src, ld_src, stride_src, rows, cols, hi, lo, ld_dst,
+                                            stride_dst, transpose ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace vsa

@@ -65,14 +65,20 @@ struct Workspace {
   PairItem* qpairs;       // query-cube pairs
   uint32_t* qlist;        // [n_qpairs][2*cap] union lists
   int n_qpairs;
-  float* clogit;          // fp32 [BH, Nc, Nc] coarse logits, then A_c (forward)
+  float* clogit;          // fp32 [BH, Nc, Nc] coarse logits (fwd); probabilities P (bwd)
+  // tf32 hi/lo pairs of the coarse GEMM operands (x = hi + lo); "c" arrays are
+  // [BH, Nc, ldc] or [BH, D, ldc] with ldc = Nc rounded up to 4, the others [BH, Nc, D]
+  float *qh, *ql, *kh, *kl;        // Q_c, K_c
+  float *vth, *vtl;                // V_c^T [D, ldc]
+  float *ach, *acl;                // A_c (fwd), dL (bwd)   [Nc, ldc]
+  float *vh, *vl, *doh, *dol;      // V_c, dO_c (bwd)
+  float *kth, *ktl, *qth, *qtl, *doth, *dotl;  // K_c^T, Q_c^T, dO_c^T (bwd) [D, ldc]
+  float *pth, *ptl, *dlth, *dltl;  // P^T, dL^T (bwd) [Nc, ldc]
   // backward
   void* dof;              // bf16 cube order
   float* delta;           // fp32 [BH, N]
   float* doc;             // fp32 [BH, Nc, D]
   float* dqc; float* dkc; float* dvc;
-  float* cprob;           // fp32 [BH, Nc, Nc]  coarse probabilities
-  float* cgrad;           // fp32 [BH, Nc, Nc]  coarse logit gradients
   float* cdelta;          // fp32 [BH, Nc]      rowsum(dO_c (.) O_c)
   uint32_t* tmask;        // [BH, Nc, ceil(Nc/32)] selection bit matrix
   int* toff;              // [BH, Nc + 1] offsets of transposed lists
@@ -93,7 +99,7 @@ cudaError_t launch_stage(const Geom& g, const __nv_bfloat16* in, int in_raster, 
                          float* pooled, uint32_t* status, cudaStream_t s);
 cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
                                  int kmax, const float* qc, const float* kc, const float* vc,
-                                 float* logits, float* oc, float* lse_c, int* idx, int* cnt,
+                                 float* oc, float* lse_c, int* idx, int* cnt, const Workspace& ws,
                                  cudaStream_t s);
 cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
@@ -116,6 +122,44 @@ cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, con
                             const float* lse_f, const __half* dof, const float* delta,
                             const float* dqc, const float* dkc, const float* dvc, float* dq,
                             float* dk, float* dv, const Workspace& ws, cudaStream_t s);
+
+// ------------------------------------------------ tensor-core fp32 GEMM
+// D[b] = A[b] B[b]^T, A [M x K], B [N x K], both K-major, each passed as a
+// tf32 pair hi + lo (fp32 arrays of tf32 values; hi = round(x), lo = round(x -
+// hi)), accumulated in fp32 from three tf32 products (tgemm.cu).
+enum TgemmMode { kTgScale = 0, kTgExpRow = 1, kTgDLogitRow = 2 };
+struct TgemmOperand {
+  const float* hi;
+  const float* lo;
+  int ld;                 // elements between rows (multiple of 4)
+  long long stride;       // elements between batches
+};
+struct TgemmArgs {
+  int batch, M, N, K;
+  int mode;
+  // kTgScale:     v = alpha * acc
+  // kTgExpRow:    v = exp2(alpha * acc - beta * rowv[m])
+  // kTgDLogitRow: v = pin[m][n] * (alpha * acc - rowv[m])
+  float alpha, beta;
+  const float* rowv; long long rowv_stride;
+  const float* pin; int pin_ld; long long pin_stride;
+  // outputs, each optional: fp32 [M][N]; tf32 pair [M][N]; tf32 pair transposed [N][M]
+  float* out; int out_ld; long long out_stride;
+  float *out_hi, *out_lo; int split_ld; long long split_stride;
+  float *outt_hi, *outt_lo; int splitt_ld; long long splitt_stride;
+};
+cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
+                         uint32_t* status, cudaStream_t s);
+// fp32 [batch][rows][cols] (row stride ld_src) -> tf32 pair, same orientation
+// or transposed ([batch][cols][rows]), row stride ld_dst.
+cudaError_t launch_split_tf32(const float* src, int ld_src, long long stride_src, int rows,
+                              int cols, int batch, float* hi, float* lo, int ld_dst,
+                              long long stride_dst, bool transpose, cudaStream_t s);
+// Rank-3 tiled tensor map over fp32 [batch][rows][ld] with a box of
+// (box_cols, box_rows, 1), 128-byte swizzle (api.cu).
+bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t rows,
+                         uint64_t cols, uint64_t ld, uint64_t batch_stride, uint32_t box_cols,
+                         uint32_t box_rows);
 
 // Driver entry point for tensor-map encoding, resolved once (api.cu).
 bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
