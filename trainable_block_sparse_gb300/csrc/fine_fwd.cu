@@ -37,6 +37,7 @@
 // the CTA unwinds, waits for its own in-flight copies and MMAs, frees TMEM and
 // exits.
 #include <cfloat>
+#include <cstring>
 
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
@@ -71,9 +72,12 @@ struct FwdSmem {
   static constexpr int kQBytes = kChunks * kChunkBytes;
   static constexpr int kKVBytes = kChunks * kChunkBytes;  // 2 key tiles
   static constexpr int kStagesK = (D == 128) ? 3 : 6;
-  static constexpr int kStagesV = (D == 128) ? 2 : 6;
+  static constexpr int kStagesV = (D == 128) ? 2 : 5;
   static constexpr int kTileBytes = 64 * D * 2;       // one 64-row tile
-  static constexpr int kBytes = kQBytes + (kStagesK + kStagesV) * kKVBytes + 1024;
+  // epilogue staging of one 32-column chunk of O_f: 128 rows x 128 bytes
+  static constexpr int kStageOff = kQBytes + (kStagesK + kStagesV) * kKVBytes;
+  static constexpr int kStageBytes = 128 * 128;
+  static constexpr int kBytes = kStageOff + kStageBytes + 1024;
 };
 
 struct FwdBars {
@@ -110,6 +114,21 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// Named barrier over the four epilogue warps, returning the OR of `fail`
+// over them (the warps leave an item loop together; see pair_sync_or).
+__device__ __forceinline__ bool epi_sync_or(bool fail) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 5, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(fail))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 5, 128;" ::: "memory"); }
+
 // Named barrier over the two softmax warps that share a TMEM lane quarter,
 // returning the OR of `fail` over both warps, so the pair always takes the
 // same branch after it (a warp that left alone would strand its partner at the
@@ -128,7 +147,8 @@ __device__ __forceinline__ bool pair_sync_or(int quarter, bool fail) {
 template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, FwdParams P) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tof,
+                    FwdParams P) {
   using L = FwdSmem<D>;
   constexpr int kSK = L::kStagesK, kSV = L::kStagesV;
   constexpr int kKSteps = D / 16;
@@ -138,6 +158,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + L::kQBytes;
   uint8_t* sV = sK + kSK * L::kKVBytes;
+  uint8_t* sStage = smem + L::kStageOff;  // epilogue staging of O_f
   __shared__ FwdBars sb;
   int* abort_flag = &sb.abort;
 
@@ -426,16 +447,22 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
   } else if (warp >= kWarpEpi && warp < kWarpEpi + kEpiWarps) {
     // ===================================================== epilogue
+    // O_f leaves through a shared-memory stage as TMA stores (whole lines);
+    // O (gated combine, caller layout) is written per row.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int half = row >> 6;                   // 0: first cube, 1: second cube
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool leader = threadIdx.x == kWarpEpi * 32;
+    const bool stage_of = P.o_f != nullptr;
     int it = 0;
-    for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
+    // No abort test in the loop condition: the four warps meet at named
+    // barriers and must walk the same items (see epi_sync_or).
+    for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
       const PairItem pi = P.items[item];
       if (pi.count == 0) continue;
       const int obuf = it & 1;
-      const bool live = half == 0 || pi.b >= 0;
+      const bool live = half == 0 || pi.b >= 0;  // warp-uniform
       const int cube = (half && pi.b >= 0) ? pi.b : pi.a;
       const int o_in = row & 63;
       const size_t crow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, o_in);
@@ -453,29 +480,48 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
       }
       if (lane < D / 32) prefetch_l2(ocr + 32 * lane);  // 4*D bytes of O_c: D/32 lines
-      if (!waitw(&sb.st_full[obuf], (it >> 1) & 1, abort_flag, P.status)) break;
-      const float l_sum = sb.l_part[obuf][0][row] + sb.l_part[obuf][1][row];
-      const float m_fin = sb.m_fin[obuf][row];
-      warp_arrive(&sb.st_free[obuf]);
-      if (!waitw(&sb.o_full[obuf], (it >> 1) & 1, abort_flag, P.status)) break;
+      bool got = waitw(&sb.st_full[obuf], (it >> 1) & 1, abort_flag, P.status);
+      float l_sum = 1.f, m_fin = 0.f;
+      if (got) {
+        l_sum = sb.l_part[obuf][0][row] + sb.l_part[obuf][1][row];
+        m_fin = sb.m_fin[obuf][row];
+        warp_arrive(&sb.st_free[obuf]);
+        got = waitw(&sb.o_full[obuf], (it >> 1) & 1, abort_flag, P.status);
+      }
+      if (epi_sync_or(!got)) break;
       tc_fence_after();
-      if (live) {
-        const float inv_l = 1.f / l_sum;
-        const uint32_t to = tb + lane_addr + kColO + obuf * 128;
+      const float inv_l = 1.f / l_sum;
+      const uint32_t to = tb + lane_addr + kColO + obuf * 128;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t ov[32];
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t ov[32];
+        if (live) {
           tmem_ld32(to + cc, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv_l);
-          if (P.o_f) {
-            float4* dst = reinterpret_cast<float4*>(P.o_f + frow * D + cc);
+        }
+        if (stage_of) {
+          // the previous chunk's stores have read the stage
+          if (leader) bulk_wait_group_read0();
+          epi_sync();
+          if (live) {
+            uint8_t* rp = sStage + row * 128;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                                   __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<float4*>(rp + ((u ^ (row & 7)) << 4)) =
+                  make_float4(__uint_as_float(ov[4 * u]), __uint_as_float(ov[4 * u + 1]),
+                              __uint_as_float(ov[4 * u + 2]), __uint_as_float(ov[4 * u + 3]));
           }
+          fence_proxy_async_smem();
+          epi_sync();
+          if (leader) {
+            tma_store_3d(&tof, sStage, cc, pi.bh * g.N + pi.a * kTile, 0);
+            if (pi.b >= 0) tma_store_3d(&tof, sStage + 64 * 128, cc, pi.bh * g.N + pi.b * kTile, 0);
+            bulk_commit_group();
+          }
+        }
+        if (live) {
           uint4* op = reinterpret_cast<uint4*>(P.o + crow * D + cc);
           const uint4* gcp = reinterpret_cast<const uint4*>(P.gc + crow * D + cc);
           const uint4* gfp = reinterpret_cast<const uint4*>(P.gf + crow * D + cc);
@@ -499,12 +545,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             op[v] = res;
           }
         }
-        if (P.lse_f) P.lse_f[frow] = (m_fin + __log2f(l_sum)) * 0.6931471805599453f;
       }
+      if (live && P.lse_f) P.lse_f[frow] = (m_fin + __log2f(l_sum)) * 0.6931471805599453f;
       tc_fence_before();
       warp_arrive(&sb.o_free[obuf]);
       ++it;
     }
+    if (leader) bulk_wait_group0();  // O_f stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -516,10 +563,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 template <int D>
 cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                     FwdParams p, cudaStream_t s) {
-  alignas(64) CUtensorMap mq, mk, mv;
+  alignas(64) CUtensorMap mq, mk, mv, mof;
   const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
   if (!encode_tiled_2d(&mq, q, rows, D, 64, 64) || !encode_tiled_2d(&mk, k, rows, D, 64, 64) ||
       !encode_tiled_2d(&mv, v, rows, D, 64, 64))
+    return cudaErrorInvalidValue;
+  // O_f (fp32, cube order): boxes of 64 rows (one cube) x 32 columns
+  memset(&mof, 0, sizeof(mof));
+  if (p.o_f && !encode_tiled_3d_f32(&mof, p.o_f, 1, rows, D, D, rows * D, 32, 64))
     return cudaErrorInvalidValue;
   const int smem = FwdSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D>,
@@ -530,7 +581,7 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = p.n_items < sms ? p.n_items : sms;
   if (grid <= 0) return cudaSuccess;
-  fine_fwd_kernel<D><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, p);
+  fine_fwd_kernel<D><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
 
