@@ -297,28 +297,32 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=3):
 
 
 def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
-    """Host inputs in, host outputs out, through the C ABI, every step."""
-    names = ("q", "k", "v", "gc", "gf", "do")
-    host_in = {n: getattr(inp, n).pin_memory() for n in names}
-    dev_in = {n: torch.empty_like(host_in[n], device=dev) for n in names}
+    """Host inputs in, host outputs out, every step, through the library's
+    host-buffer pipeline (HostPipeline: units of 5 heads, copies in and out
+    overlapped with the kernels of the neighbouring units)."""
+    from trainable_block_sparse_gb300.host_pipeline import HostPipeline, IN_NAMES, OUT_NAMES
+    del bufs  # the pipeline owns per-unit buffers
+    host_in = {n: getattr(inp, n).pin_memory() for n in IN_NAMES}
     B, H, N, D = wl.batch, wl.heads, wl.tokens, wl.head_dim
-    o = torch.empty(B, H, N, D, dtype=torch.bfloat16, device=dev)
-    grads = tuple(torch.empty(B, H, N, D, dtype=torch.float32, device=dev) for _ in range(5))
-    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, *grads)]
-
-    def step():
-        for n in names:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
-        vsa.forward(cfg, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["gc"], dev_in["gf"], bufs,
-                    True, out=o)
-        vsa.backward(cfg, dev_in["gc"], dev_in["gf"], dev_in["do"], bufs, grads)
-        for h, d in zip(host_out, (o, *grads)):
-            h.copy_(d, non_blocking=True)
-
-    ms = timed(step, max(2, args.steps // 3), 1, stream)
+    host_out = {n: torch.empty(B, H, N, D, dtype=torch.bfloat16 if n == "o" else torch.float32,
+                               pin_memory=True) for n in OUT_NAMES}
+    pipe = HostPipeline(cfg, dev, heads_per_unit=5)
+    reps = max(2, args.steps // 3)
+    for _ in range(2):  # warm-up: allocates the per-unit buffers
+        pipe.step(host_in, host_out)
+    if pipe.check_status() != vsa.OK:
+        raise RuntimeError("device status after the host-pipeline warm-up")
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        pipe.step(host_in, host_out)
+    torch.cuda.synchronize(dev)
+    ms = (time.perf_counter() - t0) * 1e3 / reps
+    if pipe.check_status() != vsa.OK:
+        raise RuntimeError("device status after the host-pipeline steps")
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-    d2h = sum(x.numel() * x.element_size() for x in host_out)
-    return {"ms": ms, "value": step_flops / (ms * 1e-3) / 1e12, "h2d": h2d, "d2h": d2h}
+    d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+    return {"ms": ms, "value": step_flops / (ms * 1e-3) / 1e12, "h2d": h2d, "d2h": d2h,
+            "units": sum(1 for _ in pipe.units())}
 
 
 def oracle_sample(inp, b, h, cubes):
@@ -498,7 +502,8 @@ def main():
         "clocks": r["clocks"],
         "e2e": {"value": world * r["e2e"]["value"], "unit": "TFLOPS",
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"],
-                "ms_per_step": r["e2e"]["ms"]},
+                "ms_per_step": r["e2e"]["ms"], "pipeline_units": r["e2e"]["units"],
+                "timer": "host clock between device synchronisations (three streams)"},
         "gpu_launches": (LAUNCHES_FWD + LAUNCHES_BWD) * args.steps,
         "load_balance": r["balance"],
     }
