@@ -110,9 +110,9 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.n_qpairs = npairs;
   ws.qpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
-  ws.clogit = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * g.Nc * 4));
-  // tf32 pairs of the coarse GEMM operands
+  // coarse logits [BH, Nc, ldc] and tf32 pairs of the coarse GEMM operands
   const size_t ldc = static_cast<size_t>((g.Nc + 3) & ~3);
+  ws.clogit = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * ldc * 4));
   const size_t pc_bytes = static_cast<size_t>(g.BH) * g.Nc * ldc * 4;  // [BH, Nc, ldc]
   const size_t dc_bytes = static_cast<size_t>(g.BH) * g.D * ldc * 4;   // [BH, D, ldc]
   auto f32 = [&](size_t bytes) { return static_cast<float*>(take(bytes)); };

@@ -16,9 +16,11 @@
 //                                                   (one kernel, warp per row;
 //                                                    A_c written as a pair)
 //             O_c = A_c V_c                         (GEMM)
-//   backward: P  = exp(scale Q_c K_c^T - lse)       (GEMM -> P fp32, P^T pair)
+//   backward: P  = exp(scale Q_c K_c^T - lse),
 //             dL = P (.) (dO_c V_c^T - rowsum(dO_c O_c))
-//                                                   (GEMM -> dL pair, dL^T pair)
+//                 (dual GEMM, query-major tiles -> dL pair; key-major tiles of
+//                  the transposed products -> dL^T and P^T pairs; P is never
+//                  stored in fp32)
 //             dQ_c = scale dL K_c, dK_c = scale dL^T Q_c, dV_c = P^T dO_c
 #include <cfloat>
 
@@ -47,8 +49,8 @@ struct SelectArgs {
   float mass;
 };
 
-// One warp per query cube: softmax statistics of its logits row, its row of
-// A_c as a tf32 pair (ach, acl; row stride ldc), the selection by repeated
+// One warp per query cube: softmax statistics of its logits row (row stride
+// ldc), its row of A_c as a tf32 pair (ach, acl; row stride ldc), the selection by repeated
 // warp argmax (ties go to the lower cube id), and the ascending index list.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs sa, int rows_per_cta,
                                                              const float* __restrict__ logits,
@@ -64,8 +66,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs 
   if (warp >= rows_per_cta || row >= Nc) return;
   float* Lsm = sel_smem + static_cast<size_t>(warp) * (Nc + g.cap);
   int* S = reinterpret_cast<int*>(Lsm + Nc);
-  const float* Lg = logits + (static_cast<size_t>(bh) * Nc + row) * Nc;
-  const size_t arow = (static_cast<size_t>(bh) * Nc + row) * ldc;
+  const size_t arow = (static_cast<size_t>(bh) * Nc + row) * ldc;  // logits and A_c rows
+  const float* Lg = logits + arow;
   float m = -FLT_MAX;
   for (int j = lane; j < Nc; j += 32) {
     const float v = Lg[j];
@@ -165,7 +167,7 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
                                  cudaStream_t s) {
   const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
   const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
-  const long long DC = static_cast<long long>(D) * ldc, NN = static_cast<long long>(Nc) * Nc;
+  const long long DC = static_cast<long long>(D) * ldc;
   cudaError_t e;
   // operand pairs: Q_c, K_c ([Nc, D]) and V_c^T ([D, Nc])
   if ((e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qh, ws.ql, D, ND, false, s)) ||
@@ -175,8 +177,8 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
   // L = scale Q_c K_c^T
   TgemmArgs a = gemm(g, Nc, Nc, D, g.scale);
   a.out = ws.clogit;
-  a.out_ld = Nc;
-  a.out_stride = NN;
+  a.out_ld = ldc;
+  a.out_stride = NC;
   if ((e = launch_tgemm(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND), ws.status, s)))
     return e;
   // softmax, selection and index lists; A_c as a pair
@@ -206,7 +208,7 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
                               cudaStream_t s) {
   const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
   const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
-  const long long DC = static_cast<long long>(D) * ldc, NN = static_cast<long long>(Nc) * Nc;
+  const long long DC = static_cast<long long>(D) * ldc;
   cudaError_t e;
   const int rows = g.BH * Nc;
   rowdot_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, D, doc, oc, ws.cdelta);
@@ -220,39 +222,33 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
       (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kth, ws.ktl, ldc, DC, true, s)) ||
       (e = launch_split_tf32(doc, D, ND, Nc, D, g.BH, ws.doth, ws.dotl, ldc, DC, true, s)))
     return e;
-  // P = exp(scale Q_c K_c^T - lse_c): fp32 P for dL, and P^T as a pair for dV_c
+  // query-major tiles: P = exp(scale Q_c K_c^T - lse) and dL = P (.) (dO_c V_c^T - delta)
+  // in registers from two accumulators; dL leaves as a pair
   constexpr float kLog2e = 1.4426950408889634f;
   TgemmArgs a = gemm(g, Nc, Nc, D, g.scale * kLog2e);
-  a.mode = kTgExpRow;
+  a.mode = kTgAttnBwdRow;
   a.beta = kLog2e;
-  a.rowv = lse_c;
-  a.rowv_stride = Nc;
-  a.out = ws.clogit;
-  a.out_ld = Nc;
-  a.out_stride = NN;
-  a.outt_hi = ws.pth;
-  a.outt_lo = ws.ptl;
-  a.splitt_ld = ldc;
-  a.splitt_stride = NC;
-  if ((e = launch_tgemm(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND), ws.status, s)))
-    return e;
-  // dL = P (.) (dO_c V_c^T - delta_c), as pairs in both orientations
-  a = gemm(g, Nc, Nc, D, 1.f);
-  a.mode = kTgDLogitRow;
-  a.rowv = ws.cdelta;
-  a.rowv_stride = Nc;
-  a.pin = ws.clogit;
-  a.pin_ld = Nc;
-  a.pin_stride = NN;
+  a.v1 = lse_c;
+  a.v2 = ws.cdelta;
+  a.vec_stride = Nc;
   a.out_hi = ws.ach;
   a.out_lo = ws.acl;
   a.split_ld = ldc;
   a.split_stride = NC;
-  a.outt_hi = ws.dlth;
-  a.outt_lo = ws.dltl;
-  a.splitt_ld = ldc;
-  a.splitt_stride = NC;
-  if ((e = launch_tgemm(a, pair(ws.doh, ws.dol, D, ND), pair(ws.vh, ws.vl, D, ND), ws.status, s)))
+  if ((e = launch_tgemm_dual(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND),
+                             pair(ws.doh, ws.dol, D, ND), pair(ws.vh, ws.vl, D, ND), ws.status,
+                             s)))
+    return e;
+  // key-major tiles of the same two products (the transposes): dL^T and P^T as pairs,
+  // lse and delta now per column
+  a.mode = kTgAttnBwdCol;
+  a.out_hi = ws.dlth;
+  a.out_lo = ws.dltl;
+  a.out2_hi = ws.pth;
+  a.out2_lo = ws.ptl;
+  if ((e = launch_tgemm_dual(a, pair(ws.kh, ws.kl, D, ND), pair(ws.qh, ws.ql, D, ND),
+                             pair(ws.vh, ws.vl, D, ND), pair(ws.doh, ws.dol, D, ND), ws.status,
+                             s)))
     return e;
   // dQ_c = scale dL K_c
   a = gemm(g, Nc, D, Nc, g.scale);

@@ -9,18 +9,23 @@
 // lo_a.lo_b term is below 2^-22 |a b|, comparable to fp32 rounding.
 //
 // D[b] = A[b] B[b]^T (A [M x K], B [N x K], both K-major), 128 x 128 output
-// tiles, k-blocks of 32 (one 128-byte swizzled row per operand row).
+// tiles, k-blocks of 32 (one 128-byte swizzled row per operand row).  The
+// dual form also computes E[b] = A2[b] B2[b]^T of the same tile into a second
+// accumulator, for epilogues that combine the two (the coarse attention
+// backward: P from the logits and dL = P (.) (dP - delta) from dP).
 // Persistent, one CTA per SM, six warps:
 //   warp 0    TMA: the four operand tiles of each k-block (A hi, A lo, B hi,
 //             B lo; zero-filled outside the matrices) into a 3-stage ring;
 //   warp 1    UMMA: 12 kind::tf32 products per k-block into one of two TMEM
 //             accumulators (the epilogue of tile i overlaps tile i+1);
-//   warps 2-5 epilogue: one accumulator row per thread; row-major outputs go
-//             through a padded shared-memory transpose so each warp writes
-//             whole 128-byte row segments; transposed outputs are already
-//             coalesced from that layout.
+//   warps 2-5 epilogue: one accumulator row per thread; each 32 x 32 block
+//             of an output is written into a 128-byte-swizzled shared-memory
+//             tile and leaves as one TMA store (rows and columns outside the
+//             matrix are clipped by the tensor map).
 // Every mbarrier wait is bounded; a time-out sets the status word and the CTA
 // unwinds as the fine kernels do.
+#include <cstring>
+
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
 
@@ -32,10 +37,9 @@ constexpr int kTgStages = 3;
 constexpr int kTM = 128, kTN = 128, kTK = 32;
 constexpr int kOpBytes = kTM * kTK * 4;            // one 128 x 32 fp32 operand tile
 constexpr int kStageBytes = 4 * kOpBytes;          // A hi, A lo, B hi, B lo
-constexpr int kPad = 33;                           // padded 32 x 32 transpose tile
-constexpr int kEpiBytes = 4 * 32 * kPad * 4;
-constexpr int kTgSmem = kTgStages * kStageBytes + kEpiBytes + 1024;
-constexpr uint32_t kTgTmemCols = 256;              // two 128-column accumulators
+constexpr int kBlockBytes = 32 * 32 * 4;           // one 32 x 32 fp32 output block
+constexpr int kEpiBytes = kBlockBytes + 2 * kTN * 4;  // per warp: staging block, column vectors
+constexpr int kTgSmem = kTgStages * kStageBytes + 4 * kEpiBytes + 1024;
 
 struct TgBars {
   uint64_t full[kTgStages], empty[kTgStages];
@@ -86,10 +90,22 @@ __device__ __forceinline__ TileCoord tile_of(int t, int tiles_m, int tiles_n) {
   return c;
 }
 
+struct TgMaps {
+  CUtensorMap ah, al, bh, bl;
+};
+
+// Output tensor maps (fp32 [batch][M][ld], box 32 x 32); unused ones stay zero.
+struct TgOutMaps {
+  CUtensorMap out, hi, lo, hi2, lo2;
+};
+
+template <bool kDual>
 __global__ void __launch_bounds__(kTgThreads, 1)
-    tgemm_kernel(const __grid_constant__ CUtensorMap tah, const __grid_constant__ CUtensorMap tal,
-                 const __grid_constant__ CUtensorMap tbh, const __grid_constant__ CUtensorMap tbl,
-                 TgemmArgs P, uint32_t* status) {
+    tgemm_kernel(const __grid_constant__ TgMaps m0, const __grid_constant__ TgMaps m1,
+                 const __grid_constant__ TgOutMaps om, TgemmArgs P, uint32_t* status) {
+  constexpr int kProducts = kDual ? 2 : 1;
+  constexpr uint32_t kAccCols = kTN * kProducts;     // per tile buffer
+  constexpr uint32_t kTmemCols = 2 * kAccCols;       // two tile buffers
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -115,7 +131,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sb.tmem_base, kTgTmemCols);
+    tmem_alloc(&sb.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -126,27 +142,30 @@ __global__ void __launch_bounds__(kTgThreads, 1)
   if (warp == 0) {
     // ===================================================== TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tah);
-      tma_prefetch_desc(&tal);
-      tma_prefetch_desc(&tbh);
-      tma_prefetch_desc(&tbl);
+      tma_prefetch_desc(&m0.ah);
+      tma_prefetch_desc(&m0.al);
+      tma_prefetch_desc(&m0.bh);
+      tma_prefetch_desc(&m0.bl);
       uint32_t n = 0;  // k-blocks issued
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok && !is_aborted(abort_flag); t += gridDim.x) {
         const TileCoord c = tile_of(t, tiles_m, tiles_n);
-        for (int kb = 0; kb < kblocks; ++kb, ++n) {
-          const uint32_t slot = n % kTgStages;
-          if (n >= static_cast<uint32_t>(kTgStages) &&
-              !wait1(&sb.empty[slot], ((n / kTgStages) & 1) ^ 1, abort_flag, status)) {
-            ok = false;
-            break;
+        for (int pr = 0; pr < kProducts && ok; ++pr) {
+          const TgMaps& m = pr ? m1 : m0;
+          for (int kb = 0; kb < kblocks; ++kb, ++n) {
+            const uint32_t slot = n % kTgStages;
+            if (n >= static_cast<uint32_t>(kTgStages) &&
+                !wait1(&sb.empty[slot], ((n / kTgStages) & 1) ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = smem + slot * kStageBytes;
+            mbar_arrive_expect_tx(&sb.full[slot], kStageBytes);
+            tma_load_3d(st, &m.ah, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
+            tma_load_3d(st + kOpBytes, &m.al, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
+            tma_load_3d(st + 2 * kOpBytes, &m.bh, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
+            tma_load_3d(st + 3 * kOpBytes, &m.bl, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
           }
-          uint8_t* st = smem + slot * kStageBytes;
-          mbar_arrive_expect_tx(&sb.full[slot], kStageBytes);
-          tma_load_3d(st, &tah, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
-          tma_load_3d(st + kOpBytes, &tal, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
-          tma_load_3d(st + 2 * kOpBytes, &tbh, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
-          tma_load_3d(st + 3 * kOpBytes, &tbl, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
         }
       }
       const uint32_t first = n > static_cast<uint32_t>(kTgStages) ? n - kTgStages : 0;
@@ -164,18 +183,20 @@ __global__ void __launch_bounds__(kTgThreads, 1)
       const int buf = lt & 1;
       if (lt >= 2 && !waitw(&sb.acc_free[buf], ((lt >> 1) - 1) & 1, abort_flag, status)) break;
       tc_fence_after();
-      const uint32_t dt = tb + buf * kTN;
-      for (int kb = 0; kb < kblocks; ++kb, ++n) {
-        const uint32_t slot = n % kTgStages;
-        if (!waitw(&sb.full[slot], (n / kTgStages) & 1, abort_flag, status)) {
-          ok = false;
-          break;
+      for (int pr = 0; pr < kProducts && ok; ++pr) {
+        const uint32_t dt = tb + buf * kAccCols + pr * kTN;
+        for (int kb = 0; kb < kblocks; ++kb, ++n) {
+          const uint32_t slot = n % kTgStages;
+          if (!waitw(&sb.full[slot], (n / kTgStages) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t base = d0 + ((slot * kStageBytes) >> 4);
+          issue_kblock_tf32(dt, base, base + (kOpBytes >> 4), base + ((2 * kOpBytes) >> 4),
+                            base + ((3 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
+          commit_elect(&sb.empty[slot]);
         }
-        tc_fence_after();
-        const uint64_t base = d0 + ((slot * kStageBytes) >> 4);
-        issue_kblock_tf32(dt, base, base + (kOpBytes >> 4), base + ((2 * kOpBytes) >> 4),
-                          base + ((3 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
-        commit_elect(&sb.empty[slot]);
       }
       if (!ok) break;
       commit_elect(&sb.acc_full[buf]);
@@ -186,94 +207,84 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     // ===================================================== epilogue
     const int quarter = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    float* tr = epi_smem + quarter * 32 * kPad;  // this warp's 32 x 33 transpose tile
+    uint8_t* blk = reinterpret_cast<uint8_t*>(epi_smem) + quarter * kEpiBytes;  // 1024-aligned
+    float* cvec = reinterpret_cast<float*>(blk + kBlockBytes);  // column vectors (col mode)
     int lt = 0;
     for (int t = blockIdx.x; t < ntiles && !is_aborted(abort_flag); t += gridDim.x, ++lt) {
       const int buf = lt & 1;
       const TileCoord c = tile_of(t, tiles_m, tiles_n);
       const int mbase = c.tm * kTM + quarter * 32;
       const int m = mbase + lane;
-      const bool mlive = m < P.M;
-      float rv = 0.f;
-      if (P.mode != kTgScale && mlive) rv = P.rowv[c.b * P.rowv_stride + m];
+      float r1 = 0.f, r2 = 0.f;
+      if (P.mode == kTgAttnBwdRow && m < P.M) {
+        r1 = P.v1[c.b * P.vec_stride + m];
+        r2 = P.v2[c.b * P.vec_stride + m];
+      }
+      if (P.mode == kTgAttnBwdCol) {
+#pragma unroll
+        for (int q = 0; q < kTN / 32; ++q) {
+          const int n = c.tn * kTN + 32 * q + lane;
+          cvec[32 * q + lane] = n < P.N ? P.v1[c.b * P.vec_stride + n] : 0.f;
+          cvec[kTN + 32 * q + lane] = n < P.N ? P.v2[c.b * P.vec_stride + n] : 0.f;
+        }
+        __syncwarp();
+      }
       if (!waitw(&sb.acc_full[buf], (lt >> 1) & 1, abort_flag, status)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int ch = 0; ch < kTN / 32; ++ch) {
         const int n0 = c.tn * kTN + 32 * ch;
         if (n0 >= P.N) break;
-        uint32_t v[32];
-        tmem_ld32(tb + lane_addr + buf * kTN + 32 * ch, v);
+        uint32_t v[32], e[32];
+        tmem_ld32(tb + lane_addr + buf * kAccCols + 32 * ch, v);
+        if (kDual) tmem_ld32(tb + lane_addr + buf * kAccCols + kTN + 32 * ch, e);
         tmem_wait_ld();
-        float pv[32];
-        if (P.mode == kTgDLogitRow) {
-          // this warp's 32 x 32 block of pin, row by row (each load a 128-byte
-          // segment), 16 loads in flight at a time
-          const float* src = P.pin + c.b * P.pin_stride;
-#pragma unroll
-          for (int r0 = 0; r0 < 32; r0 += 16) {
-            float pr[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              const int mr = mbase + r0 + r;
-              pr[r] = (mr < P.M && n0 + lane < P.N)
-                          ? __ldg(src + static_cast<size_t>(mr) * P.pin_ld + n0 + lane)
-                          : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) tr[(r0 + r) * kPad + lane] = pr[r];
-          }
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pv[j] = tr[lane * kPad + j];
-          __syncwarp();
-        }
-        float val[32];
+        float val[32], pv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float a = __uint_as_float(v[j]);
-          if (P.mode == kTgScale) {
+          if (!kDual || P.mode == kTgScale) {
             val[j] = P.alpha * a;
-          } else if (P.mode == kTgExpRow) {
-            val[j] = ex2_approx(fmaf(P.alpha, a, -P.beta * rv));
           } else {
-            val[j] = pv[j] * fmaf(P.alpha, a, -rv);
+            const bool col = P.mode == kTgAttnBwdCol;
+            const float l = col ? cvec[32 * ch + j] : r1;
+            const float d = col ? cvec[kTN + 32 * ch + j] : r2;
+            pv[j] = ex2_approx(fmaf(P.alpha, a, -P.beta * l));
+            val[j] = pv[j] * (__uint_as_float(e[j]) - d);
           }
         }
-        const int ncols = min(32, P.N - n0);
-        // row-major outputs through the transpose tile: each warp store is a
-        // 128-byte segment of one row
-        auto store_rows = [&](float* dst, int ld, long long stride, auto f) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) tr[lane * kPad + j] = f(val[j]);
+        // one output block: rows mbase.., columns n0.. through the staging block
+        auto store_block = [&](const CUtensorMap* map, const float (&src)[32], int part) {
+          if (lane == 0) bulk_wait_group_read0();  // the previous block has been read
           __syncwarp();
-          float* base = dst + c.b * stride;
-          for (int r = 0; r < 32; ++r) {
-            const int mr = mbase + r;
-            if (mr < P.M && lane < ncols)
-              base[static_cast<size_t>(mr) * ld + n0 + lane] = tr[r * kPad + lane];
-          }
-          __syncwarp();
-        };
-        if (P.out) store_rows(P.out, P.out_ld, P.out_stride, [](float x) { return x; });
-        if (P.out_hi) {
-          store_rows(P.out_hi, P.split_ld, P.split_stride, [](float x) { return round_tf32(x); });
-          store_rows(P.out_lo, P.split_ld, P.split_stride,
-                     [](float x) { return round_tf32(x - round_tf32(x)); });
-        }
-        if (P.outt_hi && mlive) {
-          // transposed: for each column, the warp's 32 rows are 32 consecutive floats
-          float* th = P.outt_hi + c.b * P.splitt_stride;
-          float* tl = P.outt_lo + c.b * P.splitt_stride;
+          uint8_t* rp = blk + lane * 128;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j < ncols) {
-              const float h = round_tf32(val[j]);
-              const size_t o = static_cast<size_t>(n0 + j) * P.splitt_ld + m;
-              th[o] = h;
-              tl[o] = round_tf32(val[j] - h);
+          for (int u = 0; u < 8; ++u) {
+            float q[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x = src[4 * u + e];
+              const float h = round_tf32(x);
+              q[e] = part == 0 ? x : (part == 1 ? h : round_tf32(x - h));
             }
+            *reinterpret_cast<float4*>(rp + ((u ^ (lane & 7)) << 4)) =
+                make_float4(q[0], q[1], q[2], q[3]);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(map, blk, n0, mbase, c.b);
+            bulk_commit_group();
+          }
+        };
+        if (P.out) store_block(&om.out, val, 0);
+        if (P.out_hi) {
+          store_block(&om.hi, val, 1);
+          store_block(&om.lo, val, 2);
+        }
+        if (kDual && P.out2_hi) {
+          store_block(&om.hi2, pv, 1);
+          store_block(&om.lo2, pv, 2);
         }
       }
       tc_fence_before();
@@ -282,10 +293,11 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     }
   }
 
+  if (warp >= 2 && lane == 0) bulk_wait_group0();  // output stores complete before exit
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tb, kTgTmemCols);
+  if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
 __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ src, int ld_src,
@@ -326,18 +338,37 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ sr
 
 }  // namespace
 
-cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
-                         uint32_t* status, cudaStream_t s) {
-  if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
-  if ((A.ld & 3) || (B.ld & 3) || (A.stride & 3) || (B.stride & 3)) return cudaErrorInvalidValue;
-  alignas(64) CUtensorMap mah, mal, mbh, mbl;
-  if (!encode_tiled_3d_f32(&mah, A.hi, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) ||
-      !encode_tiled_3d_f32(&mal, A.lo, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) ||
-      !encode_tiled_3d_f32(&mbh, B.hi, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN) ||
-      !encode_tiled_3d_f32(&mbl, B.lo, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN))
-    return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTgSmem);
+namespace {
+
+bool encode_maps(TgMaps* m, const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B) {
+  if ((A.ld & 3) || (B.ld & 3) || (A.stride & 3) || (B.stride & 3)) return false;
+  return encode_tiled_3d_f32(&m->ah, A.hi, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) &&
+         encode_tiled_3d_f32(&m->al, A.lo, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) &&
+         encode_tiled_3d_f32(&m->bh, B.hi, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN) &&
+         encode_tiled_3d_f32(&m->bl, B.lo, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN);
+}
+
+bool encode_outs(TgOutMaps* o, const TgemmArgs& a) {
+  memset(o, 0, sizeof(*o));
+  auto enc = [&](CUtensorMap* m, float* p, int ld, long long stride) {
+    if (!p) return true;
+    if ((ld & 3) || (stride & 3)) return false;
+    return encode_tiled_3d_f32(m, p, a.batch, a.M, a.N, ld, stride, 32, 32);
+  };
+  return enc(&o->out, a.out, a.out_ld, a.out_stride) &&
+         enc(&o->hi, a.out_hi, a.split_ld, a.split_stride) &&
+         enc(&o->lo, a.out_lo, a.split_ld, a.split_stride) &&
+         enc(&o->hi2, a.out2_hi, a.split_ld, a.split_stride) &&
+         enc(&o->lo2, a.out2_lo, a.split_ld, a.split_stride);
+}
+
+template <bool kDual>
+cudaError_t run_tgemm(const TgemmArgs& a, const TgMaps& m0, const TgMaps& m1, uint32_t* status,
+                      cudaStream_t s) {
+  alignas(64) TgOutMaps om;
+  if (!encode_outs(&om, a)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tgemm_kernel<kDual>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kTgSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -345,8 +376,29 @@ cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmO
   const long long ntiles = static_cast<long long>(a.batch) * ((a.M + kTM - 1) / kTM) *
                            ((a.N + kTN - 1) / kTN);
   const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-  tgemm_kernel<<<grid, kTgThreads, kTgSmem, s>>>(mah, mal, mbh, mbl, a, status);
+  tgemm_kernel<kDual><<<grid, kTgThreads, kTgSmem, s>>>(m0, m1, om, a, status);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
+                         uint32_t* status, cudaStream_t s) {
+  if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
+  if (a.mode != kTgScale) return cudaErrorInvalidValue;
+  alignas(64) TgMaps m0;
+  if (!encode_maps(&m0, a, A, B)) return cudaErrorInvalidValue;
+  return run_tgemm<false>(a, m0, m0, status, s);
+}
+
+cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
+                              const TgemmOperand& A2, const TgemmOperand& B2, uint32_t* status,
+                              cudaStream_t s) {
+  if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
+  if (a.mode != kTgAttnBwdRow && a.mode != kTgAttnBwdCol) return cudaErrorInvalidValue;
+  alignas(64) TgMaps m0, m1;
+  if (!encode_maps(&m0, a, A, B) || !encode_maps(&m1, a, A2, B2)) return cudaErrorInvalidValue;
+  return run_tgemm<true>(a, m0, m1, status, s);
 }
 
 cudaError_t launch_split_tf32(const float* src, int ld_src, long long stride_src, int rows,

@@ -65,7 +65,7 @@ struct Workspace {
   PairItem* qpairs;       // query-cube pairs
   uint32_t* qlist;        // [n_qpairs][2*cap] union lists
   int n_qpairs;
-  float* clogit;          // fp32 [BH, Nc, Nc] coarse logits (fwd); probabilities P (bwd)
+  float* clogit;          // fp32 [BH, Nc, Nc] coarse logits (forward)
   // tf32 hi/lo pairs of the coarse GEMM operands (x = hi + lo); "c" arrays are
   // [BH, Nc, ldc] or [BH, D, ldc] with ldc = Nc rounded up to 4, the others [BH, Nc, D]
   float *qh, *ql, *kh, *kl;        // Q_c, K_c
@@ -126,8 +126,14 @@ cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, con
 // ------------------------------------------------ tensor-core fp32 GEMM
 // D[b] = A[b] B[b]^T, A [M x K], B [N x K], both K-major, each passed as a
 // tf32 pair hi + lo (fp32 arrays of tf32 values; hi = round(x), lo = round(x -
-// hi)), accumulated in fp32 from three tf32 products (tgemm.cu).
-enum TgemmMode { kTgScale = 0, kTgExpRow = 1, kTgDLogitRow = 2 };
+// hi)), accumulated in fp32 from three tf32 products (tgemm.cu).  The
+// attention-backward modes compute a second product E = A2 B2^T of the same
+// tile into a second accumulator.
+enum TgemmMode {
+  kTgScale = 0,      // v = alpha * D
+  kTgAttnBwdRow = 1, // p = exp2(alpha * D - beta * v1[m]),  v = p * (E - v2[m])
+  kTgAttnBwdCol = 2  // p = exp2(alpha * D - beta * v1[n]),  v = p * (E - v2[n]); out2 = p
+};
 struct TgemmOperand {
   const float* hi;
   const float* lo;
@@ -137,19 +143,17 @@ struct TgemmOperand {
 struct TgemmArgs {
   int batch, M, N, K;
   int mode;
-  // kTgScale:     v = alpha * acc
-  // kTgExpRow:    v = exp2(alpha * acc - beta * rowv[m])
-  // kTgDLogitRow: v = pin[m][n] * (alpha * acc - rowv[m])
   float alpha, beta;
-  const float* rowv; long long rowv_stride;
-  const float* pin; int pin_ld; long long pin_stride;
-  // outputs, each optional: fp32 [M][N]; tf32 pair [M][N]; tf32 pair transposed [N][M]
+  const float* v1; const float* v2; long long vec_stride;  // per-row or per-column vectors
+  // outputs, each optional: fp32 [M][N]; tf32 pair [M][N]; second tf32 pair [M][N]
   float* out; int out_ld; long long out_stride;
-  float *out_hi, *out_lo; int split_ld; long long split_stride;
-  float *outt_hi, *outt_lo; int splitt_ld; long long splitt_stride;
+  float *out_hi, *out_lo; float *out2_hi, *out2_lo; int split_ld; long long split_stride;
 };
 cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
                          uint32_t* status, cudaStream_t s);
+cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
+                              const TgemmOperand& A2, const TgemmOperand& B2, uint32_t* status,
+                              cudaStream_t s);
 // fp32 [batch][rows][cols] (row stride ld_src) -> tf32 pair, same orientation
 // or transposed ([batch][cols][rows]), row stride ld_dst.
 cudaError_t launch_split_tf32(const float* src, int ld_src, long long stride_src, int rows,
