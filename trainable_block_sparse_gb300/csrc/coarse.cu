@@ -170,10 +170,12 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
   const long long DC = static_cast<long long>(D) * ldc;
   cudaError_t e;
   // operand pairs: Q_c, K_c ([Nc, D]) and V_c^T ([D, Nc])
-  if ((e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qh, ws.ql, D, ND, false, s)) ||
-      (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kh, ws.kl, D, ND, false, s)) ||
-      (e = launch_split_tf32(vc, D, ND, Nc, D, g.BH, ws.vth, ws.vtl, ldc, DC, true, s)))
-    return e;
+  {
+    const SplitSpec sp[3] = {{qc, D, ND, Nc, D, ws.qh, ws.ql, D, ND, false},
+                             {kc, D, ND, Nc, D, ws.kh, ws.kl, D, ND, false},
+                             {vc, D, ND, Nc, D, ws.vth, ws.vtl, ldc, DC, true}};
+    if ((e = launch_split_tf32(sp, 3, g.BH, s))) return e;
+  }
   // L = scale Q_c K_c^T
   TgemmArgs a = gemm(g, Nc, Nc, D, g.scale);
   a.out = ws.clogit;
@@ -214,14 +216,16 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
   rowdot_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, D, doc, oc, ws.cdelta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // operand pairs, both orientations where a product contracts over cubes
-  if ((e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qh, ws.ql, D, ND, false, s)) ||
-      (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kh, ws.kl, D, ND, false, s)) ||
-      (e = launch_split_tf32(vc, D, ND, Nc, D, g.BH, ws.vh, ws.vl, D, ND, false, s)) ||
-      (e = launch_split_tf32(doc, D, ND, Nc, D, g.BH, ws.doh, ws.dol, D, ND, false, s)) ||
-      (e = launch_split_tf32(qc, D, ND, Nc, D, g.BH, ws.qth, ws.qtl, ldc, DC, true, s)) ||
-      (e = launch_split_tf32(kc, D, ND, Nc, D, g.BH, ws.kth, ws.ktl, ldc, DC, true, s)) ||
-      (e = launch_split_tf32(doc, D, ND, Nc, D, g.BH, ws.doth, ws.dotl, ldc, DC, true, s)))
-    return e;
+  {
+    const SplitSpec sp[7] = {{qc, D, ND, Nc, D, ws.qh, ws.ql, D, ND, false},
+                             {kc, D, ND, Nc, D, ws.kh, ws.kl, D, ND, false},
+                             {vc, D, ND, Nc, D, ws.vh, ws.vl, D, ND, false},
+                             {doc, D, ND, Nc, D, ws.doh, ws.dol, D, ND, false},
+                             {qc, D, ND, Nc, D, ws.qth, ws.qtl, ldc, DC, true},
+                             {kc, D, ND, Nc, D, ws.kth, ws.ktl, ldc, DC, true},
+                             {doc, D, ND, Nc, D, ws.doth, ws.dotl, ldc, DC, true}};
+    if ((e = launch_split_tf32(sp, 7, g.BH, s))) return e;
+  }
   // query-major tiles: P = exp(scale Q_c K_c^T - lse) and dL = P (.) (dO_c V_c^T - delta)
   // in registers from two accumulators; dL leaves as a pair
   constexpr float kLog2e = 1.4426950408889634f;

@@ -300,37 +300,51 @@ __global__ void __launch_bounds__(kTgThreads, 1)
   if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
-__global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ src, int ld_src,
-                                                    long long stride_src, int rows, int cols,
-                                                    float* __restrict__ hi, float* __restrict__ lo,
-                                                    int ld_dst, long long stride_dst,
-                                                    int transpose) {
+// One tf32-pair split per job: fp32 [batch][rows][cols] -> hi, lo in the same
+// orientation or transposed, through a padded 32 x 32 shared-memory tile.
+struct SplitJob {
+  const float* src;
+  float* hi;
+  float* lo;
+  long long stride_src, stride_dst;
+  int ld_src, ld_dst, rows, cols, transpose;
+};
+constexpr int kMaxSplitJobs = 8;
+struct SplitJobs {
+  SplitJob j[kMaxSplitJobs];
+};
+
+__global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitJobs jobs,
+                                                    int batch) {
   __shared__ float t[32][33];
-  const int b = blockIdx.z, r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const float* s = src + b * stride_src;
+  const SplitJob& J = jobs.j[blockIdx.z / batch];
+  const int b = blockIdx.z % batch, r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  if (r0 >= J.rows || c0 >= J.cols) return;  // this job is smaller than the grid
+  const float* s = J.src + b * J.stride_src;
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int rr = r0 + r, cc = c0 + threadIdx.x;
-    t[r][threadIdx.x] = (rr < rows && cc < cols) ? s[static_cast<size_t>(rr) * ld_src + cc] : 0.f;
+    t[r][threadIdx.x] =
+        (rr < J.rows && cc < J.cols) ? s[static_cast<size_t>(rr) * J.ld_src + cc] : 0.f;
   }
   __syncthreads();
-  float* h = hi + b * stride_dst;
-  float* l = lo + b * stride_dst;
+  float* h = J.hi + b * J.stride_dst;
+  float* l = J.lo + b * J.stride_dst;
   for (int r = threadIdx.y; r < 32; r += 8) {
-    if (!transpose) {
+    if (!J.transpose) {
       const int rr = r0 + r, cc = c0 + threadIdx.x;
-      if (rr < rows && cc < cols) {
+      if (rr < J.rows && cc < J.cols) {
         const float x = t[r][threadIdx.x];
         const float xh = round_tf32(x);
-        h[static_cast<size_t>(rr) * ld_dst + cc] = xh;
-        l[static_cast<size_t>(rr) * ld_dst + cc] = round_tf32(x - xh);
+        h[static_cast<size_t>(rr) * J.ld_dst + cc] = xh;
+        l[static_cast<size_t>(rr) * J.ld_dst + cc] = round_tf32(x - xh);
       }
     } else {
       const int cc = c0 + r, rr = r0 + threadIdx.x;  // output row = input column
-      if (rr < rows && cc < cols) {
+      if (rr < J.rows && cc < J.cols) {
         const float x = t[threadIdx.x][r];
         const float xh = round_tf32(x);
-        h[static_cast<size_t>(cc) * ld_dst + rr] = xh;
-        l[static_cast<size_t>(cc) * ld_dst + rr] = round_tf32(x - xh);
+        h[static_cast<size_t>(cc) * J.ld_dst + rr] = xh;
+        l[static_cast<size_t>(cc) * J.ld_dst + rr] = round_tf32(x - xh);
       }
     }
   }
@@ -401,13 +415,28 @@ cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const T
   return run_tgemm<true>(a, m0, m1, status, s);
 }
 
-cudaError_t launch_split_tf32(const float* src, int ld_src, long long stride_src, int rows,
-                              int cols, int batch, float* hi, float* lo, int ld_dst,
-                              long long stride_dst, bool transpose, cudaStream_t s) {
-  if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
-  const dim3 grid((cols + 31) / 32, (rows + 31) / 32, batch);
-  split_kernel<<<grid, dim3(32, 8), 0, s>>>(src, ld_src, stride_src, rows, cols, hi, lo, ld_dst,
-                                            stride_dst, transpose ? 1 : 0);
+cudaError_t launch_split_tf32(const SplitSpec* specs, int n, int batch, cudaStream_t s) {
+  if (n <= 0 || batch <= 0) return cudaSuccess;
+  if (n > kMaxSplitJobs || batch > 65535) return cudaErrorInvalidValue;
+  if (static_cast<long long>(batch) * n > 65535) {  // grid.z limit: one launch per job
+    for (int i = 0; i < n; ++i) {
+      const cudaError_t e = launch_split_tf32(specs + i, 1, batch, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  SplitJobs jobs{};
+  int max_r = 0, max_c = 0;
+  for (int i = 0; i < n; ++i) {
+    const SplitSpec& p = specs[i];
+    jobs.j[i] = SplitJob{p.src, p.hi, p.lo, p.stride_src, p.stride_dst, p.ld_src, p.ld_dst,
+                         p.rows, p.cols, p.transpose ? 1 : 0};
+    max_r = p.rows > max_r ? p.rows : max_r;
+    max_c = p.cols > max_c ? p.cols : max_c;
+  }
+  if (max_r <= 0 || max_c <= 0) return cudaSuccess;
+  const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, batch * n);
+  split_kernel<<<grid, dim3(32, 8), 0, s>>>(jobs, batch);
   return cudaGetLastError();
 }
 

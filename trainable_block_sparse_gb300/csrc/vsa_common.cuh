@@ -154,11 +154,14 @@ cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmO
 cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
                               const TgemmOperand& A2, const TgemmOperand& B2, uint32_t* status,
                               cudaStream_t s);
-// fp32 [batch][rows][cols] (row stride ld_src) -> tf32 pair, same orientation
-// or transposed ([batch][cols][rows]), row stride ld_dst.
-cudaError_t launch_split_tf32(const float* src, int ld_src, long long stride_src, int rows,
-                              int cols, int batch, float* hi, float* lo, int ld_dst,
-                              long long stride_dst, bool transpose, cudaStream_t s);
+// tf32-pair splits, up to 8 per launch: fp32 [batch][rows][cols] (row stride
+// ld_src) -> hi, lo in the same orientation or transposed ([batch][cols][rows]),
+// row stride ld_dst.
+struct SplitSpec {
+  const float* src; int ld_src; long long stride_src; int rows, cols;
+  float* hi; float* lo; int ld_dst; long long stride_dst; bool transpose;
+};
+cudaError_t launch_split_tf32(const SplitSpec* specs, int n, int batch, cudaStream_t s);
 // Rank-3 tiled tensor map over fp32 [batch][rows][ld] with a box of
 // (box_cols, box_rows, 1), 128-byte swizzle (api.cu).
 bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t rows,
