@@ -206,7 +206,8 @@ def balance_report(vsa, bufs, wl, dev):
     idx = bufs.view("idx", torch.int32, (B * H, nc, cap)).cpu().numpy()
     cnt = bufs.view("cnt", torch.int32, (B * H, nc)).cpu().numpy()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return schedule.load_balance(idx, cnt, sms)
+    ordered = schedule.uses_cost_order(B * H, wl.tokens, wl.head_dim)
+    return schedule.load_balance(idx, cnt, sms, ordered=ordered)
 
 
 def side_workload(vsa, name, dev):

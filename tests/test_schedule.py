@@ -34,7 +34,13 @@ def _brute(idx, cnt, sms):
                     u |= L[b][2 * p + 1]
                 steps.append(math.ceil(len(u) / 2))
         grid = min(len(steps), sms)
-        work = [sum(steps[k] for k in range(c, len(steps), grid)) for c in range(grid)]
+        # schedule: largest first; full rounds of `grid` positions alternate direction
+        order = sorted(range(len(steps)), key=lambda i: (-steps[i], i))
+        rounds = [order[r:r + grid] for r in range(0, len(order), grid)]
+        seq = []
+        for r, chunk in enumerate(rounds):
+            seq += chunk[::-1] if (r % 2 and len(chunk) == grid) else chunk
+        work = [sum(steps[seq[k]] for k in range(c, len(seq), grid)) for c in range(grid)]
         res[name] = (steps, work)
     return res
 
@@ -58,10 +64,21 @@ def test_load_balance_report():
                    dtype=np.int32)
     cnt = np.array([[4, 1, 1, 1]], dtype=np.int32)
     r = schedule.load_balance(idx, cnt, sms=2)
-    # query pairs (0,1): union 4 -> 2 steps; (2,3): union 2 -> 1 step
+    # query pairs (0,1): union 4 -> 2 steps; (2,3): union 2 -> 1 step; one per CTA
     assert r["fine_fwd"]["cta_steps_max"] == 2
     assert r["fine_fwd"]["max_over_mean"] == 2 / 1.5
     # transposed: key cubes 0..3 are selected by {0},{0,1},{0,2},{0,3}
     # pairs (0,1): union {0,1} -> 1 step; (2,3): {0,2,3} -> 2 steps
     assert r["fine_bwd_dkdv"]["steps_total"] == 3
     assert r["count_histogram"] == {1: 3, 4: 1}
+
+
+def test_snake_schedule_balances_sorted_items():
+    # 8 items on 4 CTAs: sorted 8,7,6,5 | 4,3,2,1 -> CTA totals 9,9,9,9
+    steps = np.array([1, 8, 2, 7, 3, 6, 4, 5])
+    assert schedule.cta_work(steps, 4).tolist() == [9, 9, 9, 9]
+    order = schedule.schedule_order(steps, 4)
+    assert sorted(order.tolist()) == list(range(8))
+    assert steps[order].tolist() == [8, 7, 6, 5, 1, 2, 3, 4]
+    # plain item order: CTA c takes items c and c + 4
+    assert schedule.cta_work(steps, 4, scheduled=False).tolist() == [4, 14, 6, 12]

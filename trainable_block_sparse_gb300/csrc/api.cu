@@ -110,6 +110,8 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.n_qpairs = npairs;
   ws.qpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
+  ws.qorder = static_cast<int*>(take(sizeof(int) * npairs));
+  ws.order_tmp = static_cast<int*>(take(sizeof(int) * (npairs + 512)));
   // coarse logits [BH, Nc, ldc] and tf32 pairs of the coarse GEMM operands
   const size_t ldc = static_cast<size_t>((g.Nc + 3) & ~3);
   ws.clogit = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * ldc * 4));
@@ -152,6 +154,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
     ws.tlist = static_cast<int*>(take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4));
     ws.n_kpairs = npairs;
     ws.kpairs = static_cast<PairItem*>(take(sizeof(PairItem) * npairs));
+    ws.korder = static_cast<int*>(take(sizeof(int) * npairs));
     ws.klist = static_cast<uint32_t*>(take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4));
   }
   if (w) *w = ws;

@@ -88,6 +88,7 @@ struct BwdParams {
   const PairItem* items;
   const uint32_t* lists;
   int n_items;
+  const int* order;       // schedule position -> item (null: identity)
   const float* lse;     // [BH, N] cube order, natural log
   const float* delta;   // [BH, N] cube order
   const float* pooled1; // dQ_c (dQ pass) or dV_c (key-major pass), may be null
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       bool ok = true;
       for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
            item += gridDim.x) {
-        const PairItem pi = P.items[item];
+        const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
         const int nsteps = (pi.count + 1) / 2;
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     bool ok = true;
     for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
          item += gridDim.x) {
-      const PairItem pi = P.items[item];
+      const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
       if (!waitw(&sb.x_full, it & 1, abort_flag, P.status)) break;
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       PairItem prev{};
       for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
            item += gridDim.x) {
-        const PairItem pi = P.items[item];
+        const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         // X shares its buffer with the previous item's staging: each half is
         // loaded as soon as the stores from that region have read it
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     bool ok = true;
     for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
          item += gridDim.x) {
-      const PairItem pi = P.items[item];
+      const PairItem pi = P.items[P.order ? P.order[item] : item];
       const int cube = half ? pi.b : pi.a;
       const bool row_live = half == 0 || pi.b >= 0;
       const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
@@ -639,10 +640,7 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
   auto kern = fine_bwd_kernel<D, kKeyMajor>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = p.n_items < sms ? p.n_items : sms;
+  const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kThreadsBwd, smem, s>>>(m1, m2, m3, m4, mo1, mo2, p);
   return cudaGetLastError();
@@ -653,11 +651,13 @@ cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __ha
                      const float* lse_f, const __half* dof,
                      const float* delta, const float* dqc, const float* dkc, const float* dvc,
                      float* dq, float* dk, float* dv, const Workspace& ws, cudaStream_t s) {
-  BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, lse_f, delta, dqc, nullptr, dq, nullptr,
+  const bool ordered = use_cost_order(g);
+  BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, ordered ? ws.qorder : nullptr, lse_f, delta, dqc, nullptr, dq, nullptr,
                ws.status};
   cudaError_t e = run_bwd<D, false>(g, q, dof, k, v, pq, s);
   if (e != cudaSuccess) return e;
-  BwdParams pk{g, ws.kpairs, ws.klist, ws.n_kpairs, lse_f, delta, dvc, dkc, dv, dk, ws.status};
+  BwdParams pk{g, ws.kpairs, ws.klist, ws.n_kpairs, ordered ? ws.korder : nullptr, lse_f, delta, dvc, dkc, dv, dk,
+               ws.status};
   return run_bwd<D, true>(g, k, v, q, dof, pk, s);
 }
 

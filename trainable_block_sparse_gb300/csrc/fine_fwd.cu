@@ -99,6 +99,7 @@ struct FwdParams {
   const PairItem* items;
   const uint32_t* lists;
   int n_items;
+  const int* order;       // schedule position -> item (null: identity)
   const __nv_bfloat16* gc;
   const __nv_bfloat16* gf;
   const float* oc;
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       int it = 0;  // items with work seen by this CTA
       for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag);
            item += gridDim.x) {
-        const PairItem pi = P.items[item];
+        const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
         if (is_k) {
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     bool ok = true;
     for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
          item += gridDim.x) {
-      const PairItem pi = P.items[item];
+      const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
       const int obuf = it & 1;
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     // No abort test in the loop condition: both warps of a pair must walk the
     // same items and leave together (see pair_sync_or).
     for (int item = blockIdx.x; item < P.n_items && ok; item += gridDim.x) {
-      const PairItem pi = P.items[item];
+      const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const uint32_t* list = P.lists + pi.off;
       const int nsteps = (pi.count + 1) / 2;
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     // No abort test in the loop condition: the four warps meet at named
     // barriers and must walk the same items (see epi_sync_or).
     for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
-      const PairItem pi = P.items[item];
+      const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int obuf = it & 1;
       const bool live = half == 0 || pi.b >= 0;  // warp-uniform
@@ -576,10 +577,7 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
   cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = p.n_items < sms ? p.n_items : sms;
+  const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
   fine_fwd_kernel<D><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
@@ -591,7 +589,8 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
                             const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
                             __nv_bfloat16* o, float* o_f, float* lse_f, const Workspace& ws,
                             cudaStream_t s) {
-  FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, gc, gf, oc, o, o_f, lse_f, ws.status};
+  FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
+              gc, gf, oc, o, o_f, lse_f, ws.status};
   if (g.D == 64) return run_fwd<64>(g, q, k, v, p, s);
   return run_fwd<128>(g, q, k, v, p, s);
 }

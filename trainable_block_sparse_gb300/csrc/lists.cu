@@ -194,13 +194,87 @@ __global__ void build_kpairs_kernel(Geom g, Workspace ws) {
   ws.kpairs[item] = PairItem{bh, a, b, n, off};
 }
 
+// ---------------------------------------------------------- item schedule
+// Steps of an item = ceil(|union| / 2) <= 256; key index 0 = most steps.
+constexpr int kOrderKeys = 264;
+
+__device__ __forceinline__ int order_key(const PairItem& it) {
+  const int steps = min((it.count + 1) / 2, kOrderKeys - 1);
+  return kOrderKeys - 1 - steps;
+}
+
+__global__ void order_count_kernel(const PairItem* __restrict__ items, int n, int* hist) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) atomicAdd(&hist[order_key(items[i])], 1);
+}
+
+// hist -> exclusive prefix (bucket starts), one warp.
+__global__ void order_scan_kernel(int* hist) {
+  const int lane = threadIdx.x;
+  int carry = 0;
+  for (int base = 0; base < kOrderKeys; base += 32) {
+    const int k = base + lane;
+    const int v = k < kOrderKeys ? hist[k] : 0;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += u;
+    }
+    if (k < kOrderKeys) hist[k] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+// Items into their buckets (order within a bucket is arbitrary: it only
+// decides which CTA runs an item, never what the item computes).
+__global__ void order_scatter_kernel(const PairItem* __restrict__ items, int n, int* cursor,
+                                     int* sorted) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) sorted[atomicAdd(&cursor[order_key(items[i])], 1)] = i;
+}
+
+// Position k of a kernel whose CTA c takes positions c, c + grid, ...: full
+// rounds of `grid` positions alternate direction.
+__global__ void order_snake_kernel(const int* __restrict__ sorted, int n, int grid, int* order) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  const int r = k / grid, c = k % grid, base = r * grid;
+  const int src = ((r & 1) && base + grid <= n) ? base + grid - 1 - c : k;
+  order[k] = sorted[src];
+}
+
 }  // namespace
+
+int persistent_grid(int n) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return n < sms ? n : sms;
+}
+
+cudaError_t launch_item_order(const PairItem* items, int n, int* order, int* tmp,
+                              cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int* sorted = tmp;
+  int* hist = tmp + n;
+  cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int) * kOrderKeys, s);
+  if (e != cudaSuccess) return e;
+  const int blocks = (n + 255) / 256;
+  order_count_kernel<<<blocks, 256, 0, s>>>(items, n, hist);
+  order_scan_kernel<<<1, 32, 0, s>>>(hist);
+  order_scatter_kernel<<<blocks, 256, 0, s>>>(items, n, hist, sorted);
+  order_snake_kernel<<<blocks, 256, 0, s>>>(sorted, n, persistent_grid(n), order);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s) {
   const int items = g.BH * ((g.Nc + 1) / 2);
   build_qpairs_kernel<<<(items + 127) / 128, 128, 0, s>>>(g, idx, cnt, ws);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !ws.qorder || !use_cost_order(g)) return e;
+  return launch_item_order(ws.qpairs, items, ws.qorder, ws.order_tmp, s);
 }
 
 cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
@@ -218,7 +292,8 @@ cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int items = g.BH * ((g.Nc + 1) / 2);
   build_kpairs_kernel<<<(items + 127) / 128, 128, 0, s>>>(g, ws);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess || !ws.korder || !use_cost_order(g)) return e;
+  return launch_item_order(ws.kpairs, items, ws.korder, ws.order_tmp, s);
 }
 
 }  // namespace vsa

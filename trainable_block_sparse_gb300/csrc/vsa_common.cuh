@@ -86,6 +86,10 @@ struct Workspace {
   PairItem* kpairs;       // key-cube pairs
   uint32_t* klist;        // [BH, Nc * cap] union lists of key-cube pairs
   int n_kpairs;
+  // schedule orders of the pair items (null: item order); order scratch
+  int* qorder;
+  int* korder;
+  int* order_tmp;         // [n_items] sorted items, then histogram/cursors
 };
 
 // ------------------------------------------------------------------ launches
@@ -118,6 +122,22 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
                               cudaStream_t s);
 cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
+// Schedule order of n pair items for a persistent kernel of min(n, SMs) CTAs
+// that takes positions b, b + grid, ...: items sorted by step count
+// (largest first), each full round of `grid` positions dealt in alternating
+// direction (snake), so every CTA's total work is close to the mean.
+cudaError_t launch_item_order(const PairItem* items, int n, int* order, int* tmp,
+                              cudaStream_t s);
+// Grid of the persistent fine kernels for n items: min(n, SMs).
+int persistent_grid(int n);
+// Whether the fine kernels run their items in the cost-sorted order: only when
+// the fp16 K and V of all slices fit in twice the L2 (256 MB).  Otherwise the
+// plain item order wins: the 152 items in flight are neighbouring cubes of one
+// slice, which select the same K/V tiles, and those stay in L2.
+inline bool use_cost_order(const Geom& g) {
+  const double kv_bytes = 2.0 * 2.0 * g.BH * static_cast<double>(g.N) * g.D;
+  return kv_bytes <= 256.0 * 1024 * 1024;
+}
 cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const float* lse_f, const __half* dof, const float* delta,
                             const float* dqc, const float* dkc, const float* dvc, float* dq,

@@ -1,9 +1,12 @@
 """Work distribution of the persistent fine-stage kernels: a host-side report.
 
 The fine forward kernel and both fine backward passes launch one CTA per SM
-(grid = min(items, SMs)), and CTA b processes work items b, b + grid,
-b + 2*grid, ... in that order.  An item is a pair of neighbouring cubes
-(2p, 2p + 1) of one (batch, head), item index = bh * ceil(Nc / 2) + p:
+(grid = min(items, SMs)), and CTA b processes schedule positions b, b + grid,
+b + 2*grid, ....  The schedule sorts the items by step count, largest first,
+and deals each full round of `grid` positions in alternating direction
+(snake order); the last, partial round keeps its order.  An item is a pair
+of neighbouring cubes (2p, 2p + 1) of one (batch, head), item index =
+bh * ceil(Nc / 2) + p:
 
   * forward and dQ pass: two query cubes walking the union of their index
     lists;
@@ -53,30 +56,55 @@ def item_steps(sel: np.ndarray) -> dict[str, np.ndarray]:
     return {"fine_fwd": fwd.ravel(), "fine_bwd_dq": fwd.ravel(), "fine_bwd_dkdv": key.ravel()}
 
 
-def cta_work(steps: np.ndarray, sms: int) -> np.ndarray:
-    """Total steps of each CTA under the static round-robin assignment."""
+def schedule_order(steps: np.ndarray, sms: int) -> np.ndarray:
+    """Item index at each schedule position (the kernels' item order)."""
+    n = steps.size
+    grid = min(n, sms)
+    order = np.argsort(-np.asarray(steps), kind="stable")
+    out = order.copy()
+    for r in range(n // grid if grid else 0):
+        if r & 1:
+            out[r * grid:(r + 1) * grid] = order[r * grid:(r + 1) * grid][::-1]
+    return out
+
+
+def cta_work(steps: np.ndarray, sms: int, scheduled: bool = True) -> np.ndarray:
+    """Total steps of each CTA: positions c, c + grid, ... of the schedule
+    (scheduled=True) or of plain item order."""
+    steps = np.asarray(steps)
     n = steps.size
     grid = min(n, sms)
     if grid == 0:
         return np.zeros(0, dtype=np.int64)
+    seq = steps[schedule_order(steps, sms)] if scheduled else steps
     padded = np.zeros(-(-n // grid) * grid, dtype=np.int64)
-    padded[:n] = steps
+    padded[:n] = seq
     return padded.reshape(-1, grid).sum(0)
 
 
-def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int) -> dict:
-    """max/mean per-CTA steps of each fine kernel, the step count of the
+def uses_cost_order(batch_heads: int, tokens: int, head_dim: int) -> bool:
+    """The library sorts the items by cost only when the fp16 K and V of all
+    slices fit in 256 MB (twice the L2); otherwise it keeps item order, whose
+    concurrently running items share K/V tiles in L2."""
+    return 4.0 * batch_heads * tokens * head_dim <= 256.0 * 1024 * 1024
+
+
+def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int, ordered: bool = True) -> dict:
+    """max/mean per-CTA steps of each fine kernel (under the cost-sorted
+    schedule when `ordered`, else plain item order), the step count of the
     biggest item, and the histogram of per-cube list lengths."""
     sel = selection_matrix(idx, cnt)
-    out = {}
+    out = {"schedule": "cost-sorted snake" if ordered else "item order"}
     for name, steps in item_steps(sel).items():
-        w = cta_work(steps, sms)
+        w = cta_work(steps, sms, scheduled=ordered)
+        w_plain = cta_work(steps, sms, scheduled=False)
         mean = float(w.mean()) if w.size else 0.0
         out[name] = {"items": int(steps.size), "ctas": int(w.size),
                      "steps_total": int(steps.sum()),
                      "cta_steps_max": int(w.max()) if w.size else 0,
                      "cta_steps_mean": mean,
                      "max_over_mean": float(w.max() / mean) if mean > 0 else 1.0,
+                     "max_over_mean_item_order": float(w_plain.max() / mean) if mean > 0 else 1.0,
                      "item_steps_max": int(steps.max()) if steps.size else 0}
     counts = np.bincount(np.asarray(cnt).ravel(), minlength=1)
     out["count_histogram"] = {int(c): int(n) for c, n in enumerate(counts) if n}
