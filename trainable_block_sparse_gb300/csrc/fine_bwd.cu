@@ -48,6 +48,7 @@ constexpr int kSoftmaxWarpsBwd = 8;
 constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpStore = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
+// dQ pass: the item's Q and dO as TMEM A operands (D/2 columns each) at kColA2
 constexpr float kLog2e = 1.4426950408889634f;
 // Of every 8 exponentials of P, this many run as the FMA-pipe polynomial and
 // the rest on the ex2 unit (none: the polynomial measured slower here too).
@@ -78,6 +79,7 @@ struct BwdBars {
   uint64_t y1_full[4], y1_empty[4], y2_full[4], y2_empty[4];
   uint64_t s_full, s_read, dp_full[2], ds_full[2];  // dP/dS barriers by step parity
   uint64_t acc_full, acc_free, final_mma;
+  uint64_t a_ready, x_free;  // dQ pass: the item's Q, dO copied from X into TMEM
   uint64_t stage_full[2], stage_free[2];  // by column half = staging region X1 / X2
   uint32_t tmem_base;
   int abort;
@@ -187,6 +189,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
     mbar_init(&sb.acc_full, 1);
     mbar_init(&sb.acc_free, kSoftmaxWarpsBwd);
+    mbar_init(&sb.a_ready, kSoftmaxWarpsBwd);
+    mbar_init(&sb.x_free, kSoftmaxWarpsBwd);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.stage_full[i], kSoftmaxWarpsBwd / 2);  // the four warps of a column half
       mbar_init(&sb.stage_free[i], 1);
@@ -203,10 +207,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = sb.tmem_base;
-  // dP buffer of global step t
-  auto dpcol = [](uint32_t t) -> uint32_t {
-    return (!kKeyMajor && (t & 1)) ? kColA2 : kColDP;
-  };
+  // dP buffer of global step t (one buffer: the dQ pass keeps Q and dO in TMEM)
+  auto dpcol = [](uint32_t) -> uint32_t { return kColDP; };
+  constexpr uint32_t kColQT = kColA2, kColDOT = kColA2 + D / 2;  // dQ pass
 
   if (warp == kWarpLoadY) {
     // ===================================================== TMA loads of Y1, Y2
@@ -288,25 +291,33 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       for (int k = 0; k < kKSteps; ++k)
         yd[k] = base + off + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
     };
-    // S (or S^T) of global step t: X1 x Y1^T
+    // A (TMEM, packed fp16 pairs, D/2 columns) x B^T (K-major smem): D/16 MMAs
+    auto issue_ts_chain = [&](uint32_t d, uint32_t a, const uint64_t (&b)[kKSteps],
+                              uint32_t ids) {
+      issue_ts4(d, a, b[0], b[1], b[2], b[3], ids, 0u);
+      if constexpr (kKSteps == 8) issue_ts4(d, a + 32, b[4], b[5], b[6], b[7], ids, 1u);
+    };
+    // S (or S^T) of global step t: X1 x Y1^T (dQ pass: X1 = Q from TMEM)
     auto issue_s = [&](uint32_t t, uint32_t ids) -> bool {
       const uint32_t sl = t % kS1;
       if (!waitw(&sb.y1_full[sl], (t / kS1) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
       uint64_t yd[kKSteps];
       kdesc(y1k0, sl, yd);
-      issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, ids);
+      if (kKeyMajor) issue_ss_chain<kKSteps>(tb + kColS, x1d, yd, ids);
+      else issue_ts_chain(tb + kColS, tb + kColQT, yd, ids);
       commit_elect(&sb.s_full);
       return true;
     };
-    // dP (or dP^T) of global step t: X2 x Y2^T
+    // dP (or dP^T) of global step t: X2 x Y2^T (dQ pass: X2 = dO from TMEM)
     auto issue_dp = [&](uint32_t t, uint32_t ids) -> bool {
       const uint32_t sl = t % kS2;
       if (!waitw(&sb.y2_full[sl], (t / kS2) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
       uint64_t yd[kKSteps];
       kdesc(y2k0, sl, yd);
-      issue_ss_chain<kKSteps>(tb + dpcol(t), x2d, yd, ids);
+      if (kKeyMajor) issue_ss_chain<kKSteps>(tb + dpcol(t), x2d, yd, ids);
+      else issue_ts_chain(tb + dpcol(t), tb + kColDOT, yd, ids);
       commit_elect(&sb.dp_full[t & 1]);
       if (!kKeyMajor) commit_elect(&sb.y2_empty[sl]);  // V feeds only dP in the dQ pass
       return true;
@@ -319,7 +330,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
-      if (!waitw(&sb.x_full, it & 1, abort_flag, P.status)) break;
+      // key-major: X1 = K, X2 = V in shared memory; dQ pass: Q, dO in TMEM
+      if (!waitw(kKeyMajor ? &sb.x_full : &sb.a_ready, it & 1, abort_flag, P.status)) break;
       const uint32_t ids0 = pi.count > 1 ? id_s128 : id_s64;
       if (!issue_s(step, ids0) || !issue_dp(step, ids0)) break;
       for (int s = 0; s < nsteps; ++s) {
@@ -348,8 +360,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         if (more) {
           // S(t+1) overwrites S(t) (or P^T(t), after dV(t) has read it)
           if (!issue_s(t + 1, nids)) { ok = false; break; }
-          // dQ pass: dP(t+1) goes to the other dP buffer right away
-          if (!kKeyMajor && !issue_dp(t + 1, nids)) { ok = false; break; }
         }
         if (!waitw(&sb.ds_full[t & 1], (t >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
         if (!kKeyMajor && s == 0 && it > 0 &&
@@ -363,6 +373,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           issue_ts_rows(tb + kColA1, tb + dpcol(t), y1m0 + ((sl1 * L::kXBytes) >> 4), two, id_acc,
                         s > 0, 64);
           commit_elect(&sb.y1_empty[sl1]);
+          // dP(t+1) overwrites the dP columns after dQ(t) has read them
+          if (more && !issue_dp(t + 1, nids)) { ok = false; break; }
         } else {
           // dK += dS^T Q   (dS^T packed in the dP columns, Q = Y1)
           issue_ts_rows(tb + kColA2, tb + kColDP, y1m0 + ((sl1 * L::kXBytes) >> 4), two, id_acc,
@@ -436,23 +448,39 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       };
       int it = 0;
       bool ok = true;
-      PairItem prev{};
+      PairItem prev{}, pprev{};
       for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
            item += gridDim.x) {
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
-        // X shares its buffer with the previous item's staging: each half is
-        // loaded as soon as the stores from that region have read it
-        if (it > 0 && !store_item(prev, it - 1)) { ok = false; break; }
+        if (kKeyMajor) {
+          // X shares its buffer with the previous item's staging: each half is
+          // loaded as soon as the stores from that region have read it
+          if (it > 0 && !store_item(prev, it - 1)) { ok = false; break; }
+        } else if (it > 0) {
+          // dQ pass: X(it-1) has been copied into TMEM (at the end of item
+          // it-2); the epilogue of item it-2 staged into X after that copy
+          if (!wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) { ok = false; break; }
+          if (it > 1 && !store_item(pprev, it - 2)) { ok = false; break; }
+        }
+        const bool staged = kKeyMajor ? it > 0 : it > 1;  // stores from X may still be reading
         mbar_arrive_expect_tx(&sb.x_full, 2 * L::kXBytes);
-        if (it > 0) bulk_wait_group_read1();
+        if (staged) bulk_wait_group_read1();
         load_x(pi, 0);
-        if (it > 0) bulk_wait_group_read0();
+        if (staged) bulk_wait_group_read0();
         load_x(pi, 1);
+        pprev = prev;
         prev = pi;
         ++it;
       }
-      if (ok && it > 0 && !is_aborted(abort_flag)) store_item(prev, it - 1);
+      if (ok && it > 0 && !is_aborted(abort_flag)) {
+        if (kKeyMajor) {
+          store_item(prev, it - 1);
+        } else if (wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) {
+          if (it > 1 && store_item(pprev, it - 2)) store_item(prev, it - 1);
+          else if (it == 1) store_item(prev, 0);
+        }
+      }
       bulk_wait_group0();
       if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);
     }
@@ -470,6 +498,35 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     uint32_t step = 0;
     int it = 0;
     bool ok = true;
+    // dQ pass: copies this thread's half row of Q (X1) and dO (X2) of the item
+    // whose operands are in X into the TMEM A-operand columns, then signals
+    // the UMMA warp (a_ready) and the X producer (x_free).
+    auto copy_x_to_tmem = [&](int ix) -> bool {
+      if (!waitw(&sb.x_full, ix & 1, abort_flag, P.status)) return false;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint8_t* base = m ? sX2 : sX1;
+        uint32_t w[D / 4];
+#pragma unroll
+        for (int u = 0; u < D / 16; ++u) {
+          const int chunk = D == 128 ? hc : 0, unit = D == 128 ? u : 4 * hc + u;
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              base + chunk * L::kChunkBytes + row * 128 + ((unit ^ (row & 7)) << 4));
+          w[4 * u] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
+        }
+        const uint32_t col = tb + lane_addr + (m ? kColDOT : kColQT) + (D / 4) * hc;
+        if constexpr (D == 128) tmem_st32(col, w);
+        else tmem_st16(col, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive_bwd(&sb.a_ready);
+      warp_arrive_bwd(&sb.x_free);
+      return true;
+    };
     for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
          item += gridDim.x) {
       const PairItem pi = P.items[P.order ? P.order[item] : item];
@@ -486,6 +543,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         continue;
       }
       const uint32_t* list = P.lists + pi.off;
+      // dQ pass: the first item's Q and dO go to TMEM here, later items' at the
+      // end of the item before them
+      if (!kKeyMajor && it == 0 && !copy_x_to_tmem(0)) break;
       // this warp's half of the pooled rows, lane l holding column 32cc + l
       float pr1[D / 64], pr2[D / 64];
       {
@@ -596,6 +656,19 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         cd1 = nd1;
       }
       if (!ok) break;
+      if (!kKeyMajor) {
+        // every S and dP product of this item is complete (phase 2 of its last
+        // step saw its dP): the next item's Q and dO may replace these in TMEM,
+        // so its first products run while this item's epilogue does
+        int nx = item + gridDim.x;
+        while (nx < P.n_items && P.items[P.order ? P.order[nx] : nx].count == 0) nx += gridDim.x;
+        if (nx < P.n_items) {
+          if (!copy_x_to_tmem(it + 1)) break;
+          // the epilogue below stages into X: every warp's copy must be done
+          // (the two warps of a lane quarter read the same X rows)
+          if (!waitw(&sb.x_free, (it + 1) & 1, abort_flag, P.status)) break;
+        }
+      }
       // ---------------------------------------------- epilogue
       if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
       tc_fence_after();
