@@ -580,10 +580,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       };
       float cl0 = 0.f, cl1 = 0.f, cd0 = 0.f, cd1 = 0.f;
       if (kKeyMajor) tile_rows(0, cl0, cl1, cd0, cd1);
+      // list entry of this half's step tile, fetched one step ahead
+      uint32_t e_cur = hc < pi.count ? __ldg(list + hc) : 0u;
       for (int s = 0; s < nsteps; ++s, ++step) {
         const bool two = 2 * s + 1 < pi.count;
         const bool have = hc == 0 || two;   // this step has a tile for this column half
-        const bool valid = have && (list[2 * s + hc] & mybit) != 0;  // warp-uniform
+        const bool valid = have && (e_cur & mybit) != 0;  // warp-uniform
+        e_cur = 2 * s + 2 + hc < pi.count ? __ldg(list + 2 * s + 2 + hc) : 0u;
         float nl0 = 0.f, nl1 = 0.f, nd0 = 0.f, nd1 = 0.f;
         if (kKeyMajor && s + 1 < nsteps) tile_rows(s + 1, nl0, nl1, nd0, nd1);
         if (!waitw(&sb.s_full, step & 1, abort_flag, P.status)) { ok = false; break; }
@@ -596,10 +599,15 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             uint32_t sv[32];
             tmem_ld32(ts + 32 * ch, sv);
             tmem_wait_ld();
-            unroll_for<32>([&](auto J) {
-              constexpr int j = decltype(J)::value;
-              const float l2 = kKeyMajor ? __shfl_sync(kFull, ch ? cl1 : cl0, j) : row_lse;
-              p[32 * ch + j] = ex2_split_bwd<32 * ch + j>(fmaf(__uint_as_float(sv[j]), c, -l2));
+            // scale-and-shift on fp32 pairs
+            unroll_for<16>([&](auto J) {
+              constexpr int j = 2 * decltype(J)::value;
+              const float l0 = kKeyMajor ? __shfl_sync(kFull, ch ? cl1 : cl0, j) : row_lse;
+              const float l1 = kKeyMajor ? __shfl_sync(kFull, ch ? cl1 : cl0, j + 1) : row_lse;
+              float t0, t1;
+              fma2(t0, t1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c, -l0, -l1);
+              p[32 * ch + j] = ex2_split_bwd<32 * ch + j>(t0);
+              p[32 * ch + j + 1] = ex2_split_bwd<32 * ch + j + 1>(t1);
             });
           });
         } else {
@@ -630,14 +638,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                float d[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int j = 2 * i + u;
-                  const float dl = kKeyMajor ? __shfl_sync(kFull, ch ? cd1 : cd0, j) : row_delta;
-                  d[u] = p[32 * ch + j] * (__uint_as_float(dv[j]) - dl);
-                }
-                dk[i] = pack_f16x2(d[0], d[1]);
+                const int j = 2 * i;
+                const float dl0 = kKeyMajor ? __shfl_sync(kFull, ch ? cd1 : cd0, j) : row_delta;
+                const float dl1 = kKeyMajor ? __shfl_sync(kFull, ch ? cd1 : cd0, j + 1) : row_delta;
+                float d0, d1;
+                submul2(d0, d1, __uint_as_float(dv[j]), __uint_as_float(dv[j + 1]), dl0, dl1,
+                        p[32 * ch + j], p[32 * ch + j + 1]);
+                dk[i] = pack_f16x2(d0, d1);
               }
             } else {
 #pragma unroll

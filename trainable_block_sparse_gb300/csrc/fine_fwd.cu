@@ -28,9 +28,12 @@
 //      warp 12     TMA: Q once per item, then K tiles gathered by list entry;
 //      warp 13     UMMA issue (whole warp converged, one elected lane);
 //      warp 14     TMA: V tiles gathered by list entry.
-//  * TMEM (512 columns): two S buffers (QK^T of step t+1 overlaps the softmax
-//    of step t) and two O accumulators (the epilogue of item i drains one
-//    while item i+1 accumulates into the other).
+//  * TMEM (512 columns): one S buffer, two P buffers (fp16, 64 columns each)
+//    and two O accumulators.  The softmax warps signal as soon as S(t) is in
+//    their registers, so QK^T of step t+1 runs while they compute P(t), ahead
+//    of PV(t); P(t) goes to its own buffer, which PV(t-2) has finished reading
+//    by the time S(t) is seen.  The epilogue of item i drains one O
+//    accumulator while item i+1 accumulates into the other.
 //  * The running maximum is only moved (and O rescaled in TMEM) when it grows
 //    by more than 2^8, which keeps exp arguments bounded and the rescale rare.
 // Every mbarrier wait is bounded; a time-out is recorded in the status word and
@@ -49,7 +52,8 @@ constexpr int kThreadsFwd = 512;           // 16 warps
 constexpr int kSoftmaxWarps = 8, kEpiWarps = 4;
 constexpr int kWarpEpi = 8, kWarpK = 12, kWarpMma = 13, kWarpV = 14;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;              // S buffers at columns 0 and 128
+constexpr uint32_t kColS = 0;              // S (128 columns)
+constexpr uint32_t kColP = 128;            // P buffers (fp16 pairs) at columns 128 and 192
 constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Of every 8 exponentials of the softmax, this many run as the FMA-pipe
@@ -83,7 +87,7 @@ struct FwdSmem {
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full, s_read, p_full[2];  // p_full by step parity = P buffer
   uint64_t o_ready, o_full[2], o_free[2];
   uint64_t st_full[2], st_free[2];
   uint64_t final_mma;
@@ -178,13 +182,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       mbar_init(&sb.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sb.s_full[i], 1);
       mbar_init(&sb.p_full[i], kSoftmaxWarps);  // one arrival per softmax warp
       mbar_init(&sb.o_full[i], 1);
       mbar_init(&sb.o_free[i], kEpiWarps);      // one arrival per epilogue warp
       mbar_init(&sb.st_full[i], kSoftmaxWarps);
       mbar_init(&sb.st_free[i], kEpiWarps);
     }
+    mbar_init(&sb.s_full, 1);
+    mbar_init(&sb.s_read, kSoftmaxWarps);  // one arrival per softmax warp
     mbar_init(&sb.o_ready, 1);
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
@@ -273,20 +278,37 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
     for (int k = 0; k < kKSteps; ++k) qd[k] = qd0 + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
 
-    // O[obuf] += P V for global step gstep (P from the S buffer of that step).
-    auto issue_pv = [&](uint32_t gstep, bool two, bool first, int obuf) -> bool {
-      const uint32_t slot = gstep % kSV, sbuf = gstep & 1;
-      if (!waitw(&sb.p_full[sbuf], (gstep >> 1) & 1, abort_flag, P.status)) return false;
-      if (!waitw(&sb.v_full[slot], (gstep / kSV) & 1, abort_flag, P.status)) return false;
+    // S = Q K^T of global step t into the S columns (free once the softmax
+    // warps hold S(t-1) in registers)
+    auto issue_s = [&](uint32_t t, bool two) -> bool {
+      const uint32_t slot = t % kSK;
+      if (!waitw(&sb.k_full[slot], (t / kSK) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
-      issue_ts_rows(tb + kColO + obuf * 128, tb + kColS + sbuf * 128,
+      uint64_t kd[kKSteps];
+      const uint64_t kb = kd0 + ((slot * L::kKVBytes) >> 4);
+#pragma unroll
+      for (int k = 0; k < kKSteps; ++k) kd[k] = kb + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
+      issue_ss_chain<kKSteps>(tb + kColS, qd, kd, two ? idesc_s128 : idesc_s64);
+      commit_elect(&sb.s_full);
+      commit_elect(&sb.k_empty[slot]);
+      return true;
+    };
+    // O[obuf] += P V for global step t (P from P buffer t % 2).  The softmax
+    // writes P(t) only after it has seen S(t), whose commit follows PV(t-2):
+    // the P buffer is free by then without a barrier of its own.
+    auto issue_pv = [&](uint32_t t, bool two, bool first, int obuf) -> bool {
+      const uint32_t slot = t % kSV, pbuf = t & 1;
+      if (!waitw(&sb.p_full[pbuf], (t >> 1) & 1, abort_flag, P.status)) return false;
+      if (!waitw(&sb.v_full[slot], (t / kSV) & 1, abort_flag, P.status)) return false;
+      tc_fence_after();
+      issue_ts_rows(tb + kColO + obuf * 128, tb + kColP + pbuf * 64,
                     vd0 + ((slot * L::kKVBytes) >> 4), two, idesc_pv, !first);
       commit_elect(&sb.v_empty[slot]);
       commit_elect(&sb.o_ready);
       return true;
     };
 
-    uint32_t step = 0;
+    uint32_t step = 0;  // global index of the current item's first step
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
@@ -295,36 +317,32 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
       const int obuf = it & 1;
+      // S of the item's first step: Q has arrived, and the softmax warps hold
+      // the previous step's S in registers
       if (!waitw(&sb.q_full, it & 1, abort_flag, P.status)) break;
-      tc_fence_after();
-      bool prev_two = false;
-      for (int s = 0; s < nsteps; ++s, ++step) {
-        const uint32_t slot = step % kSK, sbuf = step & 1;
-        const bool two = 2 * s + 1 < pi.count;
-        if (!waitw(&sb.k_full[slot], (step / kSK) & 1, abort_flag, P.status)) { ok = false; break; }
-        tc_fence_after();
-        uint64_t kd[kKSteps];
-        const uint64_t kb = kd0 + ((slot * L::kKVBytes) >> 4);
-#pragma unroll
-        for (int k = 0; k < kKSteps; ++k) kd[k] = kb + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
-        issue_ss_chain<kKSteps>(tb + kColS + sbuf * 128, qd, kd, two ? idesc_s128 : idesc_s64);
-        commit_elect(&sb.s_full[sbuf]);
-        commit_elect(&sb.k_empty[slot]);
-        if (s == nsteps - 1) commit_elect(&sb.q_empty);
-        if (s == 1 && it >= 2 &&
+      if (step > 0 && !waitw(&sb.s_read, (step - 1) & 1, abort_flag, P.status)) break;
+      if (!issue_s(step, pi.count > 1)) break;
+      if (nsteps == 1) commit_elect(&sb.q_empty);  // the item's last S product
+      for (int s = 0; s < nsteps; ++s) {
+        const uint32_t t = step + s;
+        if (s + 1 < nsteps) {
+          // S(t+1) as soon as S(t) has been read, ahead of PV(t)
+          if (!waitw(&sb.s_read, t & 1, abort_flag, P.status) || !issue_s(t + 1, 2 * s + 3 < pi.count)) {
+            ok = false;
+            break;
+          }
+          if (s + 2 == nsteps) commit_elect(&sb.q_empty);
+        }
+        if (s == 0 && it >= 2 &&
             !waitw(&sb.o_free[obuf], ((it >> 1) - 1) & 1, abort_flag, P.status)) {
           ok = false;  // the epilogue of item it-2 has not released O[obuf]
           break;
         }
-        if (s > 0 && !issue_pv(step - 1, prev_two, s == 1, obuf)) { ok = false; break; }
-        prev_two = two;
+        if (!issue_pv(t, 2 * s + 1 < pi.count, s == 0, obuf)) { ok = false; break; }
       }
       if (!ok) break;
-      if (nsteps == 1 && it >= 2 &&
-          !waitw(&sb.o_free[obuf], ((it >> 1) - 1) & 1, abort_flag, P.status))
-        break;
-      if (!issue_pv(step - 1, prev_two, nsteps == 1, obuf)) break;
       commit_elect(&sb.o_full[obuf]);
+      step += nsteps;
       ++it;
     }
     // all issued MMAs complete before TMEM is released
@@ -350,13 +368,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const int nsteps = (pi.count + 1) / 2;
       const int obuf = it & 1;
       float m_run = -INFINITY, l_run = 0.f;
+      // list entry of this half's key tile, fetched one step ahead (its global
+      // load latency would otherwise sit between two steps)
+      uint32_t e_cur = hc < pi.count ? __ldg(list + hc) : 0u;
       for (int s = 0; s < nsteps; ++s, ++step) {
-        const uint32_t sbuf = step & 1;
         const bool two = 2 * s + 1 < pi.count;
         const bool have = hc == 0 || two;  // this step has a key tile for this half
-        const bool valid = have && (list[2 * s + hc] & mybit) != 0;
-        const bool got = waitw(&sb.s_full[sbuf], (step >> 1) & 1, abort_flag, P.status);
-        const uint32_t ts = tb + lane_addr + kColS + sbuf * 128;
+        const bool valid = have && (e_cur & mybit) != 0;
+        e_cur = 2 * s + 2 + hc < pi.count ? __ldg(list + 2 * s + 2 + hc) : 0u;
+        const bool got = waitw(&sb.s_full, step & 1, abort_flag, P.status);
+        const uint32_t ts = tb + lane_addr + kColS;
         uint32_t x[64];  // this half-row of S; its first 32 words are reused for packed P
         float mx = -INFINITY;
         if (got) {
@@ -365,21 +386,22 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tmem_ld32(ts + 64 * hc, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
             tmem_ld32(ts + 64 * hc + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
             tmem_wait_ld();
-            float m8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(x[i]));
-            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
           }
         }
-        sb.red[step & 1][hc][row] = mx;
-        // Both halves' S loads are complete before either half writes P (the
-        // half-1 P columns overlap the half-0 S columns).
+        // S(t) is in registers: the UMMA warp may issue S(t+1) over it
         tc_fence_before();
+        warp_arrive(&sb.s_read);
+        if (got && valid) {
+          float m8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            m8[i & 7] = max3f(m8[i & 7], __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+          mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+        }
+        sb.red[step & 1][hc][row] = mx;
         if (pair_sync_or(quarter, !got)) { ok = false; break; }
-        tc_fence_after();
         const float m_new = fmaxf(m_run, fmaxf(mx, sb.red[step & 1][hc ^ 1][row]) * c);
         bool resc = false;
         float alpha = 1.f;
@@ -396,12 +418,15 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
           for (int u = 0; u < 8; ++u) ls[u] = 0.f;
           const float mb = m_run;
-          // x[i] <- f16x2(p[2i], p[2i+1]); x[2i], x[2i+1] are read before x[i] is written
+          // x[i] <- f16x2(p[2i], p[2i+1]); x[2i], x[2i+1] are read before x[i] is
+          // written.  Scale-and-shift and the row sum run on fp32 pairs.
           unroll_for<32>([&](auto I) {
             constexpr int i = decltype(I)::value;
-            const float p0 = ex2_split<2 * i>(fmaf(__uint_as_float(x[2 * i]), c, -mb));
-            const float p1 = ex2_split<2 * i + 1>(fmaf(__uint_as_float(x[2 * i + 1]), c, -mb));
-            ls[i & 7] += p0 + p1;
+            float t0, t1;
+            fma2_bc(t0, t1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mb);
+            const float p0 = ex2_split<2 * i>(t0);
+            const float p1 = ex2_split<2 * i + 1>(t1);
+            add2_acc(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], p0, p1);
             x[i] = pack_f16x2(p0, p1);
           });
           l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
@@ -409,9 +434,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] = 0u;
         }
-        // P of key tile hc goes to columns [32 hc, 32 hc + 32) of this S buffer
+        // P of key tile hc goes to columns [32 hc, 32 hc + 32) of P buffer step % 2
         if (have) {
-          tmem_st32(ts + 32 * hc, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+          tmem_st32(tb + lane_addr + kColP + (step & 1) * 64 + 32 * hc,
+                    *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
         }
         if (__any_sync(0xffffffffu, resc)) {
           // O holds the previous steps' sum: wait for the last PV product,
@@ -434,7 +460,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(&sb.p_full[sbuf]);
+        warp_arrive(&sb.p_full[step & 1]);
       }
       if (!ok) break;
       // Hand this row's statistics to the epilogue through the stats buffer of

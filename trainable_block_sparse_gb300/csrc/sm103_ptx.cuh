@@ -392,6 +392,50 @@ __device__ __forceinline__ float ex2_poly(float x) {
   return __int_as_float(__float_as_int(p) + (n << 23));
 }
 
+// Packed fp32 pairs (sm_100+): each lane of the pair is an ordinary
+// round-to-nearest fp32 operation, so results equal the scalar forms; one
+// instruction covers two elements.
+// (d0, d1) = (a0, a1) * b + c
+__device__ __forceinline__ void fma2_bc(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\tmov.b64 c, {%5, %5};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void add2_acc(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 s, a;\n\t"
+      "mov.b64 s, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\t"
+      "add.rn.f32x2 s, s, a;\n\tmov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (a0 - b0) * m0, (a1 - b1) * m1, rounded after each operation
+__device__ __forceinline__ void submul2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                        float m0, float m1) {
+  asm("{\n\t.reg .b64 a, b, m, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 m, {%6, %7};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmul.rn.f32x2 d, d, m;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(m0), "f"(m1));
+}
+// max(a, b, c) in one instruction (sm_100+)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
