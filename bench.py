@@ -42,8 +42,9 @@ from trainable_block_sparse_gb300 import build, flops, synth  # noqa: E402
 METRIC = "VSA fwd/fwd+bwd ms/layer & executed TFLOPS (% of BF16 peak), 16K–70K tokens"
 WORKLOAD = "p720"
 # kernels per call of vsa_forward / vsa_backward
-LAUNCHES_FWD = 8   # stage x3, coarse logits GEMM + select + O_c GEMM, pair lists, fine forward
-LAUNCHES_BWD = 15  # combine bwd, coarse bwd (row dot + 5 GEMMs), pair lists,
+LAUNCHES_FWD = 9   # stage x3, tf32 split, coarse logits GEMM + select + O_c GEMM, pair lists,
+                   # fine forward
+LAUNCHES_BWD = 16  # combine bwd, coarse bwd (row dot, tf32 split, 5 GEMMs), pair lists,
                    # transposed lists (mask, count, scan, fill, pairs), fine bwd x2
 SIDE_WORKLOADS = ("wan13b", "dynamic")  # timed per stage beside the headline layer
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
