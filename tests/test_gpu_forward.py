@@ -208,6 +208,28 @@ def test_forward_edge_shapes(thw, D, topk):
     check_forward(_custom(*thw, D, topk, seed=7 + topk), full=True)
 
 
+@pytest.mark.parametrize("thw,select,k", [
+    ((16, 32, 32), "mass", 100),   # mass rule with kmax > 64: the shared-memory selection
+    ((16, 32, 192), "topk", 32),   # 1,536 cubes: rows of 48 values per lane
+    ((16, 32, 288), "topk", 32),   # 2,304 cubes: beyond the register rows
+])
+def test_selection_paths(thw, select, k):
+    """Lists, counts, lse_c and O_c against the oracle on the selection's
+    less common paths (row lengths and list capacities)."""
+    T, H, W = thw
+    wl = synth.Workload(f"sel_{T}x{H}x{W}_{select}{k}", 1, 1, 64, T, H, W, select,
+                        topk=k, kmin=8, kmax=k, amplitude=1.3 if select == "mass" else 1.0,
+                        seed=41 + k)
+    inp = synth.Inputs(wl, with_grad=False)
+    enforce_gaps(inp)
+    _, _, _, _, v = run_forward(inp)
+    hd = O.head_of(inp, 0, 0)
+    assert np.array_equal(v["cnt"][0, 0].cpu().numpy(), hd.cnt)
+    assert np.array_equal(v["idx"][0, 0].cpu().numpy(), hd.idx)
+    assert_close("lse_c", to_np(v["lse_c"][0, 0]), hd.coarse["lse"])
+    assert_close("O_c", to_np(v["oc"][0, 0]), hd.coarse["out"])
+
+
 def test_full_selection_with_fine_only_gates_is_dense_attention():
     """K = all cubes, G_c = 0, G_f = 1: the output is dense softmax attention."""
     inp = _custom(4, 8, 8, 64, 4, seed=11)

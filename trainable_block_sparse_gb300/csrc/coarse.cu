@@ -129,6 +129,178 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs 
   if (lane == 0) cnt[static_cast<size_t>(bh) * Nc + row] = n;
 }
 
+// The same computation with the row in registers (lane l holds columns
+// l, l + 32, ...; kPer * 32 >= Nc) and the selection by threshold instead of
+// repeated argmax: the K-th largest logit is found by bisection on its
+// order-preserving 32-bit key (count of keys >= mid, one warp reduction per
+// halving, early exit when exactly K keys lie above), then the chosen columns
+// are written in ascending order by ballots over the register rows, equal
+// keys at the threshold going to the lower cube ids.  The mass rule ranks the
+// kmax largest candidates and sums their probabilities in descending order,
+// as the argmax loop did, so lists, A_c and lse_c are bit-identical to
+// select_kernel's.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  // v > -inf and not NaN -> a key >= 1 that orders like v; others -> 0
+  const uint32_t u = v == 0.f ? 0u : __float_as_uint(v);  // -0 and +0 compare equal
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return v > -INFINITY ? k : 0u;
+}
+
+template <int kPer>
+__global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectArgs sa,
+                                                                 const float* __restrict__ logits,
+                                                                 float* __restrict__ ach,
+                                                                 float* __restrict__ acl, int ldc,
+                                                                 float* __restrict__ lse_c,
+                                                                 int* __restrict__ idx,
+                                                                 int* __restrict__ cnt) {
+  constexpr int kWarps = kSelThreads / 32;
+  // mass rule (kmax <= 64): candidate columns in ascending order, their keys,
+  // their descending ranks, and the columns by rank
+  __shared__ int s_ci[kWarps][64];
+  __shared__ uint32_t s_ck[kWarps][64];
+  __shared__ int s_rk[kWarps][64];
+  __shared__ int s_cr[kWarps][64];
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int Nc = g.Nc, bh = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int row = blockIdx.x * kWarps + warp;
+  if (row >= Nc) return;
+  const size_t arow = (static_cast<size_t>(bh) * Nc + row) * ldc;
+  const float* Lg = logits + arow;
+  float v[kPer];
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = 32 * i + lane;
+    v[i] = j < Nc ? Lg[j] : -INFINITY;
+    if (j < Nc) m = fmaxf(m, v[i]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  float e[kPer];
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    e[i] = 32 * i + lane < Nc ? expf(v[i] - m) : 0.f;
+    z += e[i];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(kFull, z, off);
+  const float inv = 1.f / z;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {  // A_c row
+    const int j = 32 * i + lane;
+    if (j < Nc) {
+      const float p = e[i] * inv;
+      const float h = round_tf32(p);
+      ach[arow + j] = h;
+      acl[arow + j] = round_tf32(p - h);
+    }
+  }
+  if (lane == 0) lse_c[static_cast<size_t>(bh) * Nc + row] = m + logf(z);
+
+  // ---- selection
+  uint32_t key[kPer];
+  uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;
+  int nvalid = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    key[i] = 32 * i + lane < Nc ? order_key(v[i]) : 0u;
+    if (key[i]) {
+      kmin_l = min(kmin_l, key[i]);
+      kmax_l = max(kmax_l, key[i]);
+      ++nvalid;
+    }
+  }
+  nvalid = __reduce_add_sync(kFull, nvalid);
+  const int kmax_eff = min(sa.kmax, Nc);
+  const int kmin_eff = min(sa.kmin, kmax_eff);
+  const int want = sa.mode == 0 ? sa.topk : kmax_eff;
+  const int K = min(want, nvalid);
+  int* out = idx + (static_cast<size_t>(bh) * Nc + row) * g.cap;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t t = 1u;  // the K-th largest key (or a key with exactly K keys at or above it)
+  if (K > 0) {
+    uint32_t lo = __reduce_min_sync(kFull, kmin_l), hi = __reduce_max_sync(kFull, kmax_l);
+    // invariant: count(key >= lo) >= K; the answer lies in [lo, hi]
+    while (lo < hi) {
+      const uint32_t mid = lo + (hi - lo + 1) / 2;
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) c += key[i] >= mid;
+      c = __reduce_add_sync(kFull, c);
+      if (c == K) { lo = mid; break; }
+      if (c > K) lo = mid;
+      else hi = mid - 1;
+    }
+    t = lo;
+  }
+  int n_gt = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) n_gt += key[i] > t;
+  n_gt = __reduce_add_sync(kFull, n_gt);
+  const int need_eq = K - n_gt;  // keys equal to t to take, lowest columns first
+  // the K chosen columns in ascending order
+  int* dst = sa.mode == 0 ? out : s_ci[warp];
+  int nout = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const bool eq = K > 0 && key[i] == t;
+    const uint32_t beq = __ballot_sync(kFull, eq);
+    const bool sel = K > 0 && (key[i] > t || (eq && eq_seen + __popc(beq & lt_mask) < need_eq));
+    eq_seen += __popc(beq);
+    const uint32_t bsel = __ballot_sync(kFull, sel);
+    if (sel) {
+      const int pos = nout + __popc(bsel & lt_mask);
+      dst[pos] = 32 * i + lane;
+      if (sa.mode != 0) s_ck[warp][pos] = key[i];
+    }
+    nout += __popc(bsel);
+  }
+  int n = K;
+  if (sa.mode != 0) {
+    // mass rule over the K (<= 64) candidates: descending rank (larger key
+    // first, the lower column on ties), then the probabilities summed in
+    // rank order by one lane, as the argmax loop summed them
+    __syncwarp();
+    for (int c = lane; c < K; c += 32) {
+      const uint32_t kc = s_ck[warp][c];
+      int r = 0;
+      for (int d = 0; d < K; ++d) {
+        const uint32_t kd = s_ck[warp][d];
+        r += kd > kc || (kd == kc && d < c);
+      }
+      s_rk[warp][c] = r;
+      s_cr[warp][r] = s_ci[warp][c];
+    }
+    __syncwarp();
+    int nn = 0;
+    if (lane == 0) {
+      float cum = 0.f;
+      int n_raw = 0;
+      for (int r = 0; r < K; ++r) {
+        cum += expf(Lg[s_cr[warp][r]] - m) * inv;
+        nn = r + 1;
+        if (n_raw == 0 && cum >= sa.mass) n_raw = nn;
+        if (nn >= kmin_eff && n_raw > 0) break;
+      }
+    }
+    n = __shfl_sync(kFull, nn, 0);
+    // the n highest-ranked candidates, in ascending column order
+    int nsel = 0;
+    for (int c0 = 0; c0 < K; c0 += 32) {
+      const int c = c0 + lane;
+      const bool sel = c < K && s_rk[warp][c] < n;
+      const uint32_t bsel = __ballot_sync(kFull, sel);
+      if (sel) out[nsel + __popc(bsel & lt_mask)] = s_ci[warp][c];
+      nsel += __popc(bsel);
+    }
+  }
+  for (int e2 = n + lane; e2 < g.cap; e2 += 32) out[e2] = -1;
+  if (lane == 0) cnt[static_cast<size_t>(bh) * Nc + row] = n;
+}
+
 // delta_c[row] = sum_d dO_c[row, d] * O_c[row, d], one warp per row.
 __global__ void rowdot_kernel(int rows, int D, const float* __restrict__ a,
                               const float* __restrict__ b, float* __restrict__ out) {
@@ -192,8 +364,21 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
                                 static_cast<int>(smem))) != cudaSuccess)
     return e;
   SelectArgs sa{mode, topk, kmin, kmax, mass};
-  select_kernel<<<dim3((Nc + rows - 1) / rows, g.BH), kSelThreads, smem, s>>>(
-      g, sa, rows, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+  // rows in registers when they fit (and the mass rule's candidates in 64 slots)
+  const dim3 rgrid((Nc + kSelThreads / 32 - 1) / (kSelThreads / 32), g.BH);
+  const bool reg_ok = mode == 0 || (kmax < Nc ? kmax : Nc) <= 64;
+  if (reg_ok && Nc <= 8 * 32) {
+    select_reg_kernel<8><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+  } else if (reg_ok && Nc <= 16 * 32) {
+    select_reg_kernel<16><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+  } else if (reg_ok && Nc <= 36 * 32) {
+    select_reg_kernel<36><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+  } else if (reg_ok && Nc <= 64 * 32) {
+    select_reg_kernel<64><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+  } else {
+    select_kernel<<<dim3((Nc + rows - 1) / rows, g.BH), kSelThreads, smem, s>>>(
+        g, sa, rows, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // O_c = A_c V_c
   a = gemm(g, Nc, D, Nc, 1.f);
