@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const bool two = 2 * s + 1 < pi.count;
         const bool have = hc == 0 || two;   // this step has a tile for this column half
         const bool valid = have && (e_cur & mybit) != 0;  // warp-uniform
-        e_cur = 2 * s + 2 + hc < pi.count ? __ldg(list + 2 * s + 2 + hc) : 0u;
+        e_cur = __ldg(list + min(2 * s + 2 + hc, pi.count - 1));  // in bounds; unused past the list
         float nl0 = 0.f, nl1 = 0.f, nd0 = 0.f, nd1 = 0.f;
         if (kKeyMajor && s + 1 < nsteps) tile_rows(s + 1, nl0, nl1, nd0, nd1);
         if (!waitw(&sb.s_full, step & 1, abort_flag, P.status)) { ok = false; break; }

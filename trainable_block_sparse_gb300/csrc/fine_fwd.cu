@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const bool two = 2 * s + 1 < pi.count;
         const bool have = hc == 0 || two;  // this step has a key tile for this half
         const bool valid = have && (e_cur & mybit) != 0;
-        e_cur = 2 * s + 2 + hc < pi.count ? __ldg(list + 2 * s + 2 + hc) : 0u;
+        e_cur = __ldg(list + min(2 * s + 2 + hc, pi.count - 1));  // in bounds; unused past the list
         const bool got = waitw(&sb.s_full, step & 1, abort_flag, P.status);
         const uint32_t ts = tb + lane_addr + kColS;
         uint32_t x[64];  // this half-row of S; its first 32 words are reused for packed P
