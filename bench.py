@@ -143,6 +143,21 @@ def workload(args):
     return wl.replace(heads=args.heads) if getattr(args, "heads", 0) else wl
 
 
+def max_over_ranks(ms: float, world: int, dev) -> float:
+    """The slowest rank's time: every rank processes its own replica of the
+    layer (no data exchange), so the job's time is the maximum."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_flops: float, world: int, ms_max: float) -> float:
+    """Whole-job TFLOPS: the work of all replicas over the slowest rank's time."""
+    return world * step_flops / (ms_max * 1e-3) / 1e12
+
+
 def gpu_arm(args, rank, world):
     from trainable_block_sparse_gb300 import vsa
     build.build()
@@ -181,11 +196,7 @@ def gpu_arm(args, rank, world):
     status = bufs.device_status()
     if status != vsa.OK:
         raise RuntimeError(f"device status {status} after the timed steps")
-    ms_max = ms_step
-    if world > 1:
-        tmax = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tmax.item())
+    ms_max = max_over_ranks(ms_step, world, dev)
 
     stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev)
     e2e = end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args)
@@ -490,7 +501,7 @@ def main():
     total = sum(stages.values())
     line = {
         "metric": METRIC,
-        "value": world * step_flops / (r["ms_step"] * 1e-3) / 1e12,
+        "value": job_throughput(step_flops, world, r["ms_step"]),
         "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config_json(wl),
