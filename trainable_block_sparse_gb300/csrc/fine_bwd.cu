@@ -21,17 +21,20 @@
 //
 // Per step the softmax warps signal twice: once S has been read (so the next
 // step's S product can be issued at once) and once dS is in TMEM.  TMEM
-// (512 columns): S at 0, dP at 128, the dQ or dV accumulator at 256, and at
-// 384 either the dK accumulator or, in the dQ pass, a second dP buffer (dP of
-// step t+1 is computed while dS of step t is still being written).
+// (512 columns): S at 0, dP at 128, the dQ or dV accumulator at 256; at 384
+// the dK accumulator (key-major pass) or, in the dQ pass, the item's Q and
+// dO as TMEM A operands (D/2 columns each), copied from X by the softmax
+// warps, so the S and dP products read only K and V from shared memory.  In
+// the dQ pass dS(t) is packed over the dP columns, so dP(t+1) is issued after
+// dQ(t) has read them.
 // Y1 and Y2 come through separate TMA rings (Y1 is read by the last product
 // of a step, Y2 earlier, so Y1 gets the deeper ring).
 // Epilogue: the accumulators (times the scale, plus the pooled gradient) are
 // written to shared memory in the X operand buffers, which are free once the
-// item's products are done, and leave through TMA stores (a 4-D box of one
-// 4x4x4 cube x 32 columns for the raster layout), so the global writes are
-// whole lines; the next item's X is loaded after those stores have read
-// shared memory.
+// item's products are done (dQ pass: once Q and dO of the next item are in
+// TMEM), and leave through TMA stores (a 4-D box of one 4x4x4 cube x 32
+// columns for the raster layout), so the global writes are whole lines; the
+// next item's X is loaded after those stores have read shared memory.
 // Warps 0-7: softmax and epilogue; warp w reads TMEM lane quarter w%4 (32
 // rows) and the 64 columns of step tile w/4, so each thread owns half a row.
 // Warp 8: TMA loads of Y1/Y2.  Warp 9: UMMA issue.  Warp 10: TMA stores of the
