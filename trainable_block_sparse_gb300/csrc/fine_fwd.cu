@@ -75,8 +75,8 @@ struct FwdSmem {
   static constexpr int kChunkBytes = 128 * 128;       // one chunk of 128 rows
   static constexpr int kQBytes = kChunks * kChunkBytes;
   static constexpr int kKVBytes = kChunks * kChunkBytes;  // 2 key tiles
-  static constexpr int kStagesK = (D == 128) ? 3 : 6;
-  static constexpr int kStagesV = (D == 128) ? 2 : 5;
+  static constexpr int kStagesK = (D == 128) ? 2 : 6;
+  static constexpr int kStagesV = (D == 128) ? 3 : 5;
   static constexpr int kTileBytes = 64 * D * 2;       // one 64-row tile
   // epilogue staging of one 32-column chunk of O_f: 128 rows x 128 bytes
   static constexpr int kStageOff = kQBytes + (kStagesK + kStagesV) * kKVBytes;
