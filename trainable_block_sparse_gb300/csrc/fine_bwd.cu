@@ -29,16 +29,25 @@
 // dQ(t) has read them.
 // Y1 and Y2 come through separate TMA rings (Y1 is read by the last product
 // of a step, Y2 earlier, so Y1 gets the deeper ring).
-// Epilogue: the accumulators (times the scale, plus the pooled gradient) are
-// written to shared memory in the X operand buffers, which are free once the
-// item's products are done (dQ pass: once Q and dO of the next item are in
-// TMEM), and leave through TMA stores (a 4-D box of one 4x4x4 cube x 32
-// columns for the raster layout), so the global writes are whole lines; the
-// next item's X is loaded after those stores have read shared memory.
-// Warps 0-7: softmax and epilogue; warp w reads TMEM lane quarter w%4 (32
-// rows) and the 64 columns of step tile w/4, so each thread owns half a row.
-// Warp 8: TMA loads of Y1/Y2.  Warp 9: UMMA issue.  Warp 10: TMA stores of the
-// epilogue and TMA loads of X.
+// Epilogue: the accumulators are scaled and the pooled gradient is added.
+//  * dQ pass: the rows are written to shared memory in the X operand buffers,
+//    which are free once Q and dO of the next item are in TMEM, and leave
+//    through TMA stores (a 4-D box of one 4x4x4 cube x 32 columns for the
+//    raster layout), so the global writes are whole lines; the item after
+//    next has its X loaded once those stores have read shared memory.
+//  * key-major pass: four epilogue warps (one per TMEM lane quarter) read dV
+//    and then dK out of TMEM and write them straight to global memory, four
+//    threads per row and 32 whole bytes of a row per group, while the softmax
+//    warps go on with the next item.  X holds no staging, so the next item's
+//    K and V are loaded as soon as the item's last S^T and dP^T products are
+//    done; its first dV product waits only until the epilogue has read dV,
+//    its first dK product until it has read dK.
+// Warps 0-7: softmax (and the dQ-pass epilogue); warp w reads TMEM lane
+// quarter w%4 (32 rows) and the 64 columns of step tile w/4, so each thread
+// owns half a row.  Warp 8: TMA loads of Y1/Y2.  Warp 9: UMMA issue.  Warp 10:
+// TMA loads of X and, in the dQ pass, the TMA stores of the epilogue.  The
+// key-major pass adds warps 11 (idle) and 12-15 (epilogue) and splits the
+// registers per warpgroup: 168 a thread for the softmax warps, 88 for the rest.
 // Bounded waits and the abort path are as in the forward kernel.
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
@@ -46,9 +55,14 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreadsBwd = 352;  // 11 warps
+constexpr int kThreadsBwd = 352;  // dQ pass: 11 warps
+constexpr int kThreadsKm = 512;   // key-major pass: 16 warps
 constexpr int kSoftmaxWarpsBwd = 8;
-constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpStore = 10;
+constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpStore = 10, kWarpEpi0 = 12;
+constexpr int kEpiWarps = 4;
+// key-major register split: the launch gives 65536 / 512 = 128 a thread
+constexpr int kRegsSoftmaxKm = 168, kRegsRestKm = 88;
+static_assert(256 * kRegsSoftmaxKm + 256 * kRegsRestKm <= 65536, "split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
 // dQ pass: the item's Q and dO as TMEM A operands (D/2 columns each) at kColA2
@@ -83,7 +97,9 @@ struct BwdBars {
   uint64_t s_full, s_read, dp_full[2], ds_full[2];  // dP/dS barriers by step parity
   uint64_t acc_full, acc_free, final_mma;
   uint64_t a_ready, x_free;  // dQ pass: the item's Q, dO copied from X into TMEM
-  uint64_t stage_full[2], stage_free[2];  // by column half = staging region X1 / X2
+  uint64_t x_empty;          // key-major pass: the item's last S^T and dP^T are done
+  uint64_t dv_free, dk_free; // key-major pass: the epilogue has read dV / dK
+  uint64_t stage_full[2];  // dQ pass, by column half = staging region X1 / X2
   uint32_t tmem_base;
   int abort;
 };
@@ -125,6 +141,48 @@ __device__ __forceinline__ void store_pooled_half(int c0, const float* pooled, s
   }
 }
 
+template <bool kOn, int N>
+__device__ __forceinline__ void regs_inc() {
+  if constexpr (kOn) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <bool kOn, int N>
+__device__ __forceinline__ void regs_dec() {
+  if constexpr (kOn) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Key-major epilogue: the 32 accumulator rows of this warp's lane quarter
+// (at TMEM address tq), times `mul` plus the pooled gradient, to global
+// memory; row 16h + 8j + t/4 of the quarter goes to output row orow[2h + j].
+// pp[k] holds, in lane l, pooled columns 2(l + 32k) and 2(l + 32k) + 1,
+// already divided by 64.
+template <int D>
+__device__ __forceinline__ void drain_acc(uint32_t tq, float mul, const float2 (&pp)[D / 64],
+                                          float* out, const size_t (&orow)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[2][16];
+    tmem_ld16x256_x4(tq + 32 * c, v[0]);
+    tmem_ld16x256_x4(tq + (16u << 16) + 32 * c, v[1]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // column pair 16c + 4i + t%4 sits in lane (that) % 32 of pp[c / 2]
+      const int src = 16 * (c & 1) + 4 * i + (lane & 3);
+      const float px = __shfl_sync(0xffffffffu, pp[c >> 1].x, src);
+      const float py = __shfl_sync(0xffffffffu, pp[c >> 1].y, src);
+      const int col = 32 * c + 8 * i + 2 * (lane & 3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          *reinterpret_cast<float2*>(out + orow[2 * h + j] * D + col) =
+              make_float2(fmaf(__uint_as_float(v[h][4 * i + 2 * j]), mul, px),
+                          fmaf(__uint_as_float(v[h][4 * i + 2 * j + 1]), mul, py));
+    }
+  }
+}
+
 // Accumulator row (times `mul`, plus pooled/64) -> staging, columns of this
 // thread's half, in the SW128 image the TMA store expects: 16-byte unit u of
 // row r of a 32-column chunk sits at unit position u ^ (r % 8).  pr[cc] holds,
@@ -152,15 +210,13 @@ __device__ __forceinline__ void stage_half_row(uint32_t tacc, int hc, int row, f
 }
 
 template <int D, bool kKeyMajor>
-__global__ void __launch_bounds__(kThreadsBwd, 1)
+__global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
     fine_bwd_kernel(const __grid_constant__ CUtensorMap tx1, const __grid_constant__ CUtensorMap tx2,
                     const __grid_constant__ CUtensorMap ty1, const __grid_constant__ CUtensorMap ty2,
-                    const __grid_constant__ CUtensorMap to1, const __grid_constant__ CUtensorMap to2,
-                    BwdParams P) {
+                    const __grid_constant__ CUtensorMap to1, BwdParams P) {
   using L = BwdSmem<D>;
   constexpr int kS1 = L::kStages1, kS2 = L::kStages2;
   constexpr int kKSteps = D / 16;
-  constexpr int kRounds = kKeyMajor ? 2 : 1;  // epilogue outputs through the staging buffer
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -168,7 +224,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   uint8_t* sX2 = sX1 + L::kXBytes;
   uint8_t* sY1 = sX2 + L::kXBytes;  // ring of kS1 operands
   uint8_t* sY2 = sY1 + kS1 * L::kXBytes;
-  uint8_t* staging = sX1;           // X1 + X2, once the item's products are done
+  uint8_t* staging = sX1;           // dQ pass: X1 + X2, once the item's products are done
   __shared__ BwdBars sb;
   int* abort_flag = &sb.abort;
   const Geom& g = P.g;
@@ -194,10 +250,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_init(&sb.acc_free, kSoftmaxWarpsBwd);
     mbar_init(&sb.a_ready, kSoftmaxWarpsBwd);
     mbar_init(&sb.x_free, kSoftmaxWarpsBwd);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(&sb.x_empty, 1);
+    mbar_init(&sb.dv_free, kEpiWarps);
+    mbar_init(&sb.dk_free, kEpiWarps);
+    for (int i = 0; i < 2; ++i)
       mbar_init(&sb.stage_full[i], kSoftmaxWarpsBwd / 2);  // the four warps of a column half
-      mbar_init(&sb.stage_free[i], 1);
-    }
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
     fence_barrier_init();
@@ -216,6 +273,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   if (warp == kWarpLoadY) {
     // ===================================================== TMA loads of Y1, Y2
+    regs_dec<kKeyMajor, kRegsRestKm>();
     if (lane == 0) {
       tma_prefetch_desc(&ty1);
       tma_prefetch_desc(&ty2);
@@ -272,6 +330,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
   } else if (warp == kWarpIssue) {
     // ===================================================== UMMA issuer
+    regs_dec<kKeyMajor, kRegsRestKm>();
     const uint32_t id_s128 = idesc_f16(128, 128, 0, 0);
     const uint32_t id_s64 = idesc_f16(128, 64, 0, 0);
     const uint32_t id_acc = idesc_f16(128, D, 0, 1);
@@ -343,6 +402,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const bool more = s + 1 < nsteps;
         const uint32_t nids = (2 * s + 3 < pi.count) ? id_s128 : id_s64;
         const uint32_t sl1 = t % kS1, sl2 = t % kS2;
+        // key-major: every S^T and dP^T product of the item has been issued;
+        // X (K and V of the item) is free once they are done
+        if (kKeyMajor && !more) commit_elect(&sb.x_empty);
         // softmax phase 1 of step t is done: S(t) has been read (and, in the
         // key-major pass, replaced by P^T)
         if ((kKeyMajor || more) && !waitw(&sb.s_read, t & 1, abort_flag, P.status)) {
@@ -350,7 +412,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           break;
         }
         if (kKeyMajor) {
-          if (s == 0 && it > 0 && !waitw(&sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
+          if (s == 0 && it > 0 && !waitw(&sb.dv_free, (it - 1) & 1, abort_flag, P.status)) {
             ok = false;
             break;
           }
@@ -365,8 +427,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           if (!issue_s(t + 1, nids)) { ok = false; break; }
         }
         if (!waitw(&sb.ds_full[t & 1], (t >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
-        if (!kKeyMajor && s == 0 && it > 0 &&
-            !waitw(&sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
+        if (s == 0 && it > 0 &&
+            !waitw(kKeyMajor ? &sb.dk_free : &sb.acc_free, (it - 1) & 1, abort_flag, P.status)) {
           ok = false;
           break;
         }
@@ -395,13 +457,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     commit_elect(&sb.final_mma);
     mbar_wait(&sb.final_mma, 0, kWaitNs);
   } else if (warp == kWarpStore) {
-    // ===================================================== epilogue stores + X loads
+    // ===================================================== X loads + dQ-pass epilogue stores
+    regs_dec<kKeyMajor, kRegsRestKm>();
     if (lane == 0) {
       tma_prefetch_desc(&tx1);
       tma_prefetch_desc(&tx2);
-      tma_prefetch_desc(&to1);
-      if (kKeyMajor) tma_prefetch_desc(&to2);
-      // one bulk group: column half h of one output of item pi, from staging region h
+      if (!kKeyMajor) tma_prefetch_desc(&to1);
+      // one bulk group: column half h of dQ of item pi, from staging region h
       auto store_half = [&](const PairItem& pi, const CUtensorMap* map, int h) {
         for (int hh = 0; hh < 2; ++hh) {
           const int cube = hh ? pi.b : pi.a;
@@ -420,20 +482,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
         bulk_commit_group();
       };
-      // every output of item ie; on return the last round's two groups may still be reading
+      // dQ of item ie; on return its two groups may still be reading
       auto store_item = [&](const PairItem& pi, int ie) -> bool {
-        for (int r = 0; r < kRounds; ++r) {
-          const CUtensorMap* map = r == 0 ? &to1 : &to2;
-          for (int h = 0; h < 2; ++h) {
-            if (!wait1(&sb.stage_full[h], (ie * kRounds + r) & 1, abort_flag, P.status)) return false;
-            store_half(pi, map, h);
-          }
-          if (r + 1 < kRounds) {
-            bulk_wait_group_read1();
-            mbar_arrive(&sb.stage_free[0]);
-            bulk_wait_group_read0();
-            mbar_arrive(&sb.stage_free[1]);
-          }
+        for (int h = 0; h < 2; ++h) {
+          if (!wait1(&sb.stage_full[h], ie & 1, abort_flag, P.status)) return false;
+          store_half(pi, &to1, h);
         }
         return true;
       };
@@ -457,16 +510,18 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         if (kKeyMajor) {
-          // X shares its buffer with the previous item's staging: each half is
-          // loaded as soon as the stores from that region have read it
-          if (it > 0 && !store_item(prev, it - 1)) { ok = false; break; }
+          // the previous item's last S^T and dP^T products have read X
+          if (it > 0 && !wait1(&sb.x_empty, (it - 1) & 1, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
         } else if (it > 0) {
           // dQ pass: X(it-1) has been copied into TMEM (at the end of item
           // it-2); the epilogue of item it-2 staged into X after that copy
           if (!wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) { ok = false; break; }
           if (it > 1 && !store_item(pprev, it - 2)) { ok = false; break; }
         }
-        const bool staged = kKeyMajor ? it > 0 : it > 1;  // stores from X may still be reading
+        const bool staged = !kKeyMajor && it > 1;  // stores from X may still be reading
         mbar_arrive_expect_tx(&sb.x_full, 2 * L::kXBytes);
         if (staged) bulk_wait_group_read1();
         load_x(pi, 0);
@@ -476,19 +531,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         prev = pi;
         ++it;
       }
-      if (ok && it > 0 && !is_aborted(abort_flag)) {
-        if (kKeyMajor) {
-          store_item(prev, it - 1);
-        } else if (wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) {
-          if (it > 1 && store_item(pprev, it - 2)) store_item(prev, it - 1);
-          else if (it == 1) store_item(prev, 0);
-        }
+      if (!kKeyMajor && ok && it > 0 && !is_aborted(abort_flag) &&
+          wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) {
+        if (it > 1 && store_item(pprev, it - 2)) store_item(prev, it - 1);
+        else if (it == 1) store_item(prev, 0);
       }
       bulk_wait_group0();
       if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);
     }
   } else if (warp < kSoftmaxWarpsBwd) {
-    // ===================================================== softmax-backward + epilogue
+    // ===================================================== softmax-backward + dQ epilogue
+    regs_inc<kKeyMajor, kRegsSoftmaxKm>();
     const int quarter = warp & 3;
     const int hc = warp >> 2;                 // step tile = column half of S and dP
     const int row = quarter * 32 + lane;
@@ -549,17 +602,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       // dQ pass: the first item's Q and dO go to TMEM here, later items' at the
       // end of the item before them
       if (!kKeyMajor && it == 0 && !copy_x_to_tmem(0)) break;
-      // this warp's half of the pooled rows, lane l holding column 32cc + l
-      float pr1[D / 64], pr2[D / 64];
+      // dQ pass: this warp's half of the pooled row, lane l holding column 32cc + l
+      float pr1[D / 64];
       {
-        const float* s1 = (row_live && P.pooled1) ? P.pooled1 + prow * D + hc * (D / 2) : nullptr;
-        const float* s2 = (kKeyMajor && row_live && P.pooled2) ? P.pooled2 + prow * D + hc * (D / 2)
-                                                               : nullptr;
+        const float* s1 =
+            (!kKeyMajor && row_live && P.pooled1) ? P.pooled1 + prow * D + hc * (D / 2) : nullptr;
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          pr1[cc] = s1 ? __ldg(s1 + 32 * cc + lane) : 0.f;
-          pr2[cc] = s2 ? __ldg(s2 + 32 * cc + lane) : 0.f;
-        }
+        for (int cc = 0; cc < D / 64; ++cc) pr1[cc] = s1 ? __ldg(s1 + 32 * cc + lane) : 0.f;
       }
       float row_lse = 0.f, row_delta = 0.f;
       if (!kKeyMajor && row_live) {
@@ -679,29 +728,67 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           if (!waitw(&sb.x_free, (it + 1) & 1, abort_flag, P.status)) break;
         }
       }
-      // ---------------------------------------------- epilogue
-      if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
-      tc_fence_after();
-      if (row_live)
-        stage_half_row<D>(tb + lane_addr + kColA1, hc, row, kKeyMajor ? 1.f : g.scale, pr1, staging);
+      // ---------------------------------------------- dQ epilogue
+      // (key-major: the epilogue warps drain dV and dK)
       if (!kKeyMajor) {
+        if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
+        tc_fence_after();
+        if (row_live) stage_half_row<D>(tb + lane_addr + kColA1, hc, row, g.scale, pr1, staging);
         tc_fence_before();
         warp_arrive_bwd(&sb.acc_free);
-      }
-      fence_proxy_async_smem();  // staging writes -> visible to the TMA store
-      warp_arrive_bwd(&sb.stage_full[hc]);
-      if (kKeyMajor) {
-        // dK once the stores of dV have read this half of the staging buffer
-        if (!waitw(&sb.stage_free[hc], it & 1, abort_flag, P.status)) break;
-        if (row_live)
-          stage_half_row<D>(tb + lane_addr + kColA2, hc, row, g.scale, pr2, staging);
-        tc_fence_before();
-        warp_arrive_bwd(&sb.acc_free);
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();  // staging writes -> visible to the TMA store
         warp_arrive_bwd(&sb.stage_full[hc]);
       }
       ++it;
     }
+  } else if (kKeyMajor && warp >= kWarpEpi0) {
+    // ===================================================== key-major epilogue
+    regs_dec<kKeyMajor, kRegsRestKm>();
+    const int quarter = warp & 3;
+    const bool second = quarter >= 2;  // rows 64..127: the item's second key cube
+    const uint32_t tq = tb + (static_cast<uint32_t>(quarter * 32) << 16);
+    int it = 0;
+    for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
+      const PairItem pi = P.items[P.order ? P.order[item] : item];
+      if (pi.count == 0) continue;  // the softmax warps write its pooled rows
+      const int cube = second ? pi.b : pi.a;
+      const bool live = !second || pi.b >= 0;  // warp-uniform
+      size_t orow[4];
+      float2 p1[D / 64], p2[D / 64];
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) p1[k] = p2[k] = make_float2(0.f, 0.f);
+      if (live) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          orow[r] = static_cast<size_t>(pi.bh) * g.N +
+                    caller_row(g, cube, (32 * quarter + 8 * r + lane / 4) & 63);
+        const size_t prow = static_cast<size_t>(pi.bh) * g.Nc + cube;
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) {
+          const size_t o = prow * D + 2 * (lane + 32 * k);
+          if (P.pooled1) {
+            const float2 a = __ldg(reinterpret_cast<const float2*>(P.pooled1 + o));
+            p1[k] = make_float2(a.x * (1.f / kTile), a.y * (1.f / kTile));
+          }
+          if (P.pooled2) {
+            const float2 a = __ldg(reinterpret_cast<const float2*>(P.pooled2 + o));
+            p2[k] = make_float2(a.x * (1.f / kTile), a.y * (1.f / kTile));
+          }
+        }
+      }
+      if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
+      tc_fence_after();
+      if (live) drain_acc<D>(tq + kColA1, 1.f, p1, P.out1, orow);
+      tc_fence_before();
+      warp_arrive_bwd(&sb.dv_free);
+      if (live) drain_acc<D>(tq + kColA2, g.scale, p2, P.out2, orow);
+      tc_fence_before();
+      warp_arrive_bwd(&sb.dk_free);
+      ++it;
+    }
+  } else if (kKeyMajor) {
+    // warp 11: no role; completes warpgroup 2's register split
+    regs_dec<kKeyMajor, kRegsRestKm>();
   }
 
   tc_fence_before();
@@ -713,11 +800,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 template <int D, bool kKeyMajor>
 cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y1, const void* y2,
                     BwdParams p, cudaStream_t s) {
-  alignas(64) CUtensorMap m1, m2, m3, m4, mo1, mo2;
+  alignas(64) CUtensorMap m1, m2, m3, m4, mo1;
   const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
   if (!encode_tiled_2d(&m1, x1, rows, D, 64, 64) || !encode_tiled_2d(&m2, x2, rows, D, 64, 64) ||
       !encode_tiled_2d(&m3, y1, rows, D, 64, 64) || !encode_tiled_2d(&m4, y2, rows, D, 64, 64) ||
-      !encode_out_f32(&mo1, p.out1, g) || !encode_out_f32(&mo2, kKeyMajor ? p.out2 : p.out1, g))
+      !encode_out_f32(&mo1, p.out1, g))
     return cudaErrorInvalidValue;
   const int smem = BwdSmem<D>::kBytes;
   auto kern = fine_bwd_kernel<D, kKeyMajor>;
@@ -725,7 +812,7 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreadsBwd, smem, s>>>(m1, m2, m3, m4, mo1, mo2, p);
+  kern<<<grid, kKeyMajor ? kThreadsKm : kThreadsBwd, smem, s>>>(m1, m2, m3, m4, mo1, p);
   return cudaGetLastError();
 }
 
