@@ -29,25 +29,21 @@
 // dQ(t) has read them.
 // Y1 and Y2 come through separate TMA rings (Y1 is read by the last product
 // of a step, Y2 earlier, so Y1 gets the deeper ring).
-// Epilogue: the accumulators are scaled and the pooled gradient is added.
-//  * dQ pass: the rows are written to shared memory in the X operand buffers,
-//    which are free once Q and dO of the next item are in TMEM, and leave
-//    through TMA stores (a 4-D box of one 4x4x4 cube x 32 columns for the
-//    raster layout), so the global writes are whole lines; the item after
-//    next has its X loaded once those stores have read shared memory.
-//  * key-major pass: four epilogue warps (one per TMEM lane quarter) read dV
-//    and then dK out of TMEM and write them straight to global memory, four
-//    threads per row and 32 whole bytes of a row per group, while the softmax
-//    warps go on with the next item.  X holds no staging, so the next item's
-//    K and V are loaded as soon as the item's last S^T and dP^T products are
-//    done; its first dV product waits only until the epilogue has read dV,
-//    its first dK product until it has read dK.
-// Warps 0-7: softmax (and the dQ-pass epilogue); warp w reads TMEM lane
-// quarter w%4 (32 rows) and the 64 columns of step tile w/4, so each thread
-// owns half a row.  Warp 8: TMA loads of Y1/Y2.  Warp 9: UMMA issue.  Warp 10:
-// TMA loads of X and, in the dQ pass, the TMA stores of the epilogue.  The
-// key-major pass adds warps 11 (idle) and 12-15 (epilogue) and splits the
-// registers per warpgroup: 168 a thread for the softmax warps, 88 for the rest.
+// Epilogue: four epilogue warps (one per TMEM lane quarter) read the
+// accumulators out of TMEM, scale them, add the pooled gradient and write them
+// straight to global memory, four threads per row and 32 whole bytes of a row
+// per group, while the softmax warps go on with the next item (a 128 KB drain
+// takes several thousand cycles at the SM's store rate, so it must not hold
+// them).  dQ pass: X(i+1) is loaded once Q and dO of item i are in TMEM, and
+// the next item's first dQ product waits until the epilogue has read dQ.
+// Key-major pass: the next item's K and V are loaded as soon as the item's
+// last S^T and dP^T products are done; its first dV product waits until the
+// epilogue has read dV, its first dK product until it has read dK.
+// Warps 0-7: softmax; warp w reads TMEM lane quarter w%4 (32 rows) and the 64
+// columns of step tile w/4, so each thread owns half a row.  Warp 8: TMA loads
+// of Y1/Y2.  Warp 9: UMMA issue.  Warp 10: TMA loads of X.  Warp 11: idle.
+// Warps 12-15: epilogue.  Registers are split per warpgroup: 168 a thread for
+// the softmax warps, 88 for the rest.
 // Bounded waits and the abort path are as in the forward kernel.
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
@@ -55,12 +51,11 @@
 namespace vsa {
 namespace {
 
-constexpr int kThreadsBwd = 352;  // dQ pass: 11 warps
-constexpr int kThreadsKm = 512;   // key-major pass: 16 warps
+constexpr int kThreadsBwd = 512;  // 16 warps
 constexpr int kSoftmaxWarpsBwd = 8;
-constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpStore = 10, kWarpEpi0 = 12;
+constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpLoadX = 10, kWarpEpi0 = 12;
 constexpr int kEpiWarps = 4;
-// key-major register split: the launch gives 65536 / 512 = 128 a thread
+// register split: the launch gives 65536 / 512 = 128 a thread
 constexpr int kRegsSoftmaxKm = 168, kRegsRestKm = 88;
 static_assert(256 * kRegsSoftmaxKm + 256 * kRegsRestKm <= 65536, "split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
@@ -85,9 +80,6 @@ struct BwdSmem {
   static constexpr int kStages1 = (D == 128) ? 3 : 4;    // Y1 ring
   static constexpr int kStages2 = (D == 128) ? 2 : 4;    // Y2 ring
   static constexpr int kTileBytes = 64 * D * 2;
-  // epilogue staging (128 rows x D fp32, 32-column chunks of 16 KB) = X1 + X2
-  static constexpr int kStageChunk = 128 * 128;
-  static_assert((D / 32) * kStageChunk == 2 * kXBytes, "staging must fill X1 + X2");
   static constexpr int kBytes = (2 + kStages1 + kStages2) * kXBytes + 1024;
 };
 
@@ -99,7 +91,6 @@ struct BwdBars {
   uint64_t a_ready, x_free;  // dQ pass: the item's Q, dO copied from X into TMEM
   uint64_t x_empty;          // key-major pass: the item's last S^T and dP^T are done
   uint64_t dv_free, dk_free; // key-major pass: the epilogue has read dV / dK
-  uint64_t stage_full[2];  // dQ pass, by column half = staging region X1 / X2
   uint32_t tmem_base;
   int abort;
 };
@@ -183,37 +174,11 @@ __device__ __forceinline__ void drain_acc(uint32_t tq, float mul, const float2 (
   }
 }
 
-// Accumulator row (times `mul`, plus pooled/64) -> staging, columns of this
-// thread's half, in the SW128 image the TMA store expects: 16-byte unit u of
-// row r of a 32-column chunk sits at unit position u ^ (r % 8).  pr[cc] holds,
-// in lane l, column 32*cc + l of this half of the warp's pooled row.
-template <int D>
-__device__ __forceinline__ void stage_half_row(uint32_t tacc, int hc, int row, float mul,
-                                               const float (&pr)[D / 64], uint8_t* staging) {
-#pragma unroll
-  for (int cc = 0; cc < D / 64; ++cc) {
-    const int c = hc * (D / 64) + cc;  // 32-column chunk index
-    uint32_t v[32];
-    tmem_ld32(tacc + 32 * c, v);
-    tmem_wait_ld();
-    uint8_t* rowp = staging + c * (128 * 128) + row * 128;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      float r[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        r[e] = fmaf(__shfl_sync(0xffffffffu, pr[cc], 4 * u + e), 1.f / kTile,
-                    __uint_as_float(v[4 * u + e]) * mul);
-      *reinterpret_cast<float4*>(rowp + ((u ^ (row & 7)) << 4)) = make_float4(r[0], r[1], r[2], r[3]);
-    }
-  }
-}
-
 template <int D, bool kKeyMajor>
-__global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
+__global__ void __launch_bounds__(kThreadsBwd, 1)
     fine_bwd_kernel(const __grid_constant__ CUtensorMap tx1, const __grid_constant__ CUtensorMap tx2,
                     const __grid_constant__ CUtensorMap ty1, const __grid_constant__ CUtensorMap ty2,
-                    const __grid_constant__ CUtensorMap to1, BwdParams P) {
+                    BwdParams P) {
   using L = BwdSmem<D>;
   constexpr int kS1 = L::kStages1, kS2 = L::kStages2;
   constexpr int kKSteps = D / 16;
@@ -224,7 +189,6 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
   uint8_t* sX2 = sX1 + L::kXBytes;
   uint8_t* sY1 = sX2 + L::kXBytes;  // ring of kS1 operands
   uint8_t* sY2 = sY1 + kS1 * L::kXBytes;
-  uint8_t* staging = sX1;           // dQ pass: X1 + X2, once the item's products are done
   __shared__ BwdBars sb;
   int* abort_flag = &sb.abort;
   const Geom& g = P.g;
@@ -247,14 +211,12 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
       mbar_init(&sb.ds_full[i], kSoftmaxWarpsBwd);
     }
     mbar_init(&sb.acc_full, 1);
-    mbar_init(&sb.acc_free, kSoftmaxWarpsBwd);
+    mbar_init(&sb.acc_free, kEpiWarps);
     mbar_init(&sb.a_ready, kSoftmaxWarpsBwd);
     mbar_init(&sb.x_free, kSoftmaxWarpsBwd);
     mbar_init(&sb.x_empty, 1);
     mbar_init(&sb.dv_free, kEpiWarps);
     mbar_init(&sb.dk_free, kEpiWarps);
-    for (int i = 0; i < 2; ++i)
-      mbar_init(&sb.stage_full[i], kSoftmaxWarpsBwd / 2);  // the four warps of a column half
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
     fence_barrier_init();
@@ -273,7 +235,7 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
 
   if (warp == kWarpLoadY) {
     // ===================================================== TMA loads of Y1, Y2
-    regs_dec<kKeyMajor, kRegsRestKm>();
+    regs_dec<true, kRegsRestKm>();
     if (lane == 0) {
       tma_prefetch_desc(&ty1);
       tma_prefetch_desc(&ty2);
@@ -330,7 +292,7 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
     }
   } else if (warp == kWarpIssue) {
     // ===================================================== UMMA issuer
-    regs_dec<kKeyMajor, kRegsRestKm>();
+    regs_dec<true, kRegsRestKm>();
     const uint32_t id_s128 = idesc_f16(128, 128, 0, 0);
     const uint32_t id_s64 = idesc_f16(128, 64, 0, 0);
     const uint32_t id_acc = idesc_f16(128, D, 0, 1);
@@ -456,40 +418,12 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
     }
     commit_elect(&sb.final_mma);
     mbar_wait(&sb.final_mma, 0, kWaitNs);
-  } else if (warp == kWarpStore) {
-    // ===================================================== X loads + dQ-pass epilogue stores
-    regs_dec<kKeyMajor, kRegsRestKm>();
+  } else if (warp == kWarpLoadX) {
+    // ===================================================== TMA loads of X
+    regs_dec<true, kRegsRestKm>();
     if (lane == 0) {
       tma_prefetch_desc(&tx1);
       tma_prefetch_desc(&tx2);
-      if (!kKeyMajor) tma_prefetch_desc(&to1);
-      // one bulk group: column half h of dQ of item pi, from staging region h
-      auto store_half = [&](const PairItem& pi, const CUtensorMap* map, int h) {
-        for (int hh = 0; hh < 2; ++hh) {
-          const int cube = hh ? pi.b : pi.a;
-          if (cube < 0) continue;
-#pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {
-            const int c = h * (D / 64) + cc;
-            const uint8_t* src = staging + c * L::kStageChunk + hh * (64 * 128);
-            if (g.raster) {
-              const int cw = cube % g.cw, ch = (cube / g.cw) % g.ch, ct = cube / (g.cw * g.ch);
-              tma_store_4d(map, src, 32 * c, 4 * cw, 4 * ch, pi.bh * g.T + 4 * ct);
-            } else {
-              tma_store_2d(map, src, 32 * c, pi.bh * g.N + cube * kTile);
-            }
-          }
-        }
-        bulk_commit_group();
-      };
-      // dQ of item ie; on return its two groups may still be reading
-      auto store_item = [&](const PairItem& pi, int ie) -> bool {
-        for (int h = 0; h < 2; ++h) {
-          if (!wait1(&sb.stage_full[h], ie & 1, abort_flag, P.status)) return false;
-          store_half(pi, &to1, h);
-        }
-        return true;
-      };
       // X1 (h = 0) or X2 (h = 1) of item pi
       auto load_x = [&](const PairItem& pi, int h) {
         const CUtensorMap* m = h ? &tx2 : &tx1;
@@ -503,45 +437,24 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
         }
       };
       int it = 0;
-      bool ok = true;
-      PairItem prev{}, pprev{};
-      for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-           item += gridDim.x) {
+      for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
-        if (kKeyMajor) {
-          // the previous item's last S^T and dP^T products have read X
-          if (it > 0 && !wait1(&sb.x_empty, (it - 1) & 1, abort_flag, P.status)) {
-            ok = false;
-            break;
-          }
-        } else if (it > 0) {
-          // dQ pass: X(it-1) has been copied into TMEM (at the end of item
-          // it-2); the epilogue of item it-2 staged into X after that copy
-          if (!wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) { ok = false; break; }
-          if (it > 1 && !store_item(pprev, it - 2)) { ok = false; break; }
-        }
-        const bool staged = !kKeyMajor && it > 1;  // stores from X may still be reading
+        // X of the previous item is no longer read: key-major, its last S^T
+        // and dP^T products are done; dQ pass, its Q and dO are in TMEM
+        if (it > 0 && !wait1(kKeyMajor ? &sb.x_empty : &sb.x_free, (it - 1) & 1, abort_flag,
+                             P.status))
+          break;
         mbar_arrive_expect_tx(&sb.x_full, 2 * L::kXBytes);
-        if (staged) bulk_wait_group_read1();
         load_x(pi, 0);
-        if (staged) bulk_wait_group_read0();
         load_x(pi, 1);
-        pprev = prev;
-        prev = pi;
         ++it;
       }
-      if (!kKeyMajor && ok && it > 0 && !is_aborted(abort_flag) &&
-          wait1(&sb.x_free, (it - 1) & 1, abort_flag, P.status)) {
-        if (it > 1 && store_item(pprev, it - 2)) store_item(prev, it - 1);
-        else if (it == 1) store_item(prev, 0);
-      }
-      bulk_wait_group0();
-      if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);
+      if (it > 0) mbar_wait(&sb.x_full, (it - 1) & 1, kWaitNs);  // the last copy lands
     }
   } else if (warp < kSoftmaxWarpsBwd) {
-    // ===================================================== softmax-backward + dQ epilogue
-    regs_inc<kKeyMajor, kRegsSoftmaxKm>();
+    // ===================================================== softmax-backward
+    regs_inc<true, kRegsSoftmaxKm>();
     const int quarter = warp & 3;
     const int hc = warp >> 2;                 // step tile = column half of S and dP
     const int row = quarter * 32 + lane;
@@ -602,14 +515,6 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
       // dQ pass: the first item's Q and dO go to TMEM here, later items' at the
       // end of the item before them
       if (!kKeyMajor && it == 0 && !copy_x_to_tmem(0)) break;
-      // dQ pass: this warp's half of the pooled row, lane l holding column 32cc + l
-      float pr1[D / 64];
-      {
-        const float* s1 =
-            (!kKeyMajor && row_live && P.pooled1) ? P.pooled1 + prow * D + hc * (D / 2) : nullptr;
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) pr1[cc] = s1 ? __ldg(s1 + 32 * cc + lane) : 0.f;
-      }
       float row_lse = 0.f, row_delta = 0.f;
       if (!kKeyMajor && row_live) {
         const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + (row & 63);
@@ -718,34 +623,18 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
       if (!kKeyMajor) {
         // every S and dP product of this item is complete (phase 2 of its last
         // step saw its dP): the next item's Q and dO may replace these in TMEM,
-        // so its first products run while this item's epilogue does
+        // so its first products run while the epilogue warps drain dQ
         int nx = item + gridDim.x;
         while (nx < P.n_items && P.items[P.order ? P.order[nx] : nx].count == 0) nx += gridDim.x;
-        if (nx < P.n_items) {
-          if (!copy_x_to_tmem(it + 1)) break;
-          // the epilogue below stages into X: every warp's copy must be done
-          // (the two warps of a lane quarter read the same X rows)
-          if (!waitw(&sb.x_free, (it + 1) & 1, abort_flag, P.status)) break;
-        }
-      }
-      // ---------------------------------------------- dQ epilogue
-      // (key-major: the epilogue warps drain dV and dK)
-      if (!kKeyMajor) {
-        if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
-        tc_fence_after();
-        if (row_live) stage_half_row<D>(tb + lane_addr + kColA1, hc, row, g.scale, pr1, staging);
-        tc_fence_before();
-        warp_arrive_bwd(&sb.acc_free);
-        fence_proxy_async_smem();  // staging writes -> visible to the TMA store
-        warp_arrive_bwd(&sb.stage_full[hc]);
+        if (nx < P.n_items && !copy_x_to_tmem(it + 1)) break;
       }
       ++it;
     }
-  } else if (kKeyMajor && warp >= kWarpEpi0) {
-    // ===================================================== key-major epilogue
-    regs_dec<kKeyMajor, kRegsRestKm>();
+  } else if (warp >= kWarpEpi0) {
+    // ===================================================== epilogue
+    regs_dec<true, kRegsRestKm>();
     const int quarter = warp & 3;
-    const bool second = quarter >= 2;  // rows 64..127: the item's second key cube
+    const bool second = quarter >= 2;  // rows 64..127: the item's second cube
     const uint32_t tq = tb + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0;
     for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
@@ -778,17 +667,20 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
       }
       if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
       tc_fence_after();
-      if (live) drain_acc<D>(tq + kColA1, 1.f, p1, P.out1, orow);
+      // dQ pass: dQ = scale * acc; key-major: dV = acc, then dK = scale * acc
+      if (live) drain_acc<D>(tq + kColA1, kKeyMajor ? 1.f : g.scale, p1, P.out1, orow);
       tc_fence_before();
-      warp_arrive_bwd(&sb.dv_free);
-      if (live) drain_acc<D>(tq + kColA2, g.scale, p2, P.out2, orow);
-      tc_fence_before();
-      warp_arrive_bwd(&sb.dk_free);
+      warp_arrive_bwd(kKeyMajor ? &sb.dv_free : &sb.acc_free);
+      if (kKeyMajor) {
+        if (live) drain_acc<D>(tq + kColA2, g.scale, p2, P.out2, orow);
+        tc_fence_before();
+        warp_arrive_bwd(&sb.dk_free);
+      }
       ++it;
     }
-  } else if (kKeyMajor) {
+  } else {
     // warp 11: no role; completes warpgroup 2's register split
-    regs_dec<kKeyMajor, kRegsRestKm>();
+    regs_dec<true, kRegsRestKm>();
   }
 
   tc_fence_before();
@@ -800,11 +692,10 @@ __global__ void __launch_bounds__(kKeyMajor ? kThreadsKm : kThreadsBwd, 1)
 template <int D, bool kKeyMajor>
 cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y1, const void* y2,
                     BwdParams p, cudaStream_t s) {
-  alignas(64) CUtensorMap m1, m2, m3, m4, mo1;
+  alignas(64) CUtensorMap m1, m2, m3, m4;
   const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
   if (!encode_tiled_2d(&m1, x1, rows, D, 64, 64) || !encode_tiled_2d(&m2, x2, rows, D, 64, 64) ||
-      !encode_tiled_2d(&m3, y1, rows, D, 64, 64) || !encode_tiled_2d(&m4, y2, rows, D, 64, 64) ||
-      !encode_out_f32(&mo1, p.out1, g))
+      !encode_tiled_2d(&m3, y1, rows, D, 64, 64) || !encode_tiled_2d(&m4, y2, rows, D, 64, 64))
     return cudaErrorInvalidValue;
   const int smem = BwdSmem<D>::kBytes;
   auto kern = fine_bwd_kernel<D, kKeyMajor>;
@@ -812,7 +703,7 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kKeyMajor ? kThreadsKm : kThreadsBwd, smem, s>>>(m1, m2, m3, m4, mo1, p);
+  kern<<<grid, kThreadsBwd, smem, s>>>(m1, m2, m3, m4, p);
   return cudaGetLastError();
 }
 
