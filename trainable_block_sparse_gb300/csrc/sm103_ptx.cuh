@@ -69,15 +69,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of being woken at the
+// hardware's own (shorter) interval to poll again.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed, for at most
 // `limit_ns` nanoseconds.  Returns false on time-out (the caller records it and
-// unwinds); a wait never spins forever.
+// unwinds); a wait never spins forever.  After the first test the thread
+// sleeps between tests, so a waiting warp takes few issue slots from the warps
+// that share its scheduler.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
