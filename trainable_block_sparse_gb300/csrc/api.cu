@@ -223,28 +223,6 @@ bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t 
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_out_f32(void* map, float* base, const Geom& g) {
-  if (!encoder()) return false;
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  const uint64_t D = static_cast<uint64_t>(g.D);
-  if (g.raster) {
-    const cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(g.W), static_cast<cuuint64_t>(g.H),
-                                static_cast<cuuint64_t>(g.BH) * g.T};
-    const cuuint64_t strides[3] = {D * 4, D * 4 * g.W, D * 4 * g.W * g.H};
-    const cuuint32_t box[4] = {32, 4, 4, 4};
-    return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims,
-                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-  }
-  const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(g.BH) * g.N};
-  const cuuint64_t strides[1] = {D * 4};
-  const cuuint32_t box[2] = {32, 64};
-  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
-                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace vsa
 
 using namespace vsa;

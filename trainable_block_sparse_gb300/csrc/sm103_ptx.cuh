@@ -147,30 +147,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // Tiled bulk copies shared -> global (TMA store), tracked by bulk groups.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
-                                             int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
                                              int32_t y, int32_t z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int32_t x,
-                                             int32_t y, int32_t z, int32_t w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
-          "l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 
@@ -181,12 +163,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 // The shared-memory sources of every committed bulk store have been read.
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// The shared-memory sources of all but the most recent committed bulk store
-// group have been read.
-__device__ __forceinline__ void bulk_wait_group_read1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // Every committed bulk store has completed.

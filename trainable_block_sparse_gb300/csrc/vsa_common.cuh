@@ -192,11 +192,4 @@ bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t 
 bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols);
 
-// TMA store map for an fp32 [BH, N, D] tensor in the caller's layout, with a
-// box of one 64-token cube x 32 columns whose shared-memory image is 64 rows of
-// 128 bytes in cube order (SW128 swizzle).  Raster layout: a 4-D view
-// (D, W, H, BH*T) with box (32, 4, 4, 4), addressed (32c, 4*cw, 4*ch, bh*T + 4*ct);
-// cube layout: a 2-D view (D, BH*N) with box (32, 64), addressed (32c, bh*N + 64*cube).
-bool encode_out_f32(void* map, float* base, const Geom& g);
-
 }  // namespace vsa
