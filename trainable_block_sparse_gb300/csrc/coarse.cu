@@ -400,19 +400,25 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
   const int rows = g.BH * Nc;
   rowdot_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, D, doc, oc, ws.cdelta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // operand pairs, both orientations where a product contracts over cubes
+  // The backward's products run as plain tf32 (operands rounded to tf32, one
+  // product per k-step): unlike the forward's logits they decide no selection,
+  // and their gradients reach dq, dk, dv divided by 64.  Operands in both
+  // orientations where a product contracts over cubes; no lo parts.
   {
-    const SplitSpec sp[7] = {{qc, D, ND, Nc, D, ws.qh, ws.ql, D, ND, false},
-                             {kc, D, ND, Nc, D, ws.kh, ws.kl, D, ND, false},
-                             {vc, D, ND, Nc, D, ws.vh, ws.vl, D, ND, false},
-                             {doc, D, ND, Nc, D, ws.doh, ws.dol, D, ND, false},
-                             {qc, D, ND, Nc, D, ws.qth, ws.qtl, ldc, DC, true},
-                             {kc, D, ND, Nc, D, ws.kth, ws.ktl, ldc, DC, true},
-                             {doc, D, ND, Nc, D, ws.doth, ws.dotl, ldc, DC, true}};
+    const SplitSpec sp[7] = {{qc, D, ND, Nc, D, ws.qh, nullptr, D, ND, false},
+                             {kc, D, ND, Nc, D, ws.kh, nullptr, D, ND, false},
+                             {vc, D, ND, Nc, D, ws.vh, nullptr, D, ND, false},
+                             {doc, D, ND, Nc, D, ws.doh, nullptr, D, ND, false},
+                             {qc, D, ND, Nc, D, ws.qth, nullptr, ldc, DC, true},
+                             {kc, D, ND, Nc, D, ws.kth, nullptr, ldc, DC, true},
+                             {doc, D, ND, Nc, D, ws.doth, nullptr, ldc, DC, true}};
     if ((e = launch_split_tf32(sp, 7, g.BH, s))) return e;
   }
+  auto hi = [](const float* h, int ld, long long stride) {
+    return TgemmOperand{h, nullptr, ld, stride};
+  };
   // query-major tiles: P = exp(scale Q_c K_c^T - lse) and dL = P (.) (dO_c V_c^T - delta)
-  // in registers from two accumulators; dL leaves as a pair
+  // in registers from two accumulators; dL leaves rounded to tf32
   constexpr float kLog2e = 1.4426950408889634f;
   TgemmArgs a = gemm(g, Nc, Nc, D, g.scale * kLog2e);
   a.mode = kTgAttnBwdRow;
@@ -421,42 +427,32 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
   a.v2 = ws.cdelta;
   a.vec_stride = Nc;
   a.out_hi = ws.ach;
-  a.out_lo = ws.acl;
   a.split_ld = ldc;
   a.split_stride = NC;
-  if ((e = launch_tgemm_dual(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND),
-                             pair(ws.doh, ws.dol, D, ND), pair(ws.vh, ws.vl, D, ND), ws.status,
-                             s)))
+  if ((e = launch_tgemm_dual(a, hi(ws.qh, D, ND), hi(ws.kh, D, ND), hi(ws.doh, D, ND),
+                             hi(ws.vh, D, ND), ws.status, s)))
     return e;
-  // key-major tiles of the same two products (the transposes): dL^T and P^T as pairs,
+  // key-major tiles of the same two products (the transposes): dL^T and P^T,
   // lse and delta now per column
   a.mode = kTgAttnBwdCol;
   a.out_hi = ws.dlth;
-  a.out_lo = ws.dltl;
   a.out2_hi = ws.pth;
-  a.out2_lo = ws.ptl;
-  if ((e = launch_tgemm_dual(a, pair(ws.kh, ws.kl, D, ND), pair(ws.qh, ws.ql, D, ND),
-                             pair(ws.vh, ws.vl, D, ND), pair(ws.doh, ws.dol, D, ND), ws.status,
-                             s)))
+  if ((e = launch_tgemm_dual(a, hi(ws.kh, D, ND), hi(ws.qh, D, ND), hi(ws.vh, D, ND),
+                             hi(ws.doh, D, ND), ws.status, s)))
     return e;
   // dQ_c = scale dL K_c
   a = gemm(g, Nc, D, Nc, g.scale);
   a.out = dqc;
   a.out_ld = D;
   a.out_stride = ND;
-  if ((e = launch_tgemm(a, pair(ws.ach, ws.acl, ldc, NC), pair(ws.kth, ws.ktl, ldc, DC),
-                        ws.status, s)))
-    return e;
+  if ((e = launch_tgemm(a, hi(ws.ach, ldc, NC), hi(ws.kth, ldc, DC), ws.status, s))) return e;
   // dK_c = scale dL^T Q_c
   a.out = dkc;
-  if ((e = launch_tgemm(a, pair(ws.dlth, ws.dltl, ldc, NC), pair(ws.qth, ws.qtl, ldc, DC),
-                        ws.status, s)))
-    return e;
+  if ((e = launch_tgemm(a, hi(ws.dlth, ldc, NC), hi(ws.qth, ldc, DC), ws.status, s))) return e;
   // dV_c = P^T dO_c
   a.alpha = 1.f;
   a.out = dvc;
-  return launch_tgemm(a, pair(ws.pth, ws.ptl, ldc, NC), pair(ws.doth, ws.dotl, ldc, DC),
-                      ws.status, s);
+  return launch_tgemm(a, hi(ws.pth, ldc, NC), hi(ws.doth, ldc, DC), ws.status, s);
 }
 
 }  // namespace vsa

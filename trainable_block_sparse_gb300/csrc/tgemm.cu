@@ -7,6 +7,10 @@
 // x = hi + lo (hi = round(x), lo = round(x - hi), |x - hi - lo| <= 2^-22 |x|)
 // and a.b is accumulated as lo_a.hi_b + hi_a.lo_b + hi_a.hi_b; the dropped
 // lo_a.lo_b term is below 2^-22 |a b|, comparable to fp32 rounding.
+// Operands given without a lo part (null) run as plain tf32 instead: one
+// product per k-step from the hi parts (round-to-nearest tf32, relative error
+// 2^-11 per element), for products whose results need no more (the coarse
+// backward: its gradients reach the outputs divided by 64).
 //
 // D[b] = A[b] B[b]^T (A [M x K], B [N x K], both K-major), 128 x 128 output
 // tiles, k-blocks of 32 (one 128-byte swizzled row per operand row).  The
@@ -78,6 +82,25 @@ __device__ __forceinline__ void issue_kblock_tf32(uint32_t d, uint64_t ah, uint6
       : "memory");
 }
 
+// Plain tf32: 4 products of one k-block from the hi parts only.
+__device__ __forceinline__ void issue_kblock_tf32_hi(uint32_t d, uint64_t ah, uint64_t bh,
+                                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b64 ah, bh;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %4, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+      "mov.b64 ah, %1;\n\tmov.b64 bh, %2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %3, f;\n\t"
+      "add.s64 ah, ah, 2;\n\tadd.s64 bh, bh, 2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %3, t;\n\t"
+      "add.s64 ah, ah, 2;\n\tadd.s64 bh, bh, 2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %3, t;\n\t"
+      "add.s64 ah, ah, 2;\n\tadd.s64 bh, bh, 2;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], ah, bh, %3, t;\n\t}" ::"r"(d),
+      "l"(ah), "l"(bh), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 struct TileCoord {
   int b, tm, tn;
 };
@@ -99,11 +122,15 @@ struct TgOutMaps {
   CUtensorMap out, hi, lo, hi2, lo2;
 };
 
-template <bool kDual>
+// kPair: operands as tf32 pairs (three products per k-step); otherwise the
+// hi parts alone (one product), whose stage holds A hi and B hi at the same
+// offsets.
+template <bool kDual, bool kPair>
 __global__ void __launch_bounds__(kTgThreads, 1)
     tgemm_kernel(const __grid_constant__ TgMaps m0, const __grid_constant__ TgMaps m1,
                  const __grid_constant__ TgOutMaps om, TgemmArgs P, uint32_t* status) {
   constexpr int kProducts = kDual ? 2 : 1;
+  constexpr uint32_t kLoadBytes = kPair ? kStageBytes : 2 * kOpBytes;
   constexpr uint32_t kAccCols = kTN * kProducts;     // per tile buffer
   constexpr uint32_t kTmemCols = 2 * kAccCols;       // two tile buffers
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -143,9 +170,11 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     // ===================================================== TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&m0.ah);
-      tma_prefetch_desc(&m0.al);
       tma_prefetch_desc(&m0.bh);
-      tma_prefetch_desc(&m0.bl);
+      if (kPair) {
+        tma_prefetch_desc(&m0.al);
+        tma_prefetch_desc(&m0.bl);
+      }
       uint32_t n = 0;  // k-blocks issued
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok && !is_aborted(abort_flag); t += gridDim.x) {
@@ -160,11 +189,13 @@ __global__ void __launch_bounds__(kTgThreads, 1)
               break;
             }
             uint8_t* st = smem + slot * kStageBytes;
-            mbar_arrive_expect_tx(&sb.full[slot], kStageBytes);
+            mbar_arrive_expect_tx(&sb.full[slot], kLoadBytes);
             tma_load_3d(st, &m.ah, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
-            tma_load_3d(st + kOpBytes, &m.al, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
             tma_load_3d(st + 2 * kOpBytes, &m.bh, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
-            tma_load_3d(st + 3 * kOpBytes, &m.bl, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
+            if (kPair) {
+              tma_load_3d(st + kOpBytes, &m.al, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
+              tma_load_3d(st + 3 * kOpBytes, &m.bl, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
+            }
           }
         }
       }
@@ -193,8 +224,11 @@ __global__ void __launch_bounds__(kTgThreads, 1)
           }
           tc_fence_after();
           const uint64_t base = d0 + ((slot * kStageBytes) >> 4);
-          issue_kblock_tf32(dt, base, base + (kOpBytes >> 4), base + ((2 * kOpBytes) >> 4),
-                            base + ((3 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
+          if (kPair)
+            issue_kblock_tf32(dt, base, base + (kOpBytes >> 4), base + ((2 * kOpBytes) >> 4),
+                              base + ((3 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
+          else
+            issue_kblock_tf32_hi(dt, base, base + ((2 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
           commit_elect(&sb.empty[slot]);
         }
       }
@@ -278,14 +312,10 @@ __global__ void __launch_bounds__(kTgThreads, 1)
           }
         };
         if (P.out) store_block(&om.out, val, 0);
-        if (P.out_hi) {
-          store_block(&om.hi, val, 1);
-          store_block(&om.lo, val, 2);
-        }
-        if (kDual && P.out2_hi) {
-          store_block(&om.hi2, pv, 1);
-          store_block(&om.lo2, pv, 2);
-        }
+        if (P.out_hi) store_block(&om.hi, val, 1);
+        if (P.out_lo) store_block(&om.lo, val, 2);
+        if (kDual && P.out2_hi) store_block(&om.hi2, pv, 1);
+        if (kDual && P.out2_lo) store_block(&om.lo2, pv, 2);
       }
       tc_fence_before();
       __syncwarp();
@@ -328,7 +358,7 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
   }
   __syncthreads();
   float* h = J.hi + b * J.stride_dst;
-  float* l = J.lo + b * J.stride_dst;
+  float* l = J.lo ? J.lo + b * J.stride_dst : nullptr;  // null: hi parts only
   for (int r = threadIdx.y; r < 32; r += 8) {
     if (!J.transpose) {
       const int rr = r0 + r, cc = c0 + threadIdx.x;
@@ -336,7 +366,7 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
         const float x = t[r][threadIdx.x];
         const float xh = round_tf32(x);
         h[static_cast<size_t>(rr) * J.ld_dst + cc] = xh;
-        l[static_cast<size_t>(rr) * J.ld_dst + cc] = round_tf32(x - xh);
+        if (l) l[static_cast<size_t>(rr) * J.ld_dst + cc] = round_tf32(x - xh);
       }
     } else {
       const int cc = c0 + r, rr = r0 + threadIdx.x;  // output row = input column
@@ -344,7 +374,7 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
         const float x = t[threadIdx.x][r];
         const float xh = round_tf32(x);
         h[static_cast<size_t>(cc) * J.ld_dst + rr] = xh;
-        l[static_cast<size_t>(cc) * J.ld_dst + rr] = round_tf32(x - xh);
+        if (l) l[static_cast<size_t>(cc) * J.ld_dst + rr] = round_tf32(x - xh);
       }
     }
   }
@@ -354,12 +384,17 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
 
 namespace {
 
-bool encode_maps(TgMaps* m, const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B) {
+// Operand maps; with `pair` false only the hi parts are read (the lo maps stay zero).
+bool encode_maps(TgMaps* m, const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
+                 bool pair) {
+  memset(m, 0, sizeof(*m));
   if ((A.ld & 3) || (B.ld & 3) || (A.stride & 3) || (B.stride & 3)) return false;
+  if (!A.hi || !B.hi || (pair && (!A.lo || !B.lo))) return false;
   return encode_tiled_3d_f32(&m->ah, A.hi, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) &&
-         encode_tiled_3d_f32(&m->al, A.lo, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) &&
          encode_tiled_3d_f32(&m->bh, B.hi, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN) &&
-         encode_tiled_3d_f32(&m->bl, B.lo, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN);
+         (!pair ||
+          (encode_tiled_3d_f32(&m->al, A.lo, a.batch, a.M, a.K, A.ld, A.stride, kTK, kTM) &&
+           encode_tiled_3d_f32(&m->bl, B.lo, a.batch, a.N, a.K, B.ld, B.stride, kTK, kTN)));
 }
 
 bool encode_outs(TgOutMaps* o, const TgemmArgs& a) {
@@ -376,12 +411,12 @@ bool encode_outs(TgOutMaps* o, const TgemmArgs& a) {
          enc(&o->lo2, a.out2_lo, a.split_ld, a.split_stride);
 }
 
-template <bool kDual>
+template <bool kDual, bool kPair>
 cudaError_t run_tgemm(const TgemmArgs& a, const TgMaps& m0, const TgMaps& m1, uint32_t* status,
                       cudaStream_t s) {
   alignas(64) TgOutMaps om;
   if (!encode_outs(&om, a)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tgemm_kernel<kDual>,
+  cudaError_t e = cudaFuncSetAttribute(tgemm_kernel<kDual, kPair>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kTgSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -390,7 +425,7 @@ cudaError_t run_tgemm(const TgemmArgs& a, const TgMaps& m0, const TgMaps& m1, ui
   const long long ntiles = static_cast<long long>(a.batch) * ((a.M + kTM - 1) / kTM) *
                            ((a.N + kTN - 1) / kTN);
   const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-  tgemm_kernel<kDual><<<grid, kTgThreads, kTgSmem, s>>>(m0, m1, om, a, status);
+  tgemm_kernel<kDual, kPair><<<grid, kTgThreads, kTgSmem, s>>>(m0, m1, om, a, status);
   return cudaGetLastError();
 }
 
@@ -400,9 +435,11 @@ cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmO
                          uint32_t* status, cudaStream_t s) {
   if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
   if (a.mode != kTgScale) return cudaErrorInvalidValue;
+  const bool pair = A.lo != nullptr;
   alignas(64) TgMaps m0;
-  if (!encode_maps(&m0, a, A, B)) return cudaErrorInvalidValue;
-  return run_tgemm<false>(a, m0, m0, status, s);
+  if (!encode_maps(&m0, a, A, B, pair)) return cudaErrorInvalidValue;
+  return pair ? run_tgemm<false, true>(a, m0, m0, status, s)
+              : run_tgemm<false, false>(a, m0, m0, status, s);
 }
 
 cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
@@ -410,9 +447,12 @@ cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const T
                               cudaStream_t s) {
   if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
   if (a.mode != kTgAttnBwdRow && a.mode != kTgAttnBwdCol) return cudaErrorInvalidValue;
+  const bool pair = A.lo != nullptr;
   alignas(64) TgMaps m0, m1;
-  if (!encode_maps(&m0, a, A, B) || !encode_maps(&m1, a, A2, B2)) return cudaErrorInvalidValue;
-  return run_tgemm<true>(a, m0, m1, status, s);
+  if (!encode_maps(&m0, a, A, B, pair) || !encode_maps(&m1, a, A2, B2, pair))
+    return cudaErrorInvalidValue;
+  return pair ? run_tgemm<true, true>(a, m0, m1, status, s)
+              : run_tgemm<true, false>(a, m0, m1, status, s);
 }
 
 cudaError_t launch_split_tf32(const SplitSpec* specs, int n, int batch, cudaStream_t s) {

@@ -146,9 +146,10 @@ cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, con
 // ------------------------------------------------ tensor-core fp32 GEMM
 // D[b] = A[b] B[b]^T, A [M x K], B [N x K], both K-major, each passed as a
 // tf32 pair hi + lo (fp32 arrays of tf32 values; hi = round(x), lo = round(x -
-// hi)), accumulated in fp32 from three tf32 products (tgemm.cu).  The
-// attention-backward modes compute a second product E = A2 B2^T of the same
-// tile into a second accumulator.
+// hi)), accumulated in fp32 from three tf32 products (tgemm.cu); with every lo
+// null, one plain tf32 product from the hi parts.  The attention-backward
+// modes compute a second product E = A2 B2^T of the same tile into a second
+// accumulator.
 enum TgemmMode {
   kTgScale = 0,      // v = alpha * D
   kTgAttnBwdRow = 1, // p = exp2(alpha * D - beta * v1[m]),  v = p * (E - v2[m])
@@ -165,7 +166,8 @@ struct TgemmArgs {
   int mode;
   float alpha, beta;
   const float* v1; const float* v2; long long vec_stride;  // per-row or per-column vectors
-  // outputs, each optional: fp32 [M][N]; tf32 pair [M][N]; second tf32 pair [M][N]
+  // outputs, each optional: fp32 [M][N]; tf32 pair [M][N]; second tf32 pair
+  // [M][N] (a null lo writes the hi part alone)
   float* out; int out_ld; long long out_stride;
   float *out_hi, *out_lo; float *out2_hi, *out2_lo; int split_ld; long long split_stride;
 };
@@ -176,7 +178,7 @@ cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const T
                               cudaStream_t s);
 // tf32-pair splits, up to 8 per launch: fp32 [batch][rows][cols] (row stride
 // ld_src) -> hi, lo in the same orientation or transposed ([batch][cols][rows]),
-// row stride ld_dst.
+// row stride ld_dst; a null lo writes the hi parts alone.
 struct SplitSpec {
   const float* src; int ld_src; long long stride_src; int rows, cols;
   float* hi; float* lo; int ld_dst; long long stride_dst; bool transpose;
