@@ -112,7 +112,8 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
   ws.qorder = static_cast<int*>(take(sizeof(int) * npairs));
   ws.order_tmp = static_cast<int*>(take(sizeof(int) * (npairs + 512)));
-  // coarse logits [BH, Nc, ldc] and tf32 pairs of the coarse GEMM operands
+  // coarse logits [BH, Nc, ldc] and the coarse GEMM operands: tf32 pairs of
+  // Q_c and K_c for the logits, everything else rounded to tf32 alone
   const size_t ldc = static_cast<size_t>((g.Nc + 3) & ~3);
   ws.clogit = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * ldc * 4));
   const size_t pc_bytes = static_cast<size_t>(g.BH) * g.Nc * ldc * 4;  // [BH, Nc, ldc]
@@ -123,9 +124,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.kh = f32(pooled_bytes(g));
   ws.kl = f32(pooled_bytes(g));
   ws.vth = f32(dc_bytes);
-  ws.vtl = f32(dc_bytes);
   ws.ach = f32(pc_bytes);
-  ws.acl = f32(pc_bytes);
   if (with_backward) {
     const size_t words = (g.Nc + 31) / 32;
     ws.dof = take(half_tensor(g));
@@ -135,19 +134,12 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
     ws.dkc = static_cast<float*>(take(pooled_bytes(g)));
     ws.dvc = static_cast<float*>(take(pooled_bytes(g)));
     ws.vh = f32(pooled_bytes(g));
-    ws.vl = f32(pooled_bytes(g));
     ws.doh = f32(pooled_bytes(g));
-    ws.dol = f32(pooled_bytes(g));
     ws.kth = f32(dc_bytes);
-    ws.ktl = f32(dc_bytes);
     ws.qth = f32(dc_bytes);
-    ws.qtl = f32(dc_bytes);
     ws.doth = f32(dc_bytes);
-    ws.dotl = f32(dc_bytes);
     ws.pth = f32(pc_bytes);
-    ws.ptl = f32(pc_bytes);
     ws.dlth = f32(pc_bytes);
-    ws.dltl = f32(pc_bytes);
     ws.cdelta = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.Nc * 4));
     ws.tmask = static_cast<uint32_t*>(take(static_cast<size_t>(g.BH) * g.Nc * words * 4));
     ws.toff = static_cast<int*>(take(static_cast<size_t>(g.BH) * (g.Nc + 1) * 4));

@@ -3,19 +3,22 @@
 // dense attention on the pooled (64x shorter) sequence, the row-wise selection
 // of key cubes and the mask-to-index conversion; and its backward.
 //
-// The selection is an integer decision taken on these logits, so every
-// contraction keeps fp32 accuracy: they run on the tensor cores as
+// The selection is an integer decision taken on the logits, so their
+// contraction keeps fp32 accuracy: it runs on the tensor cores as
 // error-compensated tf32 products (each operand split into a tf32 pair
 // hi + lo, three products per step; tgemm.cu), about 1e-6 relative, where a
 // single bf16 or tf32 product would move a logit by ~1e-3, the size of the
-// smallest gap the selection has to resolve.
+// smallest gap the selection has to resolve.  The other products decide
+// nothing and run as plain tf32 (operands rounded to tf32, relative error
+// 2^-11 per element): O_c, which reaches O through a gate and a bf16
+// rounding, and the backward, whose gradients reach dq, dk, dv divided by 64.
 //
 // Structure (per (batch, head) slice, Nc cubes; "pair" = tf32 hi/lo pair):
-//   forward : L = scale Q_c K_c^T                   (GEMM -> L, fp32)
+//   forward : L = scale Q_c K_c^T                   (pair GEMM -> L, fp32)
 //             softmax statistics, A_c, top-K / mass selection, index lists
 //                                                   (one kernel, warp per row;
-//                                                    A_c written as a pair)
-//             O_c = A_c V_c                         (GEMM)
+//                                                    A_c rounded to tf32)
+//             O_c = A_c V_c                         (plain tf32 GEMM)
 //   backward: P  = exp(scale Q_c K_c^T - lse),
 //             dL = P (.) (dO_c V_c^T - rowsum(dO_c O_c))
 //                 (dual GEMM, query-major tiles -> dL pair; key-major tiles of
@@ -50,12 +53,11 @@ struct SelectArgs {
 };
 
 // One warp per query cube: softmax statistics of its logits row (row stride
-// ldc), its row of A_c as a tf32 pair (ach, acl; row stride ldc), the selection by repeated
+// ldc), its row of A_c rounded to tf32 (ach; row stride ldc), the selection by repeated
 // warp argmax (ties go to the lower cube id), and the ascending index list.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs sa, int rows_per_cta,
                                                              const float* __restrict__ logits,
-                                                             float* __restrict__ ach,
-                                                             float* __restrict__ acl, int ldc,
+                                                             float* __restrict__ ach, int ldc,
                                                              float* __restrict__ lse_c,
                                                              int* __restrict__ idx,
                                                              int* __restrict__ cnt) {
@@ -82,10 +84,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs 
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
   const float inv = 1.f / z;
   for (int j = lane; j < Nc; j += 32) {  // A_c row
-    const float p = expf(Lsm[j] - m) * inv;
-    const float h = round_tf32(p);
-    ach[arow + j] = h;
-    acl[arow + j] = round_tf32(p - h);
+    ach[arow + j] = round_tf32(expf(Lsm[j] - m) * inv);
   }
   if (lane == 0) lse_c[static_cast<size_t>(bh) * Nc + row] = m + logf(z);
   __syncwarp();
@@ -149,8 +148,7 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 template <int kPer>
 __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectArgs sa,
                                                                  const float* __restrict__ logits,
-                                                                 float* __restrict__ ach,
-                                                                 float* __restrict__ acl, int ldc,
+                                                                 float* __restrict__ ach, int ldc,
                                                                  float* __restrict__ lse_c,
                                                                  int* __restrict__ idx,
                                                                  int* __restrict__ cnt) {
@@ -192,10 +190,7 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectA
   for (int i = 0; i < kPer; ++i) {  // A_c row
     const int j = 32 * i + lane;
     if (j < Nc) {
-      const float p = e[i] * inv;
-      const float h = round_tf32(p);
-      ach[arow + j] = h;
-      acl[arow + j] = round_tf32(p - h);
+      ach[arow + j] = round_tf32(e[i] * inv);
     }
   }
   if (lane == 0) lse_c[static_cast<size_t>(bh) * Nc + row] = m + logf(z);
@@ -341,11 +336,11 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
   const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
   const long long DC = static_cast<long long>(D) * ldc;
   cudaError_t e;
-  // operand pairs: Q_c, K_c ([Nc, D]) and V_c^T ([D, Nc])
+  // operand pairs Q_c, K_c ([Nc, D]); V_c^T ([D, Nc]) rounded to tf32
   {
     const SplitSpec sp[3] = {{qc, D, ND, Nc, D, ws.qh, ws.ql, D, ND, false},
                              {kc, D, ND, Nc, D, ws.kh, ws.kl, D, ND, false},
-                             {vc, D, ND, Nc, D, ws.vth, ws.vtl, ldc, DC, true}};
+                             {vc, D, ND, Nc, D, ws.vth, nullptr, ldc, DC, true}};
     if ((e = launch_split_tf32(sp, 3, g.BH, s))) return e;
   }
   // L = scale Q_c K_c^T
@@ -355,7 +350,7 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
   a.out_stride = NC;
   if ((e = launch_tgemm(a, pair(ws.qh, ws.ql, D, ND), pair(ws.kh, ws.kl, D, ND), ws.status, s)))
     return e;
-  // softmax, selection and index lists; A_c as a pair
+  // softmax, selection and index lists; A_c rounded to tf32
   const size_t per_row = sizeof(float) * (static_cast<size_t>(Nc) + g.cap);
   int rows = static_cast<int>((160 * 1024) / per_row);
   rows = rows < 1 ? 1 : (rows > 8 ? 8 : rows);
@@ -368,25 +363,25 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
   const dim3 rgrid((Nc + kSelThreads / 32 - 1) / (kSelThreads / 32), g.BH);
   const bool reg_ok = mode == 0 || (kmax < Nc ? kmax : Nc) <= 64;
   if (reg_ok && Nc <= 8 * 32) {
-    select_reg_kernel<8><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+    select_reg_kernel<8><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ldc, lse_c, idx, cnt);
   } else if (reg_ok && Nc <= 16 * 32) {
-    select_reg_kernel<16><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+    select_reg_kernel<16><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ldc, lse_c, idx, cnt);
   } else if (reg_ok && Nc <= 36 * 32) {
-    select_reg_kernel<36><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+    select_reg_kernel<36><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ldc, lse_c, idx, cnt);
   } else if (reg_ok && Nc <= 64 * 32) {
-    select_reg_kernel<64><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+    select_reg_kernel<64><<<rgrid, kSelThreads, 0, s>>>(g, sa, ws.clogit, ws.ach, ldc, lse_c, idx, cnt);
   } else {
     select_kernel<<<dim3((Nc + rows - 1) / rows, g.BH), kSelThreads, smem, s>>>(
-        g, sa, rows, ws.clogit, ws.ach, ws.acl, ldc, lse_c, idx, cnt);
+        g, sa, rows, ws.clogit, ws.ach, ldc, lse_c, idx, cnt);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // O_c = A_c V_c
+  // O_c = A_c V_c, plain tf32
   a = gemm(g, Nc, D, Nc, 1.f);
   a.out = oc;
   a.out_ld = D;
   a.out_stride = ND;
-  return launch_tgemm(a, pair(ws.ach, ws.acl, ldc, NC), pair(ws.vth, ws.vtl, ldc, DC), ws.status,
-                      s);
+  return launch_tgemm(a, TgemmOperand{ws.ach, nullptr, ldc, NC},
+                      TgemmOperand{ws.vth, nullptr, ldc, DC}, ws.status, s);
 }
 
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,

@@ -66,14 +66,16 @@ struct Workspace {
   uint32_t* qlist;        // [n_qpairs][2*cap] union lists
   int n_qpairs;
   float* clogit;          // fp32 [BH, Nc, Nc] coarse logits (forward)
-  // tf32 hi/lo pairs of the coarse GEMM operands (x = hi + lo); "c" arrays are
-  // [BH, Nc, ldc] or [BH, D, ldc] with ldc = Nc rounded up to 4, the others [BH, Nc, D]
+  // coarse GEMM operands: Q_c and K_c as tf32 hi/lo pairs (x = hi + lo, for
+  // the logits), the rest rounded to tf32 alone; the "t" arrays are
+  // [BH, D, ldc], A_c / dL / P^T / dL^T [BH, Nc, ldc] with ldc = Nc rounded up
+  // to 4, the others [BH, Nc, D]
   float *qh, *ql, *kh, *kl;        // Q_c, K_c
-  float *vth, *vtl;                // V_c^T [D, ldc]
-  float *ach, *acl;                // A_c (fwd), dL (bwd)   [Nc, ldc]
-  float *vh, *vl, *doh, *dol;      // V_c, dO_c (bwd)
-  float *kth, *ktl, *qth, *qtl, *doth, *dotl;  // K_c^T, Q_c^T, dO_c^T (bwd) [D, ldc]
-  float *pth, *ptl, *dlth, *dltl;  // P^T, dL^T (bwd) [Nc, ldc]
+  float* vth;                      // V_c^T
+  float* ach;                      // A_c (fwd), dL (bwd)
+  float *vh, *doh;                 // V_c, dO_c (bwd)
+  float *kth, *qth, *doth;         // K_c^T, Q_c^T, dO_c^T (bwd)
+  float *pth, *dlth;               // P^T, dL^T (bwd)
   // backward
   void* dof;              // bf16 cube order
   float* delta;           // fp32 [BH, N]
