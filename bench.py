@@ -272,7 +272,7 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=3):
     v["lse_c"] = bufs.view("lse_c", torch.float32, (B, H, nc))
     v["idx"] = bufs.view("idx", torch.int32, (B, H, nc, cap))
     v["cnt"] = bufs.view("cnt", torch.int32, (B, H, nc))
-    v["o_f"] = bufs.view("o_f", torch.float32, (B, H, N, D))
+    v["o_f"] = bufs.view("o_f", torch.float16, (B, H, N, D))
     v["lse_f"] = bufs.view("lse_f", torch.float32, (B, H, N))
     f32 = dict(dtype=torch.float32, device=dev)
     o = torch.empty_like(t["q"])

@@ -97,7 +97,7 @@ typedef struct {
   size_t lse_c;                  /* fp32 [B,heads,Nc]: coarse log-sum-exp (natural log) */
   size_t idx;                    /* int32 [B,heads,Nc,list_cap]: ascending key-cube ids, -1 padded */
   size_t cnt;                    /* int32 [B,heads,Nc]: entries used per list */
-  size_t o_f;                    /* fp32 [B,heads,N,D] cube order: fine output */
+  size_t o_f;                    /* fp16 [B,heads,N,D] cube order: fine output */
   size_t lse_f;                  /* fp32 [B,heads,N] cube order: fine log-sum-exp */
   size_t total;                  /* = vsa_saved_bytes() */
   int32_t list_cap;              /* topk (TOPK) or kmax (MASS) */
@@ -174,11 +174,12 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
  * (any ascending lists with entries in [0, Nc) work, e.g. injected ones).
  * gc, gf  : bf16 gates in cfg->layout order.  oc: fp32 [B,heads,Nc,D].
  * o       : bf16 output in cfg->layout order.
- * o_f     : fp32 CUBE order fine output, or NULL (not needed for inference).
+ * o_f     : fp16 CUBE order fine output (rounded from fp32; it feeds only the
+ *           combine backward), or NULL (not needed for inference).
  * lse_f   : fp32 [B,heads,N] CUBE order, or NULL. */
 vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* k16,
                           const void* v16, const int32_t* idx, const int32_t* cnt, const void* gc,
-                          const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
+                          const void* gf, const float* oc, void* o, void* o_f, float* lse_f,
                           void* ws, void* stream);
 
 /* vsa_fine_fwd for callers that cannot provide a scratch buffer.  The pages
@@ -204,17 +205,17 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
 vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void* q16, const void* k16,
                                   const void* v16, const int32_t* idx, const int32_t* cnt,
                                   const void* gc, const void* gf, const float* oc, void* o,
-                                  float* o_f, float* lse_f, uint32_t* status, void* stream);
+                                  void* o_f, float* lse_f, uint32_t* status, void* stream);
 
 /* Backward of the combine (gradient of O = repeat(O_c) G_c + O_f G_f).
- * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp32 CUBE order; oc: fp32.
+ * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp16 CUBE order; oc: fp32.
  * dgc, dgf   : fp32 outputs in cfg->layout order.
  * dof16      : fp16 CUBE order output (staged), dO (.) G_f.
  * doc        : fp32 [B,heads,Nc,D] output, per-cube sum of dO (.) G_c.
  * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof16 (.) o_f).
  * ws receives the range flag. */
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
-                             const void* gf, const float* o_f, const float* oc, float* dgc,
+                             const void* gf, const void* o_f, const float* oc, float* dgc,
                              float* dgf, void* dof16, float* doc, float* delta, void* ws,
                              void* stream);
 

@@ -52,7 +52,7 @@ def run_forward(inp, layout="raster"):
         "qc": bufs.view("qc", torch.float32, (B, H, nc, D)),
         "oc": bufs.view("oc", torch.float32, (B, H, nc, D)),
         "lse_c": bufs.view("lse_c", torch.float32, (B, H, nc)),
-        "o_f": bufs.view("o_f", torch.float32, (B, H, N, D)),
+        "o_f": bufs.view("o_f", torch.float16, (B, H, N, D)),
         "lse_f": bufs.view("lse_f", torch.float32, (B, H, N)),
     }
     if layout == "cube":

@@ -68,7 +68,6 @@ vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
 }
 
 size_t half_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 2; }
-size_t f32_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 4; }
 size_t pooled_bytes(const Geom& g) { return static_cast<size_t>(g.BH) * g.Nc * g.D * 4; }
 
 void saved_layout(const Geom& g, vsa_saved_layout_t* L) {
@@ -88,7 +87,7 @@ void saved_layout(const Geom& g, vsa_saved_layout_t* L) {
   L->lse_c = take(static_cast<size_t>(g.BH) * g.Nc * 4);
   L->idx = take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4);
   L->cnt = take(static_cast<size_t>(g.BH) * g.Nc * 4);
-  L->o_f = take(f32_tensor(g));
+  L->o_f = take(half_tensor(g));
   L->lse_f = take(static_cast<size_t>(g.BH) * g.N * 4);
   L->total = off;
   L->list_cap = g.cap;
@@ -320,7 +319,7 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
 
 vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* k16,
                           const void* v16, const int32_t* idx, const int32_t* cnt, const void* gc,
-                          const void* gf, const float* oc, void* o, float* o_f, float* lse_f,
+                          const void* gf, const float* oc, void* o, void* o_f, float* lse_f,
                           void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
@@ -336,11 +335,11 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
   return cuda_status(launch_fine_fwd(g, static_cast<const f16*>(q16), static_cast<const f16*>(k16),
                                      static_cast<const f16*>(v16), static_cast<const bf16*>(gc),
                                      static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
-                                     o_f, lse_f, w, s));
+                                     static_cast<f16*>(o_f), lse_f, w, s));
 }
 
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
-                             const void* gf, const float* o_f, const float* oc, float* dgc,
+                             const void* gf, const void* o_f, const float* oc, float* dgc,
                              float* dgf, void* dof16, float* doc, float* delta, void* ws,
                              void* stream) {
   Geom g;
@@ -353,7 +352,8 @@ vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const voi
   carve_ws(g, 0, ws, &w);
   return cuda_status(launch_combine_bwd(
       g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
-      static_cast<const bf16*>(gf), o_f, oc, dgc, dgf, static_cast<f16*>(dof16), doc, delta,
+      static_cast<const bf16*>(gf), static_cast<const f16*>(o_f), oc, dgc, dgf,
+      static_cast<f16*>(dof16), doc, delta,
       w.status, static_cast<cudaStream_t>(stream)));
 }
 
@@ -430,7 +430,7 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   return cuda_status(launch_fine_fwd(g, q16, k16, v16, static_cast<const bf16*>(gc),
                                      static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
-                                     with_backward ? reinterpret_cast<float*>(sv + L.o_f) : nullptr,
+                                     with_backward ? reinterpret_cast<f16*>(sv + L.o_f) : nullptr,
                                      reinterpret_cast<float*>(sv + L.lse_f), w, s));
 }
 
@@ -451,7 +451,7 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
   const f16* q16 = reinterpret_cast<const f16*>(sv + L.q16);
   const f16* k16 = reinterpret_cast<const f16*>(sv + L.k16);
   const f16* v16 = reinterpret_cast<const f16*>(sv + L.v16);
-  const float* of = reinterpret_cast<const float*>(sv + L.o_f);
+  const f16* of = reinterpret_cast<const f16*>(sv + L.o_f);
   const float* oc = reinterpret_cast<const float*>(sv + L.oc);
   const int* idx = reinterpret_cast<const int*>(sv + L.idx);
   const int* cnt = reinterpret_cast<const int*>(sv + L.cnt);

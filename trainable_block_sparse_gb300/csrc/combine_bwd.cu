@@ -6,7 +6,7 @@
 //   dO_c[cube] = sum over the cube of dO (.) G_c
 //   delta[row] = sum_d dO_f (.) O_f    (the softmax-backward row term of the fine stage)
 // HBM-bound: one CTA per (batch, head, cube) reads dO, G_c, G_f (bf16, caller
-// layout) and O_f (fp32, cube order) once and writes each output once.
+// layout) and O_f (fp16, cube order) once and writes each output once.
 #include "sm103_ptx.cuh"
 #include "vsa_common.cuh"
 
@@ -18,7 +18,7 @@ constexpr int kThreads = 256;
 template <int D>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     Geom g, const uint4* __restrict__ d_o, const uint4* __restrict__ gc,
-    const uint4* __restrict__ gf, const float* __restrict__ o_f, const float* __restrict__ oc,
+    const uint4* __restrict__ gf, const uint4* __restrict__ o_f, const float* __restrict__ oc,
     float* __restrict__ dgc, float* __restrict__ dgf, uint4* __restrict__ dof,
     float* __restrict__ doc, float* __restrict__ delta, uint32_t* status) {
   constexpr int VPR = D / 8;              // 8-element vectors per row
@@ -40,9 +40,15 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const __nv_bfloat162* pd = reinterpret_cast<const __nv_bfloat162*>(&ud);
     const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&uc);
     const __nv_bfloat162* pf = reinterpret_cast<const __nv_bfloat162*>(&uf);
-    const float4 f0 = reinterpret_cast<const float4*>(o_f + frow * D + col * 8)[0];
-    const float4 f1 = reinterpret_cast<const float4*>(o_f + frow * D + col * 8)[1];
-    const float ofv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    const uint4 uo = o_f[frow * VPR + col];  // fp16 O_f, 8 values
+    const __half2* po = reinterpret_cast<const __half2*>(&uo);
+    float ofv[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(po[e]);
+      ofv[2 * e] = f.x;
+      ofv[2 * e + 1] = f.y;
+    }
     float vdgc[8], vdgf[8];
     uint4 udof;
     __half2* pof = reinterpret_cast<__half2*>(&udof);
@@ -92,16 +98,16 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
 
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
-                               const float* o_f, const float* oc, float* dgc, float* dgf,
+                               const __half* o_f, const float* oc, float* dgc, float* dgf,
                                __half* dof, float* doc, float* delta, uint32_t* status,
                                cudaStream_t s) {
   dim3 grid(g.Nc, g.BH);
   auto u4 = [](const void* p) { return reinterpret_cast<const uint4*>(p); };
   if (g.D == 64)
-    combine_bwd_kernel<64><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), o_f, oc, dgc, dgf,
+    combine_bwd_kernel<64><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), u4(o_f), oc, dgc, dgf,
                                                      reinterpret_cast<uint4*>(dof), doc, delta, status);
   else
-    combine_bwd_kernel<128><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), o_f, oc, dgc,
+    combine_bwd_kernel<128><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), u4(o_f), oc, dgc,
                                                       dgf, reinterpret_cast<uint4*>(dof), doc,
                                                       delta, status);
   return cudaGetLastError();

@@ -23,7 +23,7 @@
 //                  P goes back into TMEM as the A operand of the PV product;
 //      warps 8-11  epilogue: normalise O_f, apply the gates with the cube's
 //                  coarse output, write O (bf16, caller layout, un-permuted on
-//                  the way out), O_f (fp32, kept for the backward) and the
+//                  the way out), O_f (fp16, kept for the backward) and the
 //                  log-sum-exp;
 //      warp 12     TMA: Q once per item, then K tiles gathered by list entry;
 //      warp 13     UMMA issue (whole warp converged, one elected lane);
@@ -108,7 +108,7 @@ struct FwdParams {
   const __nv_bfloat16* gf;
   const float* oc;
   __nv_bfloat16* o;
-  float* o_f;
+  __half* o_f;
   float* lse_f;
   uint32_t* status;
 };
@@ -529,23 +529,35 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv_l);
         }
         if (stage_of) {
-          // the previous chunk's stores have read the stage
-          if (leader) bulk_wait_group_read0();
-          epi_sync();
+          // O_f in fp16: a staged row of 128 bytes holds 64 columns, the chunks
+          // cc and cc + 32 of a pair; the pair leaves as one box per cube
+          const bool first = (cc & 63) == 0;
+          if (first) {
+            // the previous pair's stores have read the stage
+            if (leader) bulk_wait_group_read0();
+            epi_sync();
+          }
           if (live) {
             uint8_t* rp = sStage + row * 128;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<float4*>(rp + ((u ^ (row & 7)) << 4)) =
-                  make_float4(__uint_as_float(ov[4 * u]), __uint_as_float(ov[4 * u + 1]),
-                              __uint_as_float(ov[4 * u + 2]), __uint_as_float(ov[4 * u + 3]));
+            for (int u = 0; u < 4; ++u) {
+              const int unit = ((cc & 63) >> 3) + u;
+              const uint4 w = make_uint4(
+                  pack_f16x2(__uint_as_float(ov[8 * u]), __uint_as_float(ov[8 * u + 1])),
+                  pack_f16x2(__uint_as_float(ov[8 * u + 2]), __uint_as_float(ov[8 * u + 3])),
+                  pack_f16x2(__uint_as_float(ov[8 * u + 4]), __uint_as_float(ov[8 * u + 5])),
+                  pack_f16x2(__uint_as_float(ov[8 * u + 6]), __uint_as_float(ov[8 * u + 7])));
+              *reinterpret_cast<uint4*>(rp + ((unit ^ (row & 7)) << 4)) = w;
+            }
           }
-          fence_proxy_async_smem();
-          epi_sync();
-          if (leader) {
-            tma_store_3d(&tof, sStage, cc, pi.bh * g.N + pi.a * kTile, 0);
-            if (pi.b >= 0) tma_store_3d(&tof, sStage + 64 * 128, cc, pi.bh * g.N + pi.b * kTile, 0);
-            bulk_commit_group();
+          if (!first) {
+            fence_proxy_async_smem();
+            epi_sync();
+            if (leader) {
+              tma_store_2d(&tof, sStage, cc - 32, pi.bh * g.N + pi.a * kTile);
+              if (pi.b >= 0) tma_store_2d(&tof, sStage + 64 * 128, cc - 32, pi.bh * g.N + pi.b * kTile);
+              bulk_commit_group();
+            }
           }
         }
         if (live) {
@@ -595,10 +607,9 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
   if (!encode_tiled_2d(&mq, q, rows, D, 64, 64) || !encode_tiled_2d(&mk, k, rows, D, 64, 64) ||
       !encode_tiled_2d(&mv, v, rows, D, 64, 64))
     return cudaErrorInvalidValue;
-  // O_f (fp32, cube order): boxes of 64 rows (one cube) x 32 columns
+  // O_f (fp16, cube order): boxes of 64 rows (one cube) x 64 columns
   memset(&mof, 0, sizeof(mof));
-  if (p.o_f && !encode_tiled_3d_f32(&mof, p.o_f, 1, rows, D, D, rows * D, 32, 64))
-    return cudaErrorInvalidValue;
+  if (p.o_f && !encode_tiled_2d(&mof, p.o_f, rows, D, 64, 64)) return cudaErrorInvalidValue;
   const int smem = FwdSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -613,7 +624,7 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
 
 cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
-                            __nv_bfloat16* o, float* o_f, float* lse_f, const Workspace& ws,
+                            __nv_bfloat16* o, __half* o_f, float* lse_f, const Workspace& ws,
                             cudaStream_t s) {
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
               gc, gf, oc, o, o_f, lse_f, ws.status};

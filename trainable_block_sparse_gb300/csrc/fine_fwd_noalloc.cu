@@ -87,7 +87,7 @@ extern "C" vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void
                                              const void* k16, const void* v16,
                                              const int32_t* idx, const int32_t* cnt,
                                              const void* gc, const void* gf, const float* oc,
-                                             void* o, float* o_f, float* lse_f,
+                                             void* o, void* o_f, float* lse_f,
                                              uint32_t* status, void* stream) {
   const vsa_status_t st = vsa_validate(cfg);
   if (st != VSA_OK) return st;
@@ -117,7 +117,7 @@ extern "C" vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void
   if (launch_fine_fwd(g, static_cast<const __half*>(q16), static_cast<const __half*>(k16),
                       static_cast<const __half*>(v16), static_cast<const __nv_bfloat16*>(gc),
                       static_cast<const __nv_bfloat16*>(gf), oc, static_cast<__nv_bfloat16*>(o),
-                      o_f, lse_f, w, s) != cudaSuccess)
+                      static_cast<__half*>(o_f), lse_f, w, s) != cudaSuccess)
     return VSA_ERR_CUDA;
   if (status &&
       cudaMemcpyAsync(status, w.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -111,11 +111,11 @@ cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
 cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
-                            __nv_bfloat16* o, float* o_f, float* lse_f, const Workspace& ws,
+                            __nv_bfloat16* o, __half* o_f, float* lse_f, const Workspace& ws,
                             cudaStream_t s);
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
-                               const float* o_f, const float* oc, float* dgc, float* dgf,
+                               const __half* o_f, const float* oc, float* dgc, float* dgf,
                                __half* dof, float* doc, float* delta, uint32_t* status,
                                cudaStream_t s);
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,

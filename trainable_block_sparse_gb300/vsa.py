@@ -200,7 +200,7 @@ def fine_fwd(cfg: Config, q16, k16, v16, idx, cnt, gc, gf, oc, ws, want_saved=Tr
     q, k, v = q16, k16, v16
     B, Hd, N, D = q.shape
     o = torch.empty_like(gc)
-    of = torch.empty(B, Hd, N, D, dtype=torch.float32, device=q.device) if want_saved else None
+    of = torch.empty(B, Hd, N, D, dtype=torch.float16, device=q.device) if want_saved else None
     lse = torch.empty(B, Hd, N, dtype=torch.float32, device=q.device) if want_saved else None
     check(lib().vsa_fine_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(cnt),
                              _ptr(gc), _ptr(gf), _ptr(oc), _ptr(o), _ptr(of), _ptr(lse),
