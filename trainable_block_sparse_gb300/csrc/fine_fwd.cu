@@ -88,7 +88,7 @@ struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
   uint64_t s_full, s_read, p_full[2];  // p_full by step parity = P buffer
-  uint64_t o_ready, o_full[2], o_free[2];
+  uint64_t o_full[2], o_free[2];
   uint64_t st_full[2], st_free[2];
   uint64_t final_mma;
   uint32_t tmem_base;
@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
     mbar_init(&sb.s_full, 1);
     mbar_init(&sb.s_read, kSoftmaxWarps);  // one arrival per softmax warp
-    mbar_init(&sb.o_ready, 1);
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
     fence_barrier_init();
@@ -303,8 +302,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       tc_fence_after();
       issue_ts_rows(tb + kColO + obuf * 128, tb + kColP + pbuf * 64,
                     vd0 + ((slot * L::kKVBytes) >> 4), two, idesc_pv, !first);
-      commit_elect(&sb.v_empty[slot]);
-      commit_elect(&sb.o_ready);
+      commit_elect(&sb.v_empty[slot]);  // also tells the rescale that PV(t) is done
       return true;
     };
 
@@ -444,7 +442,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           // then scale this half's columns of O in TMEM.  Both warps of the
           // pair see the same rows, so both take this branch.  (Done after P
           // is stored, so no part of x[] is live here.)
-          const bool ready = waitw(&sb.o_ready, (step - 1) & 1, abort_flag, P.status);
+          // PV(step - 1) is done once its V slot is released (the slot's next
+          // phase needs P of a later step, so the phase cannot move on first)
+          const uint32_t pv = step - 1;
+          const bool ready = waitw(&sb.v_empty[pv % kSV], (pv / kSV) & 1, abort_flag, P.status);
           if (pair_sync_or(quarter, !ready)) { ok = false; break; }
           tc_fence_after();
           const uint32_t to = tb + lane_addr + kColO + obuf * 128 + hc * (D / 2);
