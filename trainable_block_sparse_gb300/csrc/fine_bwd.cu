@@ -56,8 +56,8 @@ constexpr int kSoftmaxWarpsBwd = 8;
 constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpLoadX = 10, kWarpEpi0 = 12;
 constexpr int kEpiWarps = 4;
 // register split: the launch gives 65536 / 512 = 128 a thread
-constexpr int kRegsSoftmaxKm = 168, kRegsRestKm = 88;
-static_assert(256 * kRegsSoftmaxKm + 256 * kRegsRestKm <= 65536, "split exceeds the launch's registers");
+constexpr int kRegsSoftmax = 168, kRegsRest = 88;
+static_assert(256 * kRegsSoftmax + 256 * kRegsRest <= 65536, "split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
 // dQ pass: the item's Q and dO as TMEM A operands (D/2 columns each) at kColA2
@@ -87,7 +87,7 @@ struct BwdBars {
   uint64_t x_full;
   uint64_t y1_full[4], y1_empty[4], y2_full[4], y2_empty[4];
   uint64_t s_full, s_read, dp_full[2], ds_full[2];  // dP/dS barriers by step parity
-  uint64_t acc_full, acc_free, final_mma;
+  uint64_t acc_full, acc_free, final_mma;  // acc_free: dQ pass, the epilogue has read dQ
   uint64_t a_ready, x_free;  // dQ pass: the item's Q, dO copied from X into TMEM
   uint64_t x_empty;          // key-major pass: the item's last S^T and dP^T are done
   uint64_t dv_free, dk_free; // key-major pass: the epilogue has read dV / dK
@@ -132,13 +132,14 @@ __device__ __forceinline__ void store_pooled_half(int c0, const float* pooled, s
   }
 }
 
-template <bool kOn, int N>
+// Per-warpgroup register split (every warp of a warpgroup executes the same one).
+template <int N>
 __device__ __forceinline__ void regs_inc() {
-  if constexpr (kOn) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
-template <bool kOn, int N>
+template <int N>
 __device__ __forceinline__ void regs_dec() {
-  if constexpr (kOn) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Key-major epilogue: the 32 accumulator rows of this warp's lane quarter
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   if (warp == kWarpLoadY) {
     // ===================================================== TMA loads of Y1, Y2
-    regs_dec<true, kRegsRestKm>();
+    regs_dec<kRegsRest>();
     if (lane == 0) {
       tma_prefetch_desc(&ty1);
       tma_prefetch_desc(&ty2);
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
   } else if (warp == kWarpIssue) {
     // ===================================================== UMMA issuer
-    regs_dec<true, kRegsRestKm>();
+    regs_dec<kRegsRest>();
     const uint32_t id_s128 = idesc_f16(128, 128, 0, 0);
     const uint32_t id_s64 = idesc_f16(128, 64, 0, 0);
     const uint32_t id_acc = idesc_f16(128, D, 0, 1);
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_wait(&sb.final_mma, 0, kWaitNs);
   } else if (warp == kWarpLoadX) {
     // ===================================================== TMA loads of X
-    regs_dec<true, kRegsRestKm>();
+    regs_dec<kRegsRest>();
     if (lane == 0) {
       tma_prefetch_desc(&tx1);
       tma_prefetch_desc(&tx2);
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
   } else if (warp < kSoftmaxWarpsBwd) {
     // ===================================================== softmax-backward
-    regs_inc<true, kRegsSoftmaxKm>();
+    regs_inc<kRegsSoftmax>();
     const int quarter = warp & 3;
     const int hc = warp >> 2;                 // step tile = column half of S and dP
     const int row = quarter * 32 + lane;
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
   } else if (warp >= kWarpEpi0) {
     // ===================================================== epilogue
-    regs_dec<true, kRegsRestKm>();
+    regs_dec<kRegsRest>();
     const int quarter = warp & 3;
     const bool second = quarter >= 2;  // rows 64..127: the item's second cube
     const uint32_t tq = tb + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -680,7 +681,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
   } else {
     // warp 11: no role; completes warpgroup 2's register split
-    regs_dec<true, kRegsRestKm>();
+    regs_dec<kRegsRest>();
   }
 
   tc_fence_before();
