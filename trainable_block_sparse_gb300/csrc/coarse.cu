@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectA
   uint32_t t = 1u;  // the K-th largest key (or a key with exactly K keys at or above it)
   if (K > 0) {
     uint32_t lo = __reduce_min_sync(kFull, kmin_l), hi = __reduce_max_sync(kFull, kmax_l);
+    // When every lane holds a valid key and K <= 32, the smallest of the 32
+    // lane maxima has at least 32 keys at or above it: a tighter start.
+    if (K <= 32 && nvalid >= 32 && __all_sync(kFull, kmax_l != 0u))
+      lo = max(lo, __reduce_min_sync(kFull, kmax_l));
     // invariant: count(key >= lo) >= K; the answer lies in [lo, hi]
     while (lo < hi) {
       const uint32_t mid = lo + (hi - lo + 1) / 2;
