@@ -75,11 +75,12 @@ struct FwdSmem {
   static constexpr int kChunkBytes = 128 * 128;       // one chunk of 128 rows
   static constexpr int kQBytes = kChunks * kChunkBytes;
   static constexpr int kKVBytes = kChunks * kChunkBytes;  // 2 key tiles
-  static constexpr int kStagesK = (D == 128) ? 2 : 6;
-  // D = 128: two stages each.  Deeper rings measured slower: TMA serves a CTA's
-  // copies in order, so every extra slot in flight queues ahead of the tile
-  // the next product needs (2 K / 3 V and 3 K / 2 V both lost ~1%).
-  static constexpr int kStagesV = (D == 128) ? 2 : 5;
+  static constexpr int kStagesK = (D == 128) ? 2 : 3;
+  // D = 128: two stages each; D = 64 (16 KB tiles): three each.  Deeper rings
+  // measured slower: TMA serves a CTA's copies in order, so every extra slot in
+  // flight queues ahead of the tile the next product needs (at D = 128,
+  // 2 K / 3 V and 3 K / 2 V both lost ~1%).
+  static constexpr int kStagesV = (D == 128) ? 2 : 3;
   static constexpr int kTileBytes = 64 * D * 2;       // one 64-row tile
   // epilogue staging of one 32-column chunk of O_f: 128 rows x 128 bytes
   static constexpr int kStageOff = kQBytes + (kStagesK + kStagesV) * kKVBytes;
