@@ -14,8 +14,9 @@ value: executed TFLOPS of the step (fine stage over selected 64x64 tiles only,
 plus the dense coarse stage), whole job.  e2e: the same metric through the
 C ABI with host buffers (host->device inputs and device->host outputs inside
 the timed region).  roofline: the step's dominant kernel against the measured
-dense tensor peak.  cpu_baseline: the fp64 oracle on the host cores, on a
-bounded sample of the same layer, extrapolated to the layer.
+dense tensor peak.  cpu_baseline: the fp64 oracle on the host cores, timed on
+a bounded sample of the same layer (executed FLOPs of the sample / its
+measured time).
 
 Under torchrun each rank runs its own replica of the layer ("replicas only":
 the method has no exchange step between (batch, head) slices).
@@ -44,9 +45,11 @@ WORKLOAD = "p720"
 # kernels per call of vsa_forward / vsa_backward
 LAUNCHES_FWD = 9   # stage x3, tf32 split, coarse logits GEMM + select + O_c GEMM, pair lists,
                    # fine forward
-LAUNCHES_BWD = 16  # combine bwd, coarse bwd (row dot, tf32 split, 5 GEMMs), pair lists,
-                   # transposed lists (mask, count, scan, fill, pairs), fine bwd x2
-SIDE_WORKLOADS = ("wan13b", "dynamic")  # timed per stage beside the headline layer
+LAUNCHES_BWD = 17  # gradient-scale max, combine bwd, coarse bwd (row dot, tf32 split,
+                   # 5 GEMMs), pair lists, transposed lists (mask, count, scan, fill,
+                   # pairs), fine bwd x2
+SIDE_WORKLOADS = ("wan13b", "pretrain", "dynamic")  # timed per stage beside the headline layer
+SIDE_REPS = 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -138,8 +141,37 @@ def timed(fn, steps, warmup, stream):
     return start.elapsed_time(end) / steps
 
 
+class L2Flush:
+    """Writes a buffer of twice the L2 before each timed call (outside the
+    timed events), so every call starts with a cold L2."""
+
+    def __init__(self, dev, l2_bytes=129 * 2 ** 20):
+        self.buf = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def timed_median(fn, reps, warmup, stream, flush=None):
+    """Median device time (ms) of single calls, each bracketed by its own CUDA
+    events on `stream`; with `flush`, the L2 is flushed before every call."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
 def workload(args):
-    wl = synth.WORKLOADS[WORKLOAD]
+    wl = synth.WORKLOADS[getattr(args, "workload", None) or WORKLOAD]
     return wl.replace(heads=args.heads) if getattr(args, "heads", 0) else wl
 
 
@@ -190,15 +222,18 @@ def gpu_arm(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # clocks sampled through every timed section (the step timing alone is
+    # shorter than the sampling interval)
     with ClockSampler(dev.index) as clk:
         ms_step = timed(step, args.steps, args.warmup, stream)
-    ms_fwd = timed(fwd, max(3, args.steps // 2), 1, stream)
-    status = bufs.device_status()
-    if status != vsa.OK:
-        raise RuntimeError(f"device status {status} after the timed steps")
+        ms_fwd = timed(fwd, max(3, args.steps // 2), 1, stream)
+        status = bufs.device_status()
+        if status != vsa.OK:
+            raise RuntimeError(f"device status {status} after the timed steps")
+        flush = L2Flush(dev)
+        stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, flush=flush)
+        fp8 = fp8_forward(vsa, cfg, wl, t, dev, pairs, flush)
     ms_max = max_over_ranks(ms_step, world, dev)
-
-    stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev)
     e2e = end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args)
     side = {}
     if rank == 0 and not args.no_side:
@@ -207,7 +242,68 @@ def gpu_arm(args, rank, world):
         side = {name: side_workload(vsa, name, dev) for name in SIDE_WORKLOADS}
     return {"wl": wl, "work": work, "pairs": pairs, "ms_step": ms_max, "ms_fwd": ms_fwd,
             "clocks": clk.summary(), "stages": stages, "e2e": e2e, "inp": inp,
-            "balance": balance, "side": side}
+            "balance": balance, "side": side, "fp8": fp8}
+
+
+# nominal dense rates (PFLOP/s): e4m3 against bf16
+FP8_OVER_BF16 = 4.5 / 2.25
+
+
+def fp8_forward(vsa, cfg, wl, t, dev, pairs, flush):
+    """The e4m3 variant (head_dim 128, inference): the whole forward through
+    vsa_forward_fp8 and its fine stage alone through vsa_fine_fwd_fp8, median
+    of SIDE_REPS calls with the L2 flushed before each."""
+    import ctypes
+    if wl.head_dim != 128:
+        return None
+    L, P = vsa.lib(), vsa._ptr
+    B, H, N, D, nc, cap = wl.batch, wl.heads, wl.tokens, wl.head_dim, wl.cubes, wl.list_capacity
+    stream = torch.cuda.current_stream()
+    bufs = vsa.Buffers(cfg, dev, with_backward=False)
+    o = torch.empty_like(t["q"])
+
+    def fwd():
+        vsa.forward_fp8(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, out=o)
+
+    ms_fwd = timed_median(fwd, SIDE_REPS, 3, stream, flush)
+    q8 = bufs.view("q16", torch.uint8, (B, H, N, D))
+    k8 = bufs.view("k16", torch.uint8, (B, H, N, D))
+    v8t = bufs.view("v16", torch.uint8, (B, H, nc, D, 64))
+    scales = bufs.view("o_f", torch.float32, (B, H, 3))
+    idx = bufs.view("idx", torch.int32, (B, H, nc, cap))
+    cnt = bufs.view("cnt", torch.int32, (B, H, nc))
+    oc = bufs.view("oc", torch.float32, (B, H, nc, D))
+    lse = bufs.view("lse_f", torch.float32, (B, H, N))
+    c, s = ctypes.byref(cfg), vsa._stream()
+
+    def fine():
+        st = L.vsa_fine_fwd_fp8(c, P(q8), P(k8), P(v8t), P(scales), P(idx), P(cnt), P(t["gc"]),
+                                P(t["gf"]), P(oc), P(o), P(lse), P(bufs.ws), s)
+        if st != vsa.OK:
+            raise RuntimeError(f"vsa_fine_fwd_fp8 returned {st}")
+
+    def stage():
+        st = L.vsa_stage_fp8(c, P(t["q"]), P(t["k"]), P(t["v"]), P(q8), P(k8), P(v8t),
+                             P(scales), P(bufs.view("qc", torch.float32, (B, H, nc, D))),
+                             P(bufs.view("kc", torch.float32, (B, H, nc, D))),
+                             P(bufs.view("vc", torch.float32, (B, H, nc, D))), P(bufs.ws), s)
+        if st != vsa.OK:
+            raise RuntimeError(f"vsa_stage_fp8 returned {st}")
+
+    ms_fine = timed_median(fine, SIDE_REPS, 2, stream, flush)
+    ms_stage = timed_median(stage, SIDE_REPS, 2, stream, flush)
+    if bufs.device_status() != vsa.OK:
+        raise RuntimeError(f"e4m3 forward: device status {bufs.device_status()}")
+    peaks, _ = load_peaks()
+    fine_tflops = flops.fine_fwd_pairs(pairs, D) / (ms_fine * 1e-3) / 1e12
+    return {"fwd_ms_per_layer": ms_fwd, "fine_fwd_ms": ms_fine, "stage_fp8_ms": ms_stage,
+            "fine_fwd_tflops": fine_tflops,
+            "fine_fwd_frac_of_fp8_peak": fine_tflops / (peaks["bf16_tflops"] * FP8_OVER_BF16),
+            "fine_fwd_frac_of_bf16_peak": fine_tflops / peaks["bf16_tflops"],
+            "peak_note": "e4m3 peak = measured bf16 peak x the nominal e4m3/bf16 ratio (2)",
+            "what": "vsa_forward_fp8: e4m3 staging + fp32 coarse stage + e4m3 fine stage "
+                    "(Q, K, V, P in e4m3, fp32 accumulation), inference; median of "
+                    f"{SIDE_REPS} calls, L2 flushed before each"}
 
 
 def balance_report(vsa, bufs, wl, dev):
@@ -243,26 +339,38 @@ def side_workload(vsa, name, dev):
         fwd()
         vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs, grads)
 
-    ms_fwd = timed(fwd, 5, 3, stream)
-    ms_step = timed(step, 5, 3, stream)
+    flush = L2Flush(dev)
+    ms_fwd = timed_median(fwd, SIDE_REPS, 3, stream, flush)
+    ms_step = timed_median(step, SIDE_REPS, 3, stream, flush)
+    warm_fwd = timed_median(fwd, SIDE_REPS, 1, stream)
+    warm_step = timed_median(step, SIDE_REPS, 1, stream)
     if bufs.device_status() != vsa.OK:
         raise RuntimeError(f"{name}: device status {bufs.device_status()}")
     pairs = int(bufs.view("cnt", torch.int32, (B, H, wl.cubes)).sum().item())
     work = executed_flops(wl, pairs)
     balance = balance_report(vsa, bufs, wl, dev)
-    stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev)
+    stages = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, flush=flush)
+    stages_warm = stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev)
+    fp8 = fp8_forward(vsa, cfg, wl, t, dev, pairs, flush)
     peaks, _ = load_peaks()
     return {"workload": wl.name, "selected_pairs": pairs, "fwd_ms_per_layer": ms_fwd,
             "fwdbwd_ms_per_layer": ms_step, "stages_ms": stages,
+            "timing": f"median of {SIDE_REPS} single calls, L2 flushed before each "
+                      f"(a {2 * 129} MB write); *_warm: the same without the flush",
+            "fwd_ms_per_layer_warm": warm_fwd, "fwdbwd_ms_per_layer_warm": warm_step,
+            "stages_ms_warm": stages_warm,
+            "fine_fwd_frac_of_peak_warm": work["fine_fwd"] / (stages_warm["fine_fwd"] * 1e-3)
+            / 1e12 / peaks["bf16_tflops"],
             "fine_fwd_tflops": work["fine_fwd"] / (stages["fine_fwd"] * 1e-3) / 1e12,
             "fine_fwd_frac_of_peak": work["fine_fwd"] / (stages["fine_fwd"] * 1e-3) / 1e12
             / peaks["bf16_tflops"],
             "fine_bwd_tflops": work["fine_bwd"] / (stages["fine_bwd"] * 1e-3) / 1e12,
-            "load_balance": balance}
+            "load_balance": balance, **({"fp8_forward": fp8} if fp8 else {})}
 
 
-def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=3):
-    """Each stage alone through its own C-ABI entry point: ms per call."""
+def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=SIDE_REPS, flush=None):
+    """Each stage alone through its own C-ABI entry point: median ms per call
+    (L2 flushed before each call when `flush` is given)."""
     import ctypes
     L, P = vsa.lib(), vsa._ptr
     B, H, N, D, nc, cap = wl.batch, wl.heads, wl.tokens, wl.head_dim, wl.cubes, wl.list_capacity
@@ -280,6 +388,7 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=3):
     dof = torch.empty(B, H, N, D, dtype=torch.float16, device=dev)
     doc, dqc, dkc, dvc = (torch.empty(B, H, nc, D, **f32) for _ in range(4))
     delta = torch.empty(B, H, N, **f32)
+    gscale = torch.empty(B, H, **f32)
     ws, c, s = bufs.ws, ctypes.byref(cfg), vsa._stream()
 
     def ck(st, name):
@@ -297,16 +406,16 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=3):
             P(t["gf"]), P(v["oc"]), P(o), P(v["o_f"]), P(v["lse_f"]), P(ws), s), "vsa_fine_fwd"),
         "combine_bwd": lambda: ck(L.vsa_combine_bwd(
             c, P(t["do"]), P(t["gc"]), P(t["gf"]), P(v["o_f"]), P(v["oc"]), P(dgc), P(dgf),
-            P(dof), P(doc), P(delta), P(ws), s), "vsa_combine_bwd"),
+            P(dof), P(doc), P(delta), P(gscale), P(ws), s), "vsa_combine_bwd"),
         "coarse_bwd": lambda: ck(L.vsa_coarse_bwd(
             c, P(v["qc"]), P(v["kc"]), P(v["vc"]), P(v["oc"]), P(v["lse_c"]), P(doc), P(dqc),
             P(dkc), P(dvc), P(ws), s), "vsa_coarse_bwd"),
         "fine_bwd": lambda: ck(L.vsa_fine_bwd(
             c, P(v["q16"]), P(v["k16"]), P(v["v16"]), P(v["idx"]), P(v["cnt"]), P(v["lse_f"]),
-            P(dof), P(delta), P(dqc), P(dkc), P(dvc), P(dq), P(dk), P(dv), P(ws), s),
+            P(dof), P(delta), P(gscale), P(dqc), P(dkc), P(dvc), P(dq), P(dk), P(dv), P(ws), s),
             "vsa_fine_bwd"),
     }
-    return {name: timed(fn, reps, 1, stream) for name, fn in calls.items()}
+    return {name: timed_median(fn, reps, 2, stream, flush) for name, fn in calls.items()}
 
 
 def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
@@ -338,33 +447,33 @@ def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
             "units": sum(1 for _ in pipe.units())}
 
 
-def oracle_sample(inp, b, h, cubes):
-    """Times the fp64 oracle on one (batch, head) slice and a few cubes.
-
-    Returns (estimated seconds for the whole slice, seconds actually spent).
-    The slice estimate is the oracle as it stands: the per-slice part (tiling,
-    pooling, coarse attention, selection, coarse backward) once, plus per cube
-    its fine forward rows, its query-side gradient and its key-side gradient.
-    """
+def oracle_sample(inp, b, h, cubes, budget_s=None):
+    """Runs the fp64 oracle, as it stands, on part of one layer: the whole
+    coarse stage of slice (b, h) (tiling, pooling, coarse attention, selection,
+    coarse backward) and the fine forward and backward of query cubes (their
+    rows, their query-side gradients and their terms of the key-side
+    gradients): the given cubes, or, with budget_s, cubes in a fixed spread-out
+    order until that many seconds have passed.  Returns (seconds, executed
+    FLOPs of that work counted like the GPU's: 4*Nc^2*D + 10*Nc^2*D for the
+    coarse stage, (4 + 10)*64^2*D per selected pair of the cubes, cubes done)."""
     from oracle import vsa_oracle as O
     wl = inp.wl
     t0 = time.perf_counter()
     hd = O.head_of(inp, b, h)
-    t_head = time.perf_counter() - t0
-    per_cube = []
-    for c in cubes:
-        t1 = time.perf_counter()
+    order = list(cubes) if budget_s is None else [(i * 97) % wl.cubes for i in range(wl.cubes)]
+    done = []
+    for c in order:
         hd.rows(c)
         hd.grad_query_cube(c)
-        t_q = time.perf_counter() - t1
-        for i in range(wl.cubes):  # the selectors' forward rows belong to their own cubes
-            if c in hd.idx[i][: hd.cnt[i]]:
-                hd.rows(i)
-        t2 = time.perf_counter()
-        hd.grad_key_cube(c)
-        per_cube.append(t_q + time.perf_counter() - t2)
-    spent = time.perf_counter() - t0
-    return t_head + wl.cubes * statistics.mean(per_cube), spent
+        hd.fine_key_partials([c])
+        hd.forget(c)
+        done.append(c)
+        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    pairs = int(sum(int(hd.cnt[c]) for c in done))
+    work = (4 + 10) * wl.cubes ** 2 * wl.head_dim + pairs * (4 + 10) * 64 * 64 * wl.head_dim
+    return secs, work, len(done)
 
 
 def cpu_cores():
@@ -374,28 +483,37 @@ def cpu_cores():
 
 def cpu_baseline(inp, step_flops):
     wl = inp.wl
-    cubes = [0, wl.cubes // 2]
-    slice_s, spent = oracle_sample(inp, 0, 0, cubes)
-    layer_s = slice_s * wl.bh
-    return {"value": step_flops / layer_s / 1e12, "unit": "TFLOPS", "cores": cpu_cores(),
-            "kind": "oracle", "layer_s_estimated": layer_s, "sample_s": spent,
-            "sample": f"fp64 numpy oracle, forward+backward of slice (b=0,h=0) of {wl.name}: "
-                      f"per-slice coarse work once plus {len(cubes)} of {wl.cubes} cubes "
-                      f"(fine rows, query- and key-side gradients), extrapolated to "
-                      f"{wl.cubes} cubes x {wl.bh} slices"}
+    secs, work, n = oracle_sample(inp, 0, 0, None, budget_s=12.0)
+    value = work / secs / 1e12
+    return {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+            "sample_s": secs, "sample_tflop": work / 1e12,
+            "layer_s_estimated": step_flops / 1e12 / value,
+            "sample": f"fp64 numpy oracle on slice (b=0,h=0) of {wl.name}: its whole coarse "
+                      f"stage plus the fine forward and backward of {n} of {wl.cubes} query "
+                      f"cubes (as many as ~12 s allow); value = executed FLOPs of that work / "
+                      f"its measured time (layer_s_estimated extrapolates it to the layer)"}
 
 
 def stage_roofline(name, ms, work, wl, peaks, src):
+    """Algorithmic work of one stage call against its bound.
+
+    HBM stages count the bytes the method must move once (the combine
+    backward: dO, G_c, G_f in bf16 and O_f in fp16 read; dG_c, dG_f in fp32,
+    dO_f in fp16 and delta written; its slice-maximum pre-pass re-reads dO
+    and G_f, which is not counted).  Tensor stages count executed FLOPs: the
+    fine stages on fp16 UMMAs (the bf16 rate), the coarse stages as fp32
+    contractions run on tf32 UMMAs (the tf32 rate: the measured bf16 peak
+    times the nominal tf32/bf16 ratio)."""
     S = flops.tensor_bytes(wl)  # one bf16 [B, heads, N, D] tensor
     small = wl.bh * wl.cubes * wl.head_dim * 4
-    alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12  # fp32 FMA lanes
+    rows = wl.bh * wl.tokens * 4
     table = {
         "stage_pool": ("hbm", 3 * (S + S) + 3 * small),          # read bf16, write fp16 + means
-        "combine_bwd": ("hbm", 3 * S + 2 * S + 4 * S + S + wl.bh * wl.tokens * 4 + small),
+        "combine_bwd": ("hbm", 3 * S + S + 4 * S + S + rows + small),
         "fine_fwd": ("tensor", work["fine_fwd"]),
         "fine_bwd": ("tensor", work["fine_bwd"]),
-        "coarse_select": ("alu", work["coarse_fwd"]),
-        "coarse_bwd": ("alu", work["coarse_bwd"]),
+        "coarse_select": ("tensor_tf32", work["coarse_fwd"]),
+        "coarse_bwd": ("tensor_tf32", work["coarse_bwd"]),
     }
     bound, amount = table[name]
     if bound == "hbm":
@@ -404,9 +522,10 @@ def stage_roofline(name, ms, work, wl, peaks, src):
         # fp16 and bf16 dense UMMA share one nominal rate: the measured bf16 peak applies
         achieved, peak, unit = amount / (ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
-        achieved, peak, unit = amount / (ms * 1e-3) / 1e12, alu_peak, "TFLOP/s"
+        achieved = amount / (ms * 1e-3) / 1e12
+        peak, unit, bound = peaks["bf16_tflops"] * TF32_OVER_BF16, "TFLOP/s", "tensor"
     return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "peak_source": src, "ms": ms}
+            "frac": achieved / peak, "peak_source": src, "ms": ms, "algorithmic": amount}
 
 
 def traffic_for(stage):
@@ -430,36 +549,96 @@ def config_json(wl):
             "cubes": wl.cubes, "batch": wl.batch, "heads": wl.heads, "head_dim": wl.head_dim,
             "topk": wl.topk, "step": "forward+backward of one layer",
             "io": "bf16 in/out, fp32 gradients", "mma": "fp16 x fp16 -> fp32 (tcgen05)",
-            "l2": "inputs larger than L2 (721 MB per bf16 tensor vs 129 MB): no flush",
+            "l2": (f"inputs larger than L2 ({flops.tensor_bytes(wl) / 1e6:.0f} MB per bf16 "
+                   f"tensor vs 129 MB): no flush" if flops.tensor_bytes(wl) > 129 * 2 ** 20
+                   else "inputs fit in L2: back-to-back steps are warm-L2 (profiling runs)"),
             "parallelism": "replicas"}
 
 
 def reference_arm(args):
-    """The fp64 oracle on the host cores, each step a bounded sample of the layer."""
+    """The fp64 oracle on the host cores, each step a bounded sample of the
+    layer (one slice's coarse stage and the fine forward and backward of two
+    query cubes).  value = the executed FLOPs of the samples / their measured
+    time; ms_per_step is the measured time of one sample, ms_per_step_estimated
+    the whole layer at that rate."""
     wl = workload(args)
     inp = synth.Inputs(wl, with_grad=True)
     pairs = wl.bh * wl.cubes * wl.topk
     step_flops = sum(executed_flops(wl, pairs).values())
-    layer_s = []
+    secs, work = [], []
     for i in range(args.warmup + args.steps):
         h = i % wl.heads
         c = (i * 97) % wl.cubes
-        slice_s, _ = oracle_sample(inp, 0, h, [c])
+        t, w, _ = oracle_sample(inp, 0, h, [c, (c + wl.cubes // 2) % wl.cubes])
         if i >= args.warmup:
-            layer_s.append(slice_s * wl.bh)
-    sec = statistics.mean(layer_s)
-    value = step_flops / sec / 1e12
-    sample = (f"per step: fp64 numpy oracle on one (batch, head) slice of {wl.name} (per-slice "
-              f"coarse work + 1 of {wl.cubes} cubes), extrapolated to the layer")
+            secs.append(t)
+            work.append(w)
+    value = sum(work) / sum(secs) / 1e12
+    sample = (f"per step: fp64 numpy oracle on one (batch, head) slice of {wl.name}: its "
+              f"coarse stage plus the fine forward and backward of 2 of {wl.cubes} query "
+              f"cubes; value = executed FLOPs of the samples / their measured time")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": statistics.mean(secs) * 1e3,
+            "ms_per_step_estimated": step_flops / 1e12 / value * 1e3,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_json(wl),
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def oracle_table(args):
+    """Wall time of the fp64 oracle, as it stands, per configuration on this
+    host's cores (a reported baseline, not a target).
+
+    tiny and pretrain: the whole layer measured, forward and forward+backward,
+    on every core (a spawn-started pool of single-threaded processes sharing
+    the slices' query cubes) and in one single-threaded process (tiny: the
+    whole layer; pretrain: one whole slice).  wan13b, p720, dynamic: one whole
+    slice measured on every core, the layer estimated at that rate."""
+    from oracle.pool import OraclePool
+    every = OraclePool()
+    single = OraclePool(processes=1)
+    rows = []
+
+    def run(pool, inp, slices, backward):
+        t0 = time.perf_counter()
+        pool.layer(inp, slices, "timing", backward=backward)
+        return time.perf_counter() - t0
+
+    try:
+        for name in ("tiny", "pretrain", "wan13b", "p720", "dynamic"):
+            wl = synth.WORKLOADS[name]
+            inp = synth.Inputs(wl, with_grad=True)
+            everything = [(b, h) for b in range(wl.batch) for h in range(wl.heads)]
+            whole = name in ("tiny", "pretrain")
+            slices = everything if whole else [(0, 0)]
+            row = {"workload": wl.name, "slices_timed": len(slices), "slices": wl.bh,
+                   "cores": every.processes}
+            modes = (False, True) if wl.backward else (False,)
+            for bwd in modes:
+                key = "fwdbwd" if bwd else "fwd"
+                t = run(every, inp, slices, bwd)
+                if whole:
+                    row[f"{key}_s"] = t
+                else:
+                    row[f"{key}_s_one_slice"] = t
+                    row[f"{key}_s_estimated"] = t * wl.bh
+                if name in ("tiny", "pretrain"):
+                    one = everything if name == "tiny" else [(0, 0)]
+                    t1 = run(single, inp, one, bwd)
+                    row[f"{key}_s_1thread" + ("" if name == "tiny" else "_one_slice")] = t1
+            rows.append(row)
+    finally:
+        every.close()
+        single.close()
+    return {"oracle_wall_time": rows, "host_cpus": os.cpu_count(),
+            "how": "oracle.pool.OraclePool: query cubes of each slice spread over single-"
+                   "threaded spawn-started processes; the literal masked-dense fine stage "
+                   "of the oracle; *_estimated = one slice x slices"}
 
 
 def main():
@@ -471,6 +650,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the per-stage timing of the other configurations")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default=WORKLOAD,
+                    help="layer to time (default: the 720p layer; the others are the "
+                         "parity-test configurations, for profiling)")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="print the fp64 oracle's wall time per configuration (host only)")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the layer with this many heads instead of 40 (smaller "
                          "profiling case of the same kernels)")
@@ -479,6 +663,10 @@ def main():
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.oracle_table:
+        if rank == 0:
+            print(json.dumps(oracle_table(args)), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)
@@ -520,6 +708,8 @@ def main():
         "gpu_launches": (LAUNCHES_FWD + LAUNCHES_BWD) * args.steps,
         "load_balance": r["balance"],
     }
+    if r["fp8"]:
+        line["fp8_forward"] = r["fp8"]
     if r["side"]:
         line["other_configs"] = r["side"]
     if world == 1 and not args.no_cpu_baseline:

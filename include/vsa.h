@@ -27,13 +27,21 @@
  *    in raster order (token (t,h,w) at row (t*H + h)*W + w) or in cube order
  *    (row c*64 + o, c = ((t/4)*(H/4) + h/4)*(W/4) + w/4,
  *    o = (t%4)*16 + (h%4)*4 + w%4), as cfg->layout says.  Q, K, V, G_c, G_f,
- *    dO and O are bf16; the pooled/coarse tensors, O_f, log-sum-exps and all
- *    gradients are fp32.
- *  - The tensor-core operands (Q, K, V and dO (.) G_f) are staged as fp16 copies
- *    in cube order ("staged" below): bf16 -> fp16 is exact for magnitudes in
+ *    dO and O are bf16; the pooled/coarse tensors, log-sum-exps and all
+ *    gradients are fp32; the saved fine output O_f is fp16 (cube order).
+ *  - The tensor-core operands Q, K, V are staged as fp16 copies in cube order
+ *    ("staged" below): bf16 -> fp16 is exact for magnitudes in
  *    [6.1e-5, 65504], and the fp16 significand keeps the rounding of the
- *    softmax probabilities 8x smaller than bf16 would.  Inputs whose magnitude
- *    exceeds 65504 (or are not finite) are reported as VSA_ERR_DEVICE_CHECK.
+ *    softmax probabilities 8x smaller than bf16 would.  Q, K or V values whose
+ *    magnitude exceeds 65504 (or that are not finite) are reported as
+ *    VSA_ERR_DEVICE_CHECK, not computed.
+ *  - The backward's operand dO_f = dO (.) G_f is staged in fp16 times a power
+ *    of two per (batch, head) slice (the "gradient scale"), chosen so that the
+ *    slice's largest |dO (.) G_f| lies in [4, 8); the fine backward divides its
+ *    results by it (exact).  Upstream gradients of any magnitude down to the
+ *    fp32 normal range (1e-5 .. 1e-8 is common in bf16 training without loss
+ *    scaling) thus keep fp16's full precision; only non-finite values are
+ *    reported (VSA_ERR_DEVICE_CHECK).
  *  - All pointers named without a "host" prefix are device pointers owned by
  *    the caller, 16-byte aligned.  The library never allocates, frees or
  *    synchronises (except vsa_check_device_status).  Scratch comes from the
@@ -136,13 +144,6 @@ vsa_status_t vsa_check_device_status(void* ws, void* stream);
  * VSA_ERR_INVALID_ARG for a NULL ws or a limit outside the range. */
 vsa_status_t vsa_probe_wait_timeout(void* ws, uint32_t limit_us, void* stream);
 
-/* Diagnostic (no counterpart in the method): y[i] = 2^x[i] for i < n, by
- * the exponential the fine-stage softmax kernels use: which = 0 the ex2
- * unit (approximate, ~2^-22 relative), which = 1 the FMA-pipe polynomial
- * (relative error below 7.5e-5 for x in [-126, 128); inputs below -126 give
- * results below 2^-125).  x, y: device float arrays of n elements. */
-vsa_status_t vsa_probe_exp2(const float* x, float* y, int32_t n, int32_t which, void* stream);
-
 /* Tile / untile (App. B: tiling and untiling rearrange tokens between
  * sequence and cube order).  inverse = 0: raster -> cube order; 1: cube ->
  * raster.  in, out: bf16 [B,heads,N,D], distinct buffers.  cfg->layout is
@@ -195,9 +196,15 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
  *  - status: optional device pointer to a uint32 (4-byte aligned, NULL to
  *    skip) that receives this call's device status bits (1: a bounded wait
  *    expired, 2: a bad index list entry, 4: a value outside the fp16 range).
- *  - Returns VSA_ERR_SHAPE, before any other check and any launch, when the
- *    configuration needs more scratch than VSA_NOALLOC_SCRATCH_BYTES
- *    (B*heads*ceil(Nc/2) query pairs, each with 20 bytes + 8*list_cap bytes).
+ *  - Returns VSA_ERR_SHAPE when the configuration needs more scratch than
+ *    VSA_NOALLOC_SCRATCH_BYTES (B*heads*ceil(Nc/2) query pairs, each with 20
+ *    bytes + 8*list_cap bytes): checked after vsa_validate() has accepted the
+ *    configuration (an invalid one returns vsa_validate's code), before the
+ *    pointer checks and before any launch.
+ *  - The query pairs run in their natural order (slice by slice, neighbouring
+ *    cubes together), not in the cost-sorted order vsa_fine_fwd uses for
+ *    layers whose K and V fit in L2 (that order needs more scratch); results
+ *    are bitwise the same, only the load balance differs.
  *  - The first call on each device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
  *  - Every call shares the one array: calls that overlap on the GPU (other
@@ -207,39 +214,103 @@ vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void* q16, cons
                                   const void* gc, const void* gf, const float* oc, void* o,
                                   void* o_f, float* lse_f, uint32_t* status, void* stream);
 
-/* Backward of the combine (gradient of O = repeat(O_c) G_c + O_f G_f).
+/* ---------------------------------------------------------------------------
+ * e4m3 (fp8) variant of the fine stage, head_dim 128, inference only.
+ *
+ * The pages give the fine stage no precision ("VSA: Faster Video Diffusion
+ * with Trainable Sparse Attention", §2 "Fine stage"; the successor "Improving
+ * Video Sparse Attention with Fine-grained Router and Sparse Rebasing",
+ * abstract, halves VSA's attention compute): this variant runs the same
+ * block-sparse attention and combine with Q, K, V and P in e4m3 and fp32
+ * accumulation, reading half the bytes per tile.  Its accuracy is that of e4m3
+ * (3 significand bits): results are not bit- or tolerance-equal to the fp16
+ * path's; the index lists, which the fp32 coarse stage decides, are identical.
+ * D = 64 returns VSA_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------ */
+
+/* Staging: bf16 q, k, v (cfg->layout order) -> e4m3 copies, each (batch, head)
+ * slice multiplied by a power of two 2^e that puts its largest |x| in
+ * [128, 256) (e4m3's range ends at 448).
+ * q8, k8  : [B*heads*N, 128] bytes, CUBE order (row c*64 + o of each slice).
+ * v8t     : [B*heads*Nc, 128, 64] bytes: each cube's V transposed (row d holds
+ *           the cube's 64 values of channel d).
+ * scales  : fp32 [B,heads,3] output, 2^-e of Q, K, V (the factors that undo
+ *           the scaling).
+ * qc,kc,vc: fp32 [B,heads,Nc,D] cube means (as vsa_coarse_select writes them),
+ *           each may be NULL.
+ * Non-finite inputs are reported as VSA_ERR_DEVICE_CHECK; ws also holds the
+ * slice maxima. */
+vsa_status_t vsa_stage_fp8(const vsa_config_t* cfg, const void* q, const void* k,
+                           const void* v, void* q8, void* k8, void* v8t, float* scales,
+                           float* qc, float* kc, float* vc, void* ws, void* stream);
+
+/* Fine stage and combine on the e4m3 copies (as vsa_fine_fwd, without O_f):
+ * idx, cnt, gc, gf, oc, o, ws as for vsa_fine_fwd; lse_f: fp32 [B,heads,N]
+ * CUBE order, or NULL. */
+vsa_status_t vsa_fine_fwd_fp8(const vsa_config_t* cfg, const void* q8, const void* k8,
+                              const void* v8t, const float* scales, const int32_t* idx,
+                              const int32_t* cnt, const void* gc, const void* gf, const float* oc,
+                              void* o, float* lse_f, void* ws, void* stream);
+
+/* Whole forward with the e4m3 fine stage (inference): e4m3 staging with the
+ * cube means, the fp32 coarse stage (identical lists), the e4m3 fine stage and
+ * combine.  saved: vsa_saved_bytes() bytes; the e4m3 copies go to the q16,
+ * k16, v16 offsets of its layout, their factors to the o_f offset, the coarse
+ * results and lse_f where vsa_forward puts them.  The result cannot feed
+ * vsa_backward. */
+vsa_status_t vsa_forward_fp8(const vsa_config_t* cfg, const void* q, const void* k,
+                             const void* v, const void* gc, const void* gf, void* o, void* saved,
+                             void* ws, void* stream);
+
+/* Backward of the combine: the gradient of O = repeat(O_c) G_c + O_f G_f
+ * (paper notes 关键设计 3, the gating formula; App. B "Pseudocode of VSA": the
+ * coarse output is repeated across its cube; the abstract: the whole operator
+ * is one differentiable kernel trained end to end).
  * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp16 CUBE order; oc: fp32.
- * dgc, dgf   : fp32 outputs in cfg->layout order.
- * dof16      : fp16 CUBE order output (staged), dO (.) G_f.
+ * dgc, dgf   : fp32 outputs in cfg->layout order (dO (.) repeat(O_c), dO (.) O_f).
+ * dof16      : fp16 CUBE order output, dO (.) G_f times gscale[slice].
  * doc        : fp32 [B,heads,Nc,D] output, per-cube sum of dO (.) G_c.
- * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof16 (.) o_f).
- * ws receives the range flag. */
+ * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof16 (.) o_f)
+ *              (so it carries the same factor).
+ * gscale     : fp32 [B,heads] output, the power-of-two gradient scale of each
+ *              slice (see the conventions above); pass it to vsa_fine_bwd.
+ * ws receives the range flag (non-finite dO (.) G_f) and holds the slice
+ * maxima. */
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
                              const void* gf, const void* o_f, const float* oc, float* dgc,
-                             float* dgf, void* dof16, float* doc, float* delta, void* ws,
-                             void* stream);
+                             float* dgf, void* dof16, float* doc, float* delta, float* gscale,
+                             void* ws, void* stream);
 
 /* Backward of the coarse attention on the pooled sequence, selection held
- * fixed.  Outputs dqc, dkc, dvc: fp32 [B,heads,Nc,D] (gradients w.r.t. the
+ * fixed (§2 "Coarse stage": dense attention over the cube means; abstract:
+ * trained end to end; the top-K choice is piecewise constant and passes no
+ * gradient).  Outputs dqc, dkc, dvc: fp32 [B,heads,Nc,D] (gradients w.r.t. the
  * pooled means). */
 vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const float* kc,
                             const float* vc, const float* oc, const float* lse_c,
                             const float* doc, float* dqc, float* dkc, float* dvc, void* ws,
                             void* stream);
 
-/* Backward of the fine stage plus the pooling: writes
- *   dq = dQ_fine + repeat(dqc)/64, dk = dK_fine + repeat(dkc)/64,
- *   dv = dV_fine + repeat(dvc)/64
+/* Backward of the fine stage plus the pooling (§2 "Fine stage" and App. B:
+ * the masked fine attention over the selected 64x64 blocks, differentiated with
+ * the selection held fixed; §2 "Coarse stage": each token's share of its cube
+ * mean is 1/64): writes
+ *   dq = dQ_fine / gscale + repeat(dqc)/64, dk = dK_fine / gscale + repeat(dkc)/64,
+ *   dv = dV_fine / gscale + repeat(dvc)/64
  * as fp32 in cfg->layout order.  q16, k16, v16, dof16: staged fp16 CUBE
- * order; lse_f, delta: fp32 CUBE order; dqc/dkc/dvc may be NULL (no pooled
- * contribution). */
+ * order; lse_f, delta: fp32 CUBE order; gscale: fp32 [B,heads], the factor
+ * dof16 and delta carry (vsa_combine_bwd's output), or NULL for 1;
+ * dqc/dkc/dvc may be NULL (no pooled contribution). */
 vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* k16,
                           const void* v16, const int32_t* idx, const int32_t* cnt,
                           const float* lse_f, const void* dof16, const float* delta,
-                          const float* dqc, const float* dkc, const float* dvc, float* dq,
-                          float* dk, float* dv, void* ws, void* stream);
+                          const float* gscale, const float* dqc, const float* dkc,
+                          const float* dvc, float* dq, float* dk, float* dv, void* ws,
+                          void* stream);
 
-/* Whole forward: tile, coarse stage, fine stage + combine, untile.
+/* Whole forward (§2 Methods, the coarse stage feeding the fine stage; App. B
+ * "Pseudocode of VSA"; paper notes 关键设计 1-3): tile, coarse stage, fine
+ * stage + combine, untile.
  * q, k, v, gc, gf: bf16 in cfg->layout order; o: bf16 output, same order.
  * saved: vsa_saved_bytes() bytes, filled for vsa_backward (O_f is written only
  * when with_backward != 0). */
@@ -247,7 +318,10 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
                          const void* gc, const void* gf, void* o, void* saved,
                          int with_backward, void* ws, void* stream);
 
-/* Whole backward from the upstream gradient d_o (bf16, cfg->layout order).
+/* Whole backward (abstract: VSA is a single differentiable kernel trained end
+ * to end; the gradients of every step of vsa_forward with the selection held
+ * fixed): combine backward, coarse backward, fine backward + unpooling, from
+ * the upstream gradient d_o (bf16, cfg->layout order).
  * gc, gf: the forward's gates; saved: as filled by vsa_forward with
  * with_backward = 1 (it holds the staged Q, K, V).  Outputs fp32 in
  * cfg->layout order. */

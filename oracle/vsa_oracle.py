@@ -210,6 +210,7 @@ class Head:
             self.idx, self.cnt = select_mass(self.coarse["logits"], self.coarse["probs"],
                                              sel["mass"], sel["kmin"], sel["kmax"])
         self._rows = {}
+        self._grad_rows = {}
 
     def rows(self, c):
         """P, O_f, lse_f of query cube c (cached)."""
@@ -249,13 +250,21 @@ class Head:
         self.dOc = dOc
 
     def _fine_grad_rows(self, c):
-        """dS and dO_f of query cube c (fine branch)."""
-        r = slice(c * TILE, (c + 1) * TILE)
-        p = self.rows(c)[0]
-        dof = self.dot[r] * self.gft[r]
-        dp = dof @ self.vt.T
-        ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
-        return p, ds, dof
+        """P, dS and dO_f of query cube c (fine branch; cached like rows())."""
+        if c not in self._grad_rows:
+            r = slice(c * TILE, (c + 1) * TILE)
+            p = self.rows(c)[0]
+            dof = self.dot[r] * self.gft[r]
+            dp = dof @ self.vt.T
+            ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+            self._grad_rows[c] = (p, ds, dof)
+        return self._grad_rows[c]
+
+    def forget(self, c):
+        """Drops the cached rows of query cube c (a [64, N] P per cube adds up
+        to gigabytes on large slices).  Results do not change."""
+        self._rows.pop(c, None)
+        self._grad_rows.pop(c, None)
 
     def grad_query_cube(self, c):
         """dQ, dG_c, dG_f for the 64 tokens of query cube c (cube-major rows)."""
@@ -278,6 +287,27 @@ class Head:
             p, ds, dof = self._fine_grad_rows(c)
             dk = dk + self.scale * ds[:, cols].T @ self.qt[r]
             dv = dv + p[:, cols].T @ dof
+        return dk, dv
+
+    def fine_key_partials(self, cubes):
+        """Fine-branch dK, dV [N, D] (cube-major rows) from the given query cubes.
+
+        For every query cube c in `cubes` and every key cube j it selected, the
+        two terms that grad_key_cube(j) adds for c: scale * dS[:, j]^T Q_c and
+        P[:, j]^T dO_f,c; summed over `cubes`.  The pooled part is left out.
+        Over all query cubes, plus repeat(dK_c)/64 and repeat(dV_c)/64, this is
+        grad_key_cube for every key cube at once (each query cube's P and dS
+        computed once instead of once per key cube it selected).
+        """
+        dk = np.zeros((self.N, self.D))
+        dv = np.zeros((self.N, self.D))
+        for c in cubes:
+            r = slice(c * TILE, (c + 1) * TILE)
+            p, ds, dof = self._fine_grad_rows(c)
+            for j in self.idx[c][: self.cnt[c]]:
+                cols = slice(j * TILE, (j + 1) * TILE)
+                dk[cols] += self.scale * ds[:, cols].T @ self.qt[r]
+                dv[cols] += p[:, cols].T @ dof
         return dk, dv
 
     def backward_all(self):

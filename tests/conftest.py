@@ -16,3 +16,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def oracle_pool():
+    """A spawn-started pool of oracle processes, shared by the test modules."""
+    from oracle.pool import OraclePool
+    pool = OraclePool()
+    yield pool
+    pool.close()

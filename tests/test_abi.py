@@ -106,3 +106,61 @@ def test_wait_probe_arguments_are_checked_on_the_host(lib):
     assert lib.vsa_probe_wait_timeout(ws, 0, None) == vsa.ERR_INVALID_ARG
     assert lib.vsa_probe_wait_timeout(ws, 20_000_000, None) == vsa.ERR_INVALID_ARG
     assert lib.vsa_probe_wait_timeout(ctypes.c_void_p(0x1008), 1000, None) == vsa.ERR_ALIGNMENT
+
+
+# ------------------------------------------- the autograd entry point's checks
+
+def _bf(*shape, dtype=None):
+    import torch
+    return torch.zeros(*shape, dtype=dtype or torch.bfloat16)
+
+
+def _five(shape=(1, 2, 512, 64), **over):
+    t = {n: _bf(*shape) for n in ("q", "k", "v", "gc", "gf")}
+    t.update(over)
+    return t
+
+
+@pytest.mark.parametrize("case,exc,match", [
+    ("fp16_q", TypeError, "q must be bfloat16"),
+    ("fp32_gf", TypeError, "gf must be bfloat16"),
+    ("not_tensor", TypeError, "k must be a torch.Tensor"),
+    ("three_d", ValueError, "must be 4-D"),
+    ("shape_k", ValueError, "k has shape"),
+    ("shape_gc", ValueError, "gc has shape"),
+    ("tokens", ValueError, "T\\*H\\*W"),
+    ("video_shape", ValueError, "video_shape"),
+    ("layout", ValueError, "layout"),
+    ("cpu", ValueError, "CUDA tensor"),
+])
+def test_video_sparse_attention_refuses_before_any_launch(case, exc, match):
+    """Inputs the kernels would misread raise on the host; no kernel runs
+    (these tensors are on the CPU, and the refusals come first)."""
+    import torch
+    vs = (8, 8, 8)
+    kw = {}
+    if case == "fp16_q":
+        t = _five(q=_bf(1, 2, 512, 64, dtype=torch.float16))
+    elif case == "fp32_gf":
+        t = _five(gf=_bf(1, 2, 512, 64, dtype=torch.float32))
+    elif case == "not_tensor":
+        t = _five(k=[[0.0]])
+    elif case == "three_d":
+        t = _five(shape=(2, 512, 64))
+    elif case == "shape_k":
+        t = _five(k=_bf(1, 2, 512, 128))
+    elif case == "shape_gc":
+        t = _five(gc=_bf(1, 1, 512, 64))
+    elif case == "tokens":
+        t = _five()
+        vs = (8, 8, 4)
+    elif case == "video_shape":
+        t = _five()
+        vs = (8, 64)
+    elif case == "layout":
+        t = _five()
+        kw = {"layout": "zigzag"}
+    else:
+        t = _five()
+    with pytest.raises(exc, match=match):
+        vsa.video_sparse_attention(t["q"], t["k"], t["v"], t["gc"], t["gf"], vs, topk=2, **kw)

@@ -26,7 +26,7 @@ def _built():
         pytest.skip("no CUDA device")
 
 
-@functools.lru_cache(maxsize=2)
+@functools.lru_cache(maxsize=6)
 def gapped(name, **over):
     wl = synth.WORKLOADS[name].replace(**over) if over else synth.WORKLOADS[name]
     inp = synth.Inputs(wl, with_grad=True)

@@ -38,3 +38,25 @@ def test_expired_wait_is_reported_and_context_survives():
     assert L.vsa_reset_device_status(vsa._ptr(ws), s) == vsa.OK
     assert L.vsa_check_device_status(vsa._ptr(ws), s) == vsa.OK
     check_forward(gapped("tiny"))
+
+
+@pytest.mark.gpu
+def test_device_range_flag_surfaces_through_autograd():
+    """A Q value above fp16's range is flagged by the staging kernel; the
+    autograd entry point reads the status word and raises VSAError."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    inp = gapped("tiny")
+    wl = inp.wl
+    t = {n: getattr(inp, n).cuda() for n in ("q", "k", "v", "gc", "gf")}
+    q = t["q"].clone()
+    q[0, 1, 77, 5] = 1.0e5
+    with pytest.raises(vsa.VSAError) as e:
+        vsa.video_sparse_attention(q.requires_grad_(True), t["k"], t["v"], t["gc"], t["gf"],
+                                   (wl.T, wl.H, wl.W), topk=wl.topk)
+    assert e.value.status == vsa.ERR_DEVICE_CHECK
+    # a clean call afterwards still works (the flag lives in that call's buffers)
+    o = vsa.video_sparse_attention(t["q"], t["k"], t["v"], t["gc"], t["gf"],
+                                   (wl.T, wl.H, wl.W), topk=wl.topk)
+    assert torch.isfinite(o.float()).all()

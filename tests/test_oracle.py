@@ -341,6 +341,27 @@ def test_gradient_invariants():
     np.testing.assert_allclose(dgf, do * O.untile(of, T, H, W), atol=1e-14)
 
 
+@pytest.mark.parametrize("mode", ["topk", "mass"])
+def test_key_partials_sum_to_key_gradients(mode):
+    """fine_key_partials over all query cubes (in any split) plus the pooled
+    part equals grad_key_cube of every key cube, which the finite-difference
+    test pins; forget() leaves results unchanged."""
+    T, H, W, D = 8, 8, 12, 8
+    sel = {"mode": mode, "topk": 4, "mass": 0.7, "kmin": 2, "kmax": 6}
+    hd, _ = _small_head(13, T, H, W, D, sel=sel)
+    hd.set_grad(_rng(14).normal(size=(T * H * W, D)))
+    split = [list(range(0, 7)), list(range(7, hd.nc))]
+    parts = [hd.fine_key_partials(cs) for cs in split]
+    for c in range(hd.nc):
+        hd.forget(c)
+    dk = sum(p[0] for p in parts) + np.repeat(hd.dkc / 64, 64, axis=0)
+    dv = sum(p[1] for p in parts) + np.repeat(hd.dvc / 64, 64, axis=0)
+    for j in range(hd.nc):
+        rk, rv = hd.grad_key_cube(j)
+        np.testing.assert_allclose(dk[j * 64:(j + 1) * 64], rk, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv[j * 64:(j + 1) * 64], rv, rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- pages' facts
 
 def test_workloads_match_pages_facts(golden_dir):

@@ -20,6 +20,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
   if (!cfg) return VSA_ERR_INVALID_ARG;
   if (cfg->batch < 1 || cfg->heads < 1) return VSA_ERR_INVALID_ARG;
@@ -67,6 +69,8 @@ vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
   return VSA_OK;
 }
 
+namespace {
+
 size_t half_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 2; }
 size_t pooled_bytes(const Geom& g) { return static_cast<size_t>(g.BH) * g.Nc * g.D * 4; }
 
@@ -111,6 +115,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.qlist = static_cast<uint32_t*>(take(sizeof(uint32_t) * npairs * 2 * g.cap));
   ws.qorder = static_cast<int*>(take(sizeof(int) * npairs));
   ws.order_tmp = static_cast<int*>(take(sizeof(int) * (npairs + 512)));
+  ws.gamax = static_cast<uint32_t*>(take(sizeof(uint32_t) * 3 * g.BH));
   // coarse logits [BH, Nc, ldc] and the coarse GEMM operands: tf32 pairs of
   // Q_c and K_c for the logits, everything else rounded to tf32 alone
   const size_t ldc = static_cast<size_t>((g.Nc + 3) & ~3);
@@ -126,6 +131,7 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
   ws.ach = f32(pc_bytes);
   if (with_backward) {
     const size_t words = (g.Nc + 31) / 32;
+    ws.gscale = static_cast<float*>(take(sizeof(float) * g.BH));
     ws.dof = take(half_tensor(g));
     ws.delta = static_cast<float*>(take(static_cast<size_t>(g.BH) * g.N * 4));
     ws.doc = static_cast<float*>(take(pooled_bytes(g)));
@@ -196,6 +202,21 @@ bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
   return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tiled_2d_u8(void* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, uint32_t box_cols, int swizzle_bytes) {
+  if (!encoder()) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -340,20 +361,21 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
 
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
                              const void* gf, const void* o_f, const float* oc, float* dgc,
-                             float* dgf, void* dof16, float* doc, float* delta, void* ws,
-                             void* stream) {
+                             float* dgf, void* dof16, float* doc, float* delta, float* gscale,
+                             void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(d_o, gc, gf, o_f, oc, dgc, dgf, dof16, doc, delta, ws)) return VSA_ERR_INVALID_ARG;
-  if (!all_aligned(d_o, gc, gf, o_f, oc, dgc, dgf, dof16, doc, delta, ws))
+  if (!all_set(d_o, gc, gf, o_f, oc, dgc, dgf, dof16, doc, delta, gscale, ws))
+    return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(d_o, gc, gf, o_f, oc, dgc, dgf, dof16, doc, delta, gscale, ws))
     return VSA_ERR_ALIGNMENT;
   Workspace w;
   carve_ws(g, 0, ws, &w);
   return cuda_status(launch_combine_bwd(
       g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
       static_cast<const bf16*>(gf), static_cast<const f16*>(o_f), oc, dgc, dgf,
-      static_cast<f16*>(dof16), doc, delta,
+      static_cast<f16*>(dof16), doc, delta, w.gamax, gscale,
       w.status, static_cast<cudaStream_t>(stream)));
 }
 
@@ -375,15 +397,17 @@ vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const floa
 vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* k16,
                           const void* v16, const int32_t* idx, const int32_t* cnt,
                           const float* lse_f, const void* dof16, const float* delta,
-                          const float* dqc, const float* dkc, const float* dvc, float* dq,
-                          float* dk, float* dv, void* ws, void* stream) {
+                          const float* gscale, const float* dqc, const float* dkc,
+                          const float* dvc, float* dq, float* dk, float* dv, void* ws,
+                          void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
   if (!all_set(q16, k16, v16, idx, cnt, lse_f, dof16, delta, dq, dk, dv, ws))
     return VSA_ERR_INVALID_ARG;
   if (!all_aligned(q16, k16, v16, idx, cnt, lse_f, dof16, delta, dq, dk, dv, ws) ||
-      !aligned16(dqc) || !aligned16(dkc) || !aligned16(dvc))
+      !aligned16(dqc) || !aligned16(dkc) || !aligned16(dvc) ||
+      (reinterpret_cast<uintptr_t>(gscale) & 3u))
     return VSA_ERR_ALIGNMENT;
   Workspace w;
   carve_ws(g, 1, ws, &w);
@@ -392,8 +416,8 @@ vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* 
   if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   return cuda_status(launch_fine_bwd(g, static_cast<const f16*>(q16), static_cast<const f16*>(k16),
                                      static_cast<const f16*>(v16), lse_f,
-                                     static_cast<const f16*>(dof16), delta, dqc, dkc, dvc, dq, dk,
-                                     dv, w, s));
+                                     static_cast<const f16*>(dof16), delta, gscale, dqc, dkc, dvc,
+                                     dq, dk, dv, w, s));
 }
 
 vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
@@ -457,7 +481,8 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
   const int* cnt = reinterpret_cast<const int*>(sv + L.cnt);
   if (launch_combine_bwd(g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
                          static_cast<const bf16*>(gf), of, oc, dgc, dgf,
-                         static_cast<f16*>(w.dof), w.doc, w.delta, w.status, s) != cudaSuccess)
+                         static_cast<f16*>(w.dof), w.doc, w.delta, w.gamax, w.gscale, w.status,
+                         s) != cudaSuccess)
     return VSA_ERR_CUDA;
   if (launch_coarse_bwd(g, reinterpret_cast<const float*>(sv + L.qc),
                         reinterpret_cast<const float*>(sv + L.kc),
@@ -468,8 +493,89 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
   if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   return cuda_status(launch_fine_bwd(g, q16, k16, v16, reinterpret_cast<const float*>(sv + L.lse_f),
-                                     static_cast<const f16*>(w.dof), w.delta, w.dqc, w.dkc,
-                                     w.dvc, dq, dk, dv, w, s));
+                                     static_cast<const f16*>(w.dof), w.delta, w.gscale, w.dqc,
+                                     w.dkc, w.dvc, dq, dk, dv, w, s));
+}
+
+vsa_status_t vsa_stage_fp8(const vsa_config_t* cfg, const void* q, const void* k,
+                           const void* v, void* q8, void* k8, void* v8t, float* scales,
+                           float* qc, float* kc, float* vc, void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (g.D != 128) return VSA_ERR_UNSUPPORTED;
+  if (!all_set(q, k, v, q8, k8, v8t, scales, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, q8, k8, v8t, scales, ws) || !aligned16(qc) || !aligned16(kc) ||
+      !aligned16(vc))
+    return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  return cuda_status(launch_stage_fp8(g, static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                      static_cast<const bf16*>(v), static_cast<uint8_t*>(q8),
+                                      static_cast<uint8_t*>(k8), static_cast<uint8_t*>(v8t),
+                                      scales, qc, kc, vc, w.gamax, w.status,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status_t vsa_fine_fwd_fp8(const vsa_config_t* cfg, const void* q8, const void* k8,
+                              const void* v8t, const float* scales, const int32_t* idx,
+                              const int32_t* cnt, const void* gc, const void* gf, const float* oc,
+                              void* o, float* lse_f, void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (g.D != 128) return VSA_ERR_UNSUPPORTED;
+  if (!all_set(q8, k8, v8t, scales, idx, cnt, gc, gf, oc, o, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q8, k8, v8t, scales, idx, cnt, gc, gf, oc, o, ws) || !aligned16(lse_f))
+    return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_fwd_fp8(g, static_cast<const uint8_t*>(q8),
+                                         static_cast<const uint8_t*>(k8),
+                                         static_cast<const uint8_t*>(v8t), scales,
+                                         static_cast<const bf16*>(gc), static_cast<const bf16*>(gf),
+                                         oc, static_cast<bf16*>(o), lse_f, w, s));
+}
+
+vsa_status_t vsa_forward_fp8(const vsa_config_t* cfg, const void* q, const void* k,
+                             const void* v, const void* gc, const void* gf, void* o, void* saved,
+                             void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (g.D != 128) return VSA_ERR_UNSUPPORTED;
+  if (!all_set(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_ALIGNMENT;
+  vsa_saved_layout_t L;
+  saved_layout(g, &L);
+  char* sv = static_cast<char*>(saved);
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(sv + L.q16);
+  uint8_t* k8 = reinterpret_cast<uint8_t*>(sv + L.k16);
+  uint8_t* v8t = reinterpret_cast<uint8_t*>(sv + L.v16);
+  float* scales = reinterpret_cast<float*>(sv + L.o_f);
+  float* qc = reinterpret_cast<float*>(sv + L.qc);
+  float* kc = reinterpret_cast<float*>(sv + L.kc);
+  float* vc = reinterpret_cast<float*>(sv + L.vc);
+  float* oc = reinterpret_cast<float*>(sv + L.oc);
+  int* idx = reinterpret_cast<int*>(sv + L.idx);
+  int* cnt = reinterpret_cast<int*>(sv + L.cnt);
+  if (launch_stage_fp8(g, static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                       static_cast<const bf16*>(v), q8, k8, v8t, scales, qc, kc, vc, w.gamax,
+                       w.status, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
+                           kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt, w,
+                           s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_fwd_fp8(g, q8, k8, v8t, scales, static_cast<const bf16*>(gc),
+                                         static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
+                                         reinterpret_cast<float*>(sv + L.lse_f), w, s));
 }
 
 }  // extern "C"

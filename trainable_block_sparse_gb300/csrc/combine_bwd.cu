@@ -7,6 +7,17 @@
 //   delta[row] = sum_d dO_f (.) O_f    (the softmax-backward row term of the fine stage)
 // HBM-bound: one CTA per (batch, head, cube) reads dO, G_c, G_f (bf16, caller
 // layout) and O_f (fp16, cube order) once and writes each output once.
+//
+// dO_f is the fp16 tensor-core operand of the fine backward.  Upstream
+// gradients of bf16 training are often far below fp16's normal range (1e-5 to
+// 1e-8 without loss scaling), where fp16 loses significand bits or flushes to
+// zero.  So dO_f and delta are written times a power of two s per (batch, head)
+// slice, chosen so that the slice's largest |dO (.) G_f| lands in [4, 8): a
+// max-reduction over the slice (amax_kernel) runs first.  Everything the fine
+// backward computes from dO_f is linear in it, and a power of two scales
+// exactly, so the fine backward divides its results by s and nothing else
+// changes.  A per-slice (not per-row) factor is what the key-side gradients
+// need: dK and dV sum over query rows, which must share one factor.
 #include "sm103_ptx.cuh"
 #include "vsa_common.cuh"
 
@@ -14,19 +25,66 @@ namespace vsa {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kAmaxCtasPerSm = 4;
+
+// Largest |dO (.) G_f| of each slice, as the bits of a non-negative float
+// (which order like the floats), max-reduced into amax[bh] (zeroed before).
+// NaNs are skipped here (fmaxf); the combine kernel flags every non-finite
+// product itself.
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict__ d_o,
+                                                        const uint4* __restrict__ gf,
+                                                        size_t vec_per_slice, uint32_t* amax) {
+  const int bh = blockIdx.y;
+  const size_t base = static_cast<size_t>(bh) * vec_per_slice;
+  float m = 0.f;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; i < vec_per_slice;
+       i += static_cast<size_t>(gridDim.x) * kThreads) {
+    const uint4 ud = d_o[base + i], uf = gf[base + i];
+    const __nv_bfloat162* pd = reinterpret_cast<const __nv_bfloat162*>(&ud);
+    const __nv_bfloat162* pf = reinterpret_cast<const __nv_bfloat162*>(&uf);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 dd = __bfloat1622float2(pd[e]);
+      const float2 ff = __bfloat1622float2(pf[e]);
+      m = fmaxf(m, fmaxf(fabsf(dd.x * ff.x), fabsf(dd.y * ff.y)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  __shared__ float wmax[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, wmax[w]);
+    atomicMax(amax + bh, __float_as_uint(m));
+  }
+}
+
+// The power of two s that brings a slice maximum `bits` (a non-negative float)
+// into [4, 8): s = 2^(3 - x) for a maximum in [2^(x-1), 2^x), clamped so that s
+// and 1/s are normal floats.  A zero or non-finite maximum gives s = 1.
+__device__ __forceinline__ float grad_scale_of(uint32_t bits) {
+  const int E = static_cast<int>((bits >> 23) & 0xFFu);
+  if (bits == 0u || E == 0xFF) return 1.f;
+  const int e = E == 0 ? 126 : min(126, max(-126, 3 - (E - 126)));
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     Geom g, const uint4* __restrict__ d_o, const uint4* __restrict__ gc,
     const uint4* __restrict__ gf, const uint4* __restrict__ o_f, const float* __restrict__ oc,
     float* __restrict__ dgc, float* __restrict__ dgf, uint4* __restrict__ dof,
-    float* __restrict__ doc, float* __restrict__ delta, uint32_t* status) {
+    float* __restrict__ doc, float* __restrict__ delta, const uint32_t* __restrict__ amax,
+    float* __restrict__ gscale, uint32_t* status) {
   constexpr int VPR = D / 8;              // 8-element vectors per row
   constexpr int GROUPS = kThreads / VPR;  // rows processed side by side
   __shared__ float red[GROUPS][D];
   const int c = blockIdx.x, bh = blockIdx.y;
   const int col = threadIdx.x % VPR, grp = threadIdx.x / VPR;
   const size_t slice = static_cast<size_t>(bh) * g.N;
+  const float gs = grad_scale_of(amax[bh]);  // the same in every CTA of the slice
+  if (c == 0 && threadIdx.x == 0) gscale[bh] = gs;
   const float* ocr = oc + (static_cast<size_t>(bh) * g.Nc + c) * D + col * 8;
   float ocv[8];
 #pragma unroll
@@ -64,7 +122,8 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
       vdgf[2 * e + 1] = dd.y * ofv[2 * e + 1];
       acc[2 * e] += dd.x * cc.x;
       acc[2 * e + 1] += dd.y * cc.y;
-      const float2 raw = make_float2(dd.x * ff.x, dd.y * ff.y);
+      // exact: a product of two bf16 values times a power of two
+      const float2 raw = make_float2(dd.x * ff.x * gs, dd.y * ff.y * gs);
       bad |= !(fabsf(raw.x) <= 65504.f) || !(fabsf(raw.y) <= 65504.f);
       pof[e] = __floats2half2_rn(raw.x, raw.y);
       const float2 r = __half22float2(pof[e]);  // delta uses the rounded dO_f the MMAs see
@@ -99,17 +158,31 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
                                const __half* o_f, const float* oc, float* dgc, float* dgf,
-                               __half* dof, float* doc, float* delta, uint32_t* status,
-                               cudaStream_t s) {
-  dim3 grid(g.Nc, g.BH);
+                               __half* dof, float* doc, float* delta, uint32_t* amax,
+                               float* gscale, uint32_t* status, cudaStream_t s) {
   auto u4 = [](const void* p) { return reinterpret_cast<const uint4*>(p); };
+  // slice maxima first: a few CTAs per SM in total, strided over each slice
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint32_t) * g.BH, s);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const size_t vec = static_cast<size_t>(g.N) * g.D / 8;  // uint4 vectors per slice
+  const size_t per_slice_max = (vec + kThreads - 1) / kThreads;
+  const size_t want = (static_cast<size_t>(sms) * kAmaxCtasPerSm + g.BH - 1) / g.BH;
+  const dim3 agrid(static_cast<unsigned>(want < per_slice_max ? want : per_slice_max), g.BH);
+  amax_kernel<<<agrid, kThreads, 0, s>>>(u4(d_o), u4(gf), vec, amax);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  dim3 grid(g.Nc, g.BH);
   if (g.D == 64)
     combine_bwd_kernel<64><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), u4(o_f), oc, dgc, dgf,
-                                                     reinterpret_cast<uint4*>(dof), doc, delta, status);
+                                                     reinterpret_cast<uint4*>(dof), doc, delta,
+                                                     amax, gscale, status);
   else
     combine_bwd_kernel<128><<<grid, kThreads, 0, s>>>(g, u4(d_o), u4(gc), u4(gf), u4(o_f), oc, dgc,
                                                       dgf, reinterpret_cast<uint4*>(dof), doc,
-                                                      delta, status);
+                                                      delta, amax, gscale, status);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,10 @@
 //   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO_f
 // over the selected 64x64 blocks only.  The pooled (coarse) gradients enter
 // as dQ += repeat(dQ_c)/64 etc. in the epilogue, which also un-permutes.
+// dO_f and delta arrive multiplied by a power of two per (batch, head) slice
+// (the combine backward's gradient scale, which keeps small upstream gradients
+// inside fp16's normal range); dP, dS, dQ, dK and dV are linear in them, so the
+// epilogue divides the accumulators by the slice's factor (exactly).
 //
 // One tcgen05 kernel template runs two deterministic, atomic-free passes:
 //  * kKeyMajor = false (dQ pass): work item = two query cubes (M = 128 query
@@ -62,16 +66,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
 // dQ pass: the item's Q and dO as TMEM A operands (D/2 columns each) at kColA2
 constexpr float kLog2e = 1.4426950408889634f;
-// Of every 8 exponentials of P, this many run as the FMA-pipe polynomial and
-// the rest on the ex2 unit (none: the polynomial measured slower here too).
-constexpr int kPolyOf8Bwd = 0;
-
-template <int J>
-__device__ __forceinline__ float ex2_split_bwd(float x) {
-  if constexpr ((J & 7) < kPolyOf8Bwd) return ex2_poly(x);
-  else return ex2_approx(x);
-}
-
 template <int D>
 struct BwdSmem {
   static constexpr int kChunks = D / 64;
@@ -103,6 +97,7 @@ struct BwdParams {
   const int* order;       // schedule position -> item (null: identity)
   const float* lse;     // [BH, N] cube order, natural log
   const float* delta;   // [BH, N] cube order
+  const float* gscale;  // [BH] factor dO_f and delta carry (null: 1)
   const float* pooled1; // dQ_c (dQ pass) or dV_c (key-major pass), may be null
   const float* pooled2; // dK_c (key-major pass), may be null
   float* out1;          // dQ (dQ pass) or dV (key-major pass), caller layout fp32
@@ -564,8 +559,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
               const float l1 = kKeyMajor ? __shfl_sync(kFull, ch ? cl1 : cl0, j + 1) : row_lse;
               float t0, t1;
               fma2(t0, t1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), c, c, -l0, -l1);
-              p[32 * ch + j] = ex2_split_bwd<32 * ch + j>(t0);
-              p[32 * ch + j + 1] = ex2_split_bwd<32 * ch + j + 1>(t1);
+              p[32 * ch + j] = ex2_approx(t0);
+              p[32 * ch + j + 1] = ex2_approx(t1);
             });
           });
         } else {
@@ -666,14 +661,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           }
         }
       }
+      // 1 / (the slice's gradient scale): a power of two, so exact
+      const float inv_gs = P.gscale ? 1.f / __ldg(P.gscale + pi.bh) : 1.f;
       if (!waitw(&sb.acc_full, it & 1, abort_flag, P.status)) break;
       tc_fence_after();
       // dQ pass: dQ = scale * acc; key-major: dV = acc, then dK = scale * acc
-      if (live) drain_acc<D>(tq + kColA1, kKeyMajor ? 1.f : g.scale, p1, P.out1, orow);
+      // (each divided by the gradient scale)
+      if (live) drain_acc<D>(tq + kColA1, (kKeyMajor ? 1.f : g.scale) * inv_gs, p1, P.out1, orow);
       tc_fence_before();
       warp_arrive_bwd(kKeyMajor ? &sb.dv_free : &sb.acc_free);
       if (kKeyMajor) {
-        if (live) drain_acc<D>(tq + kColA2, g.scale, p2, P.out2, orow);
+        if (live) drain_acc<D>(tq + kColA2, g.scale * inv_gs, p2, P.out2, orow);
         tc_fence_before();
         warp_arrive_bwd(&sb.dk_free);
       }
@@ -710,16 +708,16 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
 
 template <int D>
 cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __half* v,
-                     const float* lse_f, const __half* dof,
-                     const float* delta, const float* dqc, const float* dkc, const float* dvc,
+                     const float* lse_f, const __half* dof, const float* delta,
+                     const float* gscale, const float* dqc, const float* dkc, const float* dvc,
                      float* dq, float* dk, float* dv, const Workspace& ws, cudaStream_t s) {
   const bool ordered = use_cost_order(g);
-  BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, ordered ? ws.qorder : nullptr, lse_f, delta, dqc, nullptr, dq, nullptr,
-               ws.status};
+  BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, ordered ? ws.qorder : nullptr, lse_f, delta,
+               gscale, dqc, nullptr, dq, nullptr, ws.status};
   cudaError_t e = run_bwd<D, false>(g, q, dof, k, v, pq, s);
   if (e != cudaSuccess) return e;
-  BwdParams pk{g, ws.kpairs, ws.klist, ws.n_kpairs, ordered ? ws.korder : nullptr, lse_f, delta, dvc, dkc, dv, dk,
-               ws.status};
+  BwdParams pk{g, ws.kpairs, ws.klist, ws.n_kpairs, ordered ? ws.korder : nullptr, lse_f, delta,
+               gscale, dvc, dkc, dv, dk, ws.status};
   return run_bwd<D, true>(g, k, v, q, dof, pk, s);
 }
 
@@ -727,10 +725,12 @@ cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __ha
 
 cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const float* lse_f, const __half* dof, const float* delta,
-                            const float* dqc, const float* dkc, const float* dvc, float* dq,
-                            float* dk, float* dv, const Workspace& ws, cudaStream_t s) {
-  if (g.D == 64) return bwd_impl<64>(g, q, k, v, lse_f, dof, delta, dqc, dkc, dvc, dq, dk, dv, ws, s);
-  return bwd_impl<128>(g, q, k, v, lse_f, dof, delta, dqc, dkc, dvc, dq, dk, dv, ws, s);
+                            const float* gscale, const float* dqc, const float* dkc,
+                            const float* dvc, float* dq, float* dk, float* dv,
+                            const Workspace& ws, cudaStream_t s) {
+  if (g.D == 64)
+    return bwd_impl<64>(g, q, k, v, lse_f, dof, delta, gscale, dqc, dkc, dvc, dq, dk, dv, ws, s);
+  return bwd_impl<128>(g, q, k, v, lse_f, dof, delta, gscale, dqc, dkc, dvc, dq, dk, dv, ws, s);
 }
 
 }  // namespace vsa

@@ -39,6 +39,16 @@
 // Every mbarrier wait is bounded; a time-out is recorded in the status word and
 // the CTA unwinds, waits for its own in-flight copies and MMAs, frees TMEM and
 // exits.
+//
+// e4m3 variant (kF8, head_dim 128, inference: no O_f): Q, K and V arrive as the
+// e4m3 copies of stage_fp8.cu (per-slice power-of-two factors), P is written
+// to TMEM as e4m3 and every UMMA is kind::f8f6f4 (K = 32 per MMA) with fp32
+// accumulation.  A K tile is 64 rows of 128 bytes (one 128-byte swizzle
+// chunk); V comes transposed per cube (64-byte rows of keys, 64-byte swizzle),
+// so the P V product reads it K-major.  The per-slice factors of Q and K fold
+// into the softmax scale, that of V into the epilogue's normalisation.  Same
+// roles, rings, barriers and schedule as the fp16 kernel, half the bytes per
+// step.
 #include <cfloat>
 #include <cstring>
 
@@ -56,32 +66,26 @@ constexpr uint32_t kColS = 0;              // S (128 columns)
 constexpr uint32_t kColP = 128;            // P buffers (fp16 pairs) at columns 128 and 192
 constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// Of every 8 exponentials of the softmax, this many run as the FMA-pipe
-// polynomial and the rest on the ex2 unit.  Measured on the 720p layer,
-// moving 2, 3 or 4 of 8 to the polynomial made the kernel 4-10% slower, so
-// the ex2 unit takes them all.
-constexpr int kPolyOf8 = 0;
-
-// 2^x for element j of a row: ex2 unit or FMA-pipe polynomial by position.
-template <int J>
-__device__ __forceinline__ float ex2_split(float x) {
-  if constexpr ((J & 7) < kPolyOf8) return ex2_poly(x);
-  else return ex2_approx(x);
-}
-
-template <int D>
+// e4m3 variant: P is kept within [0, 2^(kRescaleThresholdF8 + kP8Shift)] =
+// [0, 256] (e4m3 ends at 448) by a tighter threshold and an exponent shift, so
+// that probabilities down to 2^-12 of the row maximum stay normal e4m3 numbers
+// (3 significand bits); the row sum carries the same factor 2^kP8Shift.
+constexpr float kRescaleThresholdF8 = 2.0f;
+constexpr float kP8Shift = 6.0f;
+template <int D, bool kF8 = false>
 struct FwdSmem {
-  static constexpr int kChunks = D / 64;              // 64-column (128-byte) chunks
+  // 128-byte chunks of a row: 64 fp16 columns, or 128 e4m3 columns
+  static constexpr int kChunks = kF8 ? D / 128 : D / 64;
   static constexpr int kChunkBytes = 128 * 128;       // one chunk of 128 rows
   static constexpr int kQBytes = kChunks * kChunkBytes;
   static constexpr int kKVBytes = kChunks * kChunkBytes;  // 2 key tiles
-  static constexpr int kStagesK = (D == 128) ? 2 : 3;
+  static constexpr int kStagesK = kF8 ? 3 : (D == 128) ? 2 : 3;
   // D = 128: two stages each; D = 64 (16 KB tiles): three each.  Deeper rings
   // measured slower: TMA serves a CTA's copies in order, so every extra slot in
   // flight queues ahead of the tile the next product needs (at D = 128,
-  // 2 K / 3 V and 3 K / 2 V both lost ~1%).
-  static constexpr int kStagesV = (D == 128) ? 2 : 3;
-  static constexpr int kTileBytes = 64 * D * 2;       // one 64-row tile
+  // 2 K / 3 V and 3 K / 2 V both lost ~1%).  The e4m3 tiles are half as large.
+  static constexpr int kStagesV = kF8 ? 3 : (D == 128) ? 2 : 3;
+  static constexpr int kTileBytes = 64 * D * (kF8 ? 1 : 2);  // one 64-row tile
   // epilogue staging of one 32-column chunk of O_f: 128 rows x 128 bytes
   static constexpr int kStageOff = kQBytes + (kStagesK + kStagesV) * kKVBytes;
   static constexpr int kStageBytes = 128 * 128;
@@ -115,6 +119,7 @@ struct FwdParams {
   __half* o_f;
   float* lse_f;
   uint32_t* status;
+  const float* scales;    // e4m3 variant: [BH][3] factors of the Q, K, V copies
 };
 
 // Arrival of a whole warp counted once: lanes finish their own work first.
@@ -153,14 +158,15 @@ __device__ __forceinline__ bool pair_sync_or(int quarter, bool fail) {
   return r != 0;
 }
 
-template <int D>
+template <int D, bool kF8>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tof,
                     FwdParams P) {
-  using L = FwdSmem<D>;
+  static_assert(!kF8 || D == 128, "the e4m3 variant is for head_dim 128");
+  using L = FwdSmem<D, kF8>;
   constexpr int kSK = L::kStagesK, kSV = L::kStagesV;
-  constexpr int kKSteps = D / 16;
+  constexpr int kKSteps = kF8 ? D / 32 : D / 16;  // K per MMA: 32 e4m3 or 16 fp16 (32 bytes)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -255,10 +261,17 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           uint8_t* dst = ring + slot * L::kKVBytes;
           const int r0 = pi.bh * g.N + t0 * kTile, r1 = pi.bh * g.N + t1 * kTile;
           mbar_arrive_expect_tx(&full[slot], (two ? 2 : 1) * L::kTileBytes);
+          if (kF8 && !is_k) {
+            // transposed V: rows (cube, channel) of 64 key bytes, one box per cube
+            const int v0 = (pi.bh * g.Nc + t0) * D, v1 = (pi.bh * g.Nc + t1) * D;
+            tma_load_2d(dst, tmap, 0, v0, &full[slot]);
+            if (two) tma_load_2d(dst + 8192, tmap, 0, v1, &full[slot]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_2d(dst + c * L::kChunkBytes, tmap, c * 64, r0, &full[slot]);
-            if (two) tma_load_2d(dst + c * L::kChunkBytes + 8192, tmap, c * 64, r1, &full[slot]);
+            for (int c = 0; c < L::kChunks; ++c) {
+              tma_load_2d(dst + c * L::kChunkBytes, tmap, c * 64, r0, &full[slot]);
+              if (two) tma_load_2d(dst + c * L::kChunkBytes + 8192, tmap, c * 64, r1, &full[slot]);
+            }
           }
           ++step;
         }
@@ -271,9 +284,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
   } else if (warp == kWarpMma) {
     // ===================================================== UMMA issuer
-    const uint32_t idesc_s128 = idesc_f16(128, 128, 0, 0);
-    const uint32_t idesc_s64 = idesc_f16(128, 64, 0, 0);
-    const uint32_t idesc_pv = idesc_f16(128, D, 0, 1);
+    const uint32_t idesc_s128 = kF8 ? idesc_e4m3(128, 128) : idesc_f16(128, 128, 0, 0);
+    const uint32_t idesc_s64 = kF8 ? idesc_e4m3(128, 64) : idesc_f16(128, 64, 0, 0);
+    const uint32_t idesc_pv = kF8 ? idesc_e4m3(128, D) : idesc_f16(128, D, 0, 1);
     const uint64_t qd0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t vd0 = sdesc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
@@ -291,7 +304,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const uint64_t kb = kd0 + ((slot * L::kKVBytes) >> 4);
 #pragma unroll
       for (int k = 0; k < kKSteps; ++k) kd[k] = kb + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
-      issue_ss_chain<kKSteps>(tb + kColS, qd, kd, two ? idesc_s128 : idesc_s64);
+      if constexpr (kF8)
+        issue_ss4_f8(tb + kColS, qd, kd, two ? idesc_s128 : idesc_s64);
+      else
+        issue_ss_chain<kKSteps>(tb + kColS, qd, kd, two ? idesc_s128 : idesc_s64);
       commit_elect(&sb.s_full);
       commit_elect(&sb.k_empty[slot]);
       return true;
@@ -304,8 +320,19 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       if (!waitw(&sb.p_full[pbuf], (t >> 1) & 1, abort_flag, P.status)) return false;
       if (!waitw(&sb.v_full[slot], (t / kSV) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
-      issue_ts_rows(tb + kColO + obuf * 128, tb + kColP + pbuf * 64,
-                    vd0 + ((slot * L::kKVBytes) >> 4), two, idesc_pv, !first);
+      if constexpr (kF8) {
+        // P (e4m3, 16 columns per key tile) x V^T: per key tile one 128-row box of
+        // 64-byte rows, K steps of 32 keys at +32 bytes
+        const uint64_t vb = sdesc_sw64(smem_u32(sV) + slot * L::kKVBytes, 512);
+        const uint32_t pa = tb + kColP + pbuf * 64;
+        issue_ts2_f8(tb + kColO + obuf * 128, pa, vb, vb + 2, idesc_pv, first ? 0u : 1u);
+        if (two)
+          issue_ts2_f8(tb + kColO + obuf * 128, pa + 16, vb + (8192 >> 4), vb + (8192 >> 4) + 2,
+                       idesc_pv, 1u);
+      } else {
+        issue_ts_rows(tb + kColO + obuf * 128, tb + kColP + pbuf * 64,
+                      vd0 + ((slot * L::kKVBytes) >> 4), two, idesc_pv, !first);
+      }
       commit_elect(&sb.v_empty[slot]);  // also tells the rescale that PV(t) is done
       return true;
     };
@@ -370,6 +397,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const int nsteps = (pi.count + 1) / 2;
       const int obuf = it & 1;
       float m_run = -INFINITY, l_run = 0.f;
+      // e4m3 variant: logits of the copies times the Q and K factors
+      const float cs = kF8 ? c * __ldg(P.scales + 3 * pi.bh) * __ldg(P.scales + 3 * pi.bh + 1) : c;
       // list entry of this half's key tile, fetched one step ahead (its global
       // load latency would otherwise sit between two steps)
       uint32_t e_cur = hc < pi.count ? __ldg(list + hc) : 0u;
@@ -404,10 +433,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
         sb.red[step & 1][hc][row] = mx;
         if (pair_sync_or(quarter, !got)) { ok = false; break; }
-        const float m_new = fmaxf(m_run, fmaxf(mx, sb.red[step & 1][hc ^ 1][row]) * c);
+        const float m_new = fmaxf(m_run, fmaxf(mx, sb.red[step & 1][hc ^ 1][row]) * cs);
         bool resc = false;
         float alpha = 1.f;
-        if (m_new > m_run + kRescaleThreshold) {
+        if (m_new > m_run + (kF8 ? kRescaleThresholdF8 : kRescaleThreshold)) {
           if (m_run != -INFINITY) {
             alpha = ex2_approx(m_run - m_new);
             l_run *= alpha;
@@ -415,7 +444,26 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           }
           m_run = m_new;
         }
-        if (valid) {
+        if (valid && kF8) {
+          float ls[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+          const float mb = m_run - kP8Shift;
+          // x[i] <- e4m3x4(p[4i .. 4i+3]); x[4i .. 4i+3] are read before x[i] is
+          // written
+          unroll_for<16>([&](auto I) {
+            constexpr int i = decltype(I)::value;
+            float t0, t1, t2, t3;
+            fma2_bc(t0, t1, __uint_as_float(x[4 * i]), __uint_as_float(x[4 * i + 1]), cs, -mb);
+            fma2_bc(t2, t3, __uint_as_float(x[4 * i + 2]), __uint_as_float(x[4 * i + 3]), cs, -mb);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            const float p2 = ex2_approx(t2), p3 = ex2_approx(t3);
+            add2_acc(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], p0, p1);
+            add2_acc(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], p2, p3);
+            x[i] = pack_e4m3x4(p0, p1, p2, p3);
+          });
+          l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        } else if (valid) {
           float ls[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) ls[u] = 0.f;
@@ -426,8 +474,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             constexpr int i = decltype(I)::value;
             float t0, t1;
             fma2_bc(t0, t1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mb);
-            const float p0 = ex2_split<2 * i>(t0);
-            const float p1 = ex2_split<2 * i + 1>(t1);
+            const float p0 = ex2_approx(t0);
+            const float p1 = ex2_approx(t1);
             add2_acc(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], p0, p1);
             x[i] = pack_f16x2(p0, p1);
           });
@@ -437,9 +485,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           for (int i = 0; i < 32; ++i) x[i] = 0u;
         }
         // P of key tile hc goes to columns [32 hc, 32 hc + 32) of P buffer step % 2
+        // (e4m3: [16 hc, 16 hc + 16))
         if (have) {
-          tmem_st32(tb + lane_addr + kColP + (step & 1) * 64 + 32 * hc,
-                    *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+          if constexpr (kF8)
+            tmem_st16(tb + lane_addr + kColP + (step & 1) * 64 + 16 * hc,
+                      *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+          else
+            tmem_st32(tb + lane_addr + kColP + (step & 1) * 64 + 32 * hc,
+                      *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
         }
         if (__any_sync(0xffffffffu, resc)) {
           // O holds the previous steps' sum: wait for the last PV product,
@@ -486,7 +539,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const int half = row >> 6;                   // 0: first cube, 1: second cube
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = threadIdx.x == kWarpEpi * 32;
-    const bool stage_of = P.o_f != nullptr;
+    const bool stage_of = !kF8 && P.o_f != nullptr;
     int it = 0;
     // No abort test in the loop condition: the four warps meet at named
     // barriers and must walk the same items (see epi_sync_or).
@@ -522,7 +575,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       }
       if (epi_sync_or(!got)) break;
       tc_fence_after();
-      const float inv_l = 1.f / l_sum;
+      // e4m3 variant: the V copy's factor joins the normalisation
+      const float inv_l = (kF8 ? __ldg(P.scales + 3 * pi.bh + 2) : 1.f) / l_sum;
       const uint32_t to = tb + lane_addr + kColO + obuf * 128;
 #pragma unroll 1
       for (int cc = 0; cc < D; cc += 32) {
@@ -590,7 +644,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           }
         }
       }
-      if (live && P.lse_f) P.lse_f[frow] = (m_fin + __log2f(l_sum)) * 0.6931471805599453f;
+      if (live && P.lse_f)
+        P.lse_f[frow] = (m_fin + __log2f(l_sum) - (kF8 ? kP8Shift : 0.f)) * 0.6931471805599453f;
       tc_fence_before();
       warp_arrive(&sb.o_free[obuf]);
       ++it;
@@ -616,12 +671,36 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
   memset(&mof, 0, sizeof(mof));
   if (p.o_f && !encode_tiled_2d(&mof, p.o_f, rows, D, 64, 64)) return cudaErrorInvalidValue;
   const int smem = FwdSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
-  fine_fwd_kernel<D><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
+  fine_fwd_kernel<D, false><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
+  return cudaGetLastError();
+}
+
+// e4m3 variant, head_dim 128: Q8, K8 [BH*N, 128] bytes (boxes of 64 rows x 128
+// bytes, 128-byte swizzle); V8T [BH*Nc*128, 64] bytes (boxes of 128 rows x 64
+// bytes, 64-byte swizzle).
+cudaError_t run_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t* k8, const uint8_t* v8t,
+                        FwdParams p, cudaStream_t s) {
+  constexpr int D = 128;
+  alignas(64) CUtensorMap mq, mk, mv, mof;
+  const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
+  const uint64_t vrows = static_cast<uint64_t>(g.BH) * g.Nc * D;
+  if (!encode_tiled_2d_u8(&mq, q8, rows, D, 64, D, 128) ||
+      !encode_tiled_2d_u8(&mk, k8, rows, D, 64, D, 128) ||
+      !encode_tiled_2d_u8(&mv, v8t, vrows, kTile, D, kTile, 64))
+    return cudaErrorInvalidValue;
+  memset(&mof, 0, sizeof(mof));
+  const int smem = FwdSmem<D, true>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = persistent_grid(p.n_items);
+  if (grid <= 0) return cudaSuccess;
+  fine_fwd_kernel<D, true><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
 
@@ -632,9 +711,20 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
                             __nv_bfloat16* o, __half* o_f, float* lse_f, const Workspace& ws,
                             cudaStream_t s) {
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
-              gc, gf, oc, o, o_f, lse_f, ws.status};
+              gc, gf, oc, o, o_f, lse_f, ws.status, nullptr};
   if (g.D == 64) return run_fwd<64>(g, q, k, v, p, s);
   return run_fwd<128>(g, q, k, v, p, s);
+}
+
+cudaError_t launch_fine_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t* k8,
+                                const uint8_t* v8t, const float* scales,
+                                const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
+                                __nv_bfloat16* o, float* lse_f, const Workspace& ws,
+                                cudaStream_t s) {
+  if (g.D != 128) return cudaErrorInvalidValue;
+  FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
+              gc, gf, oc, o, nullptr, lse_f, ws.status, scales};
+  return run_fwd_fp8(g, q8, k8, v8t, p, s);
 }
 
 }  // namespace vsa

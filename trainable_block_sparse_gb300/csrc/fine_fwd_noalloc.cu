@@ -17,8 +17,9 @@
 // caches it; make that first call before any stream capture.  Every call shares
 // the one array, so calls that overlap on the GPU race with each other; the
 // status word is cleared at the start of each call, the rest is fully
-// rewritten before it is read.
-#include <cmath>
+// rewritten before it is read.  The query pairs run in their natural order
+// (the cost-sorted order of vsa_fine_fwd would need more scratch); results are
+// bitwise those of vsa_fine_fwd.
 #include <mutex>
 
 #include "../../include/vsa.h"
@@ -55,27 +56,6 @@ cudaError_t scratch_address(void** out) {
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// The geometry of a configuration that vsa_validate accepted.
-Geom geometry(const vsa_config_t* c) {
-  Geom g{};
-  g.B = c->batch;
-  g.heads = c->heads;
-  g.T = c->T;
-  g.H = c->H;
-  g.W = c->W;
-  g.D = c->head_dim;
-  g.BH = c->batch * c->heads;
-  g.N = c->T * c->H * c->W;
-  g.Nc = g.N / kTile;
-  g.ct = c->T / 4;
-  g.ch = c->H / 4;
-  g.cw = c->W / 4;
-  g.cap = c->select_mode == VSA_SELECT_TOPK ? c->topk : c->kmax;
-  g.raster = c->layout == VSA_LAYOUT_RASTER;
-  g.scale = c->scale > 0.f ? c->scale : 1.0f / sqrtf(static_cast<float>(c->head_dim));
-  return g;
-}
-
 bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -89,9 +69,9 @@ extern "C" vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void
                                              const void* gc, const void* gf, const float* oc,
                                              void* o, void* o_f, float* lse_f,
                                              uint32_t* status, void* stream) {
-  const vsa_status_t st = vsa_validate(cfg);
+  Geom g;
+  const vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  const Geom g = geometry(cfg);
   // scratch: status word | pair items | union lists (2 * capacity entries per pair)
   const size_t npairs = static_cast<size_t>(g.BH) * ((g.Nc + 1) / 2);
   const size_t items_off = 256;

@@ -28,23 +28,3 @@ extern "C" vsa_status_t vsa_probe_wait_timeout(void* ws, uint32_t limit_us, void
       static_cast<uint32_t*>(ws), static_cast<uint64_t>(limit_us) * 1000ull);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
-
-namespace vsa {
-namespace {
-
-__global__ void probe_exp2_kernel(const float* x, float* y, int n, int which) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) y[i] = which ? ex2_poly(x[i]) : ex2_approx(x[i]);
-}
-
-}  // namespace
-}  // namespace vsa
-
-extern "C" vsa_status_t vsa_probe_exp2(const float* x, float* y, int32_t n, int32_t which,
-                                       void* stream) {
-  if (!x || !y || n < 0 || (which != 0 && which != 1)) return VSA_ERR_INVALID_ARG;
-  if (n == 0) return VSA_OK;
-  vsa::probe_exp2_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      x, y, n, which);
-  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
-}

@@ -277,6 +277,30 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle, K-major operand: rows of
+// 64 bytes (the layout a TMA load with CU_TENSOR_MAP_SWIZZLE_64B writes: 16-byte
+// chunks XOR-ed with (row/2)%4, atoms of 8 rows = 512 bytes, atom-aligned
+// buffers); SBO = stride between 8-row groups (512); step K by +32 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;  // LBO: unused by swizzled K-major layouts
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05
+  d |= 4ull << 61;  // swizzle mode: 64-byte
+  return d;
+}
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (both K-major) and
+// fp32 D.  Each MMA consumes K = 32 (32 bytes of every row).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                   // D format fp32
+         | (0u << 7)                                 // A format e4m3
+         | (0u << 10)                                // B format e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Instruction descriptor, kind::f16 with fp16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4)                                   // D format fp32
@@ -320,26 +344,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x on the FMA pipe, for splitting a softmax's exponentials between this
-// and the ex2 unit.  Range reduction x = n + f, n = round(x) taken from the
-// low mantissa bits of x + 1.5*2^23, f in [-1/2, 1/2]; 2^f from a degree-3
-// polynomial fitted for minimum maximum relative error on that interval
-// (coefficients from exp2_fit.py, relative error below 7.5e-5); 2^n added to
-// the exponent field.  Inputs are clamped to >= -126 (results there are below
-// 2^-125, i.e. zero once rounded to fp16); x must be < 128.
-__device__ __forceinline__ float ex2_poly(float x) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  x = fmaxf(x, -126.0f);
-  const float t = __fadd_rn(x, kShift);
-  const float f = __fsub_rn(x, __fsub_rn(t, kShift));
-  float p = 0x1.c3f76p-5f;               // c3
-  p = __fmaf_rn(p, f, 0x1.f0de1ap-3f);    // c2
-  p = __fmaf_rn(p, f, 0x1.62f31ap-1f);    // c1
-  p = __fmaf_rn(p, f, 0x1.fff692p-1f);    // c0
-  const int n = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(p) + (n << 23));
 }
 
 // Packed fp32 pairs (sm_100+): each lane of the pair is an ordinary
@@ -389,6 +393,20 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four floats -> four e4m3 bytes (round to nearest even, saturating to
+// +-448), element 0 in the lowest byte: the order a K-major fp8 operand holds
+// consecutive K values in one 32-bit TMEM column.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float e0, float e1, float e2, float e3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -115,6 +115,36 @@ __device__ __forceinline__ void issue_ts_rows(uint32_t d_tmem, uint32_t a_tmem, 
               b_desc + (12288 >> 4), b_desc + (14336 >> 4), idesc, 1u);
 }
 
+// e4m3 SS chain of 4 MMAs (K = 32 each, 128 values of K), both operands
+// K-major in smem; the first MMA overwrites D.
+__device__ __forceinline__ void issue_ss4_f8(uint32_t d_tmem, const uint64_t (&a)[4],
+                                             const uint64_t (&b)[4], uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %10, %10;\n\tsetp.eq.b32 t, %10, %10;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %9, f;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %9, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %9, t;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %9, t;\n\t}" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(idesc), "r"(0)
+      : "memory");
+}
+
+// e4m3 TS chain over 64 values of K: A from TMEM (8 columns, four e4m3 per
+// column, per 32 K), B = 2 smem descriptors.  acc0 = 0: the first MMA
+// overwrites D.
+__device__ __forceinline__ void issue_ts2_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                             uint64_t b1, uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, t;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "setp.eq.b32 t, %5, %5;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %4, q;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%6], %3, %4, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b0), "l"(b1), "r"(idesc), "r"(acc0), "r"(a_tmem + 8)
+      : "memory");
+}
+
 __device__ __forceinline__ void commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"

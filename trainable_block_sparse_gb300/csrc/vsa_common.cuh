@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "../../include/vsa.h"
+
 namespace vsa {
 
 constexpr int kTile = 64;  // tokens per (4,4,4) cube
@@ -23,6 +25,10 @@ struct Geom {
   int raster;    // 1: caller tensors in raster order, 0: cube order
   float scale;   // softmax scale (both stages)
 };
+
+// Checks a configuration and derives its geometry (api.cu): VSA_OK, or the
+// reason the configuration is rejected (then *g is not written).
+vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g);
 
 // Raster row of token o (0..63) of cube c: cube (4,4,4) with in-cube order
 // o = (t%4)*16 + (h%4)*4 + w%4, cubes ordered (t/4, h/4, w/4) row-major.
@@ -76,8 +82,11 @@ struct Workspace {
   float *vh, *doh;                 // V_c, dO_c (bwd)
   float *kth, *qth, *doth;         // K_c^T, Q_c^T, dO_c^T (bwd)
   float *pth, *dlth;               // P^T, dL^T (bwd)
-  // backward
-  void* dof;              // bf16 cube order
+  // backward: per-slice scale of dO (.) G_f (see launch_combine_bwd)
+  uint32_t* gamax;        // [3*BH] slice maxima as float bits: |dO (.) G_f| (the
+                          // first BH), or |Q|, |K|, |V| for the e4m3 staging
+  float* gscale;          // [BH] power-of-two factor applied to dO_f and delta
+  void* dof;              // fp16 cube order, dO (.) G_f times gscale
   float* delta;           // fp32 [BH, N]
   float* doc;             // fp32 [BH, Nc, D]
   float* dqc; float* dkc; float* dvc;
@@ -113,11 +122,17 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
                             const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
                             __nv_bfloat16* o, __half* o_f, float* lse_f, const Workspace& ws,
                             cudaStream_t s);
+// Combine backward.  dO_f = dO (.) G_f and delta are written scaled by a power
+// of two per (batch, head) slice, gscale[bh] (chosen from the slice's largest
+// |dO (.) G_f|, found first by a max-reduction into amax[bh], so that this
+// largest value lands in [4, 8)): fp16 then keeps full precision for the
+// magnitudes that matter, whatever the size of the upstream gradient.  The
+// fine backward is linear in dO_f and divides its results by gscale.
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
                                const __half* o_f, const float* oc, float* dgc, float* dgf,
-                               __half* dof, float* doc, float* delta, uint32_t* status,
-                               cudaStream_t s);
+                               __half* dof, float* doc, float* delta, uint32_t* amax,
+                               float* gscale, uint32_t* status, cudaStream_t s);
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
                               const float* oc, const float* lse_c, const float* doc,
                               float* dqc, float* dkc, float* dvc, const Workspace& ws,
@@ -140,10 +155,13 @@ inline bool use_cost_order(const Geom& g) {
   const double kv_bytes = 2.0 * 2.0 * g.BH * static_cast<double>(g.N) * g.D;
   return kv_bytes <= 256.0 * 1024 * 1024;
 }
+// gscale: [BH] factor dof and delta were scaled by (null: 1); the fine
+// gradients are divided by it before the pooled ones are added.
 cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const float* lse_f, const __half* dof, const float* delta,
-                            const float* dqc, const float* dkc, const float* dvc, float* dq,
-                            float* dk, float* dv, const Workspace& ws, cudaStream_t s);
+                            const float* gscale, const float* dqc, const float* dkc,
+                            const float* dvc, float* dq, float* dk, float* dv,
+                            const Workspace& ws, cudaStream_t s);
 
 // ------------------------------------------------ tensor-core fp32 GEMM
 // D[b] = A[b] B[b]^T, A [M x K], B [N x K], both K-major, each passed as a
@@ -195,5 +213,25 @@ bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t 
 // Driver entry point for tensor-map encoding, resolved once (api.cu).
 bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols);
+// The same over bytes (e4m3 data), with a 64- or 128-byte swizzle.
+bool encode_tiled_2d_u8(void* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
+
+// ------------------------------------------------ e4m3 variant of the fine forward
+// Staging (stage_fp8.cu, head_dim 128): bf16 q, k, v (caller layout) -> e4m3
+// copies Q8, K8 ([BH*N, 128] bytes, cube order) and V8T ([BH*Nc, 128, 64]
+// bytes, each cube transposed), scales [BH][3] (1/s of Q, K, V: the power of
+// two each slice was multiplied by), and optionally the fp32 cube means.
+// amax: [3*BH] scratch.
+cudaError_t launch_stage_fp8(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                             const __nv_bfloat16* v, uint8_t* q8, uint8_t* k8, uint8_t* v8t,
+                             float* scales, float* pq, float* pk, float* pv, uint32_t* amax,
+                             uint32_t* status, cudaStream_t s);
+// The fine forward + combine on those copies (fine_fwd.cu; inference: no O_f).
+cudaError_t launch_fine_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t* k8,
+                                const uint8_t* v8t, const float* scales,
+                                const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
+                                __nv_bfloat16* o, float* lse_f, const Workspace& ws,
+                                cudaStream_t s);
 
 }  // namespace vsa

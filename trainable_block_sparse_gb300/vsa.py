@@ -50,13 +50,15 @@ _SIGS = {
     "vsa_stage": [ctypes.POINTER(Config)] + [_P] * 5,
     "vsa_coarse_select": [ctypes.POINTER(Config)] + [_P] * 12,
     "vsa_fine_fwd": [ctypes.POINTER(Config)] + [_P] * 13,
-    "vsa_combine_bwd": [ctypes.POINTER(Config)] + [_P] * 12,
+    "vsa_combine_bwd": [ctypes.POINTER(Config)] + [_P] * 13,
     "vsa_coarse_bwd": [ctypes.POINTER(Config)] + [_P] * 11,
-    "vsa_fine_bwd": [ctypes.POINTER(Config)] + [_P] * 16,
+    "vsa_fine_bwd": [ctypes.POINTER(Config)] + [_P] * 17,
     "vsa_forward": [ctypes.POINTER(Config)] + [_P] * 7 + [ctypes.c_int, _P, _P],
     "vsa_backward": [ctypes.POINTER(Config)] + [_P] * 11,
     "vsa_probe_wait_timeout": [_P, ctypes.c_uint32, _P],
-    "vsa_probe_exp2": [_P, _P, ctypes.c_int32, ctypes.c_int32, _P],
+    "vsa_stage_fp8": [ctypes.POINTER(Config)] + [_P] * 12,
+    "vsa_fine_fwd_fp8": [ctypes.POINTER(Config)] + [_P] * 13,
+    "vsa_forward_fp8": [ctypes.POINTER(Config)] + [_P] * 9,
 }
 _RESTYPES = {"vsa_status_string": ctypes.c_char_p, "vsa_saved_bytes": ctypes.c_size_t,
              "vsa_workspace_bytes": ctypes.c_size_t}
@@ -208,17 +210,57 @@ def fine_fwd(cfg: Config, q16, k16, v16, idx, cnt, gc, gf, oc, ws, want_saved=Tr
     return o, of, lse
 
 
+def stage_fp8(cfg: Config, q, k, v, ws, want_pooled=False):
+    """bf16 q, k, v (cfg.layout order) -> e4m3 copies (q8, k8, v8t as uint8),
+    scales [B, heads, 3] and, optionally, the cube means (qc, kc, vc)."""
+    B, Hd, N, D = q.shape
+    u8 = dict(dtype=torch.uint8, device=q.device)
+    q8, k8 = torch.empty(B, Hd, N, D, **u8), torch.empty(B, Hd, N, D, **u8)
+    v8t = torch.empty(B, Hd, N // 64, D, 64, **u8)
+    scales = torch.empty(B, Hd, 3, dtype=torch.float32, device=q.device)
+    pooled = [torch.empty(B, Hd, N // 64, D, dtype=torch.float32, device=q.device)
+              if want_pooled else None for _ in range(3)]
+    check(lib().vsa_stage_fp8(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8),
+                              _ptr(v8t), _ptr(scales), *(_ptr(x) for x in pooled), _ptr(ws),
+                              _stream()), "vsa_stage_fp8")
+    return (q8, k8, v8t, scales) + (tuple(pooled) if want_pooled else ())
+
+
+def fine_fwd_fp8(cfg: Config, q8, k8, v8t, scales, idx, cnt, gc, gf, oc, ws, want_lse=True):
+    """e4m3 copies from stage_fp8 -> (o, lse_f)."""
+    B, Hd, N, D = q8.shape
+    o = torch.empty_like(gc)
+    lse = torch.empty(B, Hd, N, dtype=torch.float32, device=q8.device) if want_lse else None
+    check(lib().vsa_fine_fwd_fp8(ctypes.byref(cfg), _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(scales),
+                                 _ptr(idx), _ptr(cnt), _ptr(gc), _ptr(gf), _ptr(oc), _ptr(o),
+                                 _ptr(lse), _ptr(ws), _stream()), "vsa_fine_fwd_fp8")
+    return o, lse
+
+
+def forward_fp8(cfg: Config, q, k, v, gc, gf, bufs: Buffers, out=None):
+    """Whole inference forward with the e4m3 fine stage; bufs.saved receives
+    the copies and coarse results (not usable by backward())."""
+    o = torch.empty_like(q) if out is None else out
+    check(lib().vsa_forward_fp8(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gc), _ptr(gf),
+                                _ptr(o), _ptr(bufs.saved), _ptr(bufs.ws), _stream()),
+          "vsa_forward_fp8")
+    return o
+
+
 def combine_bwd(cfg: Config, d_o, gc, gf, o_f, oc, ws):
+    """-> (dgc, dgf, dof16, doc, delta, gscale); dof16 and delta carry gscale."""
     B, Hd, N, D = d_o.shape
     f = dict(dtype=torch.float32, device=d_o.device)
     dgc, dgf = torch.empty(B, Hd, N, D, **f), torch.empty(B, Hd, N, D, **f)
     dof = torch.empty(B, Hd, N, D, dtype=torch.float16, device=d_o.device)
     doc = torch.empty(B, Hd, N // 64, D, **f)
     delta = torch.empty(B, Hd, N, **f)
+    gscale = torch.empty(B, Hd, **f)
     check(lib().vsa_combine_bwd(ctypes.byref(cfg), _ptr(d_o), _ptr(gc), _ptr(gf), _ptr(o_f),
                                 _ptr(oc), _ptr(dgc), _ptr(dgf), _ptr(dof), _ptr(doc),
-                                _ptr(delta), _ptr(ws), _stream()), "vsa_combine_bwd")
-    return dgc, dgf, dof, doc, delta
+                                _ptr(delta), _ptr(gscale), _ptr(ws), _stream()),
+          "vsa_combine_bwd")
+    return dgc, dgf, dof, doc, delta, gscale
 
 
 def coarse_bwd(cfg: Config, qc, kc, vc, oc, lse_c, doc, ws):
@@ -229,15 +271,20 @@ def coarse_bwd(cfg: Config, qc, kc, vc, oc, lse_c, doc, ws):
     return dqc, dkc, dvc
 
 
-def fine_bwd(cfg: Config, q16, k16, v16, idx, cnt, lse_f, dof16, delta, dqc, dkc, dvc, ws):
-    """Staged fp16 operands -> fp32 dq, dk, dv in cfg.layout order."""
+def fine_bwd(cfg: Config, q16, k16, v16, idx, cnt, lse_f, dof16, delta, dqc, dkc, dvc, ws,
+             gscale=None):
+    """Staged fp16 operands -> fp32 dq, dk, dv in cfg.layout order.
+
+    gscale: the per-slice factor dof16 and delta carry (combine_bwd's output),
+    or None for 1."""
     q, k, v, dof = q16, k16, v16, dof16
     B, Hd, N, D = q.shape
     f = dict(dtype=torch.float32, device=q.device)
     dq, dk, dv = (torch.empty(B, Hd, N, D, **f) for _ in range(3))
     check(lib().vsa_fine_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(cnt),
-                             _ptr(lse_f), _ptr(dof), _ptr(delta), _ptr(dqc), _ptr(dkc),
-                             _ptr(dvc), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _stream()),
+                             _ptr(lse_f), _ptr(dof), _ptr(delta), _ptr(gscale), _ptr(dqc),
+                             _ptr(dkc), _ptr(dvc), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                             _stream()),
           "vsa_fine_bwd")
     return dq, dk, dv
 
@@ -266,36 +313,82 @@ def backward(cfg: Config, gc, gf, d_o, bufs: Buffers, grads=None):
 
 class _VSAFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, gc, gf, cfg_tuple):
+    def forward(ctx, q, k, v, gc, gf, cfg_tuple, check_status):
         cfg = Config(*cfg_tuple)
         need = any(t.requires_grad for t in (q, k, v, gc, gf))
         bufs = Buffers(cfg, q.device, with_backward=need)
         o = forward(cfg, q, k, v, gc, gf, bufs, with_backward=need)
-        ctx.cfg, ctx.bufs = cfg, bufs
-        ctx.dtypes = (q.dtype, k.dtype, v.dtype)
+        if check_status:
+            check(bufs.device_status(), "video_sparse_attention (forward, device status)")
+        ctx.cfg, ctx.bufs, ctx.check_status = cfg, bufs, check_status
         ctx.save_for_backward(gc, gf)
         return o
 
     @staticmethod
     def backward(ctx, d_o):
         gc, gf = ctx.saved_tensors
+        if d_o.shape != gc.shape:
+            raise ValueError(f"gradient of O has shape {tuple(d_o.shape)}, "
+                             f"expected {tuple(gc.shape)}")
         d_o = d_o.to(torch.bfloat16).contiguous()
         dq, dk, dv, dgc, dgf = backward(ctx.cfg, gc, gf, d_o, ctx.bufs)
-        tq, tk, tv = ctx.dtypes
-        return (dq.to(tq), dk.to(tk), dv.to(tv), dgc.to(gc.dtype), dgf.to(gf.dtype), None)
+        if ctx.check_status:
+            check(ctx.bufs.device_status(), "video_sparse_attention (backward, device status)")
+        bf = torch.bfloat16
+        return dq.to(bf), dk.to(bf), dv.to(bf), dgc.to(bf), dgf.to(bf), None, None
+
+
+def _check_inputs(q, k, v, gc, gf, video_shape, layout):
+    """Refuses, before any launch, what the kernels would misread."""
+    named = (("q", q), ("k", k), ("v", v), ("gc", gc), ("gf", gf))
+    for name, t in named:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [batch, heads, tokens, head_dim], "
+                             f"got shape {tuple(t.shape)}")
+    for name, t in named[1:]:
+        if t.shape != q.shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
+    if len(video_shape) != 3:
+        raise ValueError(f"video_shape must be (T, H, W), got {video_shape!r}")
+    T, H, W = (int(x) for x in video_shape)
+    if q.shape[2] != T * H * W:
+        raise ValueError(f"tokens per slice {q.shape[2]} != T*H*W = {T * H * W}")
+    if layout not in ("raster", "cube"):
+        raise ValueError(f"layout must be 'raster' or 'cube', got {layout!r}")
+    for name, t in named:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
 
 
 def video_sparse_attention(q, k, v, gc, gf, video_shape, *, topk=32, select="topk", mass=0.9,
-                           kmin=8, kmax=64, scale=0.0, layout="raster"):
+                           kmin=8, kmax=64, scale=0.0, layout="raster", check_status=True):
     """VSA attention of [B, heads, T*H*W, D] bf16 CUDA tensors (raster or cube order).
 
     gc, gf: per-token, per-channel gates (same shape and dtype).  Returns O, bf16.
-    Gradients flow to q, k, v, gc, gf (the cube selection is held fixed).
+    Gradients flow to q, k, v, gc, gf as bf16 (the cube selection is held fixed).
+    All five inputs must be contiguous bf16 CUDA tensors of one shape with
+    T*H*W tokens; anything else raises before a kernel is launched.  With
+    check_status (the default) the forward and the backward each read the
+    library's device status word after their kernels (one stream
+    synchronisation each) and raise VSAError if a kernel recorded a failure
+    (a bounded wait that expired, a bad index list, a Q/K/V value outside the
+    fp16 range or a non-finite gradient).
     """
-    T, H, W = video_shape
+    _check_inputs(q, k, v, gc, gf, video_shape, layout)
+    T, H, W = (int(x) for x in video_shape)
     B, Hd, N, D = q.shape
+    if select not in ("topk", "mass"):
+        raise ValueError(f"select must be 'topk' or 'mass', got {select!r}")
     cfg = make_config(B, Hd, T, H, W, D, topk=topk, select=select, mass=mass, kmin=kmin,
                       kmax=kmax, scale=scale, layout=layout)
     check(lib().vsa_validate(ctypes.byref(cfg)), "video_sparse_attention")
     cfg_tuple = tuple(getattr(cfg, n) for n, _ in Config._fields_)
-    return _VSAFunction.apply(q, k, v, gc, gf, cfg_tuple)
+    return _VSAFunction.apply(q, k, v, gc, gf, cfg_tuple, bool(check_status))
