@@ -145,6 +145,132 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   return v > -INFINITY ? k : 0u;
 }
 
+// Per-warp shared scratch of the mass rule (kmax <= 64): candidate columns in
+// ascending order, their keys, their descending ranks, the columns by rank.
+struct MassScratch {
+  int ci[64];
+  uint32_t ck[64];
+  int rk[64];
+  int cr[64];
+};
+
+// Selection of one row held in registers by one warp (lane l holds columns
+// l, l + 32, ...; v[i] = -inf past Nc): the top-K by bisection on the order
+// key, or the mass rule over the kmax candidates; writes the ascending list
+// (-1 padded to the capacity) and the count.  Lrow: the row's logits (global
+// or shared memory) for the mass rule's probabilities, m and inv its softmax
+// maximum and 1 / sum.
+template <int kPer>
+__device__ __forceinline__ void select_row(const Geom& g, const SelectArgs& sa,
+                                           const float (&v)[kPer], float m, float inv,
+                                           const float* Lrow, int* out, int* cnt_out,
+                                           MassScratch& ms) {
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int Nc = g.Nc;
+  const int lane = threadIdx.x % 32;
+  uint32_t key[kPer];
+  uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;
+  int nvalid = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    key[i] = 32 * i + lane < Nc ? order_key(v[i]) : 0u;
+    if (key[i]) {
+      kmin_l = min(kmin_l, key[i]);
+      kmax_l = max(kmax_l, key[i]);
+      ++nvalid;
+    }
+  }
+  nvalid = __reduce_add_sync(kFull, nvalid);
+  const int kmax_eff = min(sa.kmax, Nc);
+  const int kmin_eff = min(sa.kmin, kmax_eff);
+  const int want = sa.mode == 0 ? sa.topk : kmax_eff;
+  const int K = min(want, nvalid);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t t = 1u;  // the K-th largest key (or a key with exactly K keys at or above it)
+  if (K > 0) {
+    uint32_t lo = __reduce_min_sync(kFull, kmin_l), hi = __reduce_max_sync(kFull, kmax_l);
+    // When every lane holds a valid key and K <= 32, the smallest of the 32
+    // lane maxima has at least 32 keys at or above it: a tighter start.
+    if (K <= 32 && nvalid >= 32 && __all_sync(kFull, kmax_l != 0u))
+      lo = max(lo, __reduce_min_sync(kFull, kmax_l));
+    // invariant: count(key >= lo) >= K; the answer lies in [lo, hi]
+    while (lo < hi) {
+      const uint32_t mid = lo + (hi - lo + 1) / 2;
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) c += key[i] >= mid;
+      c = __reduce_add_sync(kFull, c);
+      if (c == K) { lo = mid; break; }
+      if (c > K) lo = mid;
+      else hi = mid - 1;
+    }
+    t = lo;
+  }
+  int n_gt = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) n_gt += key[i] > t;
+  n_gt = __reduce_add_sync(kFull, n_gt);
+  const int need_eq = K - n_gt;  // keys equal to t to take, lowest columns first
+  // the K chosen columns in ascending order
+  int* dst = sa.mode == 0 ? out : ms.ci;
+  int nout = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const bool eq = K > 0 && key[i] == t;
+    const uint32_t beq = __ballot_sync(kFull, eq);
+    const bool sel = K > 0 && (key[i] > t || (eq && eq_seen + __popc(beq & lt_mask) < need_eq));
+    eq_seen += __popc(beq);
+    const uint32_t bsel = __ballot_sync(kFull, sel);
+    if (sel) {
+      const int pos = nout + __popc(bsel & lt_mask);
+      dst[pos] = 32 * i + lane;
+      if (sa.mode != 0) ms.ck[pos] = key[i];
+    }
+    nout += __popc(bsel);
+  }
+  int n = K;
+  if (sa.mode != 0) {
+    // mass rule over the K (<= 64) candidates: descending rank (larger key
+    // first, the lower column on ties), then the probabilities summed in
+    // rank order by one lane, as the argmax loop summed them
+    __syncwarp();
+    for (int c = lane; c < K; c += 32) {
+      const uint32_t kc = ms.ck[c];
+      int r = 0;
+      for (int d = 0; d < K; ++d) {
+        const uint32_t kd = ms.ck[d];
+        r += kd > kc || (kd == kc && d < c);
+      }
+      ms.rk[c] = r;
+      ms.cr[r] = ms.ci[c];
+    }
+    __syncwarp();
+    int nn = 0;
+    if (lane == 0) {
+      float cum = 0.f;
+      int n_raw = 0;
+      for (int r = 0; r < K; ++r) {
+        cum += expf(Lrow[ms.cr[r]] - m) * inv;
+        nn = r + 1;
+        if (n_raw == 0 && cum >= sa.mass) n_raw = nn;
+        if (nn >= kmin_eff && n_raw > 0) break;
+      }
+    }
+    n = __shfl_sync(kFull, nn, 0);
+    // the n highest-ranked candidates, in ascending column order
+    int nsel = 0;
+    for (int c0 = 0; c0 < K; c0 += 32) {
+      const int c = c0 + lane;
+      const bool sel = c < K && ms.rk[c] < n;
+      const uint32_t bsel = __ballot_sync(kFull, sel);
+      if (sel) out[nsel + __popc(bsel & lt_mask)] = ms.ci[c];
+      nsel += __popc(bsel);
+    }
+  }
+  for (int e2 = n + lane; e2 < g.cap; e2 += 32) out[e2] = -1;
+  if (lane == 0) *cnt_out = n;
+}
+
 template <int kPer>
 __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectArgs sa,
                                                                  const float* __restrict__ logits,
@@ -153,12 +279,7 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectA
                                                                  int* __restrict__ idx,
                                                                  int* __restrict__ cnt) {
   constexpr int kWarps = kSelThreads / 32;
-  // mass rule (kmax <= 64): candidate columns in ascending order, their keys,
-  // their descending ranks, and the columns by rank
-  __shared__ int s_ci[kWarps][64];
-  __shared__ uint32_t s_ck[kWarps][64];
-  __shared__ int s_rk[kWarps][64];
-  __shared__ int s_cr[kWarps][64];
+  __shared__ MassScratch s_mass[kWarps];
   constexpr uint32_t kFull = 0xffffffffu;
   const int Nc = g.Nc, bh = blockIdx.y;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -194,110 +315,8 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectA
     }
   }
   if (lane == 0) lse_c[static_cast<size_t>(bh) * Nc + row] = m + logf(z);
-
-  // ---- selection
-  uint32_t key[kPer];
-  uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;
-  int nvalid = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    key[i] = 32 * i + lane < Nc ? order_key(v[i]) : 0u;
-    if (key[i]) {
-      kmin_l = min(kmin_l, key[i]);
-      kmax_l = max(kmax_l, key[i]);
-      ++nvalid;
-    }
-  }
-  nvalid = __reduce_add_sync(kFull, nvalid);
-  const int kmax_eff = min(sa.kmax, Nc);
-  const int kmin_eff = min(sa.kmin, kmax_eff);
-  const int want = sa.mode == 0 ? sa.topk : kmax_eff;
-  const int K = min(want, nvalid);
-  int* out = idx + (static_cast<size_t>(bh) * Nc + row) * g.cap;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t t = 1u;  // the K-th largest key (or a key with exactly K keys at or above it)
-  if (K > 0) {
-    uint32_t lo = __reduce_min_sync(kFull, kmin_l), hi = __reduce_max_sync(kFull, kmax_l);
-    // When every lane holds a valid key and K <= 32, the smallest of the 32
-    // lane maxima has at least 32 keys at or above it: a tighter start.
-    if (K <= 32 && nvalid >= 32 && __all_sync(kFull, kmax_l != 0u))
-      lo = max(lo, __reduce_min_sync(kFull, kmax_l));
-    // invariant: count(key >= lo) >= K; the answer lies in [lo, hi]
-    while (lo < hi) {
-      const uint32_t mid = lo + (hi - lo + 1) / 2;
-      int c = 0;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) c += key[i] >= mid;
-      c = __reduce_add_sync(kFull, c);
-      if (c == K) { lo = mid; break; }
-      if (c > K) lo = mid;
-      else hi = mid - 1;
-    }
-    t = lo;
-  }
-  int n_gt = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) n_gt += key[i] > t;
-  n_gt = __reduce_add_sync(kFull, n_gt);
-  const int need_eq = K - n_gt;  // keys equal to t to take, lowest columns first
-  // the K chosen columns in ascending order
-  int* dst = sa.mode == 0 ? out : s_ci[warp];
-  int nout = 0, eq_seen = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const bool eq = K > 0 && key[i] == t;
-    const uint32_t beq = __ballot_sync(kFull, eq);
-    const bool sel = K > 0 && (key[i] > t || (eq && eq_seen + __popc(beq & lt_mask) < need_eq));
-    eq_seen += __popc(beq);
-    const uint32_t bsel = __ballot_sync(kFull, sel);
-    if (sel) {
-      const int pos = nout + __popc(bsel & lt_mask);
-      dst[pos] = 32 * i + lane;
-      if (sa.mode != 0) s_ck[warp][pos] = key[i];
-    }
-    nout += __popc(bsel);
-  }
-  int n = K;
-  if (sa.mode != 0) {
-    // mass rule over the K (<= 64) candidates: descending rank (larger key
-    // first, the lower column on ties), then the probabilities summed in
-    // rank order by one lane, as the argmax loop summed them
-    __syncwarp();
-    for (int c = lane; c < K; c += 32) {
-      const uint32_t kc = s_ck[warp][c];
-      int r = 0;
-      for (int d = 0; d < K; ++d) {
-        const uint32_t kd = s_ck[warp][d];
-        r += kd > kc || (kd == kc && d < c);
-      }
-      s_rk[warp][c] = r;
-      s_cr[warp][r] = s_ci[warp][c];
-    }
-    __syncwarp();
-    int nn = 0;
-    if (lane == 0) {
-      float cum = 0.f;
-      int n_raw = 0;
-      for (int r = 0; r < K; ++r) {
-        cum += expf(Lg[s_cr[warp][r]] - m) * inv;
-        nn = r + 1;
-        if (n_raw == 0 && cum >= sa.mass) n_raw = nn;
-        if (nn >= kmin_eff && n_raw > 0) break;
-      }
-    }
-    n = __shfl_sync(kFull, nn, 0);
-    // the n highest-ranked candidates, in ascending column order
-    int nsel = 0;
-    for (int c0 = 0; c0 < K; c0 += 32) {
-      const int c = c0 + lane;
-      const bool sel = c < K && s_rk[warp][c] < n;
-      const uint32_t bsel = __ballot_sync(kFull, sel);
-      if (sel) out[nsel + __popc(bsel & lt_mask)] = s_ci[warp][c];
-      nsel += __popc(bsel);
-    }
-  }
-  for (int e2 = n + lane; e2 < g.cap; e2 += 32) out[e2] = -1;
-  if (lane == 0) cnt[static_cast<size_t>(bh) * Nc + row] = n;
+  const size_t lrow = static_cast<size_t>(bh) * Nc + row;
+  select_row<kPer>(g, sa, v, m, inv, Lg, idx + lrow * g.cap, cnt + lrow, s_mass[warp]);
 }
 
 // delta_c[row] = sum_d dO_c[row, d] * O_c[row, d], one warp per row.

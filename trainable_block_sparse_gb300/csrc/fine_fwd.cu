@@ -65,13 +65,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;              // S (128 columns)
 constexpr uint32_t kColP = 128;            // P buffers (fp16 pairs) at columns 128 and 192
 constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// e4m3 variant: P is kept within [0, 2^(kRescaleThresholdF8 + kP8Shift)] =
-// [0, 256] (e4m3 ends at 448) by a tighter threshold and an exponent shift, so
-// that probabilities down to 2^-12 of the row maximum stay normal e4m3 numbers
-// (3 significand bits); the row sum carries the same factor 2^kP8Shift.
-constexpr float kRescaleThresholdF8 = 2.0f;
-constexpr float kP8Shift = 6.0f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units (P stays within [0, 256])
 template <int D, bool kF8 = false>
 struct FwdSmem {
   // 128-byte chunks of a row: 64 fp16 columns, or 128 e4m3 columns
@@ -436,7 +430,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const float m_new = fmaxf(m_run, fmaxf(mx, sb.red[step & 1][hc ^ 1][row]) * cs);
         bool resc = false;
         float alpha = 1.f;
-        if (m_new > m_run + (kF8 ? kRescaleThresholdF8 : kRescaleThreshold)) {
+        if (m_new > m_run + kRescaleThreshold) {
           if (m_run != -INFINITY) {
             alpha = ex2_approx(m_run - m_new);
             l_run *= alpha;
@@ -448,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           float ls[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-          const float mb = m_run - kP8Shift;
+          const float mb = m_run;
           // x[i] <- e4m3x4(p[4i .. 4i+3]); x[4i .. 4i+3] are read before x[i] is
           // written
           unroll_for<16>([&](auto I) {
@@ -644,8 +638,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           }
         }
       }
-      if (live && P.lse_f)
-        P.lse_f[frow] = (m_fin + __log2f(l_sum) - (kF8 ? kP8Shift : 0.f)) * 0.6931471805599453f;
+      if (live && P.lse_f) P.lse_f[frow] = (m_fin + __log2f(l_sum)) * 0.6931471805599453f;
       tc_fence_before();
       warp_arrive(&sb.o_free[obuf]);
       ++it;
