@@ -183,6 +183,19 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
                           const void* gf, const float* oc, void* o, void* o_f, float* lse_f,
                           void* ws, void* stream);
 
+/* Fine stage and combine reading the caller's bf16 tensors in place (no staged
+ * copies; App. B: tiling "can be moved outside individual attention layers" --
+ * here it happens inside the tile copies): in raster layout each 64-token tile
+ * is one 5-D copy of a (4,4,4) cube of the [B*heads, T, H, W, D] view, landing
+ * in the in-cube token order.  Operands, P and the MMAs are bf16 (fp32
+ * accumulation), for inference: no O_f.
+ * q, k, v, gc, gf: bf16 [B,heads,N,D] in cfg->layout order; idx, cnt, oc, o,
+ * lse_f (may be NULL), ws: as for vsa_fine_fwd.  Q, K, V need no fp16 range. */
+vsa_status_t vsa_fine_fwd_bf16(const vsa_config_t* cfg, const void* q, const void* k,
+                               const void* v, const int32_t* idx, const int32_t* cnt,
+                               const void* gc, const void* gf, const float* oc, void* o,
+                               float* lse_f, void* ws, void* stream);
+
 /* vsa_fine_fwd for callers that cannot provide a scratch buffer.  The pages
  * have no counterpart: this is a calling convention, not a step of the method.
  * A caller with no device allocator of its own (for example a plugin run by a
@@ -312,8 +325,13 @@ vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* 
  * "Pseudocode of VSA"; paper notes 关键设计 1-3): tile, coarse stage, fine
  * stage + combine, untile.
  * q, k, v, gc, gf: bf16 in cfg->layout order; o: bf16 output, same order.
- * saved: vsa_saved_bytes() bytes, filled for vsa_backward (O_f is written only
- * when with_backward != 0). */
+ * saved: vsa_saved_bytes() bytes.
+ * with_backward != 0: stages fp16 copies of Q, K, V with the cube means, and
+ *   fills everything vsa_backward needs (O_f included).
+ * with_backward == 0 (inference): computes only the cube means, the coarse
+ *   results and lse_f into `saved`, and runs the fine stage on q, k, v in place
+ *   (vsa_fine_fwd_bf16): no staged copies, no fp16 range limit; the result
+ *   cannot feed vsa_backward. */
 vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
                          const void* gc, const void* gf, void* o, void* saved,
                          int with_backward, void* ws, void* stream);

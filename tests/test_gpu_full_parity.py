@@ -6,7 +6,9 @@ benchmark times (one vsa_forward + vsa_backward over the whole layer).
   layer (mass >= 0.9, 8..64 cubes): every slice, every cube, forward and
   backward;
 * Wan-1.3B layer (20x32x48, 12 heads, D = 128, forward only): every slice,
-  every cube;
+  every cube (the inference path: the fine stage reads the bf16 inputs in
+  place through 5-D cube copies); the same path on every slice and cube of the
+  pretraining and dynamic layers;
 * 720p layer (20x44x80, 40 heads, D = 128): every cube of one slice, forward
   and backward, index lists of every slice.
 
@@ -122,6 +124,19 @@ def test_wan13b_every_slice_every_cube(oracle_pool):
     slices = all_slices(wl)
     got = gpu_layer(inp, slices, backward=False)
     ref = oracle_pool.layer(inp, slices, "wan13b", backward=False)
+    for key in slices:
+        compare_slice(wl, key, got[key], ref[key], backward=False)
+
+
+@pytest.mark.parametrize("name", ["pretrain", "dynamic"])
+def test_inference_forward_every_slice_every_cube(name, oracle_pool):
+    """vsa_forward without the backward: the fine stage reads the raster bf16
+    inputs in place (5-D cube copies) with bf16 operands."""
+    inp = gapped(name)
+    wl = inp.wl
+    slices = all_slices(wl)
+    got = gpu_layer(inp, slices, backward=False)
+    ref = oracle_pool.layer_memo(("full", name), inp, slices, name, backward=True)
     for key in slices:
         compare_slice(wl, key, got[key], ref[key], backward=False)
 

@@ -205,6 +205,33 @@ bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tiled_2d_bf16(void* map, const void* base, uint64_t rows, uint64_t cols) {
+  if (!encoder()) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_raster_cubes_bf16(void* map, const void* base, const Geom& g) {
+  if (!encoder()) return false;
+  const uint64_t D = static_cast<uint64_t>(g.D);
+  const cuuint64_t dims[5] = {D, static_cast<cuuint64_t>(g.W), static_cast<cuuint64_t>(g.H),
+                              static_cast<cuuint64_t>(g.T), static_cast<cuuint64_t>(g.BH)};
+  const cuuint64_t strides[4] = {D * 2, D * 2 * g.W, D * 2 * g.W * g.H,
+                                 D * 2 * g.W * g.H * g.T};
+  const cuuint32_t box[5] = {64, 4, 4, 4, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tiled_2d_u8(void* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows, uint32_t box_cols, int swizzle_bytes) {
   if (!encoder()) return false;
@@ -359,6 +386,28 @@ vsa_status_t vsa_fine_fwd(const vsa_config_t* cfg, const void* q16, const void* 
                                      static_cast<f16*>(o_f), lse_f, w, s));
 }
 
+vsa_status_t vsa_fine_fwd_bf16(const vsa_config_t* cfg, const void* q, const void* k,
+                               const void* v, const int32_t* idx, const int32_t* cnt,
+                               const void* gc, const void* gf, const float* oc, void* o,
+                               float* lse_f, void* ws, void* stream) {
+  Geom g;
+  vsa_status_t st = make_geom(cfg, &g);
+  if (st != VSA_OK) return st;
+  if (!all_set(q, k, v, idx, cnt, gc, gf, oc, o, ws)) return VSA_ERR_INVALID_ARG;
+  if (!all_aligned(q, k, v, idx, cnt, gc, gf, oc, o, ws) || !aligned16(lse_f))
+    return VSA_ERR_ALIGNMENT;
+  Workspace w;
+  carve_ws(g, 0, ws, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  return cuda_status(launch_fine_fwd_bf16(g, static_cast<const bf16*>(q),
+                                          static_cast<const bf16*>(k),
+                                          static_cast<const bf16*>(v),
+                                          static_cast<const bf16*>(gc),
+                                          static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
+                                          lse_f, w, s));
+}
+
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
                              const void* gf, const void* o_f, const float* oc, float* dgc,
                              float* dgf, void* dof16, float* doc, float* delta, float* gscale,
@@ -434,6 +483,28 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   Workspace w;
   carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!with_backward) {
+    // inference: cube means only, then the fine stage reads q, k, v in place
+    float* qc = reinterpret_cast<float*>(sv + L.qc);
+    float* kc = reinterpret_cast<float*>(sv + L.kc);
+    float* vc = reinterpret_cast<float*>(sv + L.vc);
+    float* oc = reinterpret_cast<float*>(sv + L.oc);
+    int* idx = reinterpret_cast<int*>(sv + L.idx);
+    int* cnt = reinterpret_cast<int*>(sv + L.cnt);
+    if (launch_stage(g, static_cast<const bf16*>(q), g.raster, nullptr, qc, w.status, s) ||
+        launch_stage(g, static_cast<const bf16*>(k), g.raster, nullptr, kc, w.status, s) ||
+        launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s))
+      return VSA_ERR_CUDA;
+    if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
+                             kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt, w,
+                             s) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+    return cuda_status(launch_fine_fwd_bf16(
+        g, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+        static_cast<const bf16*>(gc), static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
+        reinterpret_cast<float*>(sv + L.lse_f), w, s));
+  }
   f16* q16 = reinterpret_cast<f16*>(sv + L.q16);
   f16* k16 = reinterpret_cast<f16*>(sv + L.k16);
   f16* v16 = reinterpret_cast<f16*>(sv + L.v16);

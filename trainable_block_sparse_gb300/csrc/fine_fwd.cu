@@ -40,6 +40,13 @@
 // the CTA unwinds, waits for its own in-flight copies and MMAs, frees TMEM and
 // exits.
 //
+// bf16 variant (inference: no O_f): Q, K, V are read in place from the caller's
+// bf16 tensors, P is written as bf16 and the UMMAs are kind::f16 with bf16
+// operands.  In raster layout every 64-token tile is fetched as one 5-D TMA box
+// (64 channels x 4 x 4 x 4 tokens of a [BH, T, H, W, D] view), which lands in
+// shared memory in the in-cube token order: the permute happens inside the
+// copy and no staged copy is made.
+//
 // e4m3 variant (kF8, head_dim 128, inference: no O_f): Q, K and V arrive as the
 // e4m3 copies of stage_fp8.cu (per-slice power-of-two factors), P is written
 // to TMEM as e4m3 and every UMMA is kind::f8f6f4 (K = 32 per MMA) with fp32
@@ -66,6 +73,9 @@ constexpr uint32_t kColS = 0;              // S (128 columns)
 constexpr uint32_t kColP = 128;            // P buffers (fp16 pairs) at columns 128 and 192
 constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (P stays within [0, 256])
+// Operand kinds of the kernel: the fp16 staged copies, the e4m3 copies, or the
+// caller's bf16 tensors read in place.
+enum : int { kOpF16 = 0, kOpE4M3 = 1, kOpBF16 = 2 };
 template <int D, bool kF8 = false>
 struct FwdSmem {
   // 128-byte chunks of a row: 64 fp16 columns, or 128 e4m3 columns
@@ -152,11 +162,12 @@ __device__ __forceinline__ bool pair_sync_or(int quarter, bool fail) {
   return r != 0;
 }
 
-template <int D, bool kF8>
+template <int D, int kOp>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tof,
                     FwdParams P) {
+  constexpr bool kF8 = kOp == kOpE4M3, kBF = kOp == kOpBF16;
   static_assert(!kF8 || D == 128, "the e4m3 variant is for head_dim 128");
   using L = FwdSmem<D, kF8>;
   constexpr int kSK = L::kStagesK, kSV = L::kStagesV;
@@ -221,6 +232,18 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const uint32_t kS = is_k ? kSK : kSV;
       tma_prefetch_desc(tmap);
       if (is_k) tma_prefetch_desc(&tq);
+      // one 64-row tile (64 columns of it) of a cube of slice bh: a 2-D box of a
+      // cube-order tensor, or (bf16 variant, raster layout) a 5-D box of the
+      // caller's raster tensor
+      auto load_tile = [&](uint8_t* dst, const CUtensorMap* m, int c, int bh, int cube,
+                           uint64_t* bar) {
+        if (kBF && g.raster) {
+          const int cw_ = cube % g.cw, rest = cube / g.cw;
+          tma_load_5d(dst, m, c * 64, 4 * cw_, 4 * (rest % g.ch), 4 * (rest / g.ch), bh, bar);
+        } else {
+          tma_load_2d(dst, m, c * 64, bh * g.N + cube * kTile, bar);
+        }
+      };
       uint32_t step = 0;
       int it = 0;  // items with work seen by this CTA
       for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag);
@@ -231,12 +254,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         if (is_k) {
           if (it > 0 && !wait1(&sb.q_empty, (it - 1) & 1, abort_flag, P.status)) break;
           mbar_arrive_expect_tx(&sb.q_full, L::kQBytes);
-          const int row_a = pi.bh * g.N + pi.a * kTile;
-          const int row_b = pi.bh * g.N + (pi.b >= 0 ? pi.b : pi.a) * kTile;
+          const int cube_b = pi.b >= 0 ? pi.b : pi.a;
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_2d(sQ + c * L::kChunkBytes, &tq, c * 64, row_a, &sb.q_full);
-            tma_load_2d(sQ + c * L::kChunkBytes + 8192, &tq, c * 64, row_b, &sb.q_full);
+            load_tile(sQ + c * L::kChunkBytes, &tq, c, pi.bh, pi.a, &sb.q_full);
+            load_tile(sQ + c * L::kChunkBytes + 8192, &tq, c, pi.bh, cube_b, &sb.q_full);
           }
         }
         ++it;
@@ -253,7 +275,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             break;
           }
           uint8_t* dst = ring + slot * L::kKVBytes;
-          const int r0 = pi.bh * g.N + t0 * kTile, r1 = pi.bh * g.N + t1 * kTile;
           mbar_arrive_expect_tx(&full[slot], (two ? 2 : 1) * L::kTileBytes);
           if (kF8 && !is_k) {
             // transposed V: rows (cube, channel) of 64 key bytes, one box per cube
@@ -263,8 +284,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           } else {
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
-              tma_load_2d(dst + c * L::kChunkBytes, tmap, c * 64, r0, &full[slot]);
-              if (two) tma_load_2d(dst + c * L::kChunkBytes + 8192, tmap, c * 64, r1, &full[slot]);
+              load_tile(dst + c * L::kChunkBytes, tmap, c, pi.bh, t0, &full[slot]);
+              if (two) load_tile(dst + c * L::kChunkBytes + 8192, tmap, c, pi.bh, t1, &full[slot]);
             }
           }
           ++step;
@@ -278,9 +299,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
   } else if (warp == kWarpMma) {
     // ===================================================== UMMA issuer
-    const uint32_t idesc_s128 = kF8 ? idesc_e4m3(128, 128) : idesc_f16(128, 128, 0, 0);
-    const uint32_t idesc_s64 = kF8 ? idesc_e4m3(128, 64) : idesc_f16(128, 64, 0, 0);
-    const uint32_t idesc_pv = kF8 ? idesc_e4m3(128, D) : idesc_f16(128, D, 0, 1);
+    const uint32_t idesc_s128 = kF8 ? idesc_e4m3(128, 128)
+                                : kBF ? idesc_bf16(128, 128, 0, 0) : idesc_f16(128, 128, 0, 0);
+    const uint32_t idesc_s64 = kF8 ? idesc_e4m3(128, 64)
+                               : kBF ? idesc_bf16(128, 64, 0, 0) : idesc_f16(128, 64, 0, 0);
+    const uint32_t idesc_pv = kF8 ? idesc_e4m3(128, D)
+                              : kBF ? idesc_bf16(128, D, 0, 1) : idesc_f16(128, D, 0, 1);
     const uint64_t qd0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t vd0 = sdesc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
@@ -471,7 +495,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             const float p0 = ex2_approx(t0);
             const float p1 = ex2_approx(t1);
             add2_acc(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], p0, p1);
-            x[i] = pack_f16x2(p0, p1);
+            x[i] = kBF ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
           });
           l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         } else {
@@ -533,7 +557,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const int half = row >> 6;                   // 0: first cube, 1: second cube
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = threadIdx.x == kWarpEpi * 32;
-    const bool stage_of = !kF8 && P.o_f != nullptr;
+    const bool stage_of = kOp == kOpF16 && P.o_f != nullptr;
     int it = 0;
     // No abort test in the loop condition: the four warps meet at named
     // barriers and must walk the same items (see epi_sync_or).
@@ -664,12 +688,37 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
   memset(&mof, 0, sizeof(mof));
   if (p.o_f && !encode_tiled_2d(&mof, p.o_f, rows, D, 64, 64)) return cudaErrorInvalidValue;
   const int smem = FwdSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, false>,
+  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, kOpF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
-  fine_fwd_kernel<D, false><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
+  fine_fwd_kernel<D, kOpF16><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
+  return cudaGetLastError();
+}
+
+// bf16 variant: the caller's q, k, v in place (5-D cube boxes of the raster
+// layout, or 2-D 64-row boxes of the cube layout).
+template <int D>
+cudaError_t run_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                         const __nv_bfloat16* v, FwdParams p, cudaStream_t s) {
+  alignas(64) CUtensorMap mq, mk, mv, mof;
+  const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
+  const bool ok = g.raster ? (encode_raster_cubes_bf16(&mq, q, g) &&
+                              encode_raster_cubes_bf16(&mk, k, g) &&
+                              encode_raster_cubes_bf16(&mv, v, g))
+                           : (encode_tiled_2d_bf16(&mq, q, rows, D) &&
+                              encode_tiled_2d_bf16(&mk, k, rows, D) &&
+                              encode_tiled_2d_bf16(&mv, v, rows, D));
+  if (!ok) return cudaErrorInvalidValue;
+  memset(&mof, 0, sizeof(mof));
+  const int smem = FwdSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, kOpBF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = persistent_grid(p.n_items);
+  if (grid <= 0) return cudaSuccess;
+  fine_fwd_kernel<D, kOpBF16><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
 
@@ -688,12 +737,12 @@ cudaError_t run_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t* k8, con
     return cudaErrorInvalidValue;
   memset(&mof, 0, sizeof(mof));
   const int smem = FwdSmem<D, true>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, true>,
+  cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel<D, kOpE4M3>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
-  fine_fwd_kernel<D, true><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
+  fine_fwd_kernel<D, kOpE4M3><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
 
@@ -707,6 +756,16 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
               gc, gf, oc, o, o_f, lse_f, ws.status, nullptr};
   if (g.D == 64) return run_fwd<64>(g, q, k, v, p, s);
   return run_fwd<128>(g, q, k, v, p, s);
+}
+
+cudaError_t launch_fine_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                 const __nv_bfloat16* v, const __nv_bfloat16* gc,
+                                 const __nv_bfloat16* gf, const float* oc, __nv_bfloat16* o,
+                                 float* lse_f, const Workspace& ws, cudaStream_t s) {
+  FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
+              gc, gf, oc, o, nullptr, lse_f, ws.status, nullptr};
+  if (g.D == 64) return run_fwd_bf16<64>(g, q, k, v, p, s);
+  return run_fwd_bf16<128>(g, q, k, v, p, s);
 }
 
 cudaError_t launch_fine_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t* k8,

@@ -213,9 +213,22 @@ bool encode_tiled_3d_f32(void* map, const float* base, uint64_t batch, uint64_t 
 // Driver entry point for tensor-map encoding, resolved once (api.cu).
 bool encode_tiled_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols);
+// bf16 tensors read in place by the fine forward, 128-byte swizzle, boxes of
+// 64 columns: 2-D over [rows, cols] (64-row boxes: a cube in cube order), or
+// 5-D over a raster [BH, T, H, W, D] (boxes of 64 x 4 x 4 x 4 x 1: one (4,4,4)
+// cube, its rows landing in the in-cube order (t%4)*16 + (h%4)*4 + w%4).
+bool encode_tiled_2d_bf16(void* map, const void* base, uint64_t rows, uint64_t cols);
+bool encode_raster_cubes_bf16(void* map, const void* base, const Geom& g);
 // The same over bytes (e4m3 data), with a 64- or 128-byte swizzle.
 bool encode_tiled_2d_u8(void* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
+
+// The fine forward + combine reading the caller's bf16 q, k, v (cfg layout)
+// in place: no staged copies (fine_fwd.cu; inference: no O_f).
+cudaError_t launch_fine_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                 const __nv_bfloat16* v, const __nv_bfloat16* gc,
+                                 const __nv_bfloat16* gf, const float* oc, __nv_bfloat16* o,
+                                 float* lse_f, const Workspace& ws, cudaStream_t s);
 
 // ------------------------------------------------ e4m3 variant of the fine forward
 // Staging (stage_fp8.cu, head_dim 128): bf16 q, k, v (caller layout) -> e4m3

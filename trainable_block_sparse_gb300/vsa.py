@@ -56,6 +56,7 @@ _SIGS = {
     "vsa_forward": [ctypes.POINTER(Config)] + [_P] * 7 + [ctypes.c_int, _P, _P],
     "vsa_backward": [ctypes.POINTER(Config)] + [_P] * 11,
     "vsa_probe_wait_timeout": [_P, ctypes.c_uint32, _P],
+    "vsa_fine_fwd_bf16": [ctypes.POINTER(Config)] + [_P] * 12,
     "vsa_stage_fp8": [ctypes.POINTER(Config)] + [_P] * 12,
     "vsa_fine_fwd_fp8": [ctypes.POINTER(Config)] + [_P] * 13,
     "vsa_forward_fp8": [ctypes.POINTER(Config)] + [_P] * 9,
@@ -245,6 +246,17 @@ def forward_fp8(cfg: Config, q, k, v, gc, gf, bufs: Buffers, out=None):
                                 _ptr(o), _ptr(bufs.saved), _ptr(bufs.ws), _stream()),
           "vsa_forward_fp8")
     return o
+
+
+def fine_fwd_bf16(cfg: Config, q, k, v, idx, cnt, gc, gf, oc, ws, want_lse=True):
+    """bf16 q, k, v read in place (cfg.layout order) -> (o, lse_f)."""
+    B, Hd, N, D = q.shape
+    o = torch.empty_like(gc)
+    lse = torch.empty(B, Hd, N, dtype=torch.float32, device=q.device) if want_lse else None
+    check(lib().vsa_fine_fwd_bf16(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx),
+                                  _ptr(cnt), _ptr(gc), _ptr(gf), _ptr(oc), _ptr(o), _ptr(lse),
+                                  _ptr(ws), _stream()), "vsa_fine_fwd_bf16")
+    return o, lse
 
 
 def combine_bwd(cfg: Config, d_o, gc, gf, o_f, oc, ws):
