@@ -328,10 +328,12 @@ vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* 
  * saved: vsa_saved_bytes() bytes.
  * with_backward != 0: stages fp16 copies of Q, K, V with the cube means, and
  *   fills everything vsa_backward needs (O_f included).
- * with_backward == 0 (inference): computes only the cube means, the coarse
- *   results and lse_f into `saved`, and runs the fine stage on q, k, v in place
- *   (vsa_fine_fwd_bf16): no staged copies, no fp16 range limit; the result
- *   cannot feed vsa_backward. */
+ * with_backward == 0 (inference): no O_f.  In cube layout, or at head_dim 64,
+ *   computes only the cube means, the coarse results and lse_f into `saved` and
+ *   runs the fine stage on q, k, v in place (vsa_fine_fwd_bf16): no staged
+ *   copies, no fp16 range limit.  Raster tensors of head_dim 128 are staged as
+ *   for training (a raster cube of 128 channels reads slower in place than its
+ *   staged copy).  Either way the result cannot feed vsa_backward. */
 vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, const void* v,
                          const void* gc, const void* gf, void* o, void* saved,
                          int with_backward, void* ws, void* stream);

@@ -136,6 +136,45 @@ def test_inference_forward_edge_shapes(thw, D, topk):
     check_forward(_custom(*thw, D, topk, seed=7 + topk), full=True, with_backward=False)
 
 
+@pytest.mark.parametrize("thw,topk", [((8, 4, 12), 5), ((4, 4, 4), 1)])
+def test_inference_forward_cube_layout_head_dim_128(thw, topk):
+    check_forward(_custom(*thw, 128, topk, seed=9 + topk), layout="cube", full=True,
+                  with_backward=False)
+
+
+@pytest.mark.parametrize("layout", ["raster", "cube"])
+def test_fine_stage_in_place_head_dim_128(layout):
+    """vsa_fine_fwd_bf16 itself at head_dim 128 (5-D cube copies in raster
+    layout), fed the oracle's lists and O_c, on every cube of the tiny-shaped
+    layer at D = 128."""
+    inp = _custom(8, 8, 8, 128, 3, seed=17)
+    wl = inp.wl
+    cfg = vsa.config_for(wl, layout)
+    heads = {(0, h): O.head_of(inp, 0, h) for h in range(wl.heads)}
+    idx = np.stack([[heads[(0, h)].idx for h in range(wl.heads)]])
+    cnt = np.stack([[heads[(0, h)].cnt for h in range(wl.heads)]])
+    oc = np.stack([[heads[(0, h)].coarse["out"] for h in range(wl.heads)]])
+    t = cuda_inputs(inp)
+    if layout == "cube":
+        for n in ("q", "k", "v", "gc", "gf"):
+            t[n] = vsa.permute(cfg, t[n])
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    vsa.lib().vsa_reset_device_status(vsa._ptr(ws), vsa._stream())
+    o, lse = vsa.fine_fwd_bf16(cfg, t["q"], t["k"], t["v"], torch.from_numpy(idx).int().cuda(),
+                               torch.from_numpy(cnt).int().cuda(), t["gc"], t["gf"],
+                               torch.from_numpy(oc).float().cuda(), ws)
+    torch.cuda.synchronize()
+    assert vsa.lib().vsa_check_device_status(vsa._ptr(ws), vsa._stream()) == vsa.OK
+    if layout == "cube":
+        o = vsa.permute(cfg, o, inverse=True)
+    o_np, lse_np = to_np(o), to_np(lse)
+    for h, hd in ((h, heads[(0, h)]) for h in range(wl.heads)):
+        for c in range(wl.cubes):
+            _, _, lse_r = hd.rows(c)
+            assert_close("O", o_np[0, h, synth.raster_rows_of_cube(wl, c)], hd.output_tiled(c))
+            assert_close("lse_f", lse_np[0, h, c * 64:(c + 1) * 64], lse_r)
+
+
 def test_inference_forward_accepts_values_beyond_fp16():
     """No staged fp16 copy on the inference path: a Q value above 65504 is
     computed, not refused (the oracle agrees)."""

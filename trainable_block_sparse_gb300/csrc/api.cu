@@ -483,7 +483,12 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   Workspace w;
   carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!with_backward) {
+  // Inference reads q, k, v in place unless they are raster tensors of head_dim
+  // 128: there a cube's 64-channel box is 16 runs spread over a 4 x 4 patch of
+  // image rows, and the fine stage measured 23-31% slower than on the staged
+  // cube-order copy (which is one contiguous block per cube); at head_dim 64
+  // (whole 512-byte runs) and in cube layout it runs at the staged speed.
+  if (!with_backward && (!g.raster || g.D == 64)) {
     // inference: cube means only, then the fine stage reads q, k, v in place
     float* qc = reinterpret_cast<float*>(sv + L.qc);
     float* kc = reinterpret_cast<float*>(sv + L.kc);
