@@ -127,16 +127,6 @@ __device__ __forceinline__ void store_pooled_half(int c0, const float* pooled, s
   }
 }
 
-// Per-warpgroup register split (every warp of a warpgroup executes the same one).
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Key-major epilogue: the 32 accumulator rows of this warp's lane quarter
 // (at TMEM address tq), times `mul` plus the pooled gradient, to global
 // memory; row 16h + 8j + t/4 of the quarter goes to output row orow[2h + j].

@@ -145,6 +145,18 @@ __device__ __forceinline__ void issue_ts2_f8(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Per-warpgroup register split (every warp of a warpgroup executes the same
+// one; the increases and decreases of a block must add up within the
+// registers it was launched with).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
