@@ -50,6 +50,10 @@ LAUNCHES_BWD = 17  # gradient-scale max, combine bwd, coarse bwd (row dot, tf32 
                    # pairs), fine bwd x2
 SIDE_WORKLOADS = ("wan13b", "pretrain", "dynamic")  # timed per stage beside the headline layer
 SIDE_REPS = 20
+# Gradients leave the layer in the inputs' dtype, bf16 (what autograd hands back
+# for bf16 tensors): the kernels accumulate in fp32 and round once at the store.
+# The fp32-gradient step is timed beside it (fwdbwd_ms_fp32_grads).
+GRAD_DTYPE = "bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -197,12 +201,13 @@ def gpu_arm(args, rank, world):
     torch.cuda.set_device(dev)
     wl = workload(args)
     inp = synth.Inputs(wl, with_grad=True)
-    cfg = vsa.config_for(wl)
+    cfg = vsa.config_for(wl, grad_dtype=GRAD_DTYPE)
     t = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "gc", "gf", "do")}
     bufs = vsa.Buffers(cfg, dev, with_backward=True)
     B, H, N, D = wl.batch, wl.heads, wl.tokens, wl.head_dim
     o = torch.empty_like(t["q"])
-    grads = tuple(torch.empty(B, H, N, D, dtype=torch.float32, device=dev) for _ in range(5))
+    grads = tuple(torch.empty(B, H, N, D, dtype=vsa.grad_torch_dtype(cfg), device=dev)
+                  for _ in range(5))
     stream = torch.cuda.current_stream()
 
     def fwd():
@@ -211,6 +216,13 @@ def gpu_arm(args, rank, world):
     def step():
         fwd()
         vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs, grads)
+
+    cfg32 = vsa.config_for(wl, grad_dtype="fp32")
+    grads32 = tuple(torch.empty(B, H, N, D, dtype=torch.float32, device=dev) for _ in range(5))
+
+    def step_fp32_grads():
+        fwd()
+        vsa.backward(cfg32, t["gc"], t["gf"], t["do"], bufs, grads32)
 
     bufs_inf = vsa.Buffers(cfg, dev, with_backward=False)
     o_inf = torch.empty_like(t["q"])
@@ -234,6 +246,7 @@ def gpu_arm(args, rank, world):
         ms_step = timed(step, args.steps, args.warmup, stream)
         ms_fwd = timed(fwd, max(3, args.steps // 2), 1, stream)
         ms_fwd_inf = timed(fwd_inference, max(3, args.steps // 2), 1, stream)
+        ms_step32 = timed(step_fp32_grads, max(3, args.steps // 2), 1, stream)
         status = bufs.device_status() or bufs_inf.device_status()
         if status != vsa.OK:
             raise RuntimeError(f"device status {status} after the timed steps")
@@ -245,11 +258,11 @@ def gpu_arm(args, rank, world):
     e2e = end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args)
     side = {}
     if rank == 0 and not args.no_side:
-        del bufs, grads, o, t
+        del bufs, grads, grads32, o, t
         torch.cuda.empty_cache()
         side = {name: side_workload(vsa, name, dev) for name in SIDE_WORKLOADS}
     return {"wl": wl, "work": work, "pairs": pairs, "ms_step": ms_max, "ms_fwd": ms_fwd,
-            "ms_fwd_inf": ms_fwd_inf,
+            "ms_fwd_inf": ms_fwd_inf, "ms_step_fp32_grads": ms_step32,
             "clocks": clk.summary(), "stages": stages, "stages_warm": stages_warm,
             "e2e": e2e, "inp": inp,
             "balance": balance, "side": side, "fp8": fp8}
@@ -334,12 +347,13 @@ def side_workload(vsa, name, dev):
     and the fine kernels' work distribution."""
     wl = synth.WORKLOADS[name]
     inp = synth.Inputs(wl, with_grad=True)
-    cfg = vsa.config_for(wl)
+    cfg = vsa.config_for(wl, grad_dtype=GRAD_DTYPE)
     t = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "gc", "gf", "do")}
     bufs = vsa.Buffers(cfg, dev, with_backward=True)
     B, H, N, D = wl.batch, wl.heads, wl.tokens, wl.head_dim
     o = torch.empty_like(t["q"])
-    grads = tuple(torch.empty(B, H, N, D, dtype=torch.float32, device=dev) for _ in range(5))
+    grads = tuple(torch.empty(B, H, N, D, dtype=vsa.grad_torch_dtype(cfg), device=dev)
+                  for _ in range(5))
     stream = torch.cuda.current_stream()
 
     def fwd():
@@ -401,7 +415,8 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=SIDE_REPS, flush=No
     v["lse_f"] = bufs.view("lse_f", torch.float32, (B, H, N))
     f32 = dict(dtype=torch.float32, device=dev)
     o = torch.empty_like(t["q"])
-    dgc, dgf, dq, dk, dv = (torch.empty(B, H, N, D, **f32) for _ in range(5))
+    dgc, dgf, dq, dk, dv = (torch.empty(B, H, N, D, dtype=vsa.grad_torch_dtype(cfg), device=dev)
+                            for _ in range(5))
     dof = torch.empty(B, H, N, D, dtype=torch.float16, device=dev)
     doc, dqc, dkc, dvc = (torch.empty(B, H, nc, D, **f32) for _ in range(4))
     delta = torch.empty(B, H, N, **f32)
@@ -446,8 +461,9 @@ def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
     del bufs  # the pipeline owns per-unit buffers
     host_in = {n: getattr(inp, n).pin_memory() for n in IN_NAMES}
     B, H, N, D = wl.batch, wl.heads, wl.tokens, wl.head_dim
-    host_out = {n: torch.empty(B, H, N, D, dtype=torch.bfloat16 if n == "o" else torch.float32,
-                               pin_memory=True) for n in OUT_NAMES}
+    host_out = {n: torch.empty(B, H, N, D, pin_memory=True,
+                               dtype=torch.bfloat16 if n == "o" else vsa.grad_torch_dtype(cfg))
+                for n in OUT_NAMES}
     pipe = HostPipeline(cfg, dev, heads_per_unit=5)
     reps = max(2, args.steps // 3)
     for _ in range(2):  # warm-up: allocates the per-unit buffers
@@ -518,12 +534,12 @@ def cpu_baseline(inp, step_flops):
 TF32_OVER_BF16 = 1.1 / 2.25
 
 
-def stage_roofline(name, ms, work, wl, peaks, src):
+def stage_roofline(name, ms, work, wl, peaks, src, grad_bytes):
     """Algorithmic work of one stage call against its bound.
 
     HBM stages count the bytes the method must move once (the combine
-    backward: dO, G_c, G_f in bf16 and O_f in fp16 read; dG_c, dG_f in fp32,
-    dO_f in fp16 and delta written; its slice-maximum pre-pass re-reads dO
+    backward: dO, G_c, G_f in bf16 and O_f in fp16 read; dG_c, dG_f
+    (grad_bytes per element), dO_f in fp16 and delta written; its slice-maximum pre-pass re-reads dO
     and G_f, which is not counted).  Tensor stages count executed FLOPs: the
     fine stages on fp16 UMMAs (the bf16 rate), the coarse stages as fp32
     contractions run on tf32 UMMAs (the tf32 rate: the measured bf16 peak
@@ -533,7 +549,7 @@ def stage_roofline(name, ms, work, wl, peaks, src):
     rows = wl.bh * wl.tokens * 4
     table = {
         "stage_pool": ("hbm", 3 * (S + S) + 3 * small),          # read bf16, write fp16 + means
-        "combine_bwd": ("hbm", 3 * S + S + 4 * S + S + rows + small),
+        "combine_bwd": ("hbm", 3 * S + S + grad_bytes * S + S + rows + small),
         "fine_fwd": ("tensor", work["fine_fwd"]),
         "fine_fwd_bf16": ("tensor", work["fine_fwd"]),
         "fine_bwd": ("tensor", work["fine_bwd"]),
@@ -573,7 +589,8 @@ def config_json(wl):
     return {"workload": wl.name, "T": wl.T, "H": wl.H, "W": wl.W, "tokens": wl.tokens,
             "cubes": wl.cubes, "batch": wl.batch, "heads": wl.heads, "head_dim": wl.head_dim,
             "topk": wl.topk, "step": "forward+backward of one layer",
-            "io": "bf16 in/out, fp32 gradients", "mma": "fp16 x fp16 -> fp32 (tcgen05)",
+            "io": f"bf16 in/out, {GRAD_DTYPE} gradients (fp32 accumulation, one rounding "
+                  f"at the store)", "mma": "fp16 x fp16 -> fp32 (tcgen05)",
             "l2": (f"inputs larger than L2 ({flops.tensor_bytes(wl) / 1e6:.0f} MB per bf16 "
                    f"tensor vs 129 MB): no flush" if flops.tensor_bytes(wl) > 129 * 2 ** 20
                    else "inputs fit in L2: back-to-back steps are warm-L2 (profiling runs)"),
@@ -718,7 +735,8 @@ def main():
     # nothing); the L2-flushed medians are reported beside it
     warm = r["stages_warm"]
     top = max((k for k in warm if k != "fine_fwd_bf16"), key=warm.get)
-    roof = stage_roofline(top, warm[top], work, wl, peaks, src)
+    roof = stage_roofline(top, warm[top], work, wl, peaks, src,
+                          grad_bytes=2 if GRAD_DTYPE == "bf16" else 4)
     roof["traffic"] = traffic_for(top)
     roof["timing"] = (f"median of {SIDE_REPS} calls of the stage's C-ABI entry point, "
                       f"back to back (as in the step); includes its list building")
@@ -733,6 +751,7 @@ def main():
         "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config_json(wl),
         "fwd_ms_per_layer": r["ms_fwd"], "fwdbwd_ms_per_layer": r["ms_step"],
         "fwd_inference_ms_per_layer": r["ms_fwd_inf"],
+        "fwdbwd_ms_fp32_grads": r["ms_step_fp32_grads"],
         "fwd_inference_note": "vsa_forward without the backward: cube means, coarse stage, "
                               "and the fine stage reading the bf16 inputs in place (5-D "
                               "cube copies, no staged fp16 copies)",

@@ -27,8 +27,11 @@
  *    in raster order (token (t,h,w) at row (t*H + h)*W + w) or in cube order
  *    (row c*64 + o, c = ((t/4)*(H/4) + h/4)*(W/4) + w/4,
  *    o = (t%4)*16 + (h%4)*4 + w%4), as cfg->layout says.  Q, K, V, G_c, G_f,
- *    dO and O are bf16; the pooled/coarse tensors, log-sum-exps and all
- *    gradients are fp32; the saved fine output O_f is fp16 (cube order).
+ *    dO and O are bf16; the pooled/coarse tensors and log-sum-exps are fp32;
+ *    the saved fine output O_f is fp16 (cube order).  The gradients dQ, dK,
+ *    dV, dG_c, dG_f are fp32 or bf16 as cfg->grad_dtype says (bf16: the fp32
+ *    result rounded to nearest even once, at the store; everything before it
+ *    is the same).  The pooled and coarse gradients stay fp32.
  *  - The tensor-core operands Q, K, V are staged as fp16 copies in cube order
  *    ("staged" below): bf16 -> fp16 is exact for magnitudes in
  *    [6.1e-5, 65504], and the fp16 significand keeps the rounding of the
@@ -79,6 +82,7 @@ typedef enum {
 
 enum { VSA_SELECT_TOPK = 0, VSA_SELECT_MASS = 1 };
 enum { VSA_LAYOUT_RASTER = 0, VSA_LAYOUT_CUBE = 1 };
+enum { VSA_GRAD_FP32 = 0, VSA_GRAD_BF16 = 1 };
 
 /* Largest supported sizes. */
 #define VSA_MAX_CUBES 8192   /* cubes per (batch, head) */
@@ -95,6 +99,7 @@ typedef struct {
   int32_t kmin, kmax;       /* MASS: count clamp, 1 <= kmin <= kmax <= VSA_MAX_LIST */
   float scale;              /* softmax scale for both stages; <= 0 means 1/sqrt(D) */
   int32_t layout;           /* VSA_LAYOUT_RASTER or VSA_LAYOUT_CUBE (caller tensors) */
+  int32_t grad_dtype;       /* VSA_GRAD_FP32 or VSA_GRAD_BF16: dq, dk, dv, dgc, dgf */
 } vsa_config_t;
 
 /* Byte offsets of the pieces of the `saved` buffer written by vsa_forward.
@@ -280,7 +285,8 @@ vsa_status_t vsa_forward_fp8(const vsa_config_t* cfg, const void* q, const void*
  * coarse output is repeated across its cube; the abstract: the whole operator
  * is one differentiable kernel trained end to end).
  * d_o, gc, gf: bf16 in cfg->layout order; o_f: fp16 CUBE order; oc: fp32.
- * dgc, dgf   : fp32 outputs in cfg->layout order (dO (.) repeat(O_c), dO (.) O_f).
+ * dgc, dgf   : outputs in cfg->layout order (dO (.) repeat(O_c), dO (.) O_f),
+ *              of cfg->grad_dtype.
  * dof16      : fp16 CUBE order output, dO (.) G_f times gscale[slice].
  * doc        : fp32 [B,heads,Nc,D] output, per-cube sum of dO (.) G_c.
  * delta      : fp32 [B,heads,N] CUBE order output, rowsum(dof16 (.) o_f)
@@ -290,8 +296,8 @@ vsa_status_t vsa_forward_fp8(const vsa_config_t* cfg, const void* q, const void*
  * ws receives the range flag (non-finite dO (.) G_f) and holds the slice
  * maxima. */
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
-                             const void* gf, const void* o_f, const float* oc, float* dgc,
-                             float* dgf, void* dof16, float* doc, float* delta, float* gscale,
+                             const void* gf, const void* o_f, const float* oc, void* dgc,
+                             void* dgf, void* dof16, float* doc, float* delta, float* gscale,
                              void* ws, void* stream);
 
 /* Backward of the coarse attention on the pooled sequence, selection held
@@ -310,7 +316,7 @@ vsa_status_t vsa_coarse_bwd(const vsa_config_t* cfg, const float* qc, const floa
  * mean is 1/64): writes
  *   dq = dQ_fine / gscale + repeat(dqc)/64, dk = dK_fine / gscale + repeat(dkc)/64,
  *   dv = dV_fine / gscale + repeat(dvc)/64
- * as fp32 in cfg->layout order.  q16, k16, v16, dof16: staged fp16 CUBE
+ * in cfg->layout order, of cfg->grad_dtype.  q16, k16, v16, dof16: staged fp16 CUBE
  * order; lse_f, delta: fp32 CUBE order; gscale: fp32 [B,heads], the factor
  * dof16 and delta carry (vsa_combine_bwd's output), or NULL for 1;
  * dqc/dkc/dvc may be NULL (no pooled contribution). */
@@ -318,7 +324,7 @@ vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* 
                           const void* v16, const int32_t* idx, const int32_t* cnt,
                           const float* lse_f, const void* dof16, const float* delta,
                           const float* gscale, const float* dqc, const float* dkc,
-                          const float* dvc, float* dq, float* dk, float* dv, void* ws,
+                          const float* dvc, void* dq, void* dk, void* dv, void* ws,
                           void* stream);
 
 /* Whole forward (§2 Methods, the coarse stage feeding the fine stage; App. B
@@ -343,11 +349,11 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
  * fixed): combine backward, coarse backward, fine backward + unpooling, from
  * the upstream gradient d_o (bf16, cfg->layout order).
  * gc, gf: the forward's gates; saved: as filled by vsa_forward with
- * with_backward = 1 (it holds the staged Q, K, V).  Outputs fp32 in
- * cfg->layout order. */
+ * with_backward = 1 (it holds the staged Q, K, V).  Outputs dq, dk, dv, dgc,
+ * dgf of cfg->grad_dtype in cfg->layout order. */
 vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* gf,
-                          const void* saved, const void* d_o, float* dq, float* dk, float* dv,
-                          float* dgc, float* dgf, void* ws, void* stream);
+                          const void* saved, const void* d_o, void* dq, void* dk, void* dv,
+                          void* dgc, void* dgf, void* ws, void* stream);
 
 #ifdef __cplusplus
 }

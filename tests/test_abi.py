@@ -51,10 +51,19 @@ def _cfg(**kw):
     ({"select": "mass", "kmax": 300}, vsa.ERR_INVALID_ARG),
     ({"select": "mass"}, vsa.OK),
     ({"T": 4096, "H": 64, "W": 64}, vsa.ERR_SHAPE),  # too many cubes
+    ({"grad_dtype": "bf16"}, vsa.OK),
 ])
 def test_validate(lib, kw, status):
     cfg = _cfg(**kw)
     assert lib.vsa_validate(ctypes.byref(cfg)) == status
+
+
+def test_unknown_gradient_dtype_is_rejected(lib):
+    cfg = _cfg()
+    cfg.grad_dtype = 2
+    assert lib.vsa_validate(ctypes.byref(cfg)) == vsa.ERR_INVALID_ARG
+    with pytest.raises(ValueError, match="grad_dtype"):
+        _cfg(grad_dtype="fp16")
 
 
 def test_null_config_and_pointers(lib):

@@ -30,6 +30,8 @@ vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
   if (cfg->head_dim != 64 && cfg->head_dim != 128) return VSA_ERR_UNSUPPORTED;
   if (cfg->layout != VSA_LAYOUT_RASTER && cfg->layout != VSA_LAYOUT_CUBE)
     return VSA_ERR_INVALID_ARG;
+  if (cfg->grad_dtype != VSA_GRAD_FP32 && cfg->grad_dtype != VSA_GRAD_BF16)
+    return VSA_ERR_INVALID_ARG;
   const long long bh = static_cast<long long>(cfg->batch) * cfg->heads;
   const long long n = static_cast<long long>(cfg->T) * cfg->H * cfg->W;
   const long long nc = n / kTile;
@@ -65,6 +67,7 @@ vsa_status_t make_geom(const vsa_config_t* cfg, Geom* g) {
   g->cw = cfg->W / 4;
   g->cap = cap;
   g->raster = cfg->layout == VSA_LAYOUT_RASTER;
+  g->grad_bf16 = cfg->grad_dtype == VSA_GRAD_BF16;
   g->scale = scale;
   return VSA_OK;
 }
@@ -409,8 +412,8 @@ vsa_status_t vsa_fine_fwd_bf16(const vsa_config_t* cfg, const void* q, const voi
 }
 
 vsa_status_t vsa_combine_bwd(const vsa_config_t* cfg, const void* d_o, const void* gc,
-                             const void* gf, const void* o_f, const float* oc, float* dgc,
-                             float* dgf, void* dof16, float* doc, float* delta, float* gscale,
+                             const void* gf, const void* o_f, const float* oc, void* dgc,
+                             void* dgf, void* dof16, float* doc, float* delta, float* gscale,
                              void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
@@ -447,7 +450,7 @@ vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* 
                           const void* v16, const int32_t* idx, const int32_t* cnt,
                           const float* lse_f, const void* dof16, const float* delta,
                           const float* gscale, const float* dqc, const float* dkc,
-                          const float* dvc, float* dq, float* dk, float* dv, void* ws,
+                          const float* dvc, void* dq, void* dk, void* dv, void* ws,
                           void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
@@ -535,8 +538,8 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
 }
 
 vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* gf,
-                          const void* saved, const void* d_o, float* dq, float* dk, float* dv,
-                          float* dgc, float* dgf, void* ws, void* stream) {
+                          const void* saved, const void* d_o, void* dq, void* dk, void* dv,
+                          void* dgc, void* dgf, void* ws, void* stream) {
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;

@@ -6,7 +6,9 @@
 //   dO_c[cube] = sum over the cube of dO (.) G_c
 //   delta[row] = sum_d dO_f (.) O_f    (the softmax-backward row term of the fine stage)
 // HBM-bound: one CTA per (batch, head, cube) reads dO, G_c, G_f (bf16, caller
-// layout) and O_f (fp16, cube order) once and writes each output once.
+// layout) and O_f (fp16, cube order) once and writes each output once (dG_c
+// and dG_f as fp32, or rounded once to bf16 when the caller asks for bf16
+// gradients).
 //
 // dO_f is the fp16 tensor-core operand of the fine backward.  Upstream
 // gradients of bf16 training are often far below fp16's normal range (1e-5 to
@@ -70,11 +72,20 @@ __device__ __forceinline__ float grad_scale_of(uint32_t bits) {
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
+// Eight fp32 values rounded to bf16 (nearest even), packed in order.
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
+  uint4 u;
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) p[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+  return u;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     Geom g, const uint4* __restrict__ d_o, const uint4* __restrict__ gc,
     const uint4* __restrict__ gf, const uint4* __restrict__ o_f, const float* __restrict__ oc,
-    float* __restrict__ dgc, float* __restrict__ dgf, uint4* __restrict__ dof,
+    void* __restrict__ dgc, void* __restrict__ dgf, uint4* __restrict__ dof,
     float* __restrict__ doc, float* __restrict__ delta, const uint32_t* __restrict__ amax,
     float* __restrict__ gscale, uint32_t* status) {
   constexpr int VPR = D / 8;              // 8-element vectors per row
@@ -129,12 +140,18 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
       const float2 r = __half22float2(pof[e]);  // delta uses the rounded dO_f the MMAs see
       dsum = fmaf(r.x, ofv[2 * e], fmaf(r.y, ofv[2 * e + 1], dsum));
     }
-    float4* dc = reinterpret_cast<float4*>(dgc + crow * D + col * 8);
-    float4* df = reinterpret_cast<float4*>(dgf + crow * D + col * 8);
-    dc[0] = make_float4(vdgc[0], vdgc[1], vdgc[2], vdgc[3]);
-    dc[1] = make_float4(vdgc[4], vdgc[5], vdgc[6], vdgc[7]);
-    df[0] = make_float4(vdgf[0], vdgf[1], vdgf[2], vdgf[3]);
-    df[1] = make_float4(vdgf[4], vdgf[5], vdgf[6], vdgf[7]);
+    const size_t o8 = crow * D + col * 8;  // first of this thread's 8 elements
+    if (g.grad_bf16) {
+      reinterpret_cast<uint4*>(dgc)[o8 / 8] = pack_bf16x8(vdgc);
+      reinterpret_cast<uint4*>(dgf)[o8 / 8] = pack_bf16x8(vdgf);
+    } else {
+      float4* dc = reinterpret_cast<float4*>(static_cast<float*>(dgc) + o8);
+      float4* df = reinterpret_cast<float4*>(static_cast<float*>(dgf) + o8);
+      dc[0] = make_float4(vdgc[0], vdgc[1], vdgc[2], vdgc[3]);
+      dc[1] = make_float4(vdgc[4], vdgc[5], vdgc[6], vdgc[7]);
+      df[0] = make_float4(vdgf[0], vdgf[1], vdgf[2], vdgf[3]);
+      df[1] = make_float4(vdgf[4], vdgf[5], vdgf[6], vdgf[7]);
+    }
     dof[frow * VPR + col] = udof;
     // row sum over the VPR consecutive lanes that share this row
 #pragma unroll
@@ -157,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
 
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
-                               const __half* o_f, const float* oc, float* dgc, float* dgf,
+                               const __half* o_f, const float* oc, void* dgc, void* dgf,
                                __half* dof, float* doc, float* delta, uint32_t* amax,
                                float* gscale, uint32_t* status, cudaStream_t s) {
   auto u4 = [](const void* p) { return reinterpret_cast<const uint4*>(p); };

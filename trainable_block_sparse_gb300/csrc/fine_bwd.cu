@@ -35,6 +35,7 @@
 // of a step, Y2 earlier, so Y1 gets the deeper ring).
 // Epilogue: four epilogue warps (one per TMEM lane quarter) read the
 // accumulators out of TMEM, scale them, add the pooled gradient and write them
+// (fp32, or rounded once to bf16 if the caller asks for bf16 gradients)
 // straight to global memory, four threads per row and 32 whole bytes of a row
 // per group, while the softmax warps go on with the next item (a 128 KB drain
 // takes several thousand cycles at the SM's store rate, so it must not hold
@@ -100,8 +101,9 @@ struct BwdParams {
   const float* gscale;  // [BH] factor dO_f and delta carry (null: 1)
   const float* pooled1; // dQ_c (dQ pass) or dV_c (key-major pass), may be null
   const float* pooled2; // dK_c (key-major pass), may be null
-  float* out1;          // dQ (dQ pass) or dV (key-major pass), caller layout fp32
-  float* out2;          // dK (key-major pass)
+  void* out1;           // dQ (dQ pass) or dV (key-major pass), caller layout, fp32 or
+                        // bf16 (g.grad_bf16)
+  void* out2;           // dK (key-major pass)
   uint32_t* status;
 };
 
@@ -110,21 +112,39 @@ __device__ __forceinline__ void warp_arrive_bwd(uint64_t* bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// Two gradient values to out[i], out[i + 1] (8 bytes fp32, or 4 bytes bf16
+// rounded to nearest even).
+template <class T>
+__device__ __forceinline__ void store2(T* out, size_t i, float x, float y) {
+  if constexpr (std::is_same<T, float>::value)
+    *reinterpret_cast<float2*>(out + i) = make_float2(x, y);
+  else
+    *reinterpret_cast<__nv_bfloat162*>(out + i) = __floats2bfloat162_rn(x, y);
+}
+
 // Columns [c0, c0 + D/2) of one output row of an item with no selected
 // blocks: only pooled[cube]/64 reaches it (plain stores; a rare path).
-template <int D>
+template <int D, class T>
 __device__ __forceinline__ void store_pooled_half(int c0, const float* pooled, size_t pooled_row,
-                                                  float* out, size_t out_row) {
+                                                  T* out, size_t out_row) {
 #pragma unroll 1
-  for (int cc = c0; cc < c0 + D / 2; cc += 4) {
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cc = c0; cc < c0 + D / 2; cc += 2) {
+    float2 r = make_float2(0.f, 0.f);
     if (pooled) {
-      const float4 a = *reinterpret_cast<const float4*>(pooled + pooled_row * D + cc);
-      r = make_float4(a.x * (1.f / kTile), a.y * (1.f / kTile), a.z * (1.f / kTile),
-                      a.w * (1.f / kTile));
+      const float2 a = *reinterpret_cast<const float2*>(pooled + pooled_row * D + cc);
+      r = make_float2(a.x * (1.f / kTile), a.y * (1.f / kTile));
     }
-    *reinterpret_cast<float4*>(out + out_row * D + cc) = r;
+    store2(out, out_row * D + cc, r.x, r.y);
   }
+}
+
+template <int D>
+__device__ __forceinline__ void store_pooled_half(bool bf16, int c0, const float* pooled,
+                                                  size_t pooled_row, void* out, size_t out_row) {
+  if (bf16)
+    store_pooled_half<D>(c0, pooled, pooled_row, static_cast<__nv_bfloat16*>(out), out_row);
+  else
+    store_pooled_half<D>(c0, pooled, pooled_row, static_cast<float*>(out), out_row);
 }
 
 // Key-major epilogue: the 32 accumulator rows of this warp's lane quarter
@@ -132,9 +152,9 @@ __device__ __forceinline__ void store_pooled_half(int c0, const float* pooled, s
 // memory; row 16h + 8j + t/4 of the quarter goes to output row orow[2h + j].
 // pp[k] holds, in lane l, pooled columns 2(l + 32k) and 2(l + 32k) + 1,
 // already divided by 64.
-template <int D>
+template <int D, class T>
 __device__ __forceinline__ void drain_acc(uint32_t tq, float mul, const float2 (&pp)[D / 64],
-                                          float* out, const size_t (&orow)[4]) {
+                                          T* out, const size_t (&orow)[4]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
@@ -153,11 +173,21 @@ __device__ __forceinline__ void drain_acc(uint32_t tq, float mul, const float2 (
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-          *reinterpret_cast<float2*>(out + orow[2 * h + j] * D + col) =
-              make_float2(fmaf(__uint_as_float(v[h][4 * i + 2 * j]), mul, px),
-                          fmaf(__uint_as_float(v[h][4 * i + 2 * j + 1]), mul, py));
+          store2(out, orow[2 * h + j] * D + col,
+                 fmaf(__uint_as_float(v[h][4 * i + 2 * j]), mul, px),
+                 fmaf(__uint_as_float(v[h][4 * i + 2 * j + 1]), mul, py));
     }
   }
+}
+
+template <int D>
+__device__ __forceinline__ void drain_acc(bool bf16, uint32_t tq, float mul,
+                                          const float2 (&pp)[D / 64], void* out,
+                                          const size_t (&orow)[4]) {
+  if (bf16)
+    drain_acc<D>(tq, mul, pp, static_cast<__nv_bfloat16*>(out), orow);
+  else
+    drain_acc<D>(tq, mul, pp, static_cast<float*>(out), orow);
 }
 
 template <int D, bool kKeyMajor>
@@ -492,8 +522,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         // no fine contribution: only the pooled gradient reaches these rows
         if (row_live) {
           const size_t orow = static_cast<size_t>(pi.bh) * g.N + caller_row(g, cube, row & 63);
-          store_pooled_half<D>(hc * (D / 2), P.pooled1, prow, P.out1, orow);
-          if (kKeyMajor) store_pooled_half<D>(hc * (D / 2), P.pooled2, prow, P.out2, orow);
+          store_pooled_half<D>(g.grad_bf16, hc * (D / 2), P.pooled1, prow, P.out1, orow);
+          if (kKeyMajor)
+            store_pooled_half<D>(g.grad_bf16, hc * (D / 2), P.pooled2, prow, P.out2, orow);
         }
         continue;
       }
@@ -657,11 +688,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       tc_fence_after();
       // dQ pass: dQ = scale * acc; key-major: dV = acc, then dK = scale * acc
       // (each divided by the gradient scale)
-      if (live) drain_acc<D>(tq + kColA1, (kKeyMajor ? 1.f : g.scale) * inv_gs, p1, P.out1, orow);
+      if (live)
+        drain_acc<D>(g.grad_bf16, tq + kColA1, (kKeyMajor ? 1.f : g.scale) * inv_gs, p1, P.out1,
+                     orow);
       tc_fence_before();
       warp_arrive_bwd(kKeyMajor ? &sb.dv_free : &sb.acc_free);
       if (kKeyMajor) {
-        if (live) drain_acc<D>(tq + kColA2, g.scale * inv_gs, p2, P.out2, orow);
+        if (live) drain_acc<D>(g.grad_bf16, tq + kColA2, g.scale * inv_gs, p2, P.out2, orow);
         tc_fence_before();
         warp_arrive_bwd(&sb.dk_free);
       }
@@ -700,7 +733,7 @@ template <int D>
 cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __half* v,
                      const float* lse_f, const __half* dof, const float* delta,
                      const float* gscale, const float* dqc, const float* dkc, const float* dvc,
-                     float* dq, float* dk, float* dv, const Workspace& ws, cudaStream_t s) {
+                     void* dq, void* dk, void* dv, const Workspace& ws, cudaStream_t s) {
   const bool ordered = use_cost_order(g);
   BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, ordered ? ws.qorder : nullptr, lse_f, delta,
                gscale, dqc, nullptr, dq, nullptr, ws.status};
@@ -716,7 +749,7 @@ cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __ha
 cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const float* lse_f, const __half* dof, const float* delta,
                             const float* gscale, const float* dqc, const float* dkc,
-                            const float* dvc, float* dq, float* dk, float* dv,
+                            const float* dvc, void* dq, void* dk, void* dv,
                             const Workspace& ws, cudaStream_t s) {
   if (g.D == 64)
     return bwd_impl<64>(g, q, k, v, lse_f, dof, delta, gscale, dqc, dkc, dvc, dq, dk, dv, ws, s);

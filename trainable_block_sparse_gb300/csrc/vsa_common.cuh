@@ -23,6 +23,7 @@ struct Geom {
   int ct, ch, cw;  // cubes along T, H, W
   int cap;       // index-list capacity per query cube
   int raster;    // 1: caller tensors in raster order, 0: cube order
+  int grad_bf16; // 1: dQ, dK, dV, dG_c, dG_f are written as bf16, 0: fp32
   float scale;   // softmax scale (both stages)
 };
 
@@ -130,7 +131,7 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
 // fine backward is linear in dO_f and divides its results by gscale.
 cudaError_t launch_combine_bwd(const Geom& g, const __nv_bfloat16* d_o,
                                const __nv_bfloat16* gc, const __nv_bfloat16* gf,
-                               const __half* o_f, const float* oc, float* dgc, float* dgf,
+                               const __half* o_f, const float* oc, void* dgc, void* dgf,
                                __half* dof, float* doc, float* delta, uint32_t* amax,
                                float* gscale, uint32_t* status, cudaStream_t s);
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
@@ -160,7 +161,7 @@ inline bool use_cost_order(const Geom& g) {
 cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, const __half* v,
                             const float* lse_f, const __half* dof, const float* delta,
                             const float* gscale, const float* dqc, const float* dkc,
-                            const float* dvc, float* dq, float* dk, float* dv,
+                            const float* dvc, void* dq, void* dk, void* dv,
                             const Workspace& ws, cudaStream_t s);
 
 // ------------------------------------------------ tensor-core fp32 GEMM

@@ -30,7 +30,8 @@ class HostPipeline:
     cfg: the layer's vsa.Config (batch, heads, video shape, selection).
     heads_per_unit: heads per pipeline unit (the last unit of a batch entry
     may hold fewer).  Inputs q, k, v, gc, gf, do: bf16 [B, heads, N, D];
-    outputs: o bf16, dq, dk, dv, dgc, dgf fp32, same shape; all pinned.
+    outputs: o bf16, dq, dk, dv, dgc, dgf of cfg's gradient dtype (fp32 or bf16),
+    same shape; all pinned.
     """
 
     def __init__(self, cfg: vsa.Config, device, heads_per_unit: int, n_sets: int = 2,
@@ -55,8 +56,9 @@ class HostPipeline:
             s["in"] = {n: torch.empty(shape, dtype=torch.bfloat16, device=self.device)
                        for n in IN_NAMES}
             s["out"] = {"o": torch.empty(shape, dtype=torch.bfloat16, device=self.device)}
+            gdt = vsa.grad_torch_dtype(cfg)
             for n in OUT_NAMES[1:]:
-                s["out"][n] = torch.empty(shape, dtype=torch.float32, device=self.device)
+                s["out"][n] = torch.empty(shape, dtype=gdt, device=self.device)
             s["events"] = {"comp": torch.cuda.Event(),
                            "in": [torch.cuda.Event() for _ in range(copy_streams)],
                            "out": [torch.cuda.Event() for _ in range(copy_streams)]}
@@ -68,7 +70,7 @@ class HostPipeline:
         if heads not in s["cfg"]:
             c = self.cfg
             sub = vsa.Config(1, heads, c.T, c.H, c.W, c.head_dim, c.select_mode, c.topk, c.mass,
-                             c.kmin, c.kmax, c.scale, c.layout)
+                             c.kmin, c.kmax, c.scale, c.layout, c.grad_dtype)
             s["cfg"][heads] = sub
             with torch.cuda.stream(self.streams["comp"]):
                 s["bufs"][heads] = vsa.Buffers(sub, self.device, with_backward=True)

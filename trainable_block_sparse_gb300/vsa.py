@@ -21,6 +21,7 @@ OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TI
     ERR_DEVICE_CHECK = range(8)
 SELECT_TOPK, SELECT_MASS = 0, 1
 LAYOUT_RASTER, LAYOUT_CUBE = 0, 1
+GRAD_FP32, GRAD_BF16 = 0, 1
 
 
 class Config(ctypes.Structure):
@@ -29,7 +30,8 @@ class Config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("select_mode", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("mass", ctypes.c_float),
                 ("kmin", ctypes.c_int32), ("kmax", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("layout", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("layout", ctypes.c_int32),
+                ("grad_dtype", ctypes.c_int32)]
 
 
 class SavedLayout(ctypes.Structure):
@@ -97,17 +99,25 @@ def check(status: int, where: str) -> None:
 
 
 def make_config(batch, heads, T, H, W, head_dim, *, topk=32, select="topk", mass=0.9,
-                kmin=8, kmax=64, scale=0.0, layout="raster") -> Config:
+                kmin=8, kmax=64, scale=0.0, layout="raster", grad_dtype="fp32") -> Config:
+    if grad_dtype not in ("fp32", "bf16"):
+        raise ValueError(f"grad_dtype must be 'fp32' or 'bf16', got {grad_dtype!r}")
     return Config(batch, heads, T, H, W, head_dim,
                   SELECT_TOPK if select == "topk" else SELECT_MASS, topk, mass, kmin, kmax,
-                  scale, LAYOUT_RASTER if layout == "raster" else LAYOUT_CUBE)
+                  scale, LAYOUT_RASTER if layout == "raster" else LAYOUT_CUBE,
+                  GRAD_FP32 if grad_dtype == "fp32" else GRAD_BF16)
 
 
-def config_for(wl, layout="raster") -> Config:
+def grad_torch_dtype(cfg: Config):
+    """torch dtype of the gradients the library writes for cfg."""
+    return torch.bfloat16 if cfg.grad_dtype == GRAD_BF16 else torch.float32
+
+
+def config_for(wl, layout="raster", grad_dtype="fp32") -> Config:
     """Config of a synth.Workload."""
     return make_config(wl.batch, wl.heads, wl.T, wl.H, wl.W, wl.head_dim, topk=wl.topk,
                        select=wl.select, mass=wl.mass, kmin=wl.kmin, kmax=wl.kmax,
-                       layout=layout)
+                       layout=layout, grad_dtype=grad_dtype)
 
 
 def saved_layout(cfg: Config) -> SavedLayout:
@@ -263,7 +273,8 @@ def combine_bwd(cfg: Config, d_o, gc, gf, o_f, oc, ws):
     """-> (dgc, dgf, dof16, doc, delta, gscale); dof16 and delta carry gscale."""
     B, Hd, N, D = d_o.shape
     f = dict(dtype=torch.float32, device=d_o.device)
-    dgc, dgf = torch.empty(B, Hd, N, D, **f), torch.empty(B, Hd, N, D, **f)
+    gd = dict(dtype=grad_torch_dtype(cfg), device=d_o.device)
+    dgc, dgf = torch.empty(B, Hd, N, D, **gd), torch.empty(B, Hd, N, D, **gd)
     dof = torch.empty(B, Hd, N, D, dtype=torch.float16, device=d_o.device)
     doc = torch.empty(B, Hd, N // 64, D, **f)
     delta = torch.empty(B, Hd, N, **f)
@@ -285,13 +296,13 @@ def coarse_bwd(cfg: Config, qc, kc, vc, oc, lse_c, doc, ws):
 
 def fine_bwd(cfg: Config, q16, k16, v16, idx, cnt, lse_f, dof16, delta, dqc, dkc, dvc, ws,
              gscale=None):
-    """Staged fp16 operands -> fp32 dq, dk, dv in cfg.layout order.
+    """Staged fp16 operands -> dq, dk, dv (cfg.grad_dtype) in cfg.layout order.
 
     gscale: the per-slice factor dof16 and delta carry (combine_bwd's output),
     or None for 1."""
     q, k, v, dof = q16, k16, v16, dof16
     B, Hd, N, D = q.shape
-    f = dict(dtype=torch.float32, device=q.device)
+    f = dict(dtype=grad_torch_dtype(cfg), device=q.device)
     dq, dk, dv = (torch.empty(B, Hd, N, D, **f) for _ in range(3))
     check(lib().vsa_fine_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(cnt),
                              _ptr(lse_f), _ptr(dof), _ptr(delta), _ptr(gscale), _ptr(dqc),
@@ -312,7 +323,7 @@ def forward(cfg: Config, q, k, v, gc, gf, bufs: Buffers, with_backward=True, out
 def backward(cfg: Config, gc, gf, d_o, bufs: Buffers, grads=None):
     B, Hd, N, D = gc.shape
     if grads is None:
-        grads = tuple(torch.empty(B, Hd, N, D, dtype=torch.float32, device=gc.device)
+        grads = tuple(torch.empty(B, Hd, N, D, dtype=grad_torch_dtype(cfg), device=gc.device)
                       for _ in range(5))
     dq, dk, dv, dgc, dgf = grads
     check(lib().vsa_backward(ctypes.byref(cfg), _ptr(gc), _ptr(gf), _ptr(bufs.saved), _ptr(d_o),
@@ -343,11 +354,11 @@ class _VSAFunction(torch.autograd.Function):
             raise ValueError(f"gradient of O has shape {tuple(d_o.shape)}, "
                              f"expected {tuple(gc.shape)}")
         d_o = d_o.to(torch.bfloat16).contiguous()
+        # the library writes bf16 gradients directly (the config asks for them)
         dq, dk, dv, dgc, dgf = backward(ctx.cfg, gc, gf, d_o, ctx.bufs)
         if ctx.check_status:
             check(ctx.bufs.device_status(), "video_sparse_attention (backward, device status)")
-        bf = torch.bfloat16
-        return dq.to(bf), dk.to(bf), dv.to(bf), dgc.to(bf), dgf.to(bf), None, None
+        return dq, dk, dv, dgc, dgf, None, None
 
 
 def _check_inputs(q, k, v, gc, gf, video_shape, layout):
@@ -400,7 +411,7 @@ def video_sparse_attention(q, k, v, gc, gf, video_shape, *, topk=32, select="top
     if select not in ("topk", "mass"):
         raise ValueError(f"select must be 'topk' or 'mass', got {select!r}")
     cfg = make_config(B, Hd, T, H, W, D, topk=topk, select=select, mass=mass, kmin=kmin,
-                      kmax=kmax, scale=scale, layout=layout)
+                      kmax=kmax, scale=scale, layout=layout, grad_dtype="bf16")
     check(lib().vsa_validate(ctypes.byref(cfg)), "video_sparse_attention")
     cfg_tuple = tuple(getattr(cfg, n) for n, _ in Config._fields_)
     return _VSAFunction.apply(q, k, v, gc, gf, cfg_tuple, bool(check_status))
