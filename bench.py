@@ -480,7 +480,42 @@ def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values())
     return {"ms": ms, "value": step_flops / (ms * 1e-3) / 1e12, "h2d": h2d, "d2h": d2h,
-            "units": sum(1 for _ in pipe.units())}
+            "units": sum(1 for _ in pipe.units()), "link": host_link(dev)}
+
+
+def host_link(dev, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy rates of this machine (GB/s): each direction
+    alone, and both at once on two streams (the bound under the end-to-end
+    number)."""
+    h = torch.empty(2, nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(2, nbytes, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def rate(fn, moved):
+        fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return moved * reps / (time.perf_counter() - t0) / 1e9
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            d[0].copy_(h[0], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            h[1].copy_(d[1], non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    out = {"h2d_gbs": rate(h2d, nbytes), "d2h_gbs": rate(d2h, nbytes),
+           "both_gbs": rate(both, 2 * nbytes), "copy_bytes": nbytes}
+    del h, d
+    return out
 
 
 def oracle_sample(inp, b, h, cubes, budget_s=None):
@@ -768,7 +803,8 @@ def main():
         "e2e": {"value": world * r["e2e"]["value"], "unit": "TFLOPS",
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"],
                 "ms_per_step": r["e2e"]["ms"], "pipeline_units": r["e2e"]["units"],
-                "timer": "host clock between device synchronisations (three streams)"},
+                "timer": "host clock between device synchronisations (three streams)",
+                "host_link": r["e2e"]["link"]},
         "gpu_launches": (LAUNCHES_FWD + LAUNCHES_BWD) * args.steps,
         "load_balance": r["balance"],
     }

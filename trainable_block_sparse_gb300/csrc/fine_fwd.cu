@@ -3,6 +3,7 @@
 // token-level attention only inside the selected 64x64 blocks; paper notes
 // 关键设计 3: O = O_c (.) G_c + O_f (.) G_f).
 //
+// Head_dim 128 (head_dim 64 runs in fine_fwd64.cu, two CTAs per SM).
 // GB300 design (tcgen05 + TMEM + TMA, one persistent CTA per SM):
 //  * Work item = two query cubes of one (batch, head): their 2 x 64 token rows
 //    form one M = 128 tensor-core tile, and the item walks the union of the two
@@ -83,12 +84,12 @@ struct FwdSmem {
   static constexpr int kChunkBytes = 128 * 128;       // one chunk of 128 rows
   static constexpr int kQBytes = kChunks * kChunkBytes;
   static constexpr int kKVBytes = kChunks * kChunkBytes;  // 2 key tiles
-  static constexpr int kStagesK = kF8 ? 3 : (D == 128) ? 2 : 3;
-  // D = 128: two stages each; D = 64 (16 KB tiles): three each.  Deeper rings
-  // measured slower: TMA serves a CTA's copies in order, so every extra slot in
-  // flight queues ahead of the tile the next product needs (at D = 128,
-  // 2 K / 3 V and 3 K / 2 V both lost ~1%).  The e4m3 tiles are half as large.
-  static constexpr int kStagesV = kF8 ? 3 : (D == 128) ? 2 : 3;
+  static constexpr int kStagesK = kF8 ? 3 : 2;
+  // Two stages each.  Deeper rings measured slower: TMA serves a CTA's copies
+  // in order, so every extra slot in flight queues ahead of the tile the next
+  // product needs (2 K / 3 V and 3 K / 2 V both lost ~1%).  The e4m3 tiles are
+  // half as large.
+  static constexpr int kStagesV = kF8 ? 3 : 2;
   static constexpr int kTileBytes = 64 * D * (kF8 ? 1 : 2);  // one 64-row tile
   // epilogue staging of one 32-column chunk of O_f: 128 rows x 128 bytes
   static constexpr int kStageOff = kQBytes + (kStagesK + kStagesV) * kKVBytes;
@@ -754,7 +755,7 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
                             cudaStream_t s) {
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
               gc, gf, oc, o, o_f, lse_f, ws.status, nullptr};
-  if (g.D == 64) return run_fwd<64>(g, q, k, v, p, s);
+  if (g.D == 64) return launch_fine_fwd64(g, q, k, v, gc, gf, oc, o, o_f, lse_f, ws, s);
   return run_fwd<128>(g, q, k, v, p, s);
 }
 
@@ -764,7 +765,7 @@ cudaError_t launch_fine_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __
                                  float* lse_f, const Workspace& ws, cudaStream_t s) {
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
               gc, gf, oc, o, nullptr, lse_f, ws.status, nullptr};
-  if (g.D == 64) return run_fwd_bf16<64>(g, q, k, v, p, s);
+  if (g.D == 64) return launch_fine_fwd64_bf16(g, q, k, v, gc, gf, oc, o, lse_f, ws, s);
   return run_fwd_bf16<128>(g, q, k, v, p, s);
 }
 

@@ -224,6 +224,17 @@ bool encode_raster_cubes_bf16(void* map, const void* base, const Geom& g);
 bool encode_tiled_2d_u8(void* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
 
+// Head_dim 64 forms of the two above (fine_fwd64.cu: two CTAs per SM).
+cudaError_t launch_fine_fwd64(const Geom& g, const __half* q, const __half* k, const __half* v,
+                              const __nv_bfloat16* gc, const __nv_bfloat16* gf, const float* oc,
+                              __nv_bfloat16* o, __half* o_f, float* lse_f, const Workspace& ws,
+                              cudaStream_t s);
+cudaError_t launch_fine_fwd64_bf16(const Geom& g, const __nv_bfloat16* q,
+                                   const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                   const __nv_bfloat16* gc, const __nv_bfloat16* gf,
+                                   const float* oc, __nv_bfloat16* o, float* lse_f,
+                                   const Workspace& ws, cudaStream_t s);
+
 // The fine forward + combine reading the caller's bf16 q, k, v (cfg layout)
 // in place: no staged copies (fine_fwd.cu; inference: no O_f).
 cudaError_t launch_fine_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __nv_bfloat16* k,
