@@ -338,7 +338,7 @@ def balance_report(vsa, bufs, wl, dev):
     cnt = bufs.view("cnt", torch.int32, (B * H, nc)).cpu().numpy()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ordered = schedule.uses_cost_order(B * H, wl.tokens, wl.head_dim)
-    return schedule.load_balance(idx, cnt, sms, ordered=ordered)
+    return schedule.load_balance(idx, cnt, sms, ordered=ordered, head_dim=wl.head_dim)
 
 
 def side_workload(vsa, name, dev):

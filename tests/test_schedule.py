@@ -82,3 +82,25 @@ def test_snake_schedule_balances_sorted_items():
     assert steps[order].tolist() == [8, 7, 6, 5, 1, 2, 3, 4]
     # plain item order: CTA c takes items c and c + 4
     assert schedule.cta_work(steps, 4, scheduled=False).tolist() == [4, 14, 6, 12]
+
+
+def test_head_dim_64_forward_runs_two_ctas_per_sm_with_one_key_tile_per_step():
+    # the same 4-cube selection as above; the head_dim-64 forward takes one key
+    # tile per step (pair (0,1): 4 steps, pair (2,3): 2) on up to 2 x sms CTAs,
+    # in the schedule built from the two-tile costs
+    idx = np.array([[[0, 1, 2, 3], [1, -1, -1, -1], [2, -1, -1, -1], [3, -1, -1, -1]]],
+                   dtype=np.int32)
+    cnt = np.array([[4, 1, 1, 1]], dtype=np.int32)
+    r = schedule.load_balance(idx, cnt, sms=1, head_dim=64)
+    assert r["fine_fwd"]["ctas"] == 2 and r["fine_fwd"]["steps_total"] == 6
+    assert r["fine_fwd"]["cta_steps_max"] == 4
+    assert r["fine_bwd_dq"]["ctas"] == 1 and r["fine_bwd_dq"]["steps_total"] == 3
+    assert schedule.kernel_grid("fine_fwd", 1000, 152, 64) == 304
+    assert schedule.kernel_grid("fine_fwd", 1000, 152, 128) == 152
+    # 8 items, 2 SMs: the schedule deals rounds of 2 positions by the two-tile cost,
+    # the kernel's 4 CTAs take positions c, c + 4
+    steps = np.array([1, 8, 2, 7, 3, 6, 4, 5])
+    order = schedule.schedule_order(steps, 2)
+    seq = steps[order]
+    want = [int(seq[c::4].sum()) for c in range(4)]
+    assert schedule.cta_work(steps, 2, grid=4).tolist() == want

@@ -1,10 +1,11 @@
 """Work distribution of the persistent fine-stage kernels: a host-side report.
 
 The fine forward kernel and both fine backward passes launch one CTA per SM
-(grid = min(items, SMs)), and CTA b processes schedule positions b, b + grid,
+(grid = min(items, SMs); the head_dim-64 forward two per SM, grid =
+min(items, 2 SMs)), and CTA b processes schedule positions b, b + grid,
 b + 2*grid, ....  The schedule sorts the items by step count, largest first,
-and deals each full round of `grid` positions in alternating direction
-(snake order); the last, partial round keeps its order.  An item is a pair
+and deals each full round of SMs positions in alternating direction (snake
+order); the last, partial round keeps its order.  An item is a pair
 of neighbouring cubes (2p, 2p + 1) of one (batch, head), item index =
 bh * ceil(Nc / 2) + p:
 
@@ -14,7 +15,8 @@ bh * ceil(Nc / 2) + p:
     lists (the query cubes that selected them).
 
 Each step of an item covers two key (or query) tiles, so an item costs
-ceil(|union| / 2) steps.  This module recomputes those costs from the index
+ceil(|union| / 2) steps (the schedule's cost); a step of the head_dim-64
+forward covers one key tile, so there an item takes |union| steps.  This module recomputes those costs from the index
 lists that the coarse stage emitted and reports how evenly the static
 assignment spreads them over the CTAs ("VSA: Faster Video Diffusion with
 Trainable Sparse Attention", §2: the fine stage attends only within the
@@ -49,11 +51,19 @@ def pair_union_sizes(sel: np.ndarray) -> np.ndarray:
     return (even | odd).sum(-1)
 
 
-def item_steps(sel: np.ndarray) -> dict[str, np.ndarray]:
+def item_steps(sel: np.ndarray, head_dim: int = 128) -> dict[str, np.ndarray]:
     """Steps per work item, flattened in item order, for each fine kernel."""
-    fwd = (pair_union_sizes(sel) + 1) // 2
+    union = pair_union_sizes(sel)
+    fwd = (union + 1) // 2
     key = (pair_union_sizes(np.swapaxes(sel, 1, 2)) + 1) // 2
-    return {"fine_fwd": fwd.ravel(), "fine_bwd_dq": fwd.ravel(), "fine_bwd_dkdv": key.ravel()}
+    return {"fine_fwd": (union if head_dim == 64 else fwd).ravel(), "fine_bwd_dq": fwd.ravel(),
+            "fine_bwd_dkdv": key.ravel()}
+
+
+def kernel_grid(name: str, items: int, sms: int, head_dim: int) -> int:
+    """CTAs a fine kernel launches for `items` work items."""
+    per_sm = 2 if (name == "fine_fwd" and head_dim == 64) else 1
+    return min(items, per_sm * sms)
 
 
 def schedule_order(steps: np.ndarray, sms: int) -> np.ndarray:
@@ -68,15 +78,19 @@ def schedule_order(steps: np.ndarray, sms: int) -> np.ndarray:
     return out
 
 
-def cta_work(steps: np.ndarray, sms: int, scheduled: bool = True) -> np.ndarray:
+def cta_work(steps: np.ndarray, sms: int, scheduled: bool = True, grid: int | None = None,
+             cost: np.ndarray | None = None) -> np.ndarray:
     """Total steps of each CTA: positions c, c + grid, ... of the schedule
-    (scheduled=True) or of plain item order."""
+    (scheduled=True) or of plain item order.  The schedule is built from
+    `cost` (default: the steps) in rounds of min(n, sms) positions; `grid`
+    (default min(n, sms)) is the kernel's CTA count."""
     steps = np.asarray(steps)
     n = steps.size
-    grid = min(n, sms)
+    grid = min(n, sms) if grid is None else grid
     if grid == 0:
         return np.zeros(0, dtype=np.int64)
-    seq = steps[schedule_order(steps, sms)] if scheduled else steps
+    order_cost = steps if cost is None else np.asarray(cost)
+    seq = steps[schedule_order(order_cost, sms)] if scheduled else steps
     padded = np.zeros(-(-n // grid) * grid, dtype=np.int64)
     padded[:n] = seq
     return padded.reshape(-1, grid).sum(0)
@@ -89,15 +103,20 @@ def uses_cost_order(batch_heads: int, tokens: int, head_dim: int) -> bool:
     return 4.0 * batch_heads * tokens * head_dim <= 256.0 * 1024 * 1024
 
 
-def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int, ordered: bool = True) -> dict:
+def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int, ordered: bool = True,
+                 head_dim: int = 128) -> dict:
     """max/mean per-CTA steps of each fine kernel (under the cost-sorted
     schedule when `ordered`, else plain item order), the step count of the
     biggest item, and the histogram of per-cube list lengths."""
     sel = selection_matrix(idx, cnt)
     out = {"schedule": "cost-sorted snake" if ordered else "item order"}
-    for name, steps in item_steps(sel).items():
-        w = cta_work(steps, sms, scheduled=ordered)
-        w_plain = cta_work(steps, sms, scheduled=False)
+    all_steps = item_steps(sel, head_dim)
+    cost = item_steps(sel)["fine_fwd"]  # the schedule's cost: two key tiles per step
+    for name, steps in all_steps.items():
+        grid = kernel_grid(name, steps.size, sms, head_dim)
+        c = cost if name != "fine_bwd_dkdv" else steps
+        w = cta_work(steps, sms, scheduled=ordered, grid=grid, cost=c)
+        w_plain = cta_work(steps, sms, scheduled=False, grid=grid)
         mean = float(w.mean()) if w.size else 0.0
         out[name] = {"items": int(steps.size), "ctas": int(w.size),
                      "steps_total": int(steps.sum()),
