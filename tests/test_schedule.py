@@ -104,3 +104,15 @@ def test_head_dim_64_forward_runs_two_ctas_per_sm_with_one_key_tile_per_step():
     seq = steps[order]
     want = [int(seq[c::4].sum()) for c in range(4)]
     assert schedule.cta_work(steps, 2, grid=4).tolist() == want
+
+
+def test_two_ctas_per_sm_report_the_pairs_of_ctas_that_share_an_sm():
+    # CTAs s and s + sms share SM s
+    assert schedule.sm_work(np.array([5, 1, 2, 7]), 2).tolist() == [7, 8]
+    assert schedule.sm_work(np.array([5, 1, 2]), 2).tolist() == [7, 1]
+    idx = np.array([[[0, 1, 2, 3], [1, -1, -1, -1], [2, -1, -1, -1], [3, -1, -1, -1]]],
+                   dtype=np.int32)
+    cnt = np.array([[4, 1, 1, 1]], dtype=np.int32)
+    r = schedule.load_balance(idx, cnt, sms=1, head_dim=64)
+    # both items on the one SM: its load is all 6 steps, the mean is 6
+    assert r["fine_fwd"]["sm_max_over_mean"] == 1.0

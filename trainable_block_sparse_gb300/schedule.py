@@ -96,6 +96,16 @@ def cta_work(steps: np.ndarray, sms: int, scheduled: bool = True, grid: int | No
     return padded.reshape(-1, grid).sum(0)
 
 
+def sm_work(cta: np.ndarray, sms: int) -> np.ndarray:
+    """Per-SM totals of a kernel whose CTAs s, s + sms, s + 2 sms, ... share
+    SM s."""
+    cta = np.asarray(cta)
+    n = -(-cta.size // sms) * sms
+    padded = np.zeros(n, dtype=cta.dtype)
+    padded[:cta.size] = cta
+    return padded.reshape(-1, sms).sum(0)
+
+
 def uses_cost_order(batch_heads: int, tokens: int, head_dim: int) -> bool:
     """The library sorts the items by cost only when the fp16 K and V of all
     slices fit in 256 MB (twice the L2); otherwise it keeps item order, whose
@@ -125,6 +135,11 @@ def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int, ordered: bool = Tru
                      "max_over_mean": float(w.max() / mean) if mean > 0 else 1.0,
                      "max_over_mean_item_order": float(w_plain.max() / mean) if mean > 0 else 1.0,
                      "item_steps_max": int(steps.max()) if steps.size else 0}
+        if grid > sms:
+            # two CTAs per SM: CTAs s and s + sms share SM s (the block
+            # scheduler places a grid round-robin), so the SMs' loads are the pairs
+            sm = sm_work(w, sms)
+            out[name]["sm_max_over_mean"] = float(sm.max() / sm.mean()) if sm.size else 1.0
     counts = np.bincount(np.asarray(cnt).ravel(), minlength=1)
     out["count_histogram"] = {int(c): int(n) for c, n in enumerate(counts) if n}
     return out
