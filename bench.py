@@ -256,6 +256,8 @@ def gpu_arm(args, rank, world):
         fp8 = fp8_forward(vsa, cfg, wl, t, dev, pairs, flush)
     ms_max = max_over_ranks(ms_step, world, dev)
     e2e = end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args)
+    e2e["fp32_gradients"] = end_to_end(vsa, cfg32, wl, inp, None, stream, dev, step_flops, args,
+                                       link=False)
     side = {}
     if rank == 0 and not args.no_side:
         del bufs, grads, grads32, o, t
@@ -453,7 +455,7 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=SIDE_REPS, flush=No
     return {name: timed_median(fn, reps, 2, stream, flush) for name, fn in calls.items()}
 
 
-def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
+def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args, link=True):
     """Host inputs in, host outputs out, every step, through the library's
     host-buffer pipeline (HostPipeline: units of 5 heads, copies in and out
     overlapped with the kernels of the neighbouring units)."""
@@ -479,8 +481,12 @@ def end_to_end(vsa, cfg, wl, inp, bufs, stream, dev, step_flops, args):
         raise RuntimeError("device status after the host-pipeline steps")
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values())
-    return {"ms": ms, "value": step_flops / (ms * 1e-3) / 1e12, "h2d": h2d, "d2h": d2h,
-            "units": sum(1 for _ in pipe.units()), "link": host_link(dev)}
+    out = {"ms": ms, "value": step_flops / (ms * 1e-3) / 1e12, "h2d": h2d, "d2h": d2h,
+           "units": sum(1 for _ in pipe.units())}
+    del pipe, host_in, host_out
+    if link:
+        out["link"] = host_link(dev)
+    return out
 
 
 def host_link(dev, nbytes=1 << 30, reps=3):
@@ -804,7 +810,11 @@ def main():
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"],
                 "ms_per_step": r["e2e"]["ms"], "pipeline_units": r["e2e"]["units"],
                 "timer": "host clock between device synchronisations (three streams)",
-                "host_link": r["e2e"]["link"]},
+                "host_link": r["e2e"]["link"],
+                "with_fp32_gradients": {
+                    "ms_per_step": r["e2e"]["fp32_gradients"]["ms"],
+                    "value": world * r["e2e"]["fp32_gradients"]["value"],
+                    "d2h_bytes_per_step": r["e2e"]["fp32_gradients"]["d2h"]}},
         "gpu_launches": (LAUNCHES_FWD + LAUNCHES_BWD) * args.steps,
         "load_balance": r["balance"],
     }
