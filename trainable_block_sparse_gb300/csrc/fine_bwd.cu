@@ -63,6 +63,11 @@ constexpr int kEpiWarps = 4;
 // register split: the launch gives 65536 / 512 = 128 a thread
 constexpr int kRegsSoftmax = 168, kRegsRest = 88;
 static_assert(256 * kRegsSoftmax + 256 * kRegsRest <= 65536, "split exceeds the launch's registers");
+// setmaxnreg.inc only raises and .dec only lowers a warp's count (the launch
+// gives 128): a .dec above the launch's count is an illegal instruction.
+static_assert(kRegsSoftmax >= 128 && kRegsRest <= 128 && kRegsSoftmax % 8 == 0 &&
+                  kRegsRest % 8 == 0 && kRegsRest >= 24,
+              "setmaxnreg shares must move away from the launch's count, in steps of 8");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColA1 = 256, kColA2 = 384;
 // dQ pass: the item's Q and dO as TMEM A operands (D/2 columns each) at kColA2
@@ -721,7 +726,15 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
     return cudaErrorInvalidValue;
   const int smem = BwdSmem<D>::kBytes;
   auto kern = fine_bwd_kernel<D, kKeyMajor>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the register split assumes the launch's 128 registers a thread: setmaxnreg
+  // raises the softmax warps above it and lowers the others below it
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs < kRegsRest || attr.numRegs > kRegsSoftmax ||
+      attr.numRegs * kThreadsBwd < 256 * (kRegsSoftmax + kRegsRest))
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;

@@ -64,6 +64,13 @@ constexpr int kRegsSoftmax64 = 128, kRegsEpi64 = 80, kRegsRest64 = 32;
 constexpr int kLaunchRegs64 = 80;
 static_assert(128 * (kRegsSoftmax64 + kRegsEpi64 + kRegsRest64) <= kThreads64 * kLaunchRegs64,
               "register split exceeds the launch's registers");
+// setmaxnreg.inc may only raise a warp's count and .dec only lower it: the
+// shares that decrease must not exceed the launch's count (a .dec above it is
+// an illegal instruction), the one that increases must not be below it.
+static_assert(kRegsSoftmax64 >= kLaunchRegs64 && kRegsEpi64 <= kLaunchRegs64 &&
+                  kRegsRest64 <= kLaunchRegs64 && kRegsEpi64 % 8 == 0 && kRegsRest64 % 8 == 0 &&
+                  kRegsSoftmax64 % 8 == 0 && kRegsRest64 >= 24,
+              "setmaxnreg shares must move away from the launch's count, in steps of 8");
 enum : int { kOp64F16 = 0, kOp64BF16 = 2 };
 
 constexpr int kStagesK64 = 4, kStagesV64 = 4;
@@ -574,7 +581,10 @@ cudaError_t launch64(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
-  if (attr.numRegs * kThreads64 < 128 * (kRegsSoftmax64 + kRegsEpi64 + kRegsRest64))
+  // every share must move away from the launch's count in its own direction,
+  // and the shares must fit in the launch's registers
+  if (attr.numRegs < kRegsEpi64 || attr.numRegs < kRegsRest64 || attr.numRegs > kRegsSoftmax64 ||
+      attr.numRegs * kThreads64 < 128 * (kRegsSoftmax64 + kRegsEpi64 + kRegsRest64))
     return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L64::kBytes);
   if (e != cudaSuccess) return e;
