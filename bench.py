@@ -45,9 +45,9 @@ WORKLOAD = "p720"
 # kernels per call of vsa_forward / vsa_backward
 LAUNCHES_FWD = 9   # stage x3, tf32 split, coarse logits GEMM + select + O_c GEMM, pair lists,
                    # fine forward
-LAUNCHES_BWD = 17  # gradient-scale max, combine bwd, coarse bwd (row dot, tf32 split,
-                   # 5 GEMMs), pair lists, transposed lists (mask, count, scan, fill,
-                   # pairs), fine bwd x2
+LAUNCHES_BWD = 16  # gradient-scale max, combine bwd, coarse bwd (row dot, tf32 split,
+                   # dual GEMM, 3 GEMMs), pair lists, transposed lists (mask, count, scan,
+                   # fill, pairs), fine bwd x2
 SIDE_WORKLOADS = ("wan13b", "pretrain", "dynamic")  # timed per stage beside the headline layer
 SIDE_REPS = 20
 # Gradients leave the layer in the inputs' dtype, bf16 (what autograd hands back
@@ -432,8 +432,9 @@ def stage_breakdown(vsa, cfg, wl, t, bufs, stream, dev, reps=SIDE_REPS, flush=No
     calls = {
         "stage_pool": lambda: [ck(L.vsa_stage(c, P(t[n]), P(v[n + "16"]), P(v[n + "c"]), P(ws), s),
                                   "vsa_stage") for n in ("q", "k", "v")],
+        # from the cube means the forward already holds (the pooling is stage_pool's)
         "coarse_select": lambda: ck(L.vsa_coarse_select(
-            c, P(t["q"]), P(t["k"]), P(t["v"]), P(v["qc"]), P(v["kc"]), P(v["vc"]), P(v["oc"]),
+            c, None, None, None, P(v["qc"]), P(v["kc"]), P(v["vc"]), P(v["oc"]),
             P(v["lse_c"]), P(v["idx"]), P(v["cnt"]), P(ws), s), "vsa_coarse_select"),
         "fine_fwd": lambda: ck(L.vsa_fine_fwd(
             c, P(v["q16"]), P(v["k16"]), P(v["v16"]), P(v["idx"]), P(v["cnt"]), P(t["gc"]),

@@ -164,7 +164,10 @@ vsa_status_t vsa_stage(const vsa_config_t* cfg, const void* x, void* x16, float*
 
 /* Coarse stage (§2 "Coarse stage"): per-cube means, dense attention on the
  * pooled sequence, selection and index lists, in one pass.
- * q, k, v : bf16 [B,heads,N,D] in cfg->layout order.
+ * q, k, v : bf16 [B,heads,N,D] in cfg->layout order; or all three NULL, when
+ *           qc, kc, vc already hold the cube means (e.g. from vsa_stage) and
+ *           are read instead of written (one NULL among three non-NULL is
+ *           VSA_ERR_INVALID_ARG).
  * qc, kc, vc, oc : fp32 [B,heads,Nc,D] outputs (pooled inputs, O_c).
  * lse_c   : fp32 [B,heads,Nc] output, natural-log log-sum-exp of the logits.
  * idx     : int32 [B,heads,Nc,list_cap] output, ascending key-cube ids, -1 padded.

@@ -74,6 +74,22 @@ def test_null_config_and_pointers(lib):
     assert lib.vsa_forward(ctypes.byref(cfg), *([None] * 7), 1, None, None) == vsa.ERR_INVALID_ARG
 
 
+def test_coarse_select_inputs_are_all_or_none(lib):
+    """q, k, v: all given (pooled here) or all NULL (qc, kc, vc are the means)."""
+    cfg = _cfg()
+    p = ctypes.c_void_p(0x1000)
+    outs = [p] * 8  # qc, kc, vc, oc, lse_c, idx, cnt, ws
+    for qkv in ([p, p, None], [None, p, None], [p, None, p]):
+        assert lib.vsa_coarse_select(ctypes.byref(cfg), *qkv, *outs, None) == vsa.ERR_INVALID_ARG
+    # the pooled form still needs every output
+    assert lib.vsa_coarse_select(ctypes.byref(cfg), None, None, None, *([p] * 7), None,
+                                 None) == vsa.ERR_INVALID_ARG
+    # and checks alignment on the host
+    odd = ctypes.c_void_p(0x2008)
+    assert lib.vsa_coarse_select(ctypes.byref(cfg), None, None, None, odd, *([p] * 7),
+                                 None) == vsa.ERR_ALIGNMENT
+
+
 def test_misaligned_pointer_is_rejected(lib):
     cfg = _cfg()
     a = ctypes.c_void_p(0x1000)

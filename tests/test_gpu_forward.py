@@ -208,6 +208,24 @@ def test_permute_is_oracle_tiling():
     assert torch.equal(vsa.permute(cfg, qt, inverse=True), q)
 
 
+@pytest.mark.parametrize("name", ["tiny", "dynamic"])
+def test_coarse_select_from_staged_means(name):
+    """vsa_coarse_select with q, k, v NULL reads the means vsa_stage wrote and
+    gives what the pooling call gives, bit for bit."""
+    inp = gapped(name)
+    cfg = vsa.config_for(inp.wl)
+    t = cuda_inputs(inp)
+    ws = torch.empty(vsa.workspace_bytes(cfg, False), dtype=torch.uint8, device="cuda")
+    qc, kc, vc, oc, lse, idx, cnt = vsa.coarse_select(cfg, t["q"], t["k"], t["v"], ws)
+    means = [vsa.stage(cfg, t[n], ws, want_pooled=True)[1] for n in ("q", "k", "v")]
+    for a, b in zip((qc, kc, vc), means):
+        assert torch.equal(a, b)
+    oc2, lse2, idx2, cnt2 = vsa.coarse_select_pooled(cfg, *means, ws)
+    torch.cuda.synchronize()
+    for a, b in ((oc, oc2), (lse, lse2), (idx, idx2), (cnt, cnt2)):
+        assert torch.equal(a, b)
+
+
 def test_pooled_means_within_fp32_summation_bound():
     inp = gapped("pretrain")
     wl = inp.wl

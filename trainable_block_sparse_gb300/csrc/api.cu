@@ -355,14 +355,17 @@ vsa_status_t vsa_coarse_select(const vsa_config_t* cfg, const void* q, const voi
   Geom g;
   vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  if (!all_set(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt, ws)) return VSA_ERR_INVALID_ARG;
+  const bool pooled = !q && !k && !v;  // qc, kc, vc are inputs
+  if ((!pooled && !all_set(q, k, v)) || !all_set(qc, kc, vc, oc, lse_c, idx, cnt, ws))
+    return VSA_ERR_INVALID_ARG;
   if (!all_aligned(q, k, v, qc, kc, vc, oc, lse_c, idx, cnt, ws)) return VSA_ERR_ALIGNMENT;
   Workspace w;
   carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_stage(g, static_cast<const bf16*>(q), g.raster, nullptr, qc, w.status, s) ||
-      launch_stage(g, static_cast<const bf16*>(k), g.raster, nullptr, kc, w.status, s) ||
-      launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s))
+  if (!pooled &&
+      (launch_stage(g, static_cast<const bf16*>(q), g.raster, nullptr, qc, w.status, s) ||
+       launch_stage(g, static_cast<const bf16*>(k), g.raster, nullptr, kc, w.status, s) ||
+       launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s)))
     return VSA_ERR_CUDA;
   return cuda_status(launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin,
                                           cfg->kmax, qc, kc, vc, oc, lse_c, idx, cnt, w, s));

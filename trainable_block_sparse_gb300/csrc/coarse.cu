@@ -21,9 +21,8 @@
 //             O_c = A_c V_c                         (plain tf32 GEMM)
 //   backward: P  = exp(scale Q_c K_c^T - lse),
 //             dL = P (.) (dO_c V_c^T - rowsum(dO_c O_c))
-//                 (dual GEMM, query-major tiles -> dL pair; key-major tiles of
-//                  the transposed products -> dL^T and P^T pairs; P is never
-//                  stored in fp32)
+//                 (dual GEMM, query-major tiles -> dL, dL^T and P^T rounded
+//                  to tf32; P is never stored in fp32)
 //             dQ_c = scale dL K_c, dK_c = scale dL^T Q_c, dV_c = P^T dO_c
 #include <cfloat>
 
@@ -147,11 +146,15 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 
 // Per-warp shared scratch of the mass rule (kmax <= 64): candidate columns in
 // ascending order, their keys, their descending ranks, the columns by rank.
+// Then the row's threshold candidates (below).
+constexpr int kCand = 256;  // candidates held by a warp, kCand / 32 per lane
 struct MassScratch {
   int ci[64];
   uint32_t ck[64];
   int rk[64];
   int cr[64];
+  uint32_t cand_key[kCand];
+  int cand_col[kCand];
 };
 
 // Selection of one row held in registers by one warp (lane l holds columns
@@ -169,13 +172,14 @@ __device__ __forceinline__ void select_row(const Geom& g, const SelectArgs& sa,
   const int Nc = g.Nc;
   const int lane = threadIdx.x % 32;
   uint32_t key[kPer];
-  uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;
+  uint32_t kmin_l = 0xffffffffu, kmax_l = 0u, k2_l = 0u;  // k2_l: the lane's second largest
   int nvalid = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     key[i] = 32 * i + lane < Nc ? order_key(v[i]) : 0u;
     if (key[i]) {
       kmin_l = min(kmin_l, key[i]);
+      k2_l = max(k2_l, min(kmax_l, key[i]));
       kmax_l = max(kmax_l, key[i]);
       ++nvalid;
     }
@@ -187,18 +191,69 @@ __device__ __forceinline__ void select_row(const Geom& g, const SelectArgs& sa,
   const int K = min(want, nvalid);
   const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t t = 1u;  // the K-th largest key (or a key with exactly K keys at or above it)
+  // Candidates: when the start lo below already leaves at most kCand keys at
+  // or above it, those keys (every key the threshold search and the
+  // selection can touch, since both only look at keys >= lo) are compacted
+  // into shared memory in ascending column order, and the search and the
+  // selection run over kCand / 32 slots a lane instead of the kPer-wide row.
+  // The threshold and the chosen set are the same either way.  (Rows of
+  // more than 36 x 32 cubes skip it: their registers are taken.)
+  constexpr int kSlots = kCand / 32;
+  constexpr bool kUseCand = kPer <= 36;
+  bool cand = false;
+  int ncand = 0;
+  uint32_t ck[kSlots];
   if (K > 0) {
     uint32_t lo = __reduce_min_sync(kFull, kmin_l), hi = __reduce_max_sync(kFull, kmax_l);
-    // When every lane holds a valid key and K <= 32, the smallest of the 32
-    // lane maxima has at least 32 keys at or above it: a tighter start.
-    if (K <= 32 && nvalid >= 32 && __all_sync(kFull, kmax_l != 0u))
+    // When every lane holds r = ceil(K / 32) <= 2 valid keys, the smallest of
+    // the lanes' r-th largest keys has at least 32 r >= K keys at or above
+    // it: a tighter start.
+    bool tight = false;
+    if (K <= 32 && nvalid >= 32 && __all_sync(kFull, kmax_l != 0u)) {
       lo = max(lo, __reduce_min_sync(kFull, kmax_l));
+      tight = true;
+    } else if (K <= 64 && nvalid >= 64 && __all_sync(kFull, k2_l != 0u)) {
+      lo = max(lo, __reduce_min_sync(kFull, k2_l));
+      tight = true;
+    }
+    if (kUseCand && tight) {
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) c += key[i] >= lo;
+      ncand = __reduce_add_sync(kFull, c);
+      cand = ncand <= kCand;
+    }
+    if (cand) {
+      int base = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const bool in = key[i] >= lo;
+        const uint32_t b = __ballot_sync(kFull, in);
+        if (in) {
+          const int p = base + __popc(b & lt_mask);
+          ms.cand_key[p] = key[i];
+          ms.cand_col[p] = 32 * i + lane;
+        }
+        base += __popc(b);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j) {
+        const int p = 32 * j + lane;
+        ck[j] = p < ncand ? ms.cand_key[p] : 0u;  // 0: below every valid key
+      }
+    }
     // invariant: count(key >= lo) >= K; the answer lies in [lo, hi]
     while (lo < hi) {
       const uint32_t mid = lo + (hi - lo + 1) / 2;
       int c = 0;
+      if (cand) {
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) c += key[i] >= mid;
+        for (int j = 0; j < kSlots; ++j) c += ck[j] >= mid;
+      } else {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) c += key[i] >= mid;
+      }
       c = __reduce_add_sync(kFull, c);
       if (c == K) { lo = mid; break; }
       if (c > K) lo = mid;
@@ -207,26 +262,52 @@ __device__ __forceinline__ void select_row(const Geom& g, const SelectArgs& sa,
     t = lo;
   }
   int n_gt = 0;
+  if (cand) {
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) n_gt += key[i] > t;
+    for (int j = 0; j < kSlots; ++j) n_gt += ck[j] > t;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) n_gt += key[i] > t;
+  }
   n_gt = __reduce_add_sync(kFull, n_gt);
   const int need_eq = K - n_gt;  // keys equal to t to take, lowest columns first
   // the K chosen columns in ascending order
   int* dst = sa.mode == 0 ? out : ms.ci;
   int nout = 0, eq_seen = 0;
+  if (cand) {
+    // candidate p holds the p-th smallest candidate column
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const bool eq = K > 0 && key[i] == t;
-    const uint32_t beq = __ballot_sync(kFull, eq);
-    const bool sel = K > 0 && (key[i] > t || (eq && eq_seen + __popc(beq & lt_mask) < need_eq));
-    eq_seen += __popc(beq);
-    const uint32_t bsel = __ballot_sync(kFull, sel);
-    if (sel) {
-      const int pos = nout + __popc(bsel & lt_mask);
-      dst[pos] = 32 * i + lane;
-      if (sa.mode != 0) ms.ck[pos] = key[i];
+    for (int j = 0; j < kSlots; ++j) {
+      if (32 * j >= ncand) break;
+      const uint32_t kk = ck[j];
+      const bool eq = kk == t;
+      const uint32_t beq = __ballot_sync(kFull, eq);
+      const bool sel = kk > t || (eq && eq_seen + __popc(beq & lt_mask) < need_eq);
+      eq_seen += __popc(beq);
+      const uint32_t bsel = __ballot_sync(kFull, sel);
+      if (sel) {
+        const int pos = nout + __popc(bsel & lt_mask);
+        dst[pos] = ms.cand_col[32 * j + lane];
+        if (sa.mode != 0) ms.ck[pos] = kk;
+      }
+      nout += __popc(bsel);
     }
-    nout += __popc(bsel);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const bool eq = K > 0 && key[i] == t;
+      const uint32_t beq = __ballot_sync(kFull, eq);
+      const bool sel =
+          K > 0 && (key[i] > t || (eq && eq_seen + __popc(beq & lt_mask) < need_eq));
+      eq_seen += __popc(beq);
+      const uint32_t bsel = __ballot_sync(kFull, sel);
+      if (sel) {
+        const int pos = nout + __popc(bsel & lt_mask);
+        dst[pos] = 32 * i + lane;
+        if (sa.mode != 0) ms.ck[pos] = key[i];
+      }
+      nout += __popc(bsel);
+    }
   }
   int n = K;
   if (sa.mode != 0) {
@@ -436,10 +517,11 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
     return TgemmOperand{h, nullptr, ld, stride};
   };
   // query-major tiles: P = exp(scale Q_c K_c^T - lse) and dL = P (.) (dO_c V_c^T - delta)
-  // in registers from two accumulators; dL leaves rounded to tf32
+  // in registers from two accumulators; dL leaves rounded to tf32, and so do
+  // its transpose dL^T and P^T (through transposed shared-memory blocks)
   constexpr float kLog2e = 1.4426950408889634f;
   TgemmArgs a = gemm(g, Nc, Nc, D, g.scale * kLog2e);
-  a.mode = kTgAttnBwdRow;
+  a.mode = kTgAttnBwd;
   a.beta = kLog2e;
   a.v1 = lse_c;
   a.v2 = ws.cdelta;
@@ -447,16 +529,12 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
   a.out_hi = ws.ach;
   a.split_ld = ldc;
   a.split_stride = NC;
+  a.vt_hi = ws.dlth;
+  a.pt_hi = ws.pth;
+  a.t_ld = ldc;
+  a.t_stride = NC;
   if ((e = launch_tgemm_dual(a, hi(ws.qh, D, ND), hi(ws.kh, D, ND), hi(ws.doh, D, ND),
                              hi(ws.vh, D, ND), ws.status, s)))
-    return e;
-  // key-major tiles of the same two products (the transposes): dL^T and P^T,
-  // lse and delta now per column
-  a.mode = kTgAttnBwdCol;
-  a.out_hi = ws.dlth;
-  a.out2_hi = ws.pth;
-  if ((e = launch_tgemm_dual(a, hi(ws.kh, D, ND), hi(ws.qh, D, ND), hi(ws.vh, D, ND),
-                             hi(ws.doh, D, ND), ws.status, s)))
     return e;
   // dQ_c = scale dL K_c
   a = gemm(g, Nc, D, Nc, g.scale);

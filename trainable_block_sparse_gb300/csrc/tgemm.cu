@@ -16,16 +16,23 @@
 // tiles, k-blocks of 32 (one 128-byte swizzled row per operand row).  The
 // dual form also computes E[b] = A2[b] B2[b]^T of the same tile into a second
 // accumulator, for epilogues that combine the two (the coarse attention
-// backward: P from the logits and dL = P (.) (dP - delta) from dP).
-// Persistent, one CTA per SM, six warps:
-//   warp 0    TMA: the four operand tiles of each k-block (A hi, A lo, B hi,
-//             B lo; zero-filled outside the matrices) into a 3-stage ring;
-//   warp 1    UMMA: 12 kind::tf32 products per k-block into one of two TMEM
-//             accumulators (the epilogue of tile i overlaps tile i+1);
-//   warps 2-5 epilogue: one accumulator row per thread; each 32 x 32 block
-//             of an output is written into a 128-byte-swizzled shared-memory
-//             tile and leaves as one TMA store (rows and columns outside the
-//             matrix are clipped by the tensor map).
+// backward: P from the logits and dL = P (.) (dP - delta) from dP; dL is
+// written as it stands and, like P, transposed, so the products that
+// contract over query cubes read K-major operands).
+// Persistent, one CTA per SM, six or ten warps:
+//   warp 0    TMA: the operand tiles of each k-block (A hi, A lo, B hi, B lo,
+//             or A hi, B hi; zero-filled outside the matrices) into a ring of
+//             three stages (pairs) or four (hi parts);
+//   warp 1    UMMA: 12 (pairs) or 4 kind::tf32 products per k-block into
+//             one of two TMEM accumulators (the epilogue of tile i overlaps
+//             tile i+1);
+//   warps 2-  epilogue (four warps for pairs, eight for hi parts, two per
+//             TMEM lane quarter splitting the columns): one accumulator row
+//             per thread; each 32 x 32 block of an output is written into a
+//             128-byte-swizzled shared-memory tile (directly or transposed;
+//             a ring of three per warp for hi parts) and leaves as one TMA
+//             store (rows and columns outside the matrix are clipped by the
+//             tensor map).
 // Every mbarrier wait is bounded; a time-out sets the status word and the CTA
 // unwinds as the fine kernels do.
 #include <cstring>
@@ -36,17 +43,44 @@
 namespace vsa {
 namespace {
 
-constexpr int kTgThreads = 192;
-constexpr int kTgStages = 3;
 constexpr int kTM = 128, kTN = 128, kTK = 32;
 constexpr int kOpBytes = kTM * kTK * 4;            // one 128 x 32 fp32 operand tile
-constexpr int kStageBytes = 4 * kOpBytes;          // A hi, A lo, B hi, B lo
 constexpr int kBlockBytes = 32 * 32 * 4;           // one 32 x 32 fp32 output block
-constexpr int kEpiBytes = kBlockBytes + 2 * kTN * 4;  // per warp: staging block, column vectors
-constexpr int kTgSmem = kTgStages * kStageBytes + 4 * kEpiBytes + 1024;
+
+// Shared memory and epilogue warps per operand form.  tf32 pairs take four
+// operand tiles a k-block (A hi, A lo, B hi, B lo: 64 KB) in three stages,
+// which leaves room for four epilogue warps with one output staging block
+// each; their products (three per k-step) outlast the epilogue.  Hi parts
+// alone take two tiles (A hi, B hi: 32 KB) and one product per k-step, so
+// the epilogue (exponentials and up to two outputs per element in the
+// attention-backward forms) would bind with one warp per lane quarter:
+// eight warps, two per quarter splitting the tile's columns, each with three
+// staging blocks (it fills one while the TMA stores of the others still read
+// them), beside four stages.
+template <bool kPair>
+struct TgPlan {
+  static constexpr int kStages = kPair ? 3 : 4;
+  static constexpr int kStageBytes = (kPair ? 4 : 2) * kOpBytes;
+  static constexpr int kBOff = (kPair ? 2 : 1) * kOpBytes;  // B hi within a stage
+  static constexpr int kEpiWarps = kPair ? 4 : 8;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;   // TMA, UMMA, epilogue warps
+  static constexpr int kEpiBlocks = kPair ? 1 : 3;
+  static constexpr int kEpiBytes = kEpiBlocks * kBlockBytes;  // per epilogue warp
+  static constexpr int kSmem = kStages * kStageBytes + kEpiWarps * kEpiBytes + 1024;
+  static_assert(kEpiWarps % 4 == 0 && (kTN / 32) % (kEpiWarps / 4) == 0, "column split");
+  static_assert(kSmem <= 227 * 1024, "tgemm shared memory");
+  static_assert(kEpiBytes % 1024 == 0, "staging blocks stay 1024-byte aligned");
+};
+constexpr int kTgMaxStages = 4;
+
+// The sources of all but the N most recently committed bulk stores have been read.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 struct TgBars {
-  uint64_t full[kTgStages], empty[kTgStages];
+  uint64_t full[kTgMaxStages], empty[kTgMaxStages];
   uint64_t acc_full[2], acc_free[2];
   uint64_t final_mma;
   uint32_t tmem_base;
@@ -119,18 +153,22 @@ struct TgMaps {
 
 // Output tensor maps (fp32 [batch][M][ld], box 32 x 32); unused ones stay zero.
 struct TgOutMaps {
-  CUtensorMap out, hi, lo, hi2, lo2;
+  CUtensorMap out, hi, lo, vt, pt;
 };
 
 // kPair: operands as tf32 pairs (three products per k-step); otherwise the
 // hi parts alone (one product), whose stage holds A hi and B hi at the same
 // offsets.
 template <bool kDual, bool kPair>
-__global__ void __launch_bounds__(kTgThreads, 1)
+__global__ void __launch_bounds__(TgPlan<kPair>::kThreads, 1)
     tgemm_kernel(const __grid_constant__ TgMaps m0, const __grid_constant__ TgMaps m1,
                  const __grid_constant__ TgOutMaps om, TgemmArgs P, uint32_t* status) {
+  using Plan = TgPlan<kPair>;
+  constexpr int kTgStages = Plan::kStages;
+  constexpr int kStageBytes = Plan::kStageBytes;
+  constexpr int kEpiBlocks = Plan::kEpiBlocks;
   constexpr int kProducts = kDual ? 2 : 1;
-  constexpr uint32_t kLoadBytes = kPair ? kStageBytes : 2 * kOpBytes;
+  constexpr uint32_t kLoadBytes = kStageBytes;
   constexpr uint32_t kAccCols = kTN * kProducts;     // per tile buffer
   constexpr uint32_t kTmemCols = 2 * kAccCols;       // two tile buffers
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -151,7 +189,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.acc_full[i], 1);
-      mbar_init(&sb.acc_free[i], 4);  // the four epilogue warps
+      mbar_init(&sb.acc_free[i], Plan::kEpiWarps);
     }
     mbar_init(&sb.final_mma, 1);
     sb.abort = 0;
@@ -191,7 +229,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             uint8_t* st = smem + slot * kStageBytes;
             mbar_arrive_expect_tx(&sb.full[slot], kLoadBytes);
             tma_load_3d(st, &m.ah, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
-            tma_load_3d(st + 2 * kOpBytes, &m.bh, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
+            tma_load_3d(st + Plan::kBOff, &m.bh, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
             if (kPair) {
               tma_load_3d(st + kOpBytes, &m.al, kb * kTK, c.tm * kTM, c.b, &sb.full[slot]);
               tma_load_3d(st + 3 * kOpBytes, &m.bl, kb * kTK, c.tn * kTN, c.b, &sb.full[slot]);
@@ -228,7 +266,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             issue_kblock_tf32(dt, base, base + (kOpBytes >> 4), base + ((2 * kOpBytes) >> 4),
                               base + ((3 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
           else
-            issue_kblock_tf32_hi(dt, base, base + ((2 * kOpBytes) >> 4), idesc, kb > 0 ? 1u : 0u);
+            issue_kblock_tf32_hi(dt, base, base + (Plan::kBOff >> 4), idesc, kb > 0 ? 1u : 0u);
           commit_elect(&sb.empty[slot]);
         }
       }
@@ -239,10 +277,15 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     mbar_wait(&sb.final_mma, 0, kWaitNs);
   } else {
     // ===================================================== epilogue
-    const int quarter = warp & 3;
+    // warp w reads TMEM lane quarter w % 4; with eight warps, warps 2-5 take
+    // the first half of each tile's column chunks and warps 6-9 the second
+    const int quarter = warp & 3, ew = warp - 2;
+    constexpr int kChunks = (kTN / 32) / (Plan::kEpiWarps / 4);
+    const int ch0 = (ew / 4) * kChunks;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    uint8_t* blk = reinterpret_cast<uint8_t*>(epi_smem) + quarter * kEpiBytes;  // 1024-aligned
-    float* cvec = reinterpret_cast<float*>(blk + kBlockBytes);  // column vectors (col mode)
+    // this warp's staging blocks (1024-aligned)
+    uint8_t* blk0 = reinterpret_cast<uint8_t*>(epi_smem) + ew * Plan::kEpiBytes;
+    uint32_t nblk = 0;  // output blocks this warp has staged
     int lt = 0;
     for (int t = blockIdx.x; t < ntiles && !is_aborted(abort_flag); t += gridDim.x, ++lt) {
       const int buf = lt & 1;
@@ -250,23 +293,14 @@ __global__ void __launch_bounds__(kTgThreads, 1)
       const int mbase = c.tm * kTM + quarter * 32;
       const int m = mbase + lane;
       float r1 = 0.f, r2 = 0.f;
-      if (P.mode == kTgAttnBwdRow && m < P.M) {
+      if (P.mode == kTgAttnBwd && m < P.M) {
         r1 = P.v1[c.b * P.vec_stride + m];
         r2 = P.v2[c.b * P.vec_stride + m];
-      }
-      if (P.mode == kTgAttnBwdCol) {
-#pragma unroll
-        for (int q = 0; q < kTN / 32; ++q) {
-          const int n = c.tn * kTN + 32 * q + lane;
-          cvec[32 * q + lane] = n < P.N ? P.v1[c.b * P.vec_stride + n] : 0.f;
-          cvec[kTN + 32 * q + lane] = n < P.N ? P.v2[c.b * P.vec_stride + n] : 0.f;
-        }
-        __syncwarp();
       }
       if (!waitw(&sb.acc_full[buf], (lt >> 1) & 1, abort_flag, status)) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int ch = 0; ch < kTN / 32; ++ch) {
+      for (int ch = ch0; ch < ch0 + kChunks; ++ch) {
         const int n0 = c.tn * kTN + 32 * ch;
         if (n0 >= P.N) break;
         uint32_t v[32], e[32];
@@ -280,17 +314,16 @@ __global__ void __launch_bounds__(kTgThreads, 1)
           if (!kDual || P.mode == kTgScale) {
             val[j] = P.alpha * a;
           } else {
-            const bool col = P.mode == kTgAttnBwdCol;
-            const float l = col ? cvec[32 * ch + j] : r1;
-            const float d = col ? cvec[kTN + 32 * ch + j] : r2;
-            pv[j] = ex2_approx(fmaf(P.alpha, a, -P.beta * l));
-            val[j] = pv[j] * (__uint_as_float(e[j]) - d);
+            pv[j] = ex2_approx(fmaf(P.alpha, a, -P.beta * r1));
+            val[j] = pv[j] * (__uint_as_float(e[j]) - r2);
           }
         }
         // one output block: rows mbase.., columns n0.. through the staging block
         auto store_block = [&](const CUtensorMap* map, const float (&src)[32], int part) {
-          if (lane == 0) bulk_wait_group_read0();  // the previous block has been read
+          // the store that last used this block has read it
+          if (lane == 0) bulk_wait_group_read<kEpiBlocks - 1>();
           __syncwarp();
+          uint8_t* blk = blk0 + (nblk++ % kEpiBlocks) * kBlockBytes;
           uint8_t* rp = blk + lane * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -311,11 +344,29 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             bulk_commit_group();
           }
         };
+        // the transposed block (columns n0.. as rows, rows mbase.. as
+        // columns): thread `lane` writes column `lane` of it, one word per
+        // row, the 32 lanes of a row covering all 32 banks
+        auto store_block_t = [&](const CUtensorMap* map, const float (&src)[32]) {
+          if (lane == 0) bulk_wait_group_read<kEpiBlocks - 1>();
+          __syncwarp();
+          uint8_t* blk = blk0 + (nblk++ % kEpiBlocks) * kBlockBytes;
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            *reinterpret_cast<float*>(blk + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) +
+                                      (lane & 3) * 4) = round_tf32(src[r]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(map, blk, mbase, n0, c.b);
+            bulk_commit_group();
+          }
+        };
         if (P.out) store_block(&om.out, val, 0);
         if (P.out_hi) store_block(&om.hi, val, 1);
         if (P.out_lo) store_block(&om.lo, val, 2);
-        if (kDual && P.out2_hi) store_block(&om.hi2, pv, 1);
-        if (kDual && P.out2_lo) store_block(&om.lo2, pv, 2);
+        if (kDual && P.vt_hi) store_block_t(&om.vt, val);
+        if (kDual && P.pt_hi) store_block_t(&om.pt, pv);
       }
       tc_fence_before();
       __syncwarp();
@@ -331,7 +382,10 @@ __global__ void __launch_bounds__(kTgThreads, 1)
 }
 
 // One tf32-pair split per job: fp32 [batch][rows][cols] -> hi, lo in the same
-// orientation or transposed, through a padded 32 x 32 shared-memory tile.
+// orientation or transposed, through padded 32 x 32 shared-memory tiles.  A
+// block takes kSplitTiles tiles side by side along the columns (32 rows x 128
+// columns) and issues all their loads before any store, so each thread keeps
+// sixteen loads in flight instead of four.
 struct SplitJob {
   const float* src;
   float* hi;
@@ -340,41 +394,52 @@ struct SplitJob {
   int ld_src, ld_dst, rows, cols, transpose;
 };
 constexpr int kMaxSplitJobs = 8;
+constexpr int kSplitTiles = 4;
 struct SplitJobs {
   SplitJob j[kMaxSplitJobs];
 };
 
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitJobs jobs,
                                                     int batch) {
-  __shared__ float t[32][33];
+  __shared__ float t[kSplitTiles][32][33];
   const SplitJob& J = jobs.j[blockIdx.z / batch];
-  const int b = blockIdx.z % batch, r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  if (r0 >= J.rows || c0 >= J.cols) return;  // this job is smaller than the grid
+  const int b = blockIdx.z % batch, r0 = blockIdx.y * 32;
+  const int cb = blockIdx.x * 32 * kSplitTiles;
+  if (r0 >= J.rows || cb >= J.cols) return;  // this job is smaller than the grid
   const float* s = J.src + b * J.stride_src;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int rr = r0 + r, cc = c0 + threadIdx.x;
-    t[r][threadIdx.x] =
-        (rr < J.rows && cc < J.cols) ? s[static_cast<size_t>(rr) * J.ld_src + cc] : 0.f;
+#pragma unroll
+  for (int q = 0; q < kSplitTiles; ++q) {
+#pragma unroll
+    for (int r = threadIdx.y; r < 32; r += 8) {
+      const int rr = r0 + r, cc = cb + 32 * q + threadIdx.x;
+      t[q][r][threadIdx.x] =
+          (rr < J.rows && cc < J.cols) ? s[static_cast<size_t>(rr) * J.ld_src + cc] : 0.f;
+    }
   }
   __syncthreads();
   float* h = J.hi + b * J.stride_dst;
   float* l = J.lo ? J.lo + b * J.stride_dst : nullptr;  // null: hi parts only
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    if (!J.transpose) {
-      const int rr = r0 + r, cc = c0 + threadIdx.x;
-      if (rr < J.rows && cc < J.cols) {
-        const float x = t[r][threadIdx.x];
-        const float xh = round_tf32(x);
-        h[static_cast<size_t>(rr) * J.ld_dst + cc] = xh;
-        if (l) l[static_cast<size_t>(rr) * J.ld_dst + cc] = round_tf32(x - xh);
-      }
-    } else {
-      const int cc = c0 + r, rr = r0 + threadIdx.x;  // output row = input column
-      if (rr < J.rows && cc < J.cols) {
-        const float x = t[threadIdx.x][r];
-        const float xh = round_tf32(x);
-        h[static_cast<size_t>(cc) * J.ld_dst + rr] = xh;
-        if (l) l[static_cast<size_t>(cc) * J.ld_dst + rr] = round_tf32(x - xh);
+#pragma unroll
+  for (int q = 0; q < kSplitTiles; ++q) {
+    const int c0 = cb + 32 * q;
+#pragma unroll
+    for (int r = threadIdx.y; r < 32; r += 8) {
+      if (!J.transpose) {
+        const int rr = r0 + r, cc = c0 + threadIdx.x;
+        if (rr < J.rows && cc < J.cols) {
+          const float x = t[q][r][threadIdx.x];
+          const float xh = round_tf32(x);
+          h[static_cast<size_t>(rr) * J.ld_dst + cc] = xh;
+          if (l) l[static_cast<size_t>(rr) * J.ld_dst + cc] = round_tf32(x - xh);
+        }
+      } else {
+        const int cc = c0 + r, rr = r0 + threadIdx.x;  // output row = input column
+        if (rr < J.rows && cc < J.cols) {
+          const float x = t[q][threadIdx.x][r];
+          const float xh = round_tf32(x);
+          h[static_cast<size_t>(cc) * J.ld_dst + rr] = xh;
+          if (l) l[static_cast<size_t>(cc) * J.ld_dst + rr] = round_tf32(x - xh);
+        }
       }
     }
   }
@@ -399,16 +464,18 @@ bool encode_maps(TgMaps* m, const TgemmArgs& a, const TgemmOperand& A, const Tge
 
 bool encode_outs(TgOutMaps* o, const TgemmArgs& a) {
   memset(o, 0, sizeof(*o));
-  auto enc = [&](CUtensorMap* m, float* p, int ld, long long stride) {
+  // [batch][rows][ld] with rows x cols valid: M x N, or N x M for the transposes
+  auto enc = [&](CUtensorMap* m, float* p, int ld, long long stride, bool t) {
     if (!p) return true;
     if ((ld & 3) || (stride & 3)) return false;
-    return encode_tiled_3d_f32(m, p, a.batch, a.M, a.N, ld, stride, 32, 32);
+    return encode_tiled_3d_f32(m, p, a.batch, t ? a.N : a.M, t ? a.M : a.N, ld, stride, 32,
+                               32);
   };
-  return enc(&o->out, a.out, a.out_ld, a.out_stride) &&
-         enc(&o->hi, a.out_hi, a.split_ld, a.split_stride) &&
-         enc(&o->lo, a.out_lo, a.split_ld, a.split_stride) &&
-         enc(&o->hi2, a.out2_hi, a.split_ld, a.split_stride) &&
-         enc(&o->lo2, a.out2_lo, a.split_ld, a.split_stride);
+  return enc(&o->out, a.out, a.out_ld, a.out_stride, false) &&
+         enc(&o->hi, a.out_hi, a.split_ld, a.split_stride, false) &&
+         enc(&o->lo, a.out_lo, a.split_ld, a.split_stride, false) &&
+         enc(&o->vt, a.vt_hi, a.t_ld, a.t_stride, true) &&
+         enc(&o->pt, a.pt_hi, a.t_ld, a.t_stride, true);
 }
 
 template <bool kDual, bool kPair>
@@ -417,7 +484,8 @@ cudaError_t run_tgemm(const TgemmArgs& a, const TgMaps& m0, const TgMaps& m1, ui
   alignas(64) TgOutMaps om;
   if (!encode_outs(&om, a)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tgemm_kernel<kDual, kPair>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kTgSmem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TgPlan<kPair>::kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -425,7 +493,8 @@ cudaError_t run_tgemm(const TgemmArgs& a, const TgMaps& m0, const TgMaps& m1, ui
   const long long ntiles = static_cast<long long>(a.batch) * ((a.M + kTM - 1) / kTM) *
                            ((a.N + kTN - 1) / kTN);
   const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
-  tgemm_kernel<kDual, kPair><<<grid, kTgThreads, kTgSmem, s>>>(m0, m1, om, a, status);
+  tgemm_kernel<kDual, kPair><<<grid, TgPlan<kPair>::kThreads, TgPlan<kPair>::kSmem, s>>>(
+      m0, m1, om, a, status);
   return cudaGetLastError();
 }
 
@@ -446,7 +515,7 @@ cudaError_t launch_tgemm_dual(const TgemmArgs& a, const TgemmOperand& A, const T
                               const TgemmOperand& A2, const TgemmOperand& B2, uint32_t* status,
                               cudaStream_t s) {
   if (a.batch <= 0 || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaSuccess;
-  if (a.mode != kTgAttnBwdRow && a.mode != kTgAttnBwdCol) return cudaErrorInvalidValue;
+  if (a.mode != kTgAttnBwd) return cudaErrorInvalidValue;
   const bool pair = A.lo != nullptr;
   alignas(64) TgMaps m0, m1;
   if (!encode_maps(&m0, a, A, B, pair) || !encode_maps(&m1, a, A2, B2, pair))
@@ -475,7 +544,8 @@ cudaError_t launch_split_tf32(const SplitSpec* specs, int n, int batch, cudaStre
     max_c = p.cols > max_c ? p.cols : max_c;
   }
   if (max_r <= 0 || max_c <= 0) return cudaSuccess;
-  const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, batch * n);
+  const int strip = 32 * kSplitTiles;
+  const dim3 grid((max_c + strip - 1) / strip, (max_r + 31) / 32, batch * n);
   split_kernel<<<grid, dim3(32, 8), 0, s>>>(jobs, batch);
   return cudaGetLastError();
 }

@@ -169,12 +169,11 @@ cudaError_t launch_fine_bwd(const Geom& g, const __half* q, const __half* k, con
 // tf32 pair hi + lo (fp32 arrays of tf32 values; hi = round(x), lo = round(x -
 // hi)), accumulated in fp32 from three tf32 products (tgemm.cu); with every lo
 // null, one plain tf32 product from the hi parts.  The attention-backward
-// modes compute a second product E = A2 B2^T of the same tile into a second
+// mode computes a second product E = A2 B2^T of the same tile into a second
 // accumulator.
 enum TgemmMode {
-  kTgScale = 0,      // v = alpha * D
-  kTgAttnBwdRow = 1, // p = exp2(alpha * D - beta * v1[m]),  v = p * (E - v2[m])
-  kTgAttnBwdCol = 2  // p = exp2(alpha * D - beta * v1[n]),  v = p * (E - v2[n]); out2 = p
+  kTgScale = 0,   // v = alpha * D
+  kTgAttnBwd = 1  // p = exp2(alpha * D - beta * v1[m]),  v = p * (E - v2[m])
 };
 struct TgemmOperand {
   const float* hi;
@@ -187,10 +186,12 @@ struct TgemmArgs {
   int mode;
   float alpha, beta;
   const float* v1; const float* v2; long long vec_stride;  // per-row or per-column vectors
-  // outputs, each optional: fp32 [M][N]; tf32 pair [M][N]; second tf32 pair
-  // [M][N] (a null lo writes the hi part alone)
+  // outputs, each optional: fp32 v [M][N]; v as a tf32 pair [M][N] (a null
+  // lo writes the hi part alone); the tf32 hi parts of v and p transposed,
+  // [N][M] (kTgAttnBwd)
   float* out; int out_ld; long long out_stride;
-  float *out_hi, *out_lo; float *out2_hi, *out2_lo; int split_ld; long long split_stride;
+  float *out_hi, *out_lo; int split_ld; long long split_stride;
+  float *vt_hi, *pt_hi; int t_ld; long long t_stride;
 };
 cudaError_t launch_tgemm(const TgemmArgs& a, const TgemmOperand& A, const TgemmOperand& B,
                          uint32_t* status, cudaStream_t s);

@@ -208,6 +208,22 @@ def coarse_select(cfg: Config, q, k, v, ws):
     return qc, kc, vc, oc, lse, idx, cnt
 
 
+def coarse_select_pooled(cfg: Config, qc, kc, vc, ws):
+    """fp32 cube means qc, kc, vc [B,heads,Nc,D] (e.g. from stage) -> (oc, lse_c, idx, cnt):
+    vsa_coarse_select with q, k, v NULL, so nothing is pooled again."""
+    B, Hd, nc, D = qc.shape
+    cap = cfg.topk if cfg.select_mode == SELECT_TOPK else cfg.kmax
+    f = dict(dtype=torch.float32, device=qc.device)
+    oc = torch.empty(B, Hd, nc, D, **f)
+    lse = torch.empty(B, Hd, nc, **f)
+    idx = torch.empty(B, Hd, nc, cap, dtype=torch.int32, device=qc.device)
+    cnt = torch.empty(B, Hd, nc, dtype=torch.int32, device=qc.device)
+    check(lib().vsa_coarse_select(ctypes.byref(cfg), None, None, None, _ptr(qc), _ptr(kc),
+                                  _ptr(vc), _ptr(oc), _ptr(lse), _ptr(idx), _ptr(cnt), _ptr(ws),
+                                  _stream()), "vsa_coarse_select")
+    return oc, lse, idx, cnt
+
+
 def fine_fwd(cfg: Config, q16, k16, v16, idx, cnt, gc, gf, oc, ws, want_saved=True):
     """Staged fp16 cube-order q, k, v; caller-layout bf16 gates -> (o, o_f, lse_f)."""
     q, k, v = q16, k16, v16
