@@ -46,6 +46,14 @@ __device__ __forceinline__ void argmax_pair(float& v, int& j) {
   }
 }
 
+// exp(v - m) of the softmax sums and A_c, as 2^((v - m) log2 e) on the
+// hardware exponential (about 2 ulp; A_c is then rounded to tf32, 2^-11).
+// Both selection kernels use it, in the same summation order, so their A_c
+// and lse_c agree bit for bit.  (The mass rule's running sum keeps expf.)
+__device__ __forceinline__ float softmax_term(float v, float m) {
+  return ex2_approx((v - m) * 1.4426950408889634f);
+}
+
 struct SelectArgs {
   int mode, topk, kmin, kmax;
   float mass;
@@ -78,12 +86,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Geom g, SelectArgs 
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   float z = 0.f;
-  for (int j = lane; j < Nc; j += 32) z += expf(Lsm[j] - m);
+  for (int j = lane; j < Nc; j += 32) z += softmax_term(Lsm[j], m);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
   const float inv = 1.f / z;
   for (int j = lane; j < Nc; j += 32) {  // A_c row
-    ach[arow + j] = round_tf32(expf(Lsm[j] - m) * inv);
+    ach[arow + j] = round_tf32(softmax_term(Lsm[j], m) * inv);
   }
   if (lane == 0) lse_c[static_cast<size_t>(bh) * Nc + row] = m + logf(z);
   __syncwarp();
@@ -176,7 +184,7 @@ __device__ __forceinline__ void select_row(const Geom& g, const SelectArgs& sa,
   int nvalid = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    key[i] = 32 * i + lane < Nc ? order_key(v[i]) : 0u;
+    key[i] = order_key(v[i]);  // 0 past the row (v = -inf there)
     if (key[i]) {
       kmin_l = min(kmin_l, key[i]);
       k2_l = max(k2_l, min(kmax_l, key[i]));
@@ -368,13 +376,13 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectA
   if (row >= Nc) return;
   const size_t arow = (static_cast<size_t>(bh) * Nc + row) * ldc;
   const float* Lg = logits + arow;
-  float v[kPer];
+  float v[kPer];  // -inf past the row: no term in the max, exp gives 0, order key 0
   float m = -FLT_MAX;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int j = 32 * i + lane;
     v[i] = j < Nc ? Lg[j] : -INFINITY;
-    if (j < Nc) m = fmaxf(m, v[i]);
+    m = fmaxf(m, v[i]);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(kSelThreads) select_reg_kernel(Geom g, SelectA
   float z = 0.f;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    e[i] = 32 * i + lane < Nc ? expf(v[i] - m) : 0.f;
+    e[i] = softmax_term(v[i], m);
     z += e[i];
   }
 #pragma unroll
