@@ -20,6 +20,16 @@ def _random_lists(rng, bh, nc, cap):
     return idx, cnt
 
 
+def _hand_out(seq, grid):
+    """Positions in order, each to the CTA with the least work so far (lowest
+    index on ties), by a linear scan."""
+    work = [0] * grid
+    for w in seq:
+        c = min(range(grid), key=lambda k: (work[k], k))
+        work[c] += w
+    return work
+
+
 def _brute(idx, cnt, sms):
     bh, nc, _ = idx.shape
     lists = [[set(idx[b, i, : cnt[b, i]].tolist()) for i in range(nc)] for b in range(bh)]
@@ -34,14 +44,9 @@ def _brute(idx, cnt, sms):
                     u |= L[b][2 * p + 1]
                 steps.append(math.ceil(len(u) / 2))
         grid = min(len(steps), sms)
-        # schedule: largest first; full rounds of `grid` positions alternate direction
+        # schedule: largest first (item order on ties), handed out to free CTAs
         order = sorted(range(len(steps)), key=lambda i: (-steps[i], i))
-        rounds = [order[r:r + grid] for r in range(0, len(order), grid)]
-        seq = []
-        for r, chunk in enumerate(rounds):
-            seq += chunk[::-1] if (r % 2 and len(chunk) == grid) else chunk
-        work = [sum(steps[seq[k]] for k in range(c, len(seq), grid)) for c in range(grid)]
-        res[name] = (steps, work)
+        res[name] = (steps, _hand_out([steps[i] for i in order], grid))
     return res
 
 
@@ -54,7 +59,9 @@ def test_item_steps_and_cta_work_match_set_recomputation():
         ref = _brute(idx, cnt, sms)
         for name in ("fine_fwd", "fine_bwd_dkdv"):
             assert steps[name].tolist() == ref[name][0]
-            assert schedule.cta_work(steps[name], sms).tolist() == ref[name][1]
+            grid = min(steps[name].size, sms)
+            order = schedule.schedule_order(steps[name])
+            assert schedule.cta_work(steps[name], grid, order).tolist() == ref[name][1]
         assert steps["fine_bwd_dq"].tolist() == ref["fine_fwd"][0]
 
 
@@ -73,15 +80,28 @@ def test_load_balance_report():
     assert r["count_histogram"] == {1: 3, 4: 1}
 
 
-def test_snake_schedule_balances_sorted_items():
-    # 8 items on 4 CTAs: sorted 8,7,6,5 | 4,3,2,1 -> CTA totals 9,9,9,9
+def test_counter_hands_positions_to_the_first_free_cta():
+    # 8 items on 4 CTAs, largest first: 8,7,6,5 then 4 -> the CTA at 5, 3 -> at 6,
+    # 2 -> at 7, 1 -> at 8: totals 9,9,9,9
     steps = np.array([1, 8, 2, 7, 3, 6, 4, 5])
-    assert schedule.cta_work(steps, 4).tolist() == [9, 9, 9, 9]
-    order = schedule.schedule_order(steps, 4)
-    assert sorted(order.tolist()) == list(range(8))
-    assert steps[order].tolist() == [8, 7, 6, 5, 1, 2, 3, 4]
-    # plain item order: CTA c takes items c and c + 4
-    assert schedule.cta_work(steps, 4, scheduled=False).tolist() == [4, 14, 6, 12]
+    order = schedule.schedule_order(steps)
+    assert steps[order].tolist() == [8, 7, 6, 5, 4, 3, 2, 1]
+    assert schedule.cta_work(steps, 4, order).tolist() == [9, 9, 9, 9]
+    # item order: 1,8,2,7 start; 3 -> CTA 0 (at 1), 6 -> CTA 2 (at 2), 4 -> CTA 0
+    # (at 4), 5 -> CTA 3 (at 7)
+    assert schedule.cta_work(steps, 4).tolist() == [8, 8, 8, 12]
+    # the static assignment: CTA c takes positions c and c + 4
+    assert schedule.cta_work_static(steps, 4).tolist() == [4, 14, 6, 12]
+    assert schedule.cta_work_static(steps, 4, order).tolist() == [12, 10, 8, 6]
+    # list scheduling: no CTA ends later than the mean plus the largest item
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        st = rng.integers(1, 40, size=int(rng.integers(1, 400)))
+        for grid in (1, 7, 152):
+            w = schedule.cta_work(st, grid)
+            g = min(grid, st.size)
+            assert w.sum() == st.sum() and w.size == g
+            assert w.max() <= st.sum() / g + st.max()
 
 
 def test_head_dim_64_forward_runs_two_ctas_per_sm_with_one_key_tile_per_step():
@@ -97,13 +117,12 @@ def test_head_dim_64_forward_runs_two_ctas_per_sm_with_one_key_tile_per_step():
     assert r["fine_bwd_dq"]["ctas"] == 1 and r["fine_bwd_dq"]["steps_total"] == 3
     assert schedule.kernel_grid("fine_fwd", 1000, 152, 64) == 304
     assert schedule.kernel_grid("fine_fwd", 1000, 152, 128) == 152
-    # 8 items, 2 SMs: the schedule deals rounds of 2 positions by the two-tile cost,
-    # the kernel's 4 CTAs take positions c, c + 4
+    # 8 items, 2 SMs: the kernel's 4 CTAs take positions from the counter
     steps = np.array([1, 8, 2, 7, 3, 6, 4, 5])
-    order = schedule.schedule_order(steps, 2)
-    seq = steps[order]
-    want = [int(seq[c::4].sum()) for c in range(4)]
-    assert schedule.cta_work(steps, 2, grid=4).tolist() == want
+    order = schedule.schedule_order(steps)
+    grid = schedule.kernel_grid("fine_fwd", steps.size, 2, 64)
+    assert grid == 4
+    assert schedule.cta_work(steps, grid, order).tolist() == _hand_out(steps[order].tolist(), 4)
 
 
 def test_two_ctas_per_sm_report_the_pairs_of_ctas_that_share_an_sm():

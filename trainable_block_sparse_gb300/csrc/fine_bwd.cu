@@ -50,6 +50,7 @@
 // Warps 12-15: epilogue.  Registers are split per warpgroup: 168 a thread for
 // the softmax warps, 88 for the rest.
 // Bounded waits and the abort path are as in the forward kernel.
+#include "item_seq.cuh"
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
 
@@ -58,8 +59,11 @@ namespace {
 
 constexpr int kThreadsBwd = 512;  // 16 warps
 constexpr int kSoftmaxWarpsBwd = 8;
-constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpLoadX = 10, kWarpEpi0 = 12;
+constexpr int kWarpLoadY = 8, kWarpIssue = 9, kWarpLoadX = 10, kWarpEpi0 = 12;  // 11: fetcher
 constexpr int kEpiWarps = 4;
+// readers of the item sequence: Y and X producer threads, UMMA warp, softmax
+// and epilogue warps
+constexpr int kSeqReadersBwd = 3 + kSoftmaxWarpsBwd + kEpiWarps;
 // register split: the launch gives 65536 / 512 = 128 a thread
 constexpr int kRegsSoftmax = 168, kRegsRest = 88;
 static_assert(256 * kRegsSoftmax + 256 * kRegsRest <= 65536, "split exceeds the launch's registers");
@@ -91,6 +95,7 @@ struct BwdBars {
   uint64_t a_ready, x_free;  // dQ pass: the item's Q, dO copied from X into TMEM
   uint64_t x_empty;          // key-major pass: the item's last S^T and dP^T are done
   uint64_t dv_free, dk_free; // key-major pass: the epilogue has read dV / dK
+  ItemSeq seq;
   uint32_t tmem_base;
   int abort;
 };
@@ -110,6 +115,7 @@ struct BwdParams {
                         // bf16 (g.grad_bf16)
   void* out2;           // dK (key-major pass)
   uint32_t* status;
+  int* sched;           // schedule counter, zero at launch
 };
 
 __device__ __forceinline__ void warp_arrive_bwd(uint64_t* bar) {
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_init(&sb.dv_free, kEpiWarps);
     mbar_init(&sb.dk_free, kEpiWarps);
     mbar_init(&sb.final_mma, 1);
+    seq_init(sb.seq, kSeqReadersBwd);
     sb.abort = 0;
     fence_barrier_init();
   }
@@ -261,9 +268,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       tma_prefetch_desc(&ty1);
       tma_prefetch_desc(&ty2);
       uint32_t n1 = 0, n2 = 0;  // steps whose Y1 / Y2 copies were issued
+      uint32_t sq = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-           item += gridDim.x) {
+      while (ok) {
+        const int item = seq_next<false>(sb.seq, sq, abort_flag, P.status);
+        if (item < 0 || is_aborted(abort_flag)) break;
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
@@ -368,10 +377,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       return true;
     };
     uint32_t step = 0;  // global index of the current item's first step
+    uint32_t sq = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-         item += gridDim.x) {
+    while (ok) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (item < 0 || is_aborted(abort_flag)) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
@@ -458,7 +469,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
       };
       int it = 0;
-      for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
+      uint32_t sq = 0;
+      for (;;) {
+        const int item = seq_next<false>(sb.seq, sq, abort_flag, P.status);
+        if (item < 0 || is_aborted(abort_flag)) break;
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         // X of the previous item is no longer read: key-major, its last S^T
@@ -517,8 +531,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       warp_arrive_bwd(&sb.x_free);
       return true;
     };
-    for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-         item += gridDim.x) {
+    uint32_t sq = 0;
+    bool x_in_tmem = false;  // dQ pass: this item's Q and dO are already in TMEM
+    while (ok) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (item < 0 || is_aborted(abort_flag)) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       const int cube = half ? pi.b : pi.a;
       const bool row_live = half == 0 || pi.b >= 0;
@@ -534,9 +551,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         continue;
       }
       const uint32_t* list = P.lists + pi.off;
-      // dQ pass: the first item's Q and dO go to TMEM here, later items' at the
-      // end of the item before them
-      if (!kKeyMajor && it == 0 && !copy_x_to_tmem(0)) break;
+      // dQ pass: an item's Q and dO go to TMEM at the end of the item before it
+      // (below), or here if that item did not see it coming
+      if (!kKeyMajor && !x_in_tmem && !copy_x_to_tmem(it)) break;
+      x_in_tmem = false;
       float row_lse = 0.f, row_delta = 0.f;
       if (!kKeyMajor && row_live) {
         const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + (row & 63);
@@ -645,10 +663,22 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       if (!kKeyMajor) {
         // every S and dP product of this item is complete (phase 2 of its last
         // step saw its dP): the next item's Q and dO may replace these in TMEM,
-        // so its first products run while the epilogue warps drain dQ
-        int nx = item + gridDim.x;
-        while (nx < P.n_items && P.items[P.order ? P.order[nx] : nx].count == 0) nx += gridDim.x;
-        if (nx < P.n_items && !copy_x_to_tmem(it + 1)) break;
+        // so its first products run while the epilogue warps drain dQ.  The
+        // next item with work is looked up in the sequence without reading
+        // it off, a few entries ahead at most.
+        int nx = kSeqEnd;
+        for (int a = 0; a <= kSeqSlots - 2; ++a) {
+          const int p = seq_peek(sb.seq, sq, a, abort_flag, P.status);
+          if (p < 0 || P.items[P.order ? P.order[p] : p].count > 0) {
+            nx = p;
+            break;
+          }
+        }
+        if (nx == kSeqAbort) break;
+        if (nx >= 0) {
+          if (!copy_x_to_tmem(it + 1)) break;
+          x_in_tmem = true;
+        }
       }
       ++it;
     }
@@ -659,7 +689,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     const bool second = quarter >= 2;  // rows 64..127: the item's second cube
     const uint32_t tq = tb + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0;
-    for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag); item += gridDim.x) {
+    uint32_t sq = 0;
+    for (;;) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (item < 0 || is_aborted(abort_flag)) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;  // the softmax warps write its pooled rows
       const int cube = second ? pi.b : pi.a;
@@ -706,8 +739,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       ++it;
     }
   } else {
-    // warp 11: no role; completes warpgroup 2's register split
+    // ===================================================== item fetcher
+    // (warp 11; its register share completes warpgroup 2's split)
     regs_dec<kRegsRest>();
+    if (lane == 0) seq_fetch(sb.seq, P.sched, P.n_items, abort_flag, P.status);
   }
 
   tc_fence_before();
@@ -738,6 +773,7 @@ cudaError_t run_bwd(const Geom& g, const void* x1, const void* x2, const void* y
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
+  if ((e = cudaMemsetAsync(p.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
   kern<<<grid, kThreadsBwd, smem, s>>>(m1, m2, m3, m4, p);
   return cudaGetLastError();
 }
@@ -749,11 +785,11 @@ cudaError_t bwd_impl(const Geom& g, const __half* q, const __half* k, const __ha
                      void* dq, void* dk, void* dv, const Workspace& ws, cudaStream_t s) {
   const bool ordered = use_cost_order(g);
   BwdParams pq{g, ws.qpairs, ws.qlist, ws.n_qpairs, ordered ? ws.qorder : nullptr, lse_f, delta,
-               gscale, dqc, nullptr, dq, nullptr, ws.status};
+               gscale, dqc, nullptr, dq, nullptr, ws.status, ws.counter + kCounterBwdQ};
   cudaError_t e = run_bwd<D, false>(g, q, dof, k, v, pq, s);
   if (e != cudaSuccess) return e;
   BwdParams pk{g, ws.kpairs, ws.klist, ws.n_kpairs, ordered ? ws.korder : nullptr, lse_f, delta,
-               gscale, dvc, dkc, dv, dk, ws.status};
+               gscale, dvc, dkc, dv, dk, ws.status, ws.counter + kCounterBwdK};
   return run_bwd<D, true>(g, k, v, q, dof, pk, s);
 }
 

@@ -60,6 +60,7 @@
 #include <cfloat>
 #include <cstring>
 
+#include "item_seq.cuh"
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
 
@@ -68,7 +69,10 @@ namespace {
 
 constexpr int kThreadsFwd = 512;           // 16 warps
 constexpr int kSoftmaxWarps = 8, kEpiWarps = 4;
-constexpr int kWarpEpi = 8, kWarpK = 12, kWarpMma = 13, kWarpV = 14;
+constexpr int kWarpEpi = 8, kWarpK = 12, kWarpMma = 13, kWarpV = 14, kWarpSeq = 15;
+// readers of the item sequence: K and V producer threads, UMMA warp, softmax
+// and epilogue warps
+constexpr int kSeqReaders = 3 + kSoftmaxWarps + kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;              // S (128 columns)
 constexpr uint32_t kColP = 128;            // P buffers (fp16 pairs) at columns 128 and 192
@@ -104,6 +108,7 @@ struct FwdBars {
   uint64_t o_full[2], o_free[2];
   uint64_t st_full[2], st_free[2];
   uint64_t final_mma;
+  ItemSeq seq;
   uint32_t tmem_base;
   int abort;
   float red[2][2][128];    // [step parity][row half]: the half-row maxima of a step
@@ -125,6 +130,7 @@ struct FwdParams {
   float* lse_f;
   uint32_t* status;
   const float* scales;    // e4m3 variant: [BH][3] factors of the Q, K, V copies
+  int* sched;             // schedule counter, zero at launch
 };
 
 // Arrival of a whole warp counted once: lanes finish their own work first.
@@ -207,6 +213,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     mbar_init(&sb.s_full, 1);
     mbar_init(&sb.s_read, kSoftmaxWarps);  // one arrival per softmax warp
     mbar_init(&sb.final_mma, 1);
+    seq_init(sb.seq, kSeqReaders);
     sb.abort = 0;
     fence_barrier_init();
   }
@@ -245,10 +252,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           tma_load_2d(dst, m, c * 64, bh * g.N + cube * kTile, bar);
         }
       };
-      uint32_t step = 0;
+      uint32_t step = 0, sq = 0;
       int it = 0;  // items with work seen by this CTA
-      for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag);
-           item += gridDim.x) {
+      for (;;) {
+        const int item = seq_next<false>(sb.seq, sq, abort_flag, P.status);
+        if (item < 0 || is_aborted(abort_flag)) break;
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
@@ -357,10 +365,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     };
 
     uint32_t step = 0;  // global index of the current item's first step
+    uint32_t sq = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-         item += gridDim.x) {
+    while (ok) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (item < 0 || is_aborted(abort_flag)) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
@@ -404,12 +414,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const uint32_t mybit = (row >> 6) ? kSelB : kSelA;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = g.scale * 1.4426950408889634f;  // scale * log2(e)
-    uint32_t step = 0;
+    uint32_t step = 0, sq = 0;
     int it = 0;
     bool ok = true;
     // No abort test in the loop condition: both warps of a pair must walk the
     // same items and leave together (see pair_sync_or).
-    for (int item = blockIdx.x; item < P.n_items && ok; item += gridDim.x) {
+    while (ok) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (pair_sync_or(quarter, item == kSeqAbort) || item < 0) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const uint32_t* list = P.lists + pi.off;
@@ -560,9 +572,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const bool leader = threadIdx.x == kWarpEpi * 32;
     const bool stage_of = kOp == kOpF16 && P.o_f != nullptr;
     int it = 0;
+    uint32_t sq = 0;
     // No abort test in the loop condition: the four warps meet at named
     // barriers and must walk the same items (see epi_sync_or).
-    for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
+    for (;;) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (epi_sync_or(item == kSeqAbort) || item < 0) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int obuf = it & 1;
@@ -669,6 +684,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       ++it;
     }
     if (leader) bulk_wait_group0();  // O_f stores complete before the CTA exits
+  } else if (warp == kWarpSeq) {
+    // ===================================================== item fetcher
+    if (lane == 0) seq_fetch(sb.seq, P.sched, P.n_items, abort_flag, P.status);
   }
 
   tc_fence_before();
@@ -694,6 +712,7 @@ cudaError_t run_fwd(const Geom& g, const __half* q, const __half* k, const __hal
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
+  if ((e = cudaMemsetAsync(p.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
   fine_fwd_kernel<D, kOpF16><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
@@ -719,6 +738,7 @@ cudaError_t run_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __nv_bfloa
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
+  if ((e = cudaMemsetAsync(p.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
   fine_fwd_kernel<D, kOpBF16><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
@@ -743,6 +763,7 @@ cudaError_t run_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t* k8, con
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(p.n_items);
   if (grid <= 0) return cudaSuccess;
+  if ((e = cudaMemsetAsync(p.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
   fine_fwd_kernel<D, kOpE4M3><<<grid, kThreadsFwd, smem, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
@@ -754,7 +775,7 @@ cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, con
                             __nv_bfloat16* o, __half* o_f, float* lse_f, const Workspace& ws,
                             cudaStream_t s) {
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
-              gc, gf, oc, o, o_f, lse_f, ws.status, nullptr};
+              gc, gf, oc, o, o_f, lse_f, ws.status, nullptr, ws.counter + kCounterFwd};
   if (g.D == 64) return launch_fine_fwd64(g, q, k, v, gc, gf, oc, o, o_f, lse_f, ws, s);
   return run_fwd<128>(g, q, k, v, p, s);
 }
@@ -764,7 +785,7 @@ cudaError_t launch_fine_fwd_bf16(const Geom& g, const __nv_bfloat16* q, const __
                                  const __nv_bfloat16* gf, const float* oc, __nv_bfloat16* o,
                                  float* lse_f, const Workspace& ws, cudaStream_t s) {
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
-              gc, gf, oc, o, nullptr, lse_f, ws.status, nullptr};
+              gc, gf, oc, o, nullptr, lse_f, ws.status, nullptr, ws.counter + kCounterFwd};
   if (g.D == 64) return launch_fine_fwd64_bf16(g, q, k, v, gc, gf, oc, o, lse_f, ws, s);
   return run_fwd_bf16<128>(g, q, k, v, p, s);
 }
@@ -776,7 +797,7 @@ cudaError_t launch_fine_fwd_fp8(const Geom& g, const uint8_t* q8, const uint8_t*
                                 cudaStream_t s) {
   if (g.D != 128) return cudaErrorInvalidValue;
   FwdParams p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
-              gc, gf, oc, o, nullptr, lse_f, ws.status, scales};
+              gc, gf, oc, o, nullptr, lse_f, ws.status, scales, ws.counter + kCounterFwd};
   return run_fwd_fp8(g, q8, k8, v8t, p, s);
 }
 

@@ -43,6 +43,7 @@
 #include <cfloat>
 #include <cstring>
 
+#include "item_seq.cuh"
 #include "umma_pipe.cuh"
 #include "vsa_common.cuh"
 
@@ -51,7 +52,10 @@ namespace {
 
 constexpr int kD = 64;
 constexpr int kThreads64 = 384;  // 12 warps
-constexpr int kWarpEpi64 = 4, kWarpK64 = 8, kWarpV64 = 9, kWarpMma64 = 10;
+constexpr int kWarpEpi64 = 4, kWarpK64 = 8, kWarpV64 = 9, kWarpMma64 = 10;  // 11: item fetcher
+// readers of the item sequence: K and V producer threads, UMMA warp, 4
+// softmax and 4 epilogue warps
+constexpr int kSeqReaders64 = 11;
 constexpr uint32_t kCols64 = 256;
 constexpr uint32_t kColS64 = 0;    // two S buffers of 64 columns
 constexpr uint32_t kColP64 = 128;  // P: 64 keys as 32 columns of fp16 pairs
@@ -92,6 +96,7 @@ struct Bars64 {
   uint64_t o_full, o_free;        // the item's O complete / read by the epilogue
   uint64_t st_full, st_free;      // row statistics handed to / read by the epilogue
   uint64_t final_mma;
+  ItemSeq seq;
   uint32_t tmem_base;
   int abort;
   float l_fin[128], m_fin[128];
@@ -110,6 +115,7 @@ struct FwdParams64 {
   __half* o_f;
   float* lse_f;
   uint32_t* status;
+  int* sched;  // schedule counter, zero at launch
 };
 
 __device__ __forceinline__ void warp_arrive64(uint64_t* bar) {
@@ -174,6 +180,7 @@ __global__ void __launch_bounds__(kThreads64, 2)
     mbar_init(&sb.st_full, 4);
     mbar_init(&sb.st_free, 4);
     mbar_init(&sb.final_mma, 1);
+    seq_init(sb.seq, kSeqReaders64);
     sb.abort = 0;
     fence_barrier_init();
   }
@@ -210,10 +217,11 @@ __global__ void __launch_bounds__(kThreads64, 2)
           tma_load_2d(dst, m, 0, bh * g.N + cube * kTile, bar);
         }
       };
-      uint32_t step = 0;
+      uint32_t step = 0, sq = 0;
       int it = 0;
-      for (int item = blockIdx.x; item < P.n_items && !is_aborted(abort_flag);
-           item += gridDim.x) {
+      for (;;) {
+        const int item = seq_next<false>(sb.seq, sq, abort_flag, P.status);
+        if (item < 0 || is_aborted(abort_flag)) break;
         const PairItem pi = P.items[P.order ? P.order[item] : item];
         if (pi.count == 0) continue;
         const uint32_t* list = P.lists + pi.off;
@@ -277,11 +285,12 @@ __global__ void __launch_bounds__(kThreads64, 2)
       return true;
     };
 
-    uint32_t step = 0;
+    uint32_t step = 0, sq = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-         item += gridDim.x) {
+    while (ok) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (item < 0 || is_aborted(abort_flag)) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const int n = pi.count;
@@ -329,11 +338,12 @@ __global__ void __launch_bounds__(kThreads64, 2)
     const uint32_t tp = tb + lane_addr + kColP64;
     const uint32_t to = tb + lane_addr + kColO64;
     const float c = g.scale * 1.4426950408889634f;  // scale * log2(e)
-    uint32_t step = 0;
+    uint32_t step = 0, sq = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.n_items && ok && !is_aborted(abort_flag);
-         item += gridDim.x) {
+    while (ok) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (item < 0 || is_aborted(abort_flag)) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const uint32_t* list = P.lists + pi.off;
@@ -461,9 +471,12 @@ __global__ void __launch_bounds__(kThreads64, 2)
     const bool leader = threadIdx.x == kWarpEpi64 * 32;
     const bool stage_of = !kBF && P.o_f != nullptr;
     int it = 0;
+    uint32_t sq = 0;
     // No abort test in the loop condition: the four warps meet at named
     // barriers and walk the same items.
-    for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
+    for (;;) {
+      const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
+      if (epi_sync_or64(item == kSeqAbort) || item < 0) break;
       const PairItem pi = P.items[P.order ? P.order[item] : item];
       if (pi.count == 0) continue;
       const bool live = half == 0 || pi.b >= 0;  // warp-uniform
@@ -561,8 +574,10 @@ __global__ void __launch_bounds__(kThreads64, 2)
     }
     if (leader) bulk_wait_group0();  // O_f stores complete before the CTA exits
   } else {
-    // warp 11: no role; completes warpgroup 2's register split
+    // ===================================================== item fetcher
+    // (warp 11; its register share completes warpgroup 2's split)
     regs_dec<kRegsRest64>();
+    if (lane == 0) seq_fetch(sb.seq, P.sched, P.n_items, abort_flag, P.status);
   }
 
   tc_fence_before();
@@ -595,6 +610,7 @@ cudaError_t launch64(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   if (p.n_items <= 0) return cudaSuccess;
   const int sms = persistent_grid(1 << 30);  // min(n, SMs) of a huge n: the SM count
   const int grid = p.n_items < 2 * sms ? p.n_items : 2 * sms;
+  if ((e = cudaMemsetAsync(p.sched, 0, sizeof(int), s)) != cudaSuccess) return e;
   kern<<<grid, kThreads64, L64::kBytes, s>>>(mq, mk, mv, mof, p);
   return cudaGetLastError();
 }
@@ -607,7 +623,7 @@ cudaError_t launch_fine_fwd64(const Geom& g, const __half* q, const __half* k, c
                               cudaStream_t s) {
   if (g.D != kD) return cudaErrorInvalidValue;
   FwdParams64 p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
-                gc, gf, oc, o, o_f, lse_f, ws.status};
+                gc, gf, oc, o, o_f, lse_f, ws.status, ws.counter + kCounterFwd};
   alignas(64) CUtensorMap mq, mk, mv, mof;
   const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
   if (!encode_tiled_2d(&mq, q, rows, kD, 64, 64) || !encode_tiled_2d(&mk, k, rows, kD, 64, 64) ||
@@ -625,7 +641,7 @@ cudaError_t launch_fine_fwd64_bf16(const Geom& g, const __nv_bfloat16* q,
                                    const Workspace& ws, cudaStream_t s) {
   if (g.D != kD) return cudaErrorInvalidValue;
   FwdParams64 p{g, ws.qpairs, ws.qlist, ws.n_qpairs, use_cost_order(g) ? ws.qorder : nullptr,
-                gc, gf, oc, o, nullptr, lse_f, ws.status};
+                gc, gf, oc, o, nullptr, lse_f, ws.status, ws.counter + kCounterFwd};
   alignas(64) CUtensorMap mq, mk, mv, mof;
   const uint64_t rows = static_cast<uint64_t>(g.BH) * g.N;
   const bool ok = g.raster ? (encode_raster_cubes_bf16(&mq, q, g) &&

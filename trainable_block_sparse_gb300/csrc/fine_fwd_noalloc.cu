@@ -72,7 +72,8 @@ extern "C" vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void
   Geom g;
   const vsa_status_t st = make_geom(cfg, &g);
   if (st != VSA_OK) return st;
-  // scratch: status word | pair items | union lists (2 * capacity entries per pair)
+  // scratch: status word, schedule counters (in the first 256 bytes) | pair
+  // items | union lists (2 * capacity entries per pair)
   const size_t npairs = static_cast<size_t>(g.BH) * ((g.Nc + 1) / 2);
   const size_t items_off = 256;
   const size_t lists_off = items_off + round256(sizeof(PairItem) * npairs);
@@ -88,6 +89,7 @@ extern "C" vsa_status_t vsa_fine_fwd_noalloc(const vsa_config_t* cfg, const void
   char* b = static_cast<char*>(base);
   Workspace w{};
   w.status = reinterpret_cast<uint32_t*>(b);
+  w.counter = reinterpret_cast<int*>(b + 64);
   w.qpairs = reinterpret_cast<PairItem*>(b + items_off);
   w.qlist = reinterpret_cast<uint32_t*>(b + lists_off);
   w.n_qpairs = static_cast<int>(npairs);

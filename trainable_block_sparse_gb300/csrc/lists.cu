@@ -226,22 +226,14 @@ __global__ void order_scan_kernel(int* hist) {
   }
 }
 
-// Items into their buckets (order within a bucket is arbitrary: it only
-// decides which CTA runs an item, never what the item computes).
+// Items into their buckets, largest first (order within a bucket is
+// arbitrary: it only decides which CTA runs an item, never what the item
+// computes).  The kernels' CTAs take positions from a shared counter as they
+// free up, so largest-first is the longest-processing-time rule.
 __global__ void order_scatter_kernel(const PairItem* __restrict__ items, int n, int* cursor,
                                      int* sorted) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) sorted[atomicAdd(&cursor[order_key(items[i])], 1)] = i;
-}
-
-// Position k of a kernel whose CTA c takes positions c, c + grid, ...: full
-// rounds of `grid` positions alternate direction.
-__global__ void order_snake_kernel(const int* __restrict__ sorted, int n, int grid, int* order) {
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k >= n) return;
-  const int r = k / grid, c = k % grid, base = r * grid;
-  const int src = ((r & 1) && base + grid <= n) ? base + grid - 1 - c : k;
-  order[k] = sorted[src];
 }
 
 }  // namespace
@@ -256,15 +248,13 @@ int persistent_grid(int n) {
 cudaError_t launch_item_order(const PairItem* items, int n, int* order, int* tmp,
                               cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  int* sorted = tmp;
-  int* hist = tmp + n;
+  int* hist = tmp;
   cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int) * kOrderKeys, s);
   if (e != cudaSuccess) return e;
   const int blocks = (n + 255) / 256;
   order_count_kernel<<<blocks, 256, 0, s>>>(items, n, hist);
   order_scan_kernel<<<1, 32, 0, s>>>(hist);
-  order_scatter_kernel<<<blocks, 256, 0, s>>>(items, n, hist, sorted);
-  order_snake_kernel<<<blocks, 256, 0, s>>>(sorted, n, persistent_grid(n), order);
+  order_scatter_kernel<<<blocks, 256, 0, s>>>(items, n, hist, order);
   return cudaGetLastError();
 }
 

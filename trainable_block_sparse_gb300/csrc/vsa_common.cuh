@@ -66,9 +66,13 @@ struct PairItem {
 };
 
 // Pieces of the workspace, carved by the host (api.cu).
+// Schedule counters of the persistent fine kernels (Workspace::counter):
+// each launch takes item positions from its own counter, zeroed just before.
+enum { kCounterFwd = 0, kCounterBwdQ = 1, kCounterBwdK = 2 };
+
 struct Workspace {
   uint32_t* status;       // device status word
-  int* counter;           // scratch counters
+  int* counter;           // scratch counters (16)
   PairItem* qpairs;       // query-cube pairs
   uint32_t* qlist;        // [n_qpairs][2*cap] union lists
   int n_qpairs;
@@ -101,7 +105,7 @@ struct Workspace {
   // schedule orders of the pair items (null: item order); order scratch
   int* qorder;
   int* korder;
-  int* order_tmp;         // [n_items] sorted items, then histogram/cursors
+  int* order_tmp;         // histogram / bucket cursors of the order
 };
 
 // ------------------------------------------------------------------ launches
@@ -140,10 +144,10 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
                               cudaStream_t s);
 cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
-// Schedule order of n pair items for a persistent kernel of min(n, SMs) CTAs
-// that takes positions b, b + grid, ...: items sorted by step count
-// (largest first), each full round of `grid` positions dealt in alternating
-// direction (snake), so every CTA's total work is close to the mean.
+// Schedule order of n pair items: sorted by step count, largest first.  The
+// persistent kernels' CTAs take schedule positions from a shared counter as
+// they free up (item_seq.cuh), so this is the longest-processing-time rule:
+// every CTA's total work ends within about one small item of the others.
 cudaError_t launch_item_order(const PairItem* items, int n, int* order, int* tmp,
                               cudaStream_t s);
 // Grid of the persistent fine kernels for n items: min(n, SMs).

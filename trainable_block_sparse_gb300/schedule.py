@@ -2,12 +2,13 @@
 
 The fine forward kernel and both fine backward passes launch one CTA per SM
 (grid = min(items, SMs); the head_dim-64 forward two per SM, grid =
-min(items, 2 SMs)), and CTA b processes schedule positions b, b + grid,
-b + 2*grid, ....  The schedule sorts the items by step count, largest first,
-and deals each full round of SMs positions in alternating direction (snake
-order); the last, partial round keeps its order.  An item is a pair
-of neighbouring cubes (2p, 2p + 1) of one (batch, head), item index =
-bh * ceil(Nc / 2) + p:
+min(items, 2 SMs)).  A CTA takes the next schedule position from a counter
+shared by the launch whenever it has room for another item, so positions are
+handed out in schedule order to whichever CTA frees up first.  The schedule
+is the item order, or (when the K and V of all slices fit in twice the L2)
+the items sorted by step count, largest first: the longest-processing-time
+rule.  An item is a pair of neighbouring cubes (2p, 2p + 1) of one (batch,
+head), item index = bh * ceil(Nc / 2) + p:
 
   * forward and dQ pass: two query cubes walking the union of their index
     lists;
@@ -16,14 +17,18 @@ bh * ceil(Nc / 2) + p:
 
 Each step of an item covers two key (or query) tiles, so an item costs
 ceil(|union| / 2) steps (the schedule's cost); a step of the head_dim-64
-forward covers one key tile, so there an item takes |union| steps.  This module recomputes those costs from the index
-lists that the coarse stage emitted and reports how evenly the static
-assignment spreads them over the CTAs ("VSA: Faster Video Diffusion with
+forward covers one key tile, so there an item takes |union| steps.  This
+module recomputes those costs from the index lists that the coarse stage
+emitted and reports how evenly the assignment spreads them over the CTAs,
+modelling a step as the unit of time ("VSA: Faster Video Diffusion with
 Trainable Sparse Attention", §2: the fine stage attends only within the
 selected blocks, so per-cube work varies with the selection, most of all
-with the coarse-mass rule of the dynamic variant).
+with the coarse-mass rule of the dynamic variant).  For comparison it also
+gives the static assignment (CTA c taking positions c, c + grid, ...).
 """
 from __future__ import annotations
+
+import heapq
 
 import numpy as np
 
@@ -66,31 +71,39 @@ def kernel_grid(name: str, items: int, sms: int, head_dim: int) -> int:
     return min(items, per_sm * sms)
 
 
-def schedule_order(steps: np.ndarray, sms: int) -> np.ndarray:
-    """Item index at each schedule position (the kernels' item order)."""
-    n = steps.size
-    grid = min(n, sms)
-    order = np.argsort(-np.asarray(steps), kind="stable")
-    out = order.copy()
-    for r in range(n // grid if grid else 0):
-        if r & 1:
-            out[r * grid:(r + 1) * grid] = order[r * grid:(r + 1) * grid][::-1]
-    return out
+def schedule_order(cost: np.ndarray) -> np.ndarray:
+    """Item index at each schedule position when the items are cost-sorted:
+    largest first, ties in item order."""
+    return np.argsort(-np.asarray(cost), kind="stable")
 
 
-def cta_work(steps: np.ndarray, sms: int, scheduled: bool = True, grid: int | None = None,
-             cost: np.ndarray | None = None) -> np.ndarray:
-    """Total steps of each CTA: positions c, c + grid, ... of the schedule
-    (scheduled=True) or of plain item order.  The schedule is built from
-    `cost` (default: the steps) in rounds of min(n, sms) positions; `grid`
-    (default min(n, sms)) is the kernel's CTA count."""
+def cta_work(steps: np.ndarray, grid: int, order: np.ndarray | None = None) -> np.ndarray:
+    """Total steps of each of `grid` CTAs when positions are handed out, in
+    schedule order (`order`, default item order), to the CTA with the least
+    work so far (the lowest index on ties): the counter the kernels share."""
     steps = np.asarray(steps)
-    n = steps.size
-    grid = min(n, sms) if grid is None else grid
-    if grid == 0:
+    seq = steps if order is None else steps[np.asarray(order)]
+    grid = min(int(grid), seq.size)
+    if grid <= 0:
         return np.zeros(0, dtype=np.int64)
-    order_cost = steps if cost is None else np.asarray(cost)
-    seq = steps[schedule_order(order_cost, sms)] if scheduled else steps
+    heap = [(0, c) for c in range(grid)]
+    work = np.zeros(grid, dtype=np.int64)
+    for w in seq.tolist():
+        t, c = heapq.heappop(heap)
+        work[c] = t + w
+        heapq.heappush(heap, (t + w, c))
+    return work
+
+
+def cta_work_static(steps: np.ndarray, grid: int, order: np.ndarray | None = None) -> np.ndarray:
+    """Total steps of each CTA under the static assignment: CTA c takes
+    positions c, c + grid, ... of the schedule."""
+    steps = np.asarray(steps)
+    seq = steps if order is None else steps[np.asarray(order)]
+    n = seq.size
+    grid = min(int(grid), n)
+    if grid <= 0:
+        return np.zeros(0, dtype=np.int64)
     padded = np.zeros(-(-n // grid) * grid, dtype=np.int64)
     padded[:n] = seq
     return padded.reshape(-1, grid).sum(0)
@@ -115,25 +128,28 @@ def uses_cost_order(batch_heads: int, tokens: int, head_dim: int) -> bool:
 
 def load_balance(idx: np.ndarray, cnt: np.ndarray, sms: int, ordered: bool = True,
                  head_dim: int = 128) -> dict:
-    """max/mean per-CTA steps of each fine kernel (under the cost-sorted
-    schedule when `ordered`, else plain item order), the step count of the
+    """max/mean per-CTA steps of each fine kernel (positions handed out from
+    the shared counter in the cost-sorted schedule when `ordered`, else in
+    item order), the same for the static assignment, the step count of the
     biggest item, and the histogram of per-cube list lengths."""
     sel = selection_matrix(idx, cnt)
-    out = {"schedule": "cost-sorted snake" if ordered else "item order"}
+    out = {"schedule": "cost-sorted, largest first" if ordered else "item order",
+           "assignment": "shared counter: next position to the first free CTA"}
     all_steps = item_steps(sel, head_dim)
     cost = item_steps(sel)["fine_fwd"]  # the schedule's cost: two key tiles per step
     for name, steps in all_steps.items():
         grid = kernel_grid(name, steps.size, sms, head_dim)
         c = cost if name != "fine_bwd_dkdv" else steps
-        w = cta_work(steps, sms, scheduled=ordered, grid=grid, cost=c)
-        w_plain = cta_work(steps, sms, scheduled=False, grid=grid)
+        order = schedule_order(c) if ordered else None
+        w = cta_work(steps, grid, order)
+        w_static = cta_work_static(steps, grid, order)
         mean = float(w.mean()) if w.size else 0.0
         out[name] = {"items": int(steps.size), "ctas": int(w.size),
                      "steps_total": int(steps.sum()),
                      "cta_steps_max": int(w.max()) if w.size else 0,
                      "cta_steps_mean": mean,
                      "max_over_mean": float(w.max() / mean) if mean > 0 else 1.0,
-                     "max_over_mean_item_order": float(w_plain.max() / mean) if mean > 0 else 1.0,
+                     "max_over_mean_static": float(w_static.max() / mean) if mean > 0 else 1.0,
                      "item_steps_max": int(steps.max()) if steps.size else 0}
         if grid > sms:
             # two CTAs per SM: CTAs s and s + sms share SM s (the block
