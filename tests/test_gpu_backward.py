@@ -119,3 +119,24 @@ def test_empty_key_cubes_get_only_the_pooled_gradient():
         assert_close("dk", dk[0, 0, rows], rk)
         assert_close("dv", dv[0, 0, rows], rv)
         np.testing.assert_allclose(rk, np.repeat(hd.dkc[j][None] / 64, 64, 0), atol=1e-12)
+
+
+@pytest.mark.parametrize("name,heads", [("p720", 4), ("dynamic", None)])
+def test_repeated_layers_are_bitwise_identical(name, heads):
+    """The fine kernels' CTAs take items from a shared counter as they free up,
+    so which CTA runs an item changes from run to run; every item is computed
+    by one CTA alone, so the forward and backward outputs must not change."""
+    inp = gapped(name, heads=heads) if heads else gapped(name)
+    cfg = vsa.config_for(inp.wl)
+    t = cuda_inputs(inp)
+    runs = []
+    for _ in range(3):
+        bufs = vsa.Buffers(cfg, "cuda", with_backward=True)
+        o = vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, with_backward=True)
+        grads = vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs)
+        torch.cuda.synchronize()
+        assert bufs.device_status() == vsa.OK
+        runs.append([o.clone()] + [g.clone() for g in grads])
+    for later in runs[1:]:
+        for a, b in zip(runs[0], later):
+            assert torch.equal(a, b)
