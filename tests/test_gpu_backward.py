@@ -140,3 +140,34 @@ def test_repeated_layers_are_bitwise_identical(name, heads):
     for later in runs[1:]:
         for a, b in zip(runs[0], later):
             assert torch.equal(a, b)
+
+
+def test_layer_replays_from_a_cuda_graph():
+    """vsa_forward and vsa_backward captured into a CUDA graph (the backward's
+    list building forks to a second stream and joins back inside the capture)
+    replay to the eager results, bit for bit."""
+    inp = gapped("pretrain")
+    cfg = vsa.config_for(inp.wl)
+    t = cuda_inputs(inp)
+    bufs = vsa.Buffers(cfg, "cuda", with_backward=True)
+
+    def layer():
+        o = vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, with_backward=True)
+        return [o] + list(vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs))
+
+    eager = [x.clone() for x in layer()]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer()  # warm-up on the capture's stream
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        outs = layer()
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert bufs.device_status() == vsa.OK
+        for a, b in zip(eager, outs):
+            assert torch.equal(a, b)

@@ -163,6 +163,47 @@ size_t carve_ws(const Geom& g, int with_backward, void* base, Workspace* w) {
 
 vsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? VSA_OK : VSA_ERR_CUDA; }
 
+namespace {
+
+// A second stream per device for the backward's list building, which needs
+// only the saved selection and so runs beside the combine and coarse
+// backward kernels (latency-bound small kernels next to bandwidth-bound
+// ones).  Created on first use; each call forks to it and joins back with
+// events of its own, under a lock so that two host threads never interleave
+// their fork / join on it.
+constexpr int kMaxSideDevices = 64;
+std::mutex g_side_mutex;
+cudaStream_t g_side_stream[kMaxSideDevices] = {};
+
+cudaError_t side_stream(cudaStream_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxSideDevices) return cudaErrorInvalidDevice;
+  if (!g_side_stream[dev]) {
+    e = cudaStreamCreateWithFlags(&g_side_stream[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  *out = g_side_stream[dev];
+  return cudaSuccess;
+}
+
+// Events of one fork / join, destroyed when the call returns (the waits
+// already enqueued keep their effect).
+struct ForkJoin {
+  cudaEvent_t fork = nullptr, join = nullptr;
+  ~ForkJoin() {
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+  }
+  cudaError_t create() {
+    cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    return e != cudaSuccess ? e : cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+  }
+};
+
+}  // namespace
+
 template <typename... Ptrs>
 bool all_aligned(Ptrs... ps) {
   return (aligned16(ps) && ...);
@@ -561,6 +602,19 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
   const float* oc = reinterpret_cast<const float*>(sv + L.oc);
   const int* idx = reinterpret_cast<const int*>(sv + L.idx);
   const int* cnt = reinterpret_cast<const int*>(sv + L.cnt);
+  // The pair lists and the transposed lists (ws regions of their own) on the
+  // side stream, after everything already on `s`; `s` waits for them only
+  // before the fine backward.
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  cudaStream_t side = nullptr;
+  ForkJoin fj;
+  if (side_stream(&side) != cudaSuccess || fj.create() != cudaSuccess ||
+      cudaEventRecord(fj.fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(side, fj.fork, 0) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_build_qpairs(g, idx, cnt, w, side) != cudaSuccess) return VSA_ERR_CUDA;
+  if (launch_build_kpairs(g, idx, cnt, w, side) != cudaSuccess) return VSA_ERR_CUDA;
+  if (cudaEventRecord(fj.join, side) != cudaSuccess) return VSA_ERR_CUDA;
   if (launch_combine_bwd(g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
                          static_cast<const bf16*>(gf), of, oc, dgc, dgf,
                          static_cast<f16*>(w.dof), w.doc, w.delta, w.gamax, w.gscale, w.status,
@@ -572,8 +626,7 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
                         reinterpret_cast<const float*>(sv + L.lse_c), w.doc, w.dqc, w.dkc, w.dvc,
                         w, s) != cudaSuccess)
     return VSA_ERR_CUDA;
-  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
-  if (launch_build_kpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  if (cudaStreamWaitEvent(s, fj.join, 0) != cudaSuccess) return VSA_ERR_CUDA;
   return cuda_status(launch_fine_bwd(g, q16, k16, v16, reinterpret_cast<const float*>(sv + L.lse_f),
                                      static_cast<const f16*>(w.dof), w.delta, w.gscale, w.dqc,
                                      w.dkc, w.dvc, dq, dk, dv, w, s));
