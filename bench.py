@@ -43,8 +43,8 @@ from trainable_block_sparse_gb300 import build, flops, synth  # noqa: E402
 METRIC = "VSA fwd/fwd+bwd ms/layer & executed TFLOPS (% of BF16 peak), 16K–70K tokens"
 WORKLOAD = "p720"
 # kernels per call of vsa_forward / vsa_backward
-LAUNCHES_FWD = 9   # stage x3, tf32 split, coarse logits GEMM + select + O_c GEMM, pair lists,
-                   # fine forward
+LAUNCHES_FWD = 10  # stage x3, tf32 splits x2, coarse logits GEMM + select + O_c GEMM, pair
+                   # lists, fine forward
 LAUNCHES_BWD = 16  # gradient-scale max, combine bwd, coarse bwd (row dot, tf32 split,
                    # dual GEMM, 3 GEMMs), pair lists, transposed lists (mask, count, scan,
                    # fill, pairs), fine bwd x2

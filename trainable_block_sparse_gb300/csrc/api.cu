@@ -530,51 +530,48 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   Workspace w;
   carve_ws(g, 0, ws, &w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // V is staged on the side stream while Q and K are staged and the logits,
+  // selection and lists are computed on `s` (V is needed first by O_c).
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  cudaStream_t side = nullptr;
+  ForkJoin fj;
+  if (side_stream(&side) != cudaSuccess || fj.create() != cudaSuccess ||
+      cudaEventRecord(fj.fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(side, fj.fork, 0) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  float* qc = reinterpret_cast<float*>(sv + L.qc);
+  float* kc = reinterpret_cast<float*>(sv + L.kc);
+  float* vc = reinterpret_cast<float*>(sv + L.vc);
+  float* oc = reinterpret_cast<float*>(sv + L.oc);
+  float* lse_c = reinterpret_cast<float*>(sv + L.lse_c);
+  int* idx = reinterpret_cast<int*>(sv + L.idx);
+  int* cnt = reinterpret_cast<int*>(sv + L.cnt);
   // Inference reads q, k, v in place unless they are raster tensors of head_dim
   // 128: there a cube's 64-channel box is 16 runs spread over a 4 x 4 patch of
   // image rows, and the fine stage measured 23-31% slower than on the staged
   // cube-order copy (which is one contiguous block per cube); at head_dim 64
   // (whole 512-byte runs) and in cube layout it runs at the staged speed.
-  if (!with_backward && (!g.raster || g.D == 64)) {
-    // inference: cube means only, then the fine stage reads q, k, v in place
-    float* qc = reinterpret_cast<float*>(sv + L.qc);
-    float* kc = reinterpret_cast<float*>(sv + L.kc);
-    float* vc = reinterpret_cast<float*>(sv + L.vc);
-    float* oc = reinterpret_cast<float*>(sv + L.oc);
-    int* idx = reinterpret_cast<int*>(sv + L.idx);
-    int* cnt = reinterpret_cast<int*>(sv + L.cnt);
-    if (launch_stage(g, static_cast<const bf16*>(q), g.raster, nullptr, qc, w.status, s) ||
-        launch_stage(g, static_cast<const bf16*>(k), g.raster, nullptr, kc, w.status, s) ||
-        launch_stage(g, static_cast<const bf16*>(v), g.raster, nullptr, vc, w.status, s))
-      return VSA_ERR_CUDA;
-    if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
-                             kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt, w,
-                             s) != cudaSuccess)
-      return VSA_ERR_CUDA;
-    if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
+  const bool in_place = !with_backward && (!g.raster || g.D == 64);
+  f16* q16 = in_place ? nullptr : reinterpret_cast<f16*>(sv + L.q16);
+  f16* k16 = in_place ? nullptr : reinterpret_cast<f16*>(sv + L.k16);
+  f16* v16 = in_place ? nullptr : reinterpret_cast<f16*>(sv + L.v16);
+  if (launch_stage(g, static_cast<const bf16*>(v), g.raster, v16, vc, w.status, side) ||
+      cudaEventRecord(fj.join, side) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (launch_stage(g, static_cast<const bf16*>(q), g.raster, q16, qc, w.status, s) ||
+      launch_stage(g, static_cast<const bf16*>(k), g.raster, k16, kc, w.status, s))
+    return VSA_ERR_CUDA;
+  if (launch_coarse_logits_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin,
+                                  cfg->kmax, qc, kc, lse_c, idx, cnt, w, s) != cudaSuccess ||
+      launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess ||
+      cudaStreamWaitEvent(s, fj.join, 0) != cudaSuccess ||
+      launch_coarse_out(g, vc, oc, w, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (in_place)
     return cuda_status(launch_fine_fwd_bf16(
         g, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
         static_cast<const bf16*>(gc), static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
         reinterpret_cast<float*>(sv + L.lse_f), w, s));
-  }
-  f16* q16 = reinterpret_cast<f16*>(sv + L.q16);
-  f16* k16 = reinterpret_cast<f16*>(sv + L.k16);
-  f16* v16 = reinterpret_cast<f16*>(sv + L.v16);
-  float* qc = reinterpret_cast<float*>(sv + L.qc);
-  float* kc = reinterpret_cast<float*>(sv + L.kc);
-  float* vc = reinterpret_cast<float*>(sv + L.vc);
-  if (launch_stage(g, static_cast<const bf16*>(q), g.raster, q16, qc, w.status, s) ||
-      launch_stage(g, static_cast<const bf16*>(k), g.raster, k16, kc, w.status, s) ||
-      launch_stage(g, static_cast<const bf16*>(v), g.raster, v16, vc, w.status, s))
-    return VSA_ERR_CUDA;
-  float* oc = reinterpret_cast<float*>(sv + L.oc);
-  int* idx = reinterpret_cast<int*>(sv + L.idx);
-  int* cnt = reinterpret_cast<int*>(sv + L.cnt);
-  if (launch_coarse_select(g, cfg->select_mode, cfg->topk, cfg->mass, cfg->kmin, cfg->kmax, qc,
-                           kc, vc, oc, reinterpret_cast<float*>(sv + L.lse_c), idx, cnt, w,
-                           s) != cudaSuccess)
-    return VSA_ERR_CUDA;
-  if (launch_build_qpairs(g, idx, cnt, w, s) != cudaSuccess) return VSA_ERR_CUDA;
   return cuda_status(launch_fine_fwd(g, q16, k16, v16, static_cast<const bf16*>(gc),
                                      static_cast<const bf16*>(gf), oc, static_cast<bf16*>(o),
                                      with_backward ? reinterpret_cast<f16*>(sv + L.o_f) : nullptr,

@@ -440,20 +440,17 @@ TgemmArgs gemm(const Geom& g, int M, int N, int K, float alpha) {
 
 }  // namespace
 
-cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
-                                 int kmax, const float* qc, const float* kc, const float* vc,
-                                 float* oc, float* lse_c, int* idx, int* cnt, const Workspace& ws,
-                                 cudaStream_t s) {
+cudaError_t launch_coarse_logits_select(const Geom& g, int mode, int topk, float mass, int kmin,
+                                        int kmax, const float* qc, const float* kc, float* lse_c,
+                                        int* idx, int* cnt, const Workspace& ws, cudaStream_t s) {
   const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
   const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
-  const long long DC = static_cast<long long>(D) * ldc;
   cudaError_t e;
-  // operand pairs Q_c, K_c ([Nc, D]); V_c^T ([D, Nc]) rounded to tf32
+  // operand pairs Q_c, K_c ([Nc, D]) as tf32 hi + lo
   {
-    const SplitSpec sp[3] = {{qc, D, ND, Nc, D, ws.qh, ws.ql, D, ND, false},
-                             {kc, D, ND, Nc, D, ws.kh, ws.kl, D, ND, false},
-                             {vc, D, ND, Nc, D, ws.vth, nullptr, ldc, DC, true}};
-    if ((e = launch_split_tf32(sp, 3, g.BH, s))) return e;
+    const SplitSpec sp[2] = {{qc, D, ND, Nc, D, ws.qh, ws.ql, D, ND, false},
+                             {kc, D, ND, Nc, D, ws.kh, ws.kl, D, ND, false}};
+    if ((e = launch_split_tf32(sp, 2, g.BH, s))) return e;
   }
   // L = scale Q_c K_c^T
   TgemmArgs a = gemm(g, Nc, Nc, D, g.scale);
@@ -486,14 +483,36 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
     select_kernel<<<dim3((Nc + rows - 1) / rows, g.BH), kSelThreads, smem, s>>>(
         g, sa, rows, ws.clogit, ws.ach, ldc, lse_c, idx, cnt);
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_coarse_out(const Geom& g, const float* vc, float* oc, const Workspace& ws,
+                              cudaStream_t s) {
+  const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
+  const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
+  const long long DC = static_cast<long long>(D) * ldc;
+  cudaError_t e;
+  // V_c^T ([D, Nc]) rounded to tf32
+  {
+    const SplitSpec sp[1] = {{vc, D, ND, Nc, D, ws.vth, nullptr, ldc, DC, true}};
+    if ((e = launch_split_tf32(sp, 1, g.BH, s))) return e;
+  }
   // O_c = A_c V_c, plain tf32
-  a = gemm(g, Nc, D, Nc, 1.f);
+  TgemmArgs a = gemm(g, Nc, D, Nc, 1.f);
   a.out = oc;
   a.out_ld = D;
   a.out_stride = ND;
   return launch_tgemm(a, TgemmOperand{ws.ach, nullptr, ldc, NC},
                       TgemmOperand{ws.vth, nullptr, ldc, DC}, ws.status, s);
+}
+
+cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, int kmin,
+                                 int kmax, const float* qc, const float* kc, const float* vc,
+                                 float* oc, float* lse_c, int* idx, int* cnt, const Workspace& ws,
+                                 cudaStream_t s) {
+  const cudaError_t e =
+      launch_coarse_logits_select(g, mode, topk, mass, kmin, kmax, qc, kc, lse_c, idx, cnt, ws, s);
+  return e != cudaSuccess ? e : launch_coarse_out(g, vc, oc, ws, s);
 }
 
 cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,

@@ -121,6 +121,13 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
                                  int kmax, const float* qc, const float* kc, const float* vc,
                                  float* oc, float* lse_c, int* idx, int* cnt, const Workspace& ws,
                                  cudaStream_t s);
+// The same in two phases: logits, softmax statistics, selection and A_c
+// (needs only Q_c, K_c), then O_c = A_c V_c.
+cudaError_t launch_coarse_logits_select(const Geom& g, int mode, int topk, float mass, int kmin,
+                                        int kmax, const float* qc, const float* kc, float* lse_c,
+                                        int* idx, int* cnt, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_coarse_out(const Geom& g, const float* vc, float* oc, const Workspace& ws,
+                              cudaStream_t s);
 cudaError_t launch_build_qpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
 cudaError_t launch_fine_fwd(const Geom& g, const __half* q, const __half* k, const __half* v,
