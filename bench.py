@@ -224,7 +224,7 @@ def gpu_arm(args, rank, world):
         fwd()
         vsa.backward(cfg32, t["gc"], t["gf"], t["do"], bufs, grads32)
 
-    bufs_inf = vsa.Buffers(cfg, dev, with_backward=False)
+    bufs_inf = vsa.Buffers(cfg, dev, with_backward=False, inference_only=True)
     o_inf = torch.empty_like(t["q"])
 
     def fwd_inference():
@@ -366,7 +366,7 @@ def side_workload(vsa, name, dev):
         vsa.backward(cfg, t["gc"], t["gf"], t["do"], bufs, grads)
 
     flush = L2Flush(dev)
-    bufs_inf = vsa.Buffers(cfg, dev, with_backward=False)
+    bufs_inf = vsa.Buffers(cfg, dev, with_backward=False, inference_only=True)
 
     def fwd_inference():
         vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs_inf, False, out=o)

@@ -51,7 +51,11 @@
  *    caller's `ws` buffer of vsa_workspace_bytes() bytes; data the backward
  *    pass needs comes from the caller's `saved` buffer of vsa_saved_bytes().
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *    stream) and runs asynchronously.
+ *    stream) and runs asynchronously.  vsa_forward and vsa_backward also fork
+ *    independent kernels to a second stream the library creates once per
+ *    device, and join back to `stream` with two events of their own per call
+ *    (this works inside stream capture; concurrent calls from several host
+ *    threads are serialised while they enqueue).
  *  - Arguments are checked on the host before anything is launched; an error
  *    return leaves every output untouched.  VSA_ERR_CUDA reports a launch
  *    failure.  Faults found on the device (a bounded wait that expired, an
@@ -103,7 +107,10 @@ typedef struct {
 } vsa_config_t;
 
 /* Byte offsets of the pieces of the `saved` buffer written by vsa_forward.
- * Each piece starts on a 256-byte boundary; absent pieces have size 0. */
+ * Each piece starts on a 256-byte boundary.  The offsets are the same for
+ * every use; the pieces only training needs come last (qc .. lse_f, then
+ * q16, k16, v16, then o_f), so a smaller `total` (vsa_saved_bytes_for with
+ * with_backward = 0) simply leaves off what lies at or beyond it. */
 typedef struct {
   size_t q16, k16, v16;          /* fp16 [B,heads,N,D] cube order: staged Q, K, V */
   size_t qc, kc, vc, oc;         /* fp32 [B,heads,Nc,D]: pooled Q/K/V, coarse output */
@@ -112,7 +119,7 @@ typedef struct {
   size_t cnt;                    /* int32 [B,heads,Nc]: entries used per list */
   size_t o_f;                    /* fp16 [B,heads,N,D] cube order: fine output */
   size_t lse_f;                  /* fp32 [B,heads,N] cube order: fine log-sum-exp */
-  size_t total;                  /* = vsa_saved_bytes() */
+  size_t total;                  /* bytes of the buffer for this use */
   int32_t list_cap;              /* topk (TOPK) or kmax (MASS) */
 } vsa_saved_layout_t;
 
@@ -123,8 +130,17 @@ vsa_status_t vsa_validate(const vsa_config_t* cfg);
 const char* vsa_status_string(vsa_status_t s);
 
 /* Bytes of the caller-owned `saved` buffer; fills *layout if not NULL.
- * Returns 0 for an invalid configuration. */
+ * Returns 0 for an invalid configuration.  This is the training size (every
+ * piece), which every entry point that takes `saved` accepts. */
 size_t vsa_saved_bytes(const vsa_config_t* cfg, vsa_saved_layout_t* layout);
+
+/* The same for one use: with_backward != 0 gives vsa_saved_bytes(); 0 gives the
+ * smaller buffer an inference vsa_forward (with_backward = 0) needs: without
+ * o_f, and without the staged q16, k16, v16 unless it stages them (raster
+ * layout, head_dim 128).  The offsets are those of vsa_saved_bytes();
+ * vsa_backward and vsa_forward_fp8 need the training size. */
+size_t vsa_saved_bytes_for(const vsa_config_t* cfg, int with_backward,
+                           vsa_saved_layout_t* layout);
 
 /* Bytes of the caller-owned scratch buffer `ws` for the forward pass
  * (with_backward = 0) or for forward and backward (with_backward = 1).
@@ -334,7 +350,8 @@ vsa_status_t vsa_fine_bwd(const vsa_config_t* cfg, const void* q16, const void* 
  * "Pseudocode of VSA"; paper notes 关键设计 1-3): tile, coarse stage, fine
  * stage + combine, untile.
  * q, k, v, gc, gf: bf16 in cfg->layout order; o: bf16 output, same order.
- * saved: vsa_saved_bytes() bytes.
+ * saved: vsa_saved_bytes() bytes, or vsa_saved_bytes_for(cfg, 0, ...) bytes for
+ *   with_backward == 0.
  * with_backward != 0: stages fp16 copies of Q, K, V with the cube means, and
  *   fills everything vsa_backward needs (O_f included).
  * with_backward == 0 (inference): no O_f.  In cube layout, or at head_dim 64,

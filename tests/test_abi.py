@@ -102,21 +102,49 @@ def test_buffer_sizes(lib):
     cfg = _cfg()
     L = vsa.saved_layout(cfg)
     # pieces are 256-byte aligned, in order, and fit the total
-    offs = [L.q16, L.k16, L.v16, L.qc, L.kc, L.vc, L.oc, L.lse_c, L.idx, L.cnt, L.o_f,
-            L.lse_f]
+    offs = [L.qc, L.kc, L.vc, L.oc, L.lse_c, L.idx, L.cnt, L.lse_f, L.q16, L.k16, L.v16,
+            L.o_f]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and L.total > offs[-1]
     assert L.list_cap == 2
     n_tok = 2 * 512
-    assert L.o_f - L.cnt >= 2 * 8 * 4 and L.total - L.lse_f >= n_tok * 4
+    assert L.lse_f - L.cnt >= 2 * 8 * 4 and L.q16 - L.lse_f >= n_tok * 4
+    assert L.total - L.o_f >= n_tok * 64 * 2
     fwd = vsa.workspace_bytes(cfg, False)
     bwd = vsa.workspace_bytes(cfg, True)
     assert 0 < fwd < bwd
     bad = _cfg(T=5)
     assert lib.vsa_saved_bytes(ctypes.byref(bad), None) == 0
     assert lib.vsa_workspace_bytes(ctypes.byref(bad), 1) == 0
-    # staged fp16 copies of Q, K, V come first, one [B, heads, N, D] each
-    assert L.k16 - L.q16 >= n_tok * 64 * 2 and L.qc - L.v16 >= n_tok * 64 * 2
+    # staged fp16 copies of Q, K, V, one [B, heads, N, D] each
+    assert L.k16 - L.q16 >= n_tok * 64 * 2 and L.o_f - L.v16 >= n_tok * 64 * 2
+
+
+def test_inference_saved_buffer_drops_what_only_training_needs(lib):
+    # head_dim 64 (raster): the inference forward reads q, k, v in place and
+    # writes no O_f: the buffer ends where the staged copies begin; the offsets
+    # are the training layout's
+    cfg = _cfg()
+    full = vsa.saved_layout(cfg)
+    inf = vsa.saved_layout(cfg, with_backward=False)
+    assert lib.vsa_saved_bytes_for(ctypes.byref(cfg), 1, None) == full.total
+    assert lib.vsa_saved_bytes(ctypes.byref(cfg), None) == full.total
+    for name in ("q16", "k16", "v16", "qc", "kc", "vc", "oc", "lse_c", "idx", "cnt", "o_f",
+                 "lse_f"):
+        assert getattr(inf, name) == getattr(full, name)
+    assert inf.total == full.q16
+    n_tok = 2 * 512
+    assert full.total - inf.total >= 4 * n_tok * 64 * 2
+    # raster head_dim 128: the inference forward stages, so only O_f goes
+    cfg128 = _cfg(head_dim=128)
+    full128 = vsa.saved_layout(cfg128)
+    assert vsa.saved_layout(cfg128, with_backward=False).total == full128.o_f
+    # cube layout head_dim 128 reads in place again
+    cube128 = _cfg(head_dim=128, layout="cube")
+    assert vsa.saved_layout(cube128, with_backward=False).total == \
+        vsa.saved_layout(cube128).q16
+    bad = _cfg(T=5)
+    assert lib.vsa_saved_bytes_for(ctypes.byref(bad), 0, None) == 0
 
 
 def test_status_strings(lib):

@@ -400,3 +400,32 @@ def test_worked_example_ties_keep_lower_ids():
     assert v["idx"].cpu().flatten().tolist() == [0] * (wl.heads * wl.cubes)
     vt = O.tile(O.f64(inp.v[0, 0]), wl.T, wl.H, wl.W)
     assert_close("O_f", to_np(v["o_f"][0, 0]), np.broadcast_to(vt[:64].mean(0), (128, 64)))
+
+
+@pytest.mark.parametrize("thw,D,layout", [((8, 8, 8), 64, "raster"), ((8, 4, 12), 128, "raster"),
+                                          ((8, 4, 12), 128, "cube")])
+def test_inference_forward_in_its_smaller_saved_buffer(thw, D, layout):
+    """vsa_forward(with_backward=0) into a saved buffer of vsa_saved_bytes_for(cfg, 0)
+    (no O_f; staged copies only where inference stages) gives the output and
+    the saved coarse results of the training-sized buffer, bit for bit."""
+    inp = _custom(*thw, D, 2, seed=5)
+    cfg = vsa.config_for(inp.wl, layout)
+    t = cuda_inputs(inp)
+    if layout == "cube":
+        for n in ("q", "k", "v", "gc", "gf"):
+            t[n] = vsa.permute(cfg, t[n])
+    outs = []
+    for small in (False, True):
+        bufs = vsa.Buffers(cfg, "cuda", with_backward=False, inference_only=small)
+        if small:
+            assert bufs.saved.numel() < vsa.saved_layout(cfg).total
+        o = vsa.forward(cfg, t["q"], t["k"], t["v"], t["gc"], t["gf"], bufs, with_backward=False)
+        torch.cuda.synchronize()
+        assert bufs.device_status() == vsa.OK
+        wl = inp.wl
+        B, H, N, nc, cap = wl.batch, wl.heads, wl.tokens, wl.cubes, wl.list_capacity
+        outs.append([o.clone(), bufs.view("idx", torch.int32, (B, H, nc, cap)).clone(),
+                     bufs.view("oc", torch.float32, (B, H, nc, D)).clone(),
+                     bufs.view("lse_f", torch.float32, (B, H, N)).clone()])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

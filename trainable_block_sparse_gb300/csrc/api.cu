@@ -77,16 +77,24 @@ namespace {
 size_t half_tensor(const Geom& g) { return static_cast<size_t>(g.BH) * g.N * g.D * 2; }
 size_t pooled_bytes(const Geom& g) { return static_cast<size_t>(g.BH) * g.Nc * g.D * 4; }
 
-void saved_layout(const Geom& g, vsa_saved_layout_t* L) {
+// Whether an inference forward (with_backward = 0) stages fp16 copies of Q, K,
+// V: only raster tensors of head_dim 128 (vsa_forward explains why); it reads
+// the others in place.
+bool inference_stages(const Geom& g) { return g.raster && g.D == 128; }
+
+// One layout for every use, ordered so that what an inference forward does
+// not write comes last: the coarse results and lse_f, then the staged fp16
+// copies (an inference forward writes them only when it stages), then O_f
+// (training only).  with_backward = 0 gives the total of an inference
+// forward; 1 the total of every piece (the training forward, the backward,
+// the e4m3 forward).
+void saved_layout(const Geom& g, int with_backward, vsa_saved_layout_t* L) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off += align_up(bytes);
     return o;
   };
-  L->q16 = take(half_tensor(g));
-  L->k16 = take(half_tensor(g));
-  L->v16 = take(half_tensor(g));
   L->qc = take(pooled_bytes(g));
   L->kc = take(pooled_bytes(g));
   L->vc = take(pooled_bytes(g));
@@ -94,9 +102,14 @@ void saved_layout(const Geom& g, vsa_saved_layout_t* L) {
   L->lse_c = take(static_cast<size_t>(g.BH) * g.Nc * 4);
   L->idx = take(static_cast<size_t>(g.BH) * g.Nc * g.cap * 4);
   L->cnt = take(static_cast<size_t>(g.BH) * g.Nc * 4);
-  L->o_f = take(half_tensor(g));
   L->lse_f = take(static_cast<size_t>(g.BH) * g.N * 4);
-  L->total = off;
+  const size_t end_in_place = off;
+  L->q16 = take(half_tensor(g));
+  L->k16 = take(half_tensor(g));
+  L->v16 = take(half_tensor(g));
+  const size_t end_staged = off;
+  L->o_f = take(half_tensor(g));
+  L->total = with_backward ? off : (inference_stages(g) ? end_staged : end_in_place);
   L->list_cap = g.cap;
 }
 
@@ -333,10 +346,15 @@ const char* vsa_status_string(vsa_status_t s) {
 }
 
 size_t vsa_saved_bytes(const vsa_config_t* cfg, vsa_saved_layout_t* layout) {
+  return vsa_saved_bytes_for(cfg, 1, layout);
+}
+
+size_t vsa_saved_bytes_for(const vsa_config_t* cfg, int with_backward,
+                           vsa_saved_layout_t* layout) {
   Geom g;
   if (make_geom(cfg, &g) != VSA_OK) return 0;
   vsa_saved_layout_t L;
-  saved_layout(g, &L);
+  saved_layout(g, with_backward != 0, &L);
   if (layout) *layout = L;
   return L.total;
 }
@@ -525,7 +543,7 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   if (!all_set(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_INVALID_ARG;
   if (!all_aligned(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_ALIGNMENT;
   vsa_saved_layout_t L;
-  saved_layout(g, &L);
+  saved_layout(g, with_backward != 0, &L);
   char* sv = static_cast<char*>(saved);
   Workspace w;
   carve_ws(g, 0, ws, &w);
@@ -551,7 +569,7 @@ vsa_status_t vsa_forward(const vsa_config_t* cfg, const void* q, const void* k, 
   // image rows, and the fine stage measured 23-31% slower than on the staged
   // cube-order copy (which is one contiguous block per cube); at head_dim 64
   // (whole 512-byte runs) and in cube layout it runs at the staged speed.
-  const bool in_place = !with_backward && (!g.raster || g.D == 64);
+  const bool in_place = !with_backward && !inference_stages(g);
   f16* q16 = in_place ? nullptr : reinterpret_cast<f16*>(sv + L.q16);
   f16* k16 = in_place ? nullptr : reinterpret_cast<f16*>(sv + L.k16);
   f16* v16 = in_place ? nullptr : reinterpret_cast<f16*>(sv + L.v16);
@@ -587,7 +605,7 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
   if (!all_set(gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws)) return VSA_ERR_INVALID_ARG;
   if (!all_aligned(gc, gf, saved, d_o, dq, dk, dv, dgc, dgf, ws)) return VSA_ERR_ALIGNMENT;
   vsa_saved_layout_t L;
-  saved_layout(g, &L);
+  saved_layout(g, 1, &L);
   const char* sv = static_cast<const char*>(saved);
   Workspace w;
   carve_ws(g, 1, ws, &w);
@@ -681,7 +699,7 @@ vsa_status_t vsa_forward_fp8(const vsa_config_t* cfg, const void* q, const void*
   if (!all_set(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_INVALID_ARG;
   if (!all_aligned(q, k, v, gc, gf, o, saved, ws)) return VSA_ERR_ALIGNMENT;
   vsa_saved_layout_t L;
-  saved_layout(g, &L);
+  saved_layout(g, 1, &L);
   char* sv = static_cast<char*>(saved);
   Workspace w;
   carve_ws(g, 0, ws, &w);

@@ -45,6 +45,7 @@ _SIGS = {
     "vsa_validate": [ctypes.POINTER(Config)],
     "vsa_status_string": [ctypes.c_int],
     "vsa_saved_bytes": [ctypes.POINTER(Config), ctypes.POINTER(SavedLayout)],
+    "vsa_saved_bytes_for": [ctypes.POINTER(Config), ctypes.c_int, ctypes.POINTER(SavedLayout)],
     "vsa_workspace_bytes": [ctypes.POINTER(Config), ctypes.c_int],
     "vsa_reset_device_status": [_P, _P],
     "vsa_check_device_status": [_P, _P],
@@ -64,6 +65,7 @@ _SIGS = {
     "vsa_forward_fp8": [ctypes.POINTER(Config)] + [_P] * 9,
 }
 _RESTYPES = {"vsa_status_string": ctypes.c_char_p, "vsa_saved_bytes": ctypes.c_size_t,
+             "vsa_saved_bytes_for": ctypes.c_size_t,
              "vsa_workspace_bytes": ctypes.c_size_t}
 
 _lib = None
@@ -120,9 +122,11 @@ def config_for(wl, layout="raster", grad_dtype="fp32") -> Config:
                        layout=layout, grad_dtype=grad_dtype)
 
 
-def saved_layout(cfg: Config) -> SavedLayout:
+def saved_layout(cfg: Config, with_backward: bool = True) -> SavedLayout:
+    """The `saved` buffer's layout for training (every piece) or, with
+    with_backward False, for an inference forward alone."""
     L = SavedLayout()
-    n = lib().vsa_saved_bytes(ctypes.byref(cfg), ctypes.byref(L))
+    n = lib().vsa_saved_bytes_for(ctypes.byref(cfg), int(with_backward), ctypes.byref(L))
     if n == 0:
         check(lib().vsa_validate(ctypes.byref(cfg)), "vsa_saved_bytes")
     return L
@@ -150,11 +154,14 @@ def _stream():
 
 
 class Buffers:
-    """Caller-owned device buffers of one layer: the `saved` context and `ws` scratch."""
+    """Caller-owned device buffers of one layer: the `saved` context and `ws` scratch.
+    `inference_only` sizes `saved` for forward(with_backward=False) alone."""
 
-    def __init__(self, cfg: Config, device, with_backward: bool):
+    def __init__(self, cfg: Config, device, with_backward: bool, inference_only: bool = False):
+        if with_backward and inference_only:
+            raise ValueError("inference_only buffers cannot hold a backward's context")
         self.cfg = cfg
-        self.layout = saved_layout(cfg)
+        self.layout = saved_layout(cfg, with_backward=not inference_only)
         self.saved = torch.empty(self.layout.total, dtype=torch.uint8, device=device)
         self.ws = torch.empty(workspace_bytes(cfg, with_backward), dtype=torch.uint8,
                               device=device)
@@ -355,7 +362,7 @@ class _VSAFunction(torch.autograd.Function):
     def forward(ctx, q, k, v, gc, gf, cfg_tuple, check_status):
         cfg = Config(*cfg_tuple)
         need = any(t.requires_grad for t in (q, k, v, gc, gf))
-        bufs = Buffers(cfg, q.device, with_backward=need)
+        bufs = Buffers(cfg, q.device, with_backward=need, inference_only=not need)
         o = forward(cfg, q, k, v, gc, gf, bufs, with_backward=need)
         if check_status:
             check(bufs.device_status(), "video_sparse_attention (forward, device status)")
