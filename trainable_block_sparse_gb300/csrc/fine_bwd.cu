@@ -533,6 +533,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     };
     uint32_t sq = 0;
     bool x_in_tmem = false;  // dQ pass: this item's Q and dO are already in TMEM
+    // dQ pass: the next item's row lse and delta, loaded while this item runs
+    int pre_item = kSeqEnd;
+    float pre_lse = 0.f, pre_delta = 0.f;
     while (ok) {
       const int item = seq_next<true>(sb.seq, sq, abort_flag, P.status);
       if (item < 0 || is_aborted(abort_flag)) break;
@@ -557,26 +560,53 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       x_in_tmem = false;
       float row_lse = 0.f, row_delta = 0.f;
       if (!kKeyMajor && row_live) {
-        const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + (row & 63);
-        row_lse = P.lse[frow] * kLog2e;
-        row_delta = P.delta[frow];
+        if (item == pre_item) {
+          row_lse = pre_lse * kLog2e;
+          row_delta = pre_delta;
+        } else {
+          const size_t frow = static_cast<size_t>(pi.bh) * g.N + cube * kTile + (row & 63);
+          row_lse = P.lse[frow] * kLog2e;
+          row_delta = P.delta[frow];
+        }
+      }
+      if (!kKeyMajor) {
+        // the next item's lse and delta of this row: the loads are issued now
+        // and first used when that item starts
+        const int nx = seq_peek(sb.seq, sq, 0, abort_flag, P.status);
+        if (nx == kSeqAbort) break;
+        pre_item = nx;
+        if (nx >= 0) {
+          const PairItem pn = P.items[P.order ? P.order[nx] : nx];
+          if (pn.count > 0 && (half == 0 || pn.b >= 0)) {
+            const size_t nrow =
+                static_cast<size_t>(pn.bh) * g.N + (half ? pn.b : pn.a) * kTile + (row & 63);
+            pre_lse = P.lse[nrow];
+            pre_delta = P.delta[nrow];
+          }
+        }
       }
       const int nsteps = (pi.count + 1) / 2;
       // key-major: lse (log2 units) and delta of the step tile's 64 query rows,
       // lane l holding rows l and 32 + l, broadcast with shuffles; fetched one
-      // step ahead.  (Warp-uniform 16-byte loads from L1 instead of the
-      // shuffles measured 13% slower on the 720p layer.)
+      // step ahead (the loads' values are first touched, lse scaled to log2
+      // units, when the step they belong to begins).  (Warp-uniform 16-byte
+      // loads from L1 instead of the shuffles measured 13% slower on the 720p
+      // layer.)
       auto tile_rows = [&](int s2, float& l0, float& l1, float& d0, float& d1) {
         const bool h2 = hc == 0 || 2 * s2 + 1 < pi.count;
         const uint32_t e2 = h2 ? list[2 * s2 + hc] : 0u;
         const size_t q0 = static_cast<size_t>(pi.bh) * g.N + (e2 & 0xFFFFu) * kTile;
-        l0 = __ldg(P.lse + q0 + lane) * kLog2e;
-        l1 = __ldg(P.lse + q0 + 32 + lane) * kLog2e;
+        l0 = __ldg(P.lse + q0 + lane);
+        l1 = __ldg(P.lse + q0 + 32 + lane);
         d0 = __ldg(P.delta + q0 + lane);
         d1 = __ldg(P.delta + q0 + 32 + lane);
       };
       float cl0 = 0.f, cl1 = 0.f, cd0 = 0.f, cd1 = 0.f;
-      if (kKeyMajor) tile_rows(0, cl0, cl1, cd0, cd1);
+      if (kKeyMajor) {
+        tile_rows(0, cl0, cl1, cd0, cd1);
+        cl0 *= kLog2e;
+        cl1 *= kLog2e;
+      }
       // list entry of this half's step tile, fetched one step ahead
       uint32_t e_cur = hc < pi.count ? __ldg(list + hc) : 0u;
       for (int s = 0; s < nsteps; ++s, ++step) {
@@ -654,8 +684,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
         tc_fence_before();
         warp_arrive_bwd(&sb.ds_full[b]);
-        cl0 = nl0;
-        cl1 = nl1;
+        cl0 = nl0 * kLog2e;
+        cl1 = nl1 * kLog2e;
         cd0 = nd0;
         cd1 = nd1;
       }
