@@ -45,7 +45,7 @@ WORKLOAD = "p720"
 # kernels per call of vsa_forward / vsa_backward
 LAUNCHES_FWD = 10  # stage x3, tf32 splits x2, coarse logits GEMM + select + O_c GEMM, pair
                    # lists, fine forward
-LAUNCHES_BWD = 16  # gradient-scale max, combine bwd, coarse bwd (row dot, tf32 split,
+LAUNCHES_BWD = 17  # gradient-scale max, combine bwd, coarse bwd (tf32 splits x2, row dot,
                    # dual GEMM, 3 GEMMs), pair lists, transposed lists (mask, count, scan,
                    # fill, pairs), fine bwd x2
 SIDE_WORKLOADS = ("wan13b", "pretrain", "dynamic")  # timed per stage beside the headline layer

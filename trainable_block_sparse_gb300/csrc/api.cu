@@ -201,17 +201,19 @@ cudaError_t side_stream(cudaStream_t* out) {
   return cudaSuccess;
 }
 
-// Events of one fork / join, destroyed when the call returns (the waits
-// already enqueued keep their effect).
+// Events of one fork and up to two joins, destroyed when the call returns (the
+// waits already enqueued keep their effect).
 struct ForkJoin {
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
   ~ForkJoin() {
     if (fork) cudaEventDestroy(fork);
     if (join) cudaEventDestroy(join);
+    if (join2) cudaEventDestroy(join2);
   }
   cudaError_t create() {
     cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-    return e != cudaSuccess ? e : cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    return e != cudaSuccess ? e : cudaEventCreateWithFlags(&join2, cudaEventDisableTiming);
   }
 };
 
@@ -617,9 +619,11 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
   const float* oc = reinterpret_cast<const float*>(sv + L.oc);
   const int* idx = reinterpret_cast<const int*>(sv + L.idx);
   const int* cnt = reinterpret_cast<const int*>(sv + L.cnt);
-  // The pair lists and the transposed lists (ws regions of their own) on the
-  // side stream, after everything already on `s`; `s` waits for them only
-  // before the fine backward.
+  // The coarse backward's tf32 operands of Q_c, K_c, V_c, then the pair lists
+  // and the transposed lists (ws regions of their own; none needs dO) on the
+  // side stream, after everything already on `s`; `s` waits for the operands
+  // before the coarse backward's products and for the lists before the fine
+  // backward.
   std::lock_guard<std::mutex> lock(g_side_mutex);
   cudaStream_t side = nullptr;
   ForkJoin fj;
@@ -627,21 +631,25 @@ vsa_status_t vsa_backward(const vsa_config_t* cfg, const void* gc, const void* g
       cudaEventRecord(fj.fork, s) != cudaSuccess ||
       cudaStreamWaitEvent(side, fj.fork, 0) != cudaSuccess)
     return VSA_ERR_CUDA;
+  if (launch_coarse_bwd_operands(g, reinterpret_cast<const float*>(sv + L.qc),
+                                 reinterpret_cast<const float*>(sv + L.kc),
+                                 reinterpret_cast<const float*>(sv + L.vc), w,
+                                 side) != cudaSuccess ||
+      cudaEventRecord(fj.join, side) != cudaSuccess)
+    return VSA_ERR_CUDA;
   if (launch_build_qpairs(g, idx, cnt, w, side) != cudaSuccess) return VSA_ERR_CUDA;
   if (launch_build_kpairs(g, idx, cnt, w, side) != cudaSuccess) return VSA_ERR_CUDA;
-  if (cudaEventRecord(fj.join, side) != cudaSuccess) return VSA_ERR_CUDA;
+  if (cudaEventRecord(fj.join2, side) != cudaSuccess) return VSA_ERR_CUDA;
   if (launch_combine_bwd(g, static_cast<const bf16*>(d_o), static_cast<const bf16*>(gc),
                          static_cast<const bf16*>(gf), of, oc, dgc, dgf,
                          static_cast<f16*>(w.dof), w.doc, w.delta, w.gamax, w.gscale, w.status,
                          s) != cudaSuccess)
     return VSA_ERR_CUDA;
-  if (launch_coarse_bwd(g, reinterpret_cast<const float*>(sv + L.qc),
-                        reinterpret_cast<const float*>(sv + L.kc),
-                        reinterpret_cast<const float*>(sv + L.vc), oc,
-                        reinterpret_cast<const float*>(sv + L.lse_c), w.doc, w.dqc, w.dkc, w.dvc,
-                        w, s) != cudaSuccess)
-    return VSA_ERR_CUDA;
   if (cudaStreamWaitEvent(s, fj.join, 0) != cudaSuccess) return VSA_ERR_CUDA;
+  if (launch_coarse_bwd_products(g, oc, reinterpret_cast<const float*>(sv + L.lse_c), w.doc,
+                                 w.dqc, w.dkc, w.dvc, w, s) != cudaSuccess ||
+      cudaStreamWaitEvent(s, fj.join2, 0) != cudaSuccess)
+    return VSA_ERR_CUDA;
   return cuda_status(launch_fine_bwd(g, q16, k16, v16, reinterpret_cast<const float*>(sv + L.lse_f),
                                      static_cast<const f16*>(w.dof), w.delta, w.gscale, w.dqc,
                                      w.dkc, w.dvc, dq, dk, dv, w, s));

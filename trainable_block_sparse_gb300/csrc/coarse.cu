@@ -515,10 +515,27 @@ cudaError_t launch_coarse_select(const Geom& g, int mode, int topk, float mass, 
   return e != cudaSuccess ? e : launch_coarse_out(g, vc, oc, ws, s);
 }
 
-cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
-                              const float* oc, const float* lse_c, const float* doc,
-                              float* dqc, float* dkc, float* dvc, const Workspace& ws,
-                              cudaStream_t s) {
+// The backward's products run as plain tf32 (operands rounded to tf32, one
+// product per k-step): unlike the forward's logits they decide no selection,
+// and their gradients reach dq, dk, dv divided by 64.  Operands in both
+// orientations where a product contracts over cubes; no lo parts.  Those of
+// Q_c, K_c, V_c need only the forward's results, so they can be made while
+// the combine backward computes dO_c.
+cudaError_t launch_coarse_bwd_operands(const Geom& g, const float* qc, const float* kc,
+                                       const float* vc, const Workspace& ws, cudaStream_t s) {
+  const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
+  const long long ND = static_cast<long long>(Nc) * D, DC = static_cast<long long>(D) * ldc;
+  const SplitSpec sp[5] = {{qc, D, ND, Nc, D, ws.qh, nullptr, D, ND, false},
+                           {kc, D, ND, Nc, D, ws.kh, nullptr, D, ND, false},
+                           {vc, D, ND, Nc, D, ws.vh, nullptr, D, ND, false},
+                           {qc, D, ND, Nc, D, ws.qth, nullptr, ldc, DC, true},
+                           {kc, D, ND, Nc, D, ws.kth, nullptr, ldc, DC, true}};
+  return launch_split_tf32(sp, 5, g.BH, s);
+}
+
+cudaError_t launch_coarse_bwd_products(const Geom& g, const float* oc, const float* lse_c,
+                                       const float* doc, float* dqc, float* dkc, float* dvc,
+                                       const Workspace& ws, cudaStream_t s) {
   const int Nc = g.Nc, D = g.D, ldc = ldc_of(g);
   const long long ND = static_cast<long long>(Nc) * D, NC = static_cast<long long>(Nc) * ldc;
   const long long DC = static_cast<long long>(D) * ldc;
@@ -526,19 +543,10 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
   const int rows = g.BH * Nc;
   rowdot_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, D, doc, oc, ws.cdelta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // The backward's products run as plain tf32 (operands rounded to tf32, one
-  // product per k-step): unlike the forward's logits they decide no selection,
-  // and their gradients reach dq, dk, dv divided by 64.  Operands in both
-  // orientations where a product contracts over cubes; no lo parts.
   {
-    const SplitSpec sp[7] = {{qc, D, ND, Nc, D, ws.qh, nullptr, D, ND, false},
-                             {kc, D, ND, Nc, D, ws.kh, nullptr, D, ND, false},
-                             {vc, D, ND, Nc, D, ws.vh, nullptr, D, ND, false},
-                             {doc, D, ND, Nc, D, ws.doh, nullptr, D, ND, false},
-                             {qc, D, ND, Nc, D, ws.qth, nullptr, ldc, DC, true},
-                             {kc, D, ND, Nc, D, ws.kth, nullptr, ldc, DC, true},
+    const SplitSpec sp[2] = {{doc, D, ND, Nc, D, ws.doh, nullptr, D, ND, false},
                              {doc, D, ND, Nc, D, ws.doth, nullptr, ldc, DC, true}};
-    if ((e = launch_split_tf32(sp, 7, g.BH, s))) return e;
+    if ((e = launch_split_tf32(sp, 2, g.BH, s))) return e;
   }
   auto hi = [](const float* h, int ld, long long stride) {
     return TgemmOperand{h, nullptr, ld, stride};
@@ -576,6 +584,15 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
   a.alpha = 1.f;
   a.out = dvc;
   return launch_tgemm(a, hi(ws.pth, ldc, NC), hi(ws.doth, ldc, DC), ws.status, s);
+}
+
+cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, const float* vc,
+                              const float* oc, const float* lse_c, const float* doc,
+                              float* dqc, float* dkc, float* dvc, const Workspace& ws,
+                              cudaStream_t s) {
+  const cudaError_t e = launch_coarse_bwd_operands(g, qc, kc, vc, ws, s);
+  return e != cudaSuccess ? e
+                          : launch_coarse_bwd_products(g, oc, lse_c, doc, dqc, dkc, dvc, ws, s);
 }
 
 }  // namespace vsa

@@ -149,6 +149,13 @@ cudaError_t launch_coarse_bwd(const Geom& g, const float* qc, const float* kc, c
                               const float* oc, const float* lse_c, const float* doc,
                               float* dqc, float* dkc, float* dvc, const Workspace& ws,
                               cudaStream_t s);
+// The same in two parts: the tf32 operands of Q_c, K_c, V_c (no dependence on
+// dO), then the rest.
+cudaError_t launch_coarse_bwd_operands(const Geom& g, const float* qc, const float* kc,
+                                       const float* vc, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_coarse_bwd_products(const Geom& g, const float* oc, const float* lse_c,
+                                       const float* doc, float* dqc, float* dkc, float* dvc,
+                                       const Workspace& ws, cudaStream_t s);
 cudaError_t launch_build_kpairs(const Geom& g, const int* idx, const int* cnt,
                                 const Workspace& ws, cudaStream_t s);
 // Schedule order of n pair items: sorted by step count, largest first.  The
