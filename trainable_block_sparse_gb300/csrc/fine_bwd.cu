@@ -46,7 +46,8 @@
 // epilogue has read dV, its first dK product until it has read dK.
 // Warps 0-7: softmax; warp w reads TMEM lane quarter w%4 (32 rows) and the 64
 // columns of step tile w/4, so each thread owns half a row.  Warp 8: TMA loads
-// of Y1/Y2.  Warp 9: UMMA issue.  Warp 10: TMA loads of X.  Warp 11: idle.
+// of Y1/Y2.  Warp 9: UMMA issue.  Warp 10: TMA loads of X.  Warp 11: item
+// fetcher (the next item from the launch's shared counter, item_seq.cuh).
 // Warps 12-15: epilogue.  Registers are split per warpgroup: 168 a thread for
 // the softmax warps, 88 for the rest.
 // Bounded waits and the abort path are as in the forward kernel.

@@ -28,7 +28,10 @@
 //                  log-sum-exp;
 //      warp 12     TMA: Q once per item, then K tiles gathered by list entry;
 //      warp 13     UMMA issue (whole warp converged, one elected lane);
-//      warp 14     TMA: V tiles gathered by list entry.
+//      warp 14     TMA: V tiles gathered by list entry;
+//      warp 15     item fetcher: takes the CTA's next item from the launch's
+//                  shared counter and hands it to the other roles
+//                  (item_seq.cuh), so the CTAs finish within about an item.
 //  * TMEM (512 columns): one S buffer, two P buffers (fp16, 64 columns each)
 //    and two O accumulators.  The softmax warps signal as soon as S(t) is in
 //    their registers, so QK^T of step t+1 runs while they compute P(t), ahead

@@ -27,7 +27,8 @@
 //              output, O (bf16, caller layout), O_f (fp16, cube order, kept
 //              for the backward), log-sum-exp;
 //   warp 8     TMA: Q once per item, then K tiles; warp 9: V tiles;
-//   warp 10    UMMA issue; warp 11: no role.
+//   warp 10    UMMA issue; warp 11: item fetcher (the next item from the
+//              launch's shared counter, item_seq.cuh).
 // TMEM: S buffers at columns 0 and 64, P at 128 (32 columns of fp16 pairs), Q at
 // 160 (32), O at 192 (64).  One P buffer: P(t) is stored once PV(t-1) has read
 // P(t-1) (PV(t-1) releases its V slot).  One O accumulator: an item's first P V
