@@ -29,10 +29,12 @@
 //   warp 8     TMA: Q once per item, then K tiles; warp 9: V tiles;
 //   warp 10    UMMA issue; warp 11: item fetcher (the next item from the
 //              launch's shared counter, item_seq.cuh).
-// TMEM: S buffers at columns 0 and 64, P at 128 (32 columns of fp16 pairs), Q at
-// 160 (32), O at 192 (64).  One P buffer: P(t) is stored once PV(t-1) has read
-// P(t-1) (PV(t-1) releases its V slot).  One O accumulator: an item's first P V
-// product waits until the epilogue has read the previous item's O.
+// TMEM: S buffers at columns 0 and 64, Q at 160 (32 columns of fp16 pairs), O at
+// 192 (64).  P(t) (32 columns of fp16 pairs) is written over the first half of
+// S(t)'s buffer as soon as it is computed, with a full barrier per buffer; the
+// next product into that buffer, S(t+2), is issued once PV(t) has completed,
+// and O is rescaled only after PV(t-1) is done.  One O accumulator: an item's
+// first P V product waits until the epilogue has read the previous item's O.
 // The running maximum moves, and O is rescaled, only when a row's maximum grows
 // by more than 2^8 (the rule of fine_fwd.cu, applied per 64-key step).
 // Every mbarrier wait is bounded; a time-out is recorded in the status word and
@@ -59,7 +61,6 @@ constexpr int kWarpEpi64 = 4, kWarpK64 = 8, kWarpV64 = 9, kWarpMma64 = 10;  // 1
 constexpr int kSeqReaders64 = 11;
 constexpr uint32_t kCols64 = 256;
 constexpr uint32_t kColS64 = 0;    // two S buffers of 64 columns
-constexpr uint32_t kColP64 = 128;  // P: 64 keys as 32 columns of fp16 pairs
 constexpr uint32_t kColQ64 = 160;  // Q: 64 channels as 32 columns of fp16 pairs
 constexpr uint32_t kColO64 = 192;  // O: 64 fp32 columns
 constexpr float kRescale64 = 8.0f;  // log2 units
@@ -92,8 +93,8 @@ struct Bars64 {
   uint64_t q_full, q_empty;  // Q in shared memory / copied out of it
   uint64_t q_tmem, q_done;   // Q in TMEM / the item's last S product done
   uint64_t k_full[kStagesK64], k_empty[kStagesK64], v_full[kStagesV64], v_empty[kStagesV64];
-  uint64_t s_full[2], s_read[2];  // per S buffer
-  uint64_t p_full;                // P(t) stored (one arrival per softmax warp)
+  uint64_t s_full[2];  // per S buffer
+  uint64_t p_full[2];  // P(t) stored over S buffer t % 2 (one arrival per softmax warp)
   uint64_t o_full, o_free;        // the item's O complete / read by the epilogue
   uint64_t st_full, st_free;      // row statistics handed to / read by the epilogue
   uint64_t final_mma;
@@ -173,9 +174,8 @@ __global__ void __launch_bounds__(kThreads64, 2)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.s_read[i], 4);
+      mbar_init(&sb.p_full[i], 4);
     }
-    mbar_init(&sb.p_full, 4);
     mbar_init(&sb.o_full, 1);
     mbar_init(&sb.o_free, 4);  // one arrival per epilogue warp
     mbar_init(&sb.st_full, 4);
@@ -260,11 +260,15 @@ __global__ void __launch_bounds__(kThreads64, 2)
     const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t vd0 = sdesc_sw128(smem_u32(sV), L64::kTileBytes, 1024);
 
-    // S(t) = Q K^T into S buffer t % 2 (A = Q in TMEM, B = K tile, K-major)
+    // S(t) = Q K^T into S buffer t % 2 (A = Q in TMEM, B = K tile, K-major),
+    // once PV(t-2) has read P(t-2) out of that buffer (PV(t-2) was issued
+    // earlier, after the softmax warps had read S(t-2) and stored P(t-2))
     auto issue_s = [&](uint32_t t) -> bool {
       const uint32_t slot = t % kSK, buf = t & 1;
-      if (t >= 2 && !waitw(&sb.s_read[buf], ((t - 2) >> 1) & 1, abort_flag, P.status))
-        return false;  // S(t-2) not yet read out of this buffer
+      if (t >= 2) {
+        const uint32_t pv = t - 2;
+        if (!waitw(&sb.v_empty[pv % kSV], (pv / kSV) & 1, abort_flag, P.status)) return false;
+      }
       if (!waitw(&sb.k_full[slot], (t / kSK) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
       const uint64_t kb = kd0 + ((slot * L64::kTileBytes) >> 4);
@@ -273,15 +277,16 @@ __global__ void __launch_bounds__(kThreads64, 2)
       commit_elect(&sb.k_empty[slot]);
       return true;
     };
-    // O += P V of step t (B = V tile, MN-major); its commit releases the V slot,
-    // which also tells the softmax warps that P may be overwritten
+    // O += P V of step t (A = P(t), packed over the first 32 columns of S
+    // buffer t % 2; B = V tile, MN-major); its commit releases the V slot and
+    // that S buffer, and tells the softmax warps that O may be rescaled
     auto issue_pv = [&](uint32_t t, bool first) -> bool {
       const uint32_t slot = t % kSV;
       if (!waitw(&sb.v_full[slot], (t / kSV) & 1, abort_flag, P.status)) return false;
       tc_fence_after();
       const uint64_t vb = vd0 + ((slot * L64::kTileBytes) >> 4);
-      issue_ts4(tb + kColO64, tb + kColP64, vb, vb + (2048 >> 4), vb + (4096 >> 4),
-                vb + (6144 >> 4), id_pv, first ? 0u : 1u);
+      issue_ts4(tb + kColO64, tb + kColS64 + 64 * (t & 1), vb, vb + (2048 >> 4),
+                vb + (4096 >> 4), vb + (6144 >> 4), id_pv, first ? 0u : 1u);
       commit_elect(&sb.v_empty[slot]);
       return true;
     };
@@ -301,7 +306,7 @@ __global__ void __launch_bounds__(kThreads64, 2)
       if (n <= 2) commit_elect(&sb.q_done);  // the item's last S product
       for (int s = 0; s < n; ++s) {
         const uint32_t t = step + s;
-        if (!waitw(&sb.p_full, t & 1, abort_flag, P.status)) {
+        if (!waitw(&sb.p_full[t & 1], (t >> 1) & 1, abort_flag, P.status)) {
           ok = false;
           break;
         }
@@ -336,7 +341,6 @@ __global__ void __launch_bounds__(kThreads64, 2)
     const int row = quarter * 32 + lane;
     const uint32_t mybit = (row >> 6) ? kSelB : kSelA;  // the same for the whole warp
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tp = tb + lane_addr + kColP64;
     const uint32_t to = tb + lane_addr + kColO64;
     const float c = g.scale * 1.4426950408889634f;  // scale * log2(e)
     uint32_t step = 0, sq = 0;
@@ -387,9 +391,6 @@ __global__ void __launch_bounds__(kThreads64, 2)
           tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
           tmem_wait_ld();
         }
-        // S(t) is in registers: its buffer may take S(t+2)
-        tc_fence_before();
-        warp_arrive64(&sb.s_read[buf]);
         float alpha = 1.f;
         bool resc = false;
         if (valid) {
@@ -428,8 +429,12 @@ __global__ void __launch_bounds__(kThreads64, 2)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] = 0u;
         }
-        // P(t) replaces P(t-1) once PV(t-1) has read it; O is rescaled then too
-        if (step > 0) {
+        // P(t) goes over the first half of S(t)'s columns (this warp's rows,
+        // read above); nothing else touches them until PV(t) has completed.
+        // O is rescaled only once PV(t-1) is done.
+        tmem_st32(tb + lane_addr + kColS64 + 64 * buf, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        const bool resc_any = __any_sync(0xffffffffu, resc);
+        if (resc_any && step > 0) {
           const uint32_t pv = step - 1;
           if (!waitw(&sb.v_empty[pv % kSV], (pv / kSV) & 1, abort_flag, P.status)) {
             ok = false;
@@ -437,8 +442,7 @@ __global__ void __launch_bounds__(kThreads64, 2)
           }
           tc_fence_after();
         }
-        tmem_st32(tp, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-        if (__any_sync(0xffffffffu, resc)) {
+        if (resc_any) {
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
             uint32_t ov[32];
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(kThreads64, 2)
         }
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive64(&sb.p_full);
+        warp_arrive64(&sb.p_full[buf]);
       }
       if (!ok) break;
       // the row's statistics to the epilogue (which has read the previous ones)
