@@ -217,3 +217,19 @@ def test_video_sparse_attention_refuses_before_any_launch(case, exc, match):
         t = _five()
     with pytest.raises(exc, match=match):
         vsa.video_sparse_attention(t["q"], t["k"], t["v"], t["gc"], t["gf"], vs, topk=2, **kw)
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_is_plain_c_and_cpp(lang, std):
+    """include/vsa.h compiles on its own as C99 and as C++17 (no CUDA or torch
+    types in the boundary)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                       "vsa.h")
+    r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, f"-std={std}", hdr],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
