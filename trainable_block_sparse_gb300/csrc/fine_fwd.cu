@@ -77,8 +77,7 @@ constexpr int kWarpEpi = 8, kWarpK = 12, kWarpMma = 13, kWarpV = 14, kWarpSeq = 
 // and epilogue warps
 constexpr int kSeqReaders = 3 + kSoftmaxWarps + kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;              // S (128 columns)
-constexpr uint32_t kColP = 128;            // P buffers (fp16 pairs) at columns 128 and 192
+constexpr uint32_t kColS = 0;              // two S buffers of 128 columns (P over S)
 constexpr uint32_t kColO = 256;            // O accumulators at columns 256 and 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (P stays within [0, 256])
 // Operand kinds of the kernel: the fp16 staged copies, the e4m3 copies, or the
@@ -107,7 +106,7 @@ struct FwdSmem {
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
-  uint64_t s_full, s_read, p_full[2];  // p_full by step parity = P buffer
+  uint64_t s_full[2], p_full[2];  // by step parity = S buffer (P is written over S)
   uint64_t o_full[2], o_free[2];
   uint64_t st_full[2], st_free[2];
   uint64_t final_mma;
@@ -213,8 +212,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       mbar_init(&sb.st_full[i], kSoftmaxWarps);
       mbar_init(&sb.st_free[i], kEpiWarps);
     }
-    mbar_init(&sb.s_full, 1);
-    mbar_init(&sb.s_read, kSoftmaxWarps);  // one arrival per softmax warp
+    for (int i = 0; i < 2; ++i) mbar_init(&sb.s_full[i], 1);
     mbar_init(&sb.final_mma, 1);
     seq_init(sb.seq, kSeqReaders);
     sb.abort = 0;
@@ -324,8 +322,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
     for (int k = 0; k < kKSteps; ++k) qd[k] = qd0 + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
 
-    // S = Q K^T of global step t into the S columns (free once the softmax
-    // warps hold S(t-1) in registers)
+    // S = Q K^T of global step t into S buffer t % 2.  That buffer held P(t-2),
+    // which PV(t-2), issued before this product, reads: the products run in
+    // issue order.
     auto issue_s = [&](uint32_t t, bool two) -> bool {
       const uint32_t slot = t % kSK;
       if (!waitw(&sb.k_full[slot], (t / kSK) & 1, abort_flag, P.status)) return false;
@@ -334,17 +333,17 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const uint64_t kb = kd0 + ((slot * L::kKVBytes) >> 4);
 #pragma unroll
       for (int k = 0; k < kKSteps; ++k) kd[k] = kb + (((k / 4) * L::kChunkBytes + (k % 4) * 32) >> 4);
+      const uint32_t sd = tb + kColS + 128 * (t & 1);
       if constexpr (kF8)
-        issue_ss4_f8(tb + kColS, qd, kd, two ? idesc_s128 : idesc_s64);
+        issue_ss4_f8(sd, qd, kd, two ? idesc_s128 : idesc_s64);
       else
-        issue_ss_chain<kKSteps>(tb + kColS, qd, kd, two ? idesc_s128 : idesc_s64);
-      commit_elect(&sb.s_full);
+        issue_ss_chain<kKSteps>(sd, qd, kd, two ? idesc_s128 : idesc_s64);
+      commit_elect(&sb.s_full[t & 1]);
       commit_elect(&sb.k_empty[slot]);
       return true;
     };
-    // O[obuf] += P V for global step t (P from P buffer t % 2).  The softmax
-    // writes P(t) only after it has seen S(t), whose commit follows PV(t-2):
-    // the P buffer is free by then without a barrier of its own.
+    // O[obuf] += P V for global step t (P over the first columns of S buffer
+    // t % 2, where the softmax warps write it after reading S(t)).
     auto issue_pv = [&](uint32_t t, bool two, bool first, int obuf) -> bool {
       const uint32_t slot = t % kSV, pbuf = t & 1;
       if (!waitw(&sb.p_full[pbuf], (t >> 1) & 1, abort_flag, P.status)) return false;
@@ -354,13 +353,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         // P (e4m3, 16 columns per key tile) x V^T: per key tile one 128-row box of
         // 64-byte rows, K steps of 32 keys at +32 bytes
         const uint64_t vb = sdesc_sw64(smem_u32(sV) + slot * L::kKVBytes, 512);
-        const uint32_t pa = tb + kColP + pbuf * 64;
+        const uint32_t pa = tb + kColS + pbuf * 128;
         issue_ts2_f8(tb + kColO + obuf * 128, pa, vb, vb + 2, idesc_pv, first ? 0u : 1u);
         if (two)
           issue_ts2_f8(tb + kColO + obuf * 128, pa + 16, vb + (8192 >> 4), vb + (8192 >> 4) + 2,
                        idesc_pv, 1u);
       } else {
-        issue_ts_rows(tb + kColO + obuf * 128, tb + kColP + pbuf * 64,
+        issue_ts_rows(tb + kColO + obuf * 128, tb + kColS + pbuf * 128,
                       vd0 + ((slot * L::kKVBytes) >> 4), two, idesc_pv, !first);
       }
       commit_elect(&sb.v_empty[slot]);  // also tells the rescale that PV(t) is done
@@ -378,17 +377,15 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       if (pi.count == 0) continue;
       const int nsteps = (pi.count + 1) / 2;
       const int obuf = it & 1;
-      // S of the item's first step: Q has arrived, and the softmax warps hold
-      // the previous step's S in registers
+      // S of the item's first step, once Q has arrived
       if (!waitw(&sb.q_full, it & 1, abort_flag, P.status)) break;
-      if (step > 0 && !waitw(&sb.s_read, (step - 1) & 1, abort_flag, P.status)) break;
       if (!issue_s(step, pi.count > 1)) break;
       if (nsteps == 1) commit_elect(&sb.q_empty);  // the item's last S product
       for (int s = 0; s < nsteps; ++s) {
         const uint32_t t = step + s;
         if (s + 1 < nsteps) {
-          // S(t+1) as soon as S(t) has been read, ahead of PV(t)
-          if (!waitw(&sb.s_read, t & 1, abort_flag, P.status) || !issue_s(t + 1, 2 * s + 3 < pi.count)) {
+          // S(t+1) into the other S buffer, ahead of PV(t)
+          if (!issue_s(t + 1, 2 * s + 3 < pi.count)) {
             ok = false;
             break;
           }
@@ -441,8 +438,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const bool have = hc == 0 || two;  // this step has a key tile for this half
         const bool valid = have && (e_cur & mybit) != 0;
         e_cur = __ldg(list + min(2 * s + 2 + hc, pi.count - 1));  // in bounds; unused past the list
-        const bool got = waitw(&sb.s_full, step & 1, abort_flag, P.status);
-        const uint32_t ts = tb + lane_addr + kColS;
+        const bool got = waitw(&sb.s_full[step & 1], (step >> 1) & 1, abort_flag, P.status);
+        const uint32_t ts = tb + lane_addr + kColS + 128 * (step & 1);
         uint32_t x[64];  // this half-row of S; its first 32 words are reused for packed P
         float mx = -INFINITY;
         if (got) {
@@ -453,9 +450,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tmem_wait_ld();
           }
         }
-        // S(t) is in registers: the UMMA warp may issue S(t+1) over it
-        tc_fence_before();
-        warp_arrive(&sb.s_read);
         if (got && valid) {
           float m8[8];
 #pragma unroll
@@ -518,15 +512,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] = 0u;
         }
-        // P of key tile hc goes to columns [32 hc, 32 hc + 32) of P buffer step % 2
-        // (e4m3: [16 hc, 16 hc + 16))
+        // P of key tile hc goes to columns [32 hc, 32 hc + 32) of S buffer
+        // step % 2 (e4m3: [16 hc, 16 hc + 16)): both warps of the pair have
+        // read their halves of S(t) before the exchange of maxima above
         if (have) {
           if constexpr (kF8)
-            tmem_st16(tb + lane_addr + kColP + (step & 1) * 64 + 16 * hc,
-                      *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+            tmem_st16(ts + 16 * hc, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
           else
-            tmem_st32(tb + lane_addr + kColP + (step & 1) * 64 + 32 * hc,
-                      *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tmem_st32(ts + 32 * hc, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
         }
         if (__any_sync(0xffffffffu, resc)) {
           // O holds the previous steps' sum: wait for the last PV product,
