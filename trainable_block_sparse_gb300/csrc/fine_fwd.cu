@@ -32,12 +32,16 @@
 //      warp 15     item fetcher: takes the CTA's next item from the launch's
 //                  shared counter and hands it to the other roles
 //                  (item_seq.cuh), so the CTAs finish within about an item.
-//  * TMEM (512 columns): one S buffer, two P buffers (fp16, 64 columns each)
-//    and two O accumulators.  The softmax warps signal as soon as S(t) is in
-//    their registers, so QK^T of step t+1 runs while they compute P(t), ahead
-//    of PV(t); P(t) goes to its own buffer, which PV(t-2) has finished reading
-//    by the time S(t) is seen.  The epilogue of item i drains one O
-//    accumulator while item i+1 accumulates into the other.
+//  * TMEM (512 columns): two S buffers (128 columns each) and two O
+//    accumulators.  P(t) (fp16 pairs, 64 columns) is written over the first
+//    columns of S(t)'s buffer once both warps of a row pair have read their
+//    halves of S(t).  QK^T of step t+1 goes to the other buffer right after
+//    PV(t-1) is issued, without waiting for S(t) to be read; the product that
+//    next writes a buffer, S(t+2), is issued after PV(t), which reads P(t)
+//    there, and the products run in issue order (as the backward's dP(t+1)
+//    after dQ(t)).  One full barrier per S buffer for S and one for P.  The
+//    epilogue of item i drains one O accumulator while item i+1 accumulates
+//    into the other.
 //  * The running maximum is only moved (and O rescaled in TMEM) when it grows
 //    by more than 2^8, which keeps exp arguments bounded and the rescale rare.
 // Every mbarrier wait is bounded; a time-out is recorded in the status word and
