@@ -226,7 +226,7 @@ vsa_status_t vsa_fine_fwd_bf16(const vsa_config_t* cfg, const void* q, const voi
  * host engine that owns all device memory and hands the plugin only its
  * inputs and outputs) cannot supply the `ws` buffer of vsa_fine_fwd; this
  * entry point takes no `ws` and allocates nothing.  Its scratch (status word,
- * query-pair work items and union lists) lives in a fixed array of
+ * schedule counter, query-pair work items and union lists) lives in a fixed array of
  * VSA_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that loads
  * the library until the process exits.
  *  - Arguments and results are those of vsa_fine_fwd, without `ws`.
@@ -238,10 +238,10 @@ vsa_status_t vsa_fine_fwd_bf16(const vsa_config_t* cfg, const void* q, const voi
  *    bytes + 8*list_cap bytes): checked after vsa_validate() has accepted the
  *    configuration (an invalid one returns vsa_validate's code), before the
  *    pointer checks and before any launch.
- *  - The query pairs run in their natural order (slice by slice, neighbouring
- *    cubes together), not in the cost-sorted order vsa_fine_fwd uses for
- *    layers whose K and V fit in L2 (that order needs more scratch); results
- *    are bitwise the same, only the load balance differs.
+ *  - The query pairs are handed out in their natural order (slice by slice,
+ *    neighbouring cubes together), not in the largest-first order vsa_fine_fwd
+ *    uses for layers whose K and V fit in L2 (that order needs more scratch);
+ *    results are bitwise the same, only the load balance differs.
  *  - The first call on each device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
  *  - Every call shares the one array: calls that overlap on the GPU (other
